@@ -1,0 +1,321 @@
+#!/usr/bin/env python
+"""Throughput of the GPT-2 124M training step (bf16, B=16, T=1024) on B300s.
+
+One step = zero_grad, forward (with the fused classifier and the loss read
+back), backward, and the fused global-norm clip + AdamW update: every kernel
+of the hot path, over one batch of synthetic Zipf(1.1) tokens.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) each rank trains an independent replica on its own
+batches (the step shards as data parallelism; this single-GPU build has no
+gradient exchange), so per-GPU work is fixed: weak scaling.  Rank 0 prints one
+JSON line.  ``--impl reference`` times the CPU oracle on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "GPT-2 124M train tokens/s and MFU on 1 B300 (bf16, B=16, T=1024)"
+NOMINAL_BF16_TFLOPS = 2250.0  # B300 dense bf16 tensor peak (no sparsity)
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def flops_per_token(w):
+    """Algorithmic training FLOPs per token: 3x forward; LM head over V; causal attention."""
+    L, C, V, T = w["L"], w["C"], w["V"], w["T"]
+    fwd = 24.0 * L * C * C + 2.0 * C * V + 2.0 * C * (T + 1) * L
+    return 3.0 * fwd
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK if k in d}, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, budget_s=25.0):
+    """The oracle, as it stands, on a bounded sample: the 124M step on B=1 x T=256 tokens."""
+    import torch
+
+    from oracle import gpt2 as og
+
+    torch.set_num_threads(os.cpu_count() or 1)
+    cfg = og.Config.from_dict(w)
+    B, T = 1, 256
+    x, y = synthetic.zipf_window(w["seed"], B, T, w["V"])
+    m = og.OracleGPT2(cfg, w["seed"])
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        m.zero_grad()
+        m.forward(x, y)
+        m.backward(1.0)
+        m.clip_and_adamw(6e-4)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el > budget_s * 0.5 or steps >= 3:
+            break
+    return {"value": steps * B * T / el, "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": "GPT-2 124M fp64 oracle step (fwd+bwd+clip+AdamW) on %d x %d Zipf tokens, %d step(s), %.1f s"
+                      % (B, T, steps, el)}
+
+
+def run_reference(args, w, rank, world):
+    """The CPU oracle timed as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    base = cpu_baseline(w, budget_s=max(10.0, 20.0 * max(1, args.steps) / 20.0))
+    fpt = flops_per_token(w)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w["B"] * w["T"] / base["value"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "gpt2_124m step, sample of B=1 x T=256 tokens", "seed": w["seed"]},
+        "cpu_baseline": base,
+        "e2e": {"value": base["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "mfu_note": "%.3e FLOP/token" % fpt,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gpt2_124m", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = dict(synthetic.WORKLOADS[args.workload])
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+
+    import gpt_decoder_only_train_b300 as g
+    from gpt_decoder_only_train_b300 import build
+
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps are required")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    B, T = w["B"], w["T"]
+    BT = B * T
+    nsteps = args.warmup + args.steps
+    # independent batches per rank: the replica r reads stream windows offset by r
+    xs, ys = [], []
+    for i in range(nsteps):
+        x, y = synthetic.zipf_window(w["seed"], B, T, w["V"], micro_step=rank * nsteps + i)
+        xs.append(x)
+        ys.append(y)
+    X = torch.from_numpy(np.stack(xs)).cuda()
+    Y = torch.from_numpy(np.stack(ys)).cuda()
+    stream = torch.cuda.current_stream()
+    model = g.GPT2(w, seed=w["seed"], stream=stream)
+
+    def lr_at(it):
+        from math import cos, pi
+
+        if it < 700:
+            return 6e-4 * (it + 1) / 700
+        r = (it - 700) / (19073 - 700)
+        return 6e-5 + 0.5 * (1 + cos(pi * r)) * (6e-4 - 6e-5)
+
+    def step(i, x, y):
+        model.zero_grad()
+        loss = model.forward(x, y)
+        model.backward(1.0)
+        norm = model.clip_and_adamw(lr_at(i), 0.9, 0.95, 1e-8, 0.1, 1.0)
+        return loss, norm
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    losses = []
+    for i in range(args.warmup):
+        losses.append(step(i, X[i], Y[i])[0])
+    # ---- timed region (device time, CUDA events on the model's stream)
+    barrier()
+    launches0 = g.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for i in range(args.warmup, nsteps):
+            losses.append(step(i, X[i], Y[i])[0])
+        ev1.record(stream)
+        barrier()
+    launches = g.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * args.steps * BT / (ms / 1e3)
+
+    # ---- per-launch timing pass (same steps, events around every launch) for the roofline
+    model.profile(True)
+    for i in range(args.warmup, nsteps):
+        step(i, X[i], Y[i])
+    prof = model.profile_read()
+    model.profile(False)
+
+    # ---- end to end through the public API: host buffers, copies inside the timed region
+    Xh = torch.from_numpy(np.stack(xs)).pin_memory()
+    Yh = torch.from_numpy(np.stack(ys)).pin_memory()
+    xd = torch.empty(B, T, dtype=torch.int32, device="cuda")
+    yd = torch.empty_like(xd)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.warmup, nsteps):
+        xd.copy_(Xh[i], non_blocking=True)
+        yd.copy_(Yh[i], non_blocking=True)
+        step(i, xd, yd)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * args.steps * BT / (e2e_ms / 1e3)
+
+    if rank == 0:
+        peaks, peak_src = read_peaks()
+        fpt = flops_per_token(w)
+        per_gpu = value / world
+        mm_ms, mm_flops, mm_n = prof["matmul"]
+        achieved = mm_flops / (mm_ms / 1e3) / 1e12 if mm_ms > 0 else None
+        peak = peaks["bf16_tflops_sustained"]
+        kernels = {}
+        for cat, (cms, work, n) in prof.items():
+            unit = "TFLOP/s" if cat in ("matmul", "attention") else "GB/s"
+            rate = (work / (cms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)) if cms > 0 else None
+            kernels[cat] = {"ms_per_step": cms / args.steps, "launches_per_step": n / args.steps,
+                            "achieved": rate, "unit": unit}
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic Zipf(1.1) tokens over V=50257, random-init weights (seeded)",
+            "config": {"workload": "gpt2_124m: L=12 C=768 H=12 V=50257 (Vp=50304) B=16 T=1024, one micro-step "
+                                   "(fwd+bwd+clip+AdamW) per step", "global_batch": B * world, "seq_len": T,
+                       "parallelism": "replicas x%d (no gradient exchange)" % world,
+                       "l2": "inputs larger than L2 (9 GB arena per step)"},
+            "mfu": {"flops_per_token": fpt, "vs_nominal_dense_bf16_2250": per_gpu * fpt / (NOMINAL_BF16_TFLOPS * 1e12),
+                    "vs_measured_bf16_burst": per_gpu * fpt / (peaks["bf16_tflops"] * 1e12)},
+            "roofline": {"kernel": "tcgen05 bf16 GEMM (all matmuls of the step)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "peak_source": "%s bf16_tflops_sustained" % peak_src,
+                         "launches_per_step": mm_n / args.steps,
+                         "timing": "CUDA events around each launch, second pass over the same steps"},
+            "kernels": kernels,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * BT * 4,
+                    "d2h_bytes_per_step": 8},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+            "loss_first_last": [losses[0], losses[-1]],
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,97 @@
+// Shared device helpers: bf16 <-> fp32, 16-byte vectors, warp reductions, and
+// the error word that bounded device waits and index checks write into.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gpt2b300.h"
+
+typedef __nv_bfloat16 bf16;
+
+#define GPT2_CUDA_TRY(expr)                                  \
+    do {                                                     \
+        cudaError_t e__ = (expr);                            \
+        if (e__ != cudaSuccess) {                            \
+            gpt2_set_last_cuda_error(e__, #expr, __LINE__);  \
+            return GPT2_ERR_CUDA;                            \
+        }                                                    \
+    } while (0)
+
+void gpt2_set_last_cuda_error(cudaError_t e, const char *what, int line);
+
+// Process-wide count of kernel launches made by this library.
+void gpt2_note_launches(int n);
+
+// error-word bits written by kernels (the host reads the word after a step)
+enum : int {
+    DEVERR_BAD_TOKEN = 1,
+    DEVERR_TIMEOUT = 2,
+};
+
+__device__ __forceinline__ void raise_device_error(int *err, int bit) {
+    if (err) atomicOr(err, bit);
+}
+
+// ---- element conversions --------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// A 16-byte packet of activations: 8 bf16 or 4 fp32.
+template <typename T> struct Pack16 {
+    static constexpr int N = 16 / sizeof(T);
+    uint4 raw;
+    __device__ __forceinline__ float get(int i) const {
+        const T *p = reinterpret_cast<const T *>(&raw);
+        return to_f32(p[i]);
+    }
+    __device__ __forceinline__ void set(int i, float v) {
+        T *p = reinterpret_cast<T *>(&raw);
+        p[i] = from_f32<T>(v);
+    }
+    __device__ __forceinline__ void load(const T *ptr) { raw = *reinterpret_cast<const uint4 *>(ptr); }
+    __device__ __forceinline__ void load_stream(const T *ptr) {
+        raw = __ldcs(reinterpret_cast<const uint4 *>(ptr));
+    }
+    __device__ __forceinline__ void store(T *ptr) const { *reinterpret_cast<uint4 *>(ptr) = raw; }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// GPT-2's tanh GELU and its derivative (the tanh form of "Let's reproduce
+// GPT-2 (124M)", §Bölümler 2; the constant is sqrt(2/pi)).
+__device__ __forceinline__ float gelu_tanh(float h) {
+    const float k = 0.7978845608028654f, c = 0.044715f;
+    return 0.5f * h * (1.0f + tanhf(k * (h + c * h * h * h)));
+}
+__device__ __forceinline__ float gelu_tanh_grad(float h) {
+    const float k = 0.7978845608028654f, c = 0.044715f;
+    float t = tanhf(k * (h + c * h * h * h));
+    return 0.5f * (1.0f + t) + 0.5f * h * (1.0f - t * t) * k * (1.0f + 3.0f * c * h * h);
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+static inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }

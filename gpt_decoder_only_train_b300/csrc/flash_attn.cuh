@@ -1,0 +1,23 @@
+// Flash-style causal attention for head dimension 64, bf16 in / out, fp32
+// softmax statistics.  The T x T score matrix is never stored: scores live in
+// registers one 64 x 64 block at a time ("Let's reproduce GPT-2 (124M)",
+// §Video özeti: flash attention; "Let's build GPT: from scratch", 01:02:00 and
+// 01:16:56: causal self-attention scaled by 1/sqrt(head_size)).
+#pragma once
+
+#include "common.cuh"
+
+namespace fa {
+
+// O = softmax(Q K^T / sqrt(64), j <= i) V per (b, h); lse [B, H, T] fp32.
+// Element (b, t, h, d) of q/k/v lives at ptr[(b*T + t)*rs + h*64 + d]; o uses ors.
+int attention_forward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, bf16 *o, int64_t ors, float *lse,
+                      int B, int T, int H, int hd, cudaStream_t st);
+
+// dq/dk/dv (row stride rs) from O, dO (row stride ors) and lse; Dscr holds
+// D = rowsum(dO * O) as fp32 [B, H, T].
+int attention_backward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
+                       int64_t ors, const float *lse, bf16 *dq, bf16 *dk, bf16 *dv, float *Dscr, int B, int T, int H,
+                       int hd, cudaStream_t st);
+
+}  // namespace fa

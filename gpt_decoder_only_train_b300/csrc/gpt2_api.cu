@@ -1,0 +1,806 @@
+// C ABI of the GPT-2 training step: arena planning, host initialisation,
+// and the launch sequence of forward, backward and the optimizer.
+//
+// The step follows "Let's reproduce GPT-2 (124M)" (§Bölümler 2: the GPT-2
+// module; §Bölümler 4: cross-entropy; §Video özeti: AdamW, gradient
+// accumulation, mixed precision) and "llm.c kullanarak GPT-2 modelini düşük
+// maliyetle yeniden uygulamak" (§Eğitimi çalıştırma: -b/-t/-d/-r; §Eğitim
+// süreci: gradient clipping).  Block order is pre-LN:
+//   x1 = x + proj(attn(ln1(x)));  x' = x1 + fcproj(gelu(fc(ln2(x1))))
+// with a final LayerNorm and an LM head tied to wte.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "flash_attn.cuh"
+#include "kernels.cuh"
+#include "tc_gemm.cuh"
+
+// ------------------------------------------------------------------ errors
+static thread_local char g_last_error[256] = "";
+
+void gpt2_set_last_cuda_error(cudaError_t e, const char *what, int line) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s (%s) at gpt2_api line %d: %s", cudaGetErrorName(e),
+             cudaGetErrorString(e), line, what);
+}
+
+extern "C" const char *gpt2_last_error_detail(void) { return g_last_error; }
+
+static std::atomic<long long> g_launches{0};
+void gpt2_note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+extern "C" long long gpt2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" const char *gpt2_strerror(int s) {
+    switch (s) {
+        case GPT2_OK: return "ok";
+        case GPT2_ERR_BAD_CONFIG: return "bad config";
+        case GPT2_ERR_BAD_SHAPE: return "bad shape";
+        case GPT2_ERR_BAD_TOKEN: return "token or target out of range";
+        case GPT2_ERR_ARENA_TOO_SMALL: return "arena too small";
+        case GPT2_ERR_CUDA: return "CUDA error";
+        case GPT2_ERR_NONFINITE: return "non-finite loss or gradient norm";
+        case GPT2_ERR_TIMEOUT: return "bounded device wait timed out";
+        case GPT2_ERR_BAD_ARG: return "bad argument";
+        case GPT2_ERR_UNSUPPORTED: return "unsupported device or feature";
+        case GPT2_ERR_STATE: return "call order violated";
+        default: return "unknown status";
+    }
+}
+
+// ------------------------------------------------------------------ model
+struct TensorInfo {
+    std::string name;
+    int ndim;
+    int64_t shape[2];
+    int64_t numel;
+    int64_t offset;  // elements into the flat parameter arena
+    bool decay;      // 2-D weight: receives weight decay
+    int kind;        // 0 zeros, 1 ones, 2 normal (all rows), 3 normal (first V rows)
+    double std;
+};
+
+struct LayerBuf {
+    void *resid, *ln1, *qkv, *att, *resid_mid, *ln2, *fch, *fcg;
+    float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lse;
+};
+
+struct LayerParams {
+    int ln1g, ln1b, qkvw, qkvb, projw, projb, ln2g, ln2b, fcw, fcb, fcprojw, fcprojb;  // tensor ids
+};
+
+struct gpt2_model {
+    gpt2_config cfg;
+    cudaStream_t stream;
+    uint8_t *arena;
+    size_t arena_bytes;
+    int num_sms;
+    std::vector<TensorInfo> tensors;
+    std::vector<LayerParams> lp;
+    int64_t n_params, n_decay;
+    float *params, *grads, *adam_m, *adam_v;
+    bf16 *wbf;  // bf16 copy of the weights (bf16 mode)
+    std::vector<LayerBuf> layers;
+    void *resid_final, *lnf;
+    float *lnf_mean, *lnf_rstd;
+    void *logits;
+    float *loss_rows, *loss_dev, *norm_dev;
+    int *tokens;
+    void *dres, *dbig, *dqkv, *datt, *dsmall, *gelu_buf;
+    float *attn_D;
+    double *norm_partials;
+    unsigned *barrier;
+    int *err_dev;
+    int max_adam_blocks;
+    int fwd_B, fwd_T;
+    bool have_dlogits;
+    int adam_t;
+    // optional per-launch timing (gpt2_profile): event pairs recorded around launches
+    struct Rec {
+        cudaEvent_t a, b;
+        int cat;
+        double work;
+    };
+    std::vector<Rec> prof;
+    size_t prof_used = 0;
+    bool prof_on = false;
+    double prof_ms[GPT2_PROF_NCAT] = {}, prof_work[GPT2_PROF_NCAT] = {};
+    long long prof_n[GPT2_PROF_NCAT] = {};
+};
+
+// ------------------------------------------------------------------ layout
+namespace {
+
+struct Bump {
+    uint8_t *base;
+    size_t off = 0;
+    template <typename P> P *take(size_t bytes) {
+        off = (off + 255) & ~size_t(255);
+        P *p = reinterpret_cast<P *>(base + off);
+        off += bytes;
+        return p;
+    }
+};
+
+bool valid_config(const gpt2_config &c) {
+    if (c.L <= 0 || c.C <= 0 || c.H <= 0 || c.V <= 0 || c.Vp < c.V || c.T <= 0 || c.B <= 0) return false;
+    if (c.C % c.H) return false;
+    if (c.dtype != GPT2_DTYPE_FP32 && c.dtype != GPT2_DTYPE_BF16) return false;
+    const int hd = c.C / c.H;
+    if (c.dtype == GPT2_DTYPE_FP32) {
+        if (c.C % 4 || c.Vp % 4 || (hd != 8 && hd != 16 && hd != 32 && hd != 64)) return false;
+        if (c.C > 1024) return false;
+    } else {
+        if (hd != 64 || c.C % 64 || c.Vp % 64 || c.C > 2048) return false;
+    }
+    return true;
+}
+
+void make_tensors(const gpt2_config &c, std::vector<TensorInfo> &ts, std::vector<LayerParams> &lp, int64_t &n_params,
+                  int64_t &n_decay) {
+    ts.clear();
+    lp.assign(c.L, LayerParams{});
+    const double std = 0.02, rstd = 0.02 / sqrt(2.0 * c.L);
+    auto add = [&](const std::string &name, int64_t r, int64_t cols, int kind, double s, bool decay) {
+        TensorInfo t;
+        t.name = name;
+        t.ndim = cols ? 2 : 1;
+        t.shape[0] = r;
+        t.shape[1] = cols;
+        t.numel = cols ? r * cols : r;
+        t.decay = decay;
+        t.kind = kind;
+        t.std = s;
+        t.offset = -1;
+        ts.push_back(t);
+        return (int)ts.size() - 1;
+    };
+    add("wte", c.Vp, c.C, 3, std, true);
+    add("wpe", c.T, c.C, 2, std, true);
+    for (int l = 0; l < c.L; ++l) {
+        const std::string p = "h" + std::to_string(l) + ".";
+        LayerParams &q = lp[l];
+        q.ln1g = add(p + "ln1.g", c.C, 0, 1, 0, false);
+        q.ln1b = add(p + "ln1.b", c.C, 0, 0, 0, false);
+        q.qkvw = add(p + "qkv.w", 3 * c.C, c.C, 2, std, true);
+        q.qkvb = add(p + "qkv.b", 3 * c.C, 0, 0, 0, false);
+        q.projw = add(p + "proj.w", c.C, c.C, 2, rstd, true);
+        q.projb = add(p + "proj.b", c.C, 0, 0, 0, false);
+        q.ln2g = add(p + "ln2.g", c.C, 0, 1, 0, false);
+        q.ln2b = add(p + "ln2.b", c.C, 0, 0, 0, false);
+        q.fcw = add(p + "fc.w", 4 * c.C, c.C, 2, std, true);
+        q.fcb = add(p + "fc.b", 4 * c.C, 0, 0, 0, false);
+        q.fcprojw = add(p + "fcproj.w", c.C, 4 * c.C, 2, rstd, true);
+        q.fcprojb = add(p + "fcproj.b", c.C, 0, 0, 0, false);
+    }
+    add("lnf.g", c.C, 0, 1, 0, false);
+    add("lnf.b", c.C, 0, 0, 0, false);
+    // physical order: all decayed (2-D) tensors first, each padded to 64 elements
+    int64_t off = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (auto &t : ts) {
+            if (t.decay != (pass == 0)) continue;
+            t.offset = off;
+            off += (t.numel + 63) / 64 * 64;
+        }
+        if (pass == 0) n_decay = off;
+    }
+    n_params = off;
+}
+
+template <typename P> P *take_opt(Bump &b, bool on, size_t bytes) { return on ? b.take<P>(bytes) : nullptr; }
+
+void plan(gpt2_model &m, uint8_t *base) {
+    const gpt2_config &c = m.cfg;
+    const bool bf = c.dtype == GPT2_DTYPE_BF16;
+    const size_t es = bf ? 2 : 4;
+    const int64_t BT = (int64_t)c.B * c.T, C = c.C;
+    Bump b{base};
+    m.params = b.take<float>(m.n_params * 4);
+    m.grads = b.take<float>(m.n_params * 4);
+    m.adam_m = b.take<float>(m.n_params * 4);
+    m.adam_v = b.take<float>(m.n_params * 4);
+    m.wbf = take_opt<bf16>(b, bf, m.n_params * 2);
+    m.layers.assign(c.L, LayerBuf{});
+    for (int l = 0; l < c.L; ++l) {
+        LayerBuf &y = m.layers[l];
+        y.resid = b.take<void>(BT * C * es);
+        y.ln1 = b.take<void>(BT * C * es);
+        y.qkv = b.take<void>(BT * 3 * C * es);
+        y.att = b.take<void>(BT * C * es);
+        y.resid_mid = b.take<void>(BT * C * es);
+        y.ln2 = b.take<void>(BT * C * es);
+        y.fch = b.take<void>(BT * 4 * C * es);
+        y.fcg = take_opt<void>(b, !c.recompute_gelu, BT * 4 * C * es);
+        y.ln1_mean = b.take<float>(BT * 4);
+        y.ln1_rstd = b.take<float>(BT * 4);
+        y.ln2_mean = b.take<float>(BT * 4);
+        y.ln2_rstd = b.take<float>(BT * 4);
+        y.lse = b.take<float>((int64_t)c.B * c.H * c.T * 4);
+    }
+    m.resid_final = b.take<void>(BT * C * es);
+    m.lnf = b.take<void>(BT * C * es);
+    m.lnf_mean = b.take<float>(BT * 4);
+    m.lnf_rstd = b.take<float>(BT * 4);
+    m.logits = b.take<void>(BT * (int64_t)c.Vp * es);
+    m.loss_rows = b.take<float>(BT * 4);
+    m.loss_dev = b.take<float>(64);
+    m.norm_dev = b.take<float>(64);
+    m.tokens = b.take<int>(BT * 4);
+    m.dres = b.take<void>(BT * C * es);
+    m.dbig = b.take<void>(BT * 4 * C * es);
+    m.dqkv = b.take<void>(BT * 3 * C * es);
+    m.datt = b.take<void>(BT * C * es);
+    m.dsmall = b.take<void>(BT * C * es);
+    m.gelu_buf = take_opt<void>(b, c.recompute_gelu != 0, BT * 4 * C * es);
+    m.attn_D = b.take<float>((int64_t)c.B * c.H * c.T * 4);
+    m.norm_partials = b.take<double>((size_t)m.max_adam_blocks * 8);
+    m.barrier = b.take<unsigned>(64);
+    m.err_dev = b.take<int>(64);
+    m.arena_bytes = b.off + 256;
+}
+
+// SplitMix64 output for state x (Steele, Lea & Flood, OOPSLA 2014).
+inline uint64_t sm64(uint64_t x) {
+    uint64_t z = x + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// Fill `n` fp32 values with N(0, std^2): counter draws (seed, id, 2i), (.., 2i+1),
+// Box-Muller cosine branch in double, one rounding to fp32.
+void fill_normal(uint64_t seed, uint64_t id, int64_t n, double sd, float *out) {
+    const uint64_t key = sm64(sm64(seed) + id);
+    const int nth = (int)std::max(1u, std::min(32u, std::thread::hardware_concurrency()));
+    const int64_t chunk = (n + nth - 1) / nth;
+    std::vector<std::thread> th;
+    for (int t = 0; t < nth; ++t) {
+        th.emplace_back([=]() {
+            const int64_t a = t * chunk, e = std::min(n, a + chunk);
+            for (int64_t i = a; i < e; ++i) {
+                const uint64_t r1 = sm64(key + 2 * (uint64_t)i), r2 = sm64(key + 2 * (uint64_t)i + 1);
+                const double u1 = ((double)(r1 >> 11) + 1.0) * (1.0 / 9007199254740992.0);
+                const double u2 = (double)(r2 >> 11) * (1.0 / 9007199254740992.0);
+                const double z = sqrt(-2.0 * log(u1)) * cos(6.283185307179586 * u2);
+                out[i] = (float)(sd * z);
+            }
+        });
+    }
+    for (auto &x : th) x.join();
+}
+
+int check_device(int &num_sms) {
+    int dev = 0;
+    GPT2_CUDA_TRY(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    GPT2_CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
+    num_sms = prop.multiProcessorCount;
+    return (prop.major == 10 && prop.minor == 3) ? GPT2_OK : GPT2_ERR_UNSUPPORTED;
+}
+
+// ---- per-launch timing ---------------------------------------------------------
+int prof_flush(gpt2_model *m) {
+    if (!m->prof_used) return GPT2_OK;
+    GPT2_CUDA_TRY(cudaStreamSynchronize(m->stream));
+    for (size_t i = 0; i < m->prof_used; ++i) {
+        float ms = 0.f;
+        GPT2_CUDA_TRY(cudaEventElapsedTime(&ms, m->prof[i].a, m->prof[i].b));
+        m->prof_ms[m->prof[i].cat] += ms;
+        m->prof_work[m->prof[i].cat] += m->prof[i].work;
+        m->prof_n[m->prof[i].cat] += 1;
+    }
+    m->prof_used = 0;
+    return GPT2_OK;
+}
+
+// Record an event pair around `launch()` when profiling is on.
+template <typename F> int timed(gpt2_model *m, int cat, double work, F &&launch) {
+    if (!m->prof_on) return launch();
+    if (m->prof_used == m->prof.size()) {
+        if (m->prof.size() < 4096) {
+            gpt2_model::Rec r{};
+            GPT2_CUDA_TRY(cudaEventCreate(&r.a));
+            GPT2_CUDA_TRY(cudaEventCreate(&r.b));
+            m->prof.push_back(r);
+        } else {
+            if (int rc = prof_flush(m)) return rc;
+        }
+    }
+    gpt2_model::Rec &r = m->prof[m->prof_used];
+    r.cat = cat;
+    r.work = work;
+    GPT2_CUDA_TRY(cudaEventRecord(r.a, m->stream));
+    const int rc = launch();
+    GPT2_CUDA_TRY(cudaEventRecord(r.b, m->stream));
+    m->prof_used++;
+    return rc;
+}
+
+// ---- typed helpers -------------------------------------------------------------
+template <typename T> T *W(gpt2_model *m, int id);
+template <> float *W<float>(gpt2_model *m, int id) { return m->params + m->tensors[id].offset; }
+template <> bf16 *W<bf16>(gpt2_model *m, int id) { return m->wbf + m->tensors[id].offset; }
+inline float *Pf(gpt2_model *m, int id) { return m->params + m->tensors[id].offset; }
+inline float *Gf(gpt2_model *m, int id) { return m->grads + m->tensors[id].offset; }
+
+#define TRY(x)                    \
+    do {                          \
+        int rc__ = (x);           \
+        if (rc__) return rc__;    \
+    } while (0)
+
+// launch `expr` (an int-returning launcher call) under the per-launch timer
+#define TIMED(cat, work, expr) TRY(timed(m, cat, (double)(work), [&]() -> int { return (expr); }))
+
+// acc[m,n] = sum_k A(m,k) B(n,k) with the majorness conventions of gpt2_op_matmul.
+template <typename T>
+int mm(gpt2_model *m, const void *A, int64_t lda, bool a_km, const void *B, int64_t ldb, bool b_km, void *D, void *D2,
+       const void *R, int64_t ldd, const float *bias, int M, int N, int K, int epi, float alpha = 1.0f) {
+    if constexpr (sizeof(T) == 2) {
+        tcg::GemmDesc g;
+        g.A = (const bf16 *)A;
+        g.lda = lda;
+        g.a_kmajor = a_km;
+        g.B = (const bf16 *)B;
+        g.ldb = ldb;
+        g.b_kmajor = b_km;
+        g.D = D;
+        g.D2 = (bf16 *)D2;
+        g.R = (const bf16 *)R;
+        g.ldd = ldd;
+        g.bias = bias;
+        g.M = M;
+        g.N = N;
+        g.K = K;
+        g.epi = epi;
+        g.alpha = alpha;
+        g.err = m->err_dev;
+        return timed(m, GPT2_PROF_MATMUL, 2.0 * M * N * K, [&] { return tcg::launch_gemm_tc(g, m->num_sms, m->stream); });
+    } else {
+        return timed(m, GPT2_PROF_MATMUL, 2.0 * M * N * K, [&] {
+            return k::matmul_simt<float>((const float *)A, a_km ? lda : 1, a_km ? 1 : lda, (const float *)B,
+                                         b_km ? ldb : 1, b_km ? 1 : ldb, D, (float *)D2, (const float *)R, ldd, bias,
+                                         M, N, K, epi, alpha, m->stream);
+        });
+    }
+}
+
+// algorithmic FLOP of causal attention forward: 4 hd per causal (i, j) pair
+inline double attn_flops(int B, int Tn, int H, int hd) { return 4.0 * hd * (0.5 * Tn * (Tn + 1.0)) * B * H; }
+
+template <typename T>
+int attn_fwd(gpt2_model *m, const T *qkv, T *o, float *lse, int B, int Tn) {
+    const int C = m->cfg.C, H = m->cfg.H, hd = C / H;
+    return timed(m, GPT2_PROF_ATTENTION, attn_flops(B, Tn, H, hd), [&] {
+        if constexpr (sizeof(T) == 2)
+            return fa::attention_forward(qkv, qkv + C, qkv + 2 * C, 3 * C, o, C, lse, B, Tn, H, hd, m->stream);
+        else
+            return k::attention_forward_simt<T>(qkv, qkv + C, qkv + 2 * C, 3 * C, o, C, lse, B, Tn, H, hd,
+                                                m->stream);
+    });
+}
+
+template <typename T>
+int attn_bwd(gpt2_model *m, const T *qkv, const T *o, const T *dout, const float *lse, T *dqkv, int B, int Tn) {
+    const int C = m->cfg.C, H = m->cfg.H, hd = C / H;
+    return timed(m, GPT2_PROF_ATTENTION, 2.0 * attn_flops(B, Tn, H, hd), [&] {
+        if constexpr (sizeof(T) == 2)
+            return fa::attention_backward(qkv, qkv + C, qkv + 2 * C, 3 * C, o, dout, C, lse, dqkv, dqkv + C,
+                                          dqkv + 2 * C, m->attn_D, B, Tn, H, hd, m->stream);
+        else
+            return k::attention_backward_simt<T>(qkv, qkv + C, qkv + 2 * C, 3 * C, o, dout, C, lse, dqkv, dqkv + C,
+                                                 dqkv + 2 * C, m->attn_D, B, Tn, H, hd, m->stream);
+    });
+}
+
+// ---- forward ----------------------------------------------------------------------
+template <typename T>
+int forward_impl(gpt2_model *m, const int32_t *d_targets, int B, int Tn) {
+    const gpt2_config &c = m->cfg;
+    const int BT = B * Tn, C = c.C;
+    cudaStream_t st = m->stream;
+    const double es = sizeof(T), act = (double)BT * C * es, stats = 8.0 * BT;
+    TIMED(GPT2_PROF_OTHER, 4.0 * BT + (double)BT * C * 4 + (double)Tn * C * 4 + act,
+          k::embed_forward<T>(m->tokens, Pf(m, 0), Pf(m, 1), (T *)m->layers[0].resid, B, Tn, C, c.V, m->err_dev, st));
+    for (int l = 0; l < c.L; ++l) {
+        LayerBuf &y = m->layers[l];
+        const LayerParams &p = m->lp[l];
+        T *next = (T *)(l + 1 < c.L ? m->layers[l + 1].resid : m->resid_final);
+        T *gbuf = (T *)(c.recompute_gelu ? m->gelu_buf : y.fcg);
+        TIMED(GPT2_PROF_LAYERNORM, 2 * act + stats,
+              k::layernorm_forward<T>((T *)y.resid, Pf(m, p.ln1g), Pf(m, p.ln1b), (T *)y.ln1, y.ln1_mean, y.ln1_rstd,
+                                      BT, C, st));
+        TRY(mm<T>(m, y.ln1, C, true, W<T>(m, p.qkvw), C, true, y.qkv, nullptr, nullptr, 3 * C, Pf(m, p.qkvb), BT,
+                  3 * C, C, GPT2_EPI_STORE));
+        TRY(attn_fwd<T>(m, (T *)y.qkv, (T *)y.att, y.lse, B, Tn));
+        TRY(mm<T>(m, y.att, C, true, W<T>(m, p.projw), C, true, y.resid_mid, nullptr, y.resid, C, Pf(m, p.projb), BT,
+                  C, C, GPT2_EPI_RESIDUAL));
+        TIMED(GPT2_PROF_LAYERNORM, 2 * act + stats,
+              k::layernorm_forward<T>((T *)y.resid_mid, Pf(m, p.ln2g), Pf(m, p.ln2b), (T *)y.ln2, y.ln2_mean,
+                                      y.ln2_rstd, BT, C, st));
+        TRY(mm<T>(m, y.ln2, C, true, W<T>(m, p.fcw), C, true, y.fch, gbuf, nullptr, 4 * C, Pf(m, p.fcb), BT, 4 * C, C,
+                  GPT2_EPI_GELU));
+        TRY(mm<T>(m, gbuf, 4 * C, true, W<T>(m, p.fcprojw), 4 * C, true, next, nullptr, y.resid_mid, C,
+                  Pf(m, p.fcprojb), BT, C, 4 * C, GPT2_EPI_RESIDUAL));
+    }
+    const int nt = (int)m->tensors.size();
+    TIMED(GPT2_PROF_LAYERNORM, 2 * act + stats,
+          k::layernorm_forward<T>((T *)m->resid_final, Pf(m, nt - 2), Pf(m, nt - 1), (T *)m->lnf, m->lnf_mean,
+                                  m->lnf_rstd, BT, C, st));
+    TRY(mm<T>(m, m->lnf, C, true, W<T>(m, 0), C, true, m->logits, nullptr, nullptr, c.Vp, nullptr, BT, c.Vp, C,
+              GPT2_EPI_STORE));
+    if (d_targets) {
+        TIMED(GPT2_PROF_CLASSIFIER, 2.0 * BT * c.Vp * es + 8.0 * BT,
+              k::classifier<T>((T *)m->logits, d_targets, m->loss_rows, BT, c.V, c.Vp, 1.0f / BT, m->err_dev, st));
+        TIMED(GPT2_PROF_OTHER, 4.0 * BT, k::mean_rows(m->loss_rows, BT, m->loss_dev, st));
+    }
+    return GPT2_OK;
+}
+
+// ---- backward ---------------------------------------------------------------------
+template <typename T>
+int backward_impl(gpt2_model *m, float grad_scale) {
+    const gpt2_config &c = m->cfg;
+    const int B = m->fwd_B, Tn = m->fwd_T, BT = B * Tn, C = c.C, Vp = c.Vp;
+    cudaStream_t st = m->stream;
+    const int nt = (int)m->tensors.size();
+    const double es = sizeof(T), act = (double)BT * C * es, stats = 8.0 * BT;
+    T *dres = (T *)m->dres, *dbig = (T *)m->dbig, *dqkv = (T *)m->dqkv, *datt = (T *)m->datt,
+      *dsmall = (T *)m->dsmall;
+    // LM head (tied): dy_f = alpha dz wte ; dwte += alpha dz^T y_f
+    TRY(mm<T>(m, m->logits, Vp, true, W<T>(m, 0), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, Vp,
+              GPT2_EPI_STORE, grad_scale));
+    TRY(mm<T>(m, m->logits, Vp, false, m->lnf, C, false, Gf(m, 0), nullptr, nullptr, C, nullptr, Vp, C, BT,
+              GPT2_EPI_ACCUM_F32, grad_scale));
+    TIMED(GPT2_PROF_LAYERNORM, 3 * act + stats,
+          k::layernorm_backward<T>(dsmall, (T *)m->resid_final, m->lnf_mean, m->lnf_rstd, Pf(m, nt - 2), nullptr, dres,
+                                   Gf(m, nt - 2), Gf(m, nt - 1), BT, C, st));
+    for (int l = c.L - 1; l >= 0; --l) {
+        LayerBuf &y = m->layers[l];
+        const LayerParams &p = m->lp[l];
+        T *g_in = (T *)y.fcg;
+        if (c.recompute_gelu) {
+            g_in = (T *)m->gelu_buf;
+            TIMED(GPT2_PROF_OTHER, 8 * act, k::gelu_forward<T>((T *)y.fch, g_in, (int64_t)BT * 4 * C, st));
+        }
+        // FC projection: x' = x1 + g Wfcproj^T + b
+        TRY(mm<T>(m, dres, C, false, g_in, 4 * C, false, Gf(m, p.fcprojw), nullptr, nullptr, 4 * C, nullptr, C, 4 * C,
+                  BT, GPT2_EPI_ACCUM_F32));
+        TIMED(GPT2_PROF_OTHER, act, k::column_sum<T>(dres, BT, C, Gf(m, p.fcprojb), st));
+        TRY(mm<T>(m, dres, C, true, W<T>(m, p.fcprojw), 4 * C, false, dbig, nullptr, y.fch, 4 * C, nullptr, BT, 4 * C,
+                  C, GPT2_EPI_GELU_BWD));
+        // FC: h = y2 Wfc^T + b
+        TRY(mm<T>(m, dbig, 4 * C, false, y.ln2, C, false, Gf(m, p.fcw), nullptr, nullptr, C, nullptr, 4 * C, C, BT,
+                  GPT2_EPI_ACCUM_F32));
+        TIMED(GPT2_PROF_OTHER, 4 * act, k::column_sum<T>(dbig, BT, 4 * C, Gf(m, p.fcb), st));
+        TRY(mm<T>(m, dbig, 4 * C, true, W<T>(m, p.fcw), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, 4 * C,
+                  GPT2_EPI_STORE));
+        TIMED(GPT2_PROF_LAYERNORM, 4 * act + stats,
+              k::layernorm_backward<T>(dsmall, (T *)y.resid_mid, y.ln2_mean, y.ln2_rstd, Pf(m, p.ln2g), dres, dres,
+                                       Gf(m, p.ln2g), Gf(m, p.ln2b), BT, C, st));
+        // attention projection: x1 = x + O Wproj^T + b
+        TRY(mm<T>(m, dres, C, false, y.att, C, false, Gf(m, p.projw), nullptr, nullptr, C, nullptr, C, C, BT,
+                  GPT2_EPI_ACCUM_F32));
+        TIMED(GPT2_PROF_OTHER, act, k::column_sum<T>(dres, BT, C, Gf(m, p.projb), st));
+        TRY(mm<T>(m, dres, C, true, W<T>(m, p.projw), C, false, datt, nullptr, nullptr, C, nullptr, BT, C, C,
+                  GPT2_EPI_STORE));
+        TRY(attn_bwd<T>(m, (T *)y.qkv, (T *)y.att, datt, y.lse, dqkv, B, Tn));
+        // QKV: qkv = y Wqkv^T + b
+        TRY(mm<T>(m, dqkv, 3 * C, false, y.ln1, C, false, Gf(m, p.qkvw), nullptr, nullptr, C, nullptr, 3 * C, C, BT,
+                  GPT2_EPI_ACCUM_F32));
+        TIMED(GPT2_PROF_OTHER, 3 * act, k::column_sum<T>(dqkv, BT, 3 * C, Gf(m, p.qkvb), st));
+        TRY(mm<T>(m, dqkv, 3 * C, true, W<T>(m, p.qkvw), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, 3 * C,
+                  GPT2_EPI_STORE));
+        TIMED(GPT2_PROF_LAYERNORM, 4 * act + stats,
+              k::layernorm_backward<T>(dsmall, (T *)y.resid, y.ln1_mean, y.ln1_rstd, Pf(m, p.ln1g), dres, dres,
+                                       Gf(m, p.ln1g), Gf(m, p.ln1b), BT, C, st));
+    }
+    TIMED(GPT2_PROF_OTHER, act + 8.0 * BT * C + 4.0 * BT,
+          k::embed_backward<T>(m->tokens, dres, Gf(m, 0), Gf(m, 1), B, Tn, C, c.V, st));
+    return GPT2_OK;
+}
+
+int read_error_word(gpt2_model *m, int &word) {
+    GPT2_CUDA_TRY(cudaMemcpyAsync(&word, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
+    GPT2_CUDA_TRY(cudaStreamSynchronize(m->stream));
+    if (word) GPT2_CUDA_TRY(cudaMemsetAsync(m->err_dev, 0, sizeof(int), m->stream));
+    return GPT2_OK;
+}
+
+int error_from_word(int word) {
+    if (word & DEVERR_TIMEOUT) return GPT2_ERR_TIMEOUT;
+    if (word & DEVERR_BAD_TOKEN) return GPT2_ERR_BAD_TOKEN;
+    return GPT2_OK;
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+extern "C" size_t gpt2_arena_bytes(const gpt2_config *cfg) {
+    if (!cfg || !valid_config(*cfg)) return 0;
+    gpt2_model m{};
+    m.cfg = *cfg;
+    make_tensors(m.cfg, m.tensors, m.lp, m.n_params, m.n_decay);
+    m.max_adam_blocks = k::clip_adamw_max_blocks(160);
+    plan(m, nullptr);
+    return m.arena_bytes;
+}
+
+extern "C" int gpt2_build(const gpt2_config *cfg, uint64_t seed, void *dev_arena, size_t arena_bytes,
+                          void *cuda_stream, gpt2_model **out) {
+    if (!cfg || !out || !dev_arena) return GPT2_ERR_BAD_ARG;
+    *out = nullptr;
+    if (!valid_config(*cfg)) return GPT2_ERR_BAD_CONFIG;
+    if (reinterpret_cast<uintptr_t>(dev_arena) & 255) return GPT2_ERR_BAD_ARG;
+    int num_sms = 0;
+    TRY(check_device(num_sms));
+    if (arena_bytes < gpt2_arena_bytes(cfg)) return GPT2_ERR_ARENA_TOO_SMALL;
+    gpt2_model *m = new gpt2_model{};
+    m->cfg = *cfg;
+    m->stream = (cudaStream_t)cuda_stream;
+    m->arena = (uint8_t *)dev_arena;
+    m->num_sms = num_sms;
+    make_tensors(m->cfg, m->tensors, m->lp, m->n_params, m->n_decay);
+    m->max_adam_blocks = k::clip_adamw_max_blocks(160);
+    plan(*m, m->arena);
+    // host init: one fp32 image of all parameters, copied once
+    std::vector<float> host(m->n_params, 0.0f);
+    for (size_t id = 0; id < m->tensors.size(); ++id) {
+        const TensorInfo &t = m->tensors[id];
+        float *dst = host.data() + t.offset;
+        if (t.kind == 1) std::fill(dst, dst + t.numel, 1.0f);
+        if (t.kind == 2) fill_normal(seed, id, t.numel, t.std, dst);
+        if (t.kind == 3) fill_normal(seed, id, (int64_t)cfg->V * cfg->C, t.std, dst);
+    }
+    int rc = GPT2_OK;
+    auto fail = [&](int r) {
+        delete m;
+        return r;
+    };
+    if (cudaMemcpyAsync(m->params, host.data(), m->n_params * 4, cudaMemcpyHostToDevice, m->stream) != cudaSuccess)
+        return fail(GPT2_ERR_CUDA);
+    if (cudaMemsetAsync(m->grads, 0, m->n_params * 4 * 3, m->stream) != cudaSuccess) return fail(GPT2_ERR_CUDA);
+    if (m->wbf && (rc = k::cast_f32_bf16(m->params, m->wbf, m->n_params, m->stream))) return fail(rc);
+    if (cudaMemsetAsync(m->err_dev, 0, 256, m->stream) != cudaSuccess) return fail(GPT2_ERR_CUDA);
+    if (cudaStreamSynchronize(m->stream) != cudaSuccess) return fail(GPT2_ERR_CUDA);
+    *out = m;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_forward(gpt2_model *m, const int32_t *d_tokens, const int32_t *d_targets, int B, int T,
+                            float *loss_out) {
+    if (!m || !d_tokens) return GPT2_ERR_BAD_ARG;
+    if (B <= 0 || T <= 0 || B > m->cfg.B || T > m->cfg.T) return GPT2_ERR_BAD_SHAPE;
+    if (d_targets && !loss_out) return GPT2_ERR_BAD_ARG;
+    m->have_dlogits = false;
+    GPT2_CUDA_TRY(cudaMemcpyAsync(m->tokens, d_tokens, (size_t)B * T * 4, cudaMemcpyDeviceToDevice, m->stream));
+    const int rc = m->cfg.dtype == GPT2_DTYPE_BF16 ? forward_impl<bf16>(m, d_targets, B, T)
+                                                   : forward_impl<float>(m, d_targets, B, T);
+    if (rc) return rc;
+    m->fwd_B = B;
+    m->fwd_T = T;
+    if (!d_targets) return GPT2_OK;
+    GPT2_CUDA_TRY(cudaMemcpyAsync(loss_out, m->loss_dev, 4, cudaMemcpyDeviceToHost, m->stream));
+    int word = 0;
+    TRY(read_error_word(m, word));
+    TRY(error_from_word(word));
+    m->have_dlogits = true;
+    return std::isfinite(*loss_out) ? GPT2_OK : GPT2_ERR_NONFINITE;
+}
+
+extern "C" int gpt2_backward(gpt2_model *m, float grad_scale) {
+    if (!m) return GPT2_ERR_BAD_ARG;
+    if (!m->have_dlogits) return GPT2_ERR_STATE;
+    m->have_dlogits = false;  // dlogits are consumed
+    return m->cfg.dtype == GPT2_DTYPE_BF16 ? backward_impl<bf16>(m, grad_scale) : backward_impl<float>(m, grad_scale);
+}
+
+extern "C" int gpt2_zero_grad(gpt2_model *m) {
+    if (!m) return GPT2_ERR_BAD_ARG;
+    GPT2_CUDA_TRY(cudaMemsetAsync(m->grads, 0, m->n_params * 4, m->stream));
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_clip_and_adamw(gpt2_model *m, float lr, float beta1, float beta2, float eps, float wd, float clip,
+                                   float *grad_norm_out) {
+    if (!m || !grad_norm_out) return GPT2_ERR_BAD_ARG;
+    const int t = m->adam_t + 1;
+    k::AdamArgs a;
+    a.lr = lr;
+    a.beta1 = beta1;
+    a.beta2 = beta2;
+    a.eps = eps;
+    a.wd = wd;
+    a.clip = clip;
+    a.bc1 = (float)(1.0 - pow((double)beta1, t));
+    a.bc2 = (float)(1.0 - pow((double)beta2, t));
+    const double adam_bytes = (double)m->n_params * (m->wbf ? 34.0 : 32.0);
+    TIMED(GPT2_PROF_ADAMW, adam_bytes,
+          k::clip_adamw(m->params, m->grads, m->adam_m, m->adam_v, m->wbf, m->n_params, m->n_decay, a,
+                        m->norm_partials, m->barrier, m->max_adam_blocks, m->norm_dev, m->err_dev, m->num_sms,
+                        m->stream));
+    GPT2_CUDA_TRY(cudaMemcpyAsync(grad_norm_out, m->norm_dev, 4, cudaMemcpyDeviceToHost, m->stream));
+    int word = 0;
+    TRY(read_error_word(m, word));
+    TRY(error_from_word(word));
+    if (!std::isfinite(*grad_norm_out)) return GPT2_ERR_NONFINITE;
+    m->adam_t = t;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_num_tensors(const gpt2_model *m) { return m ? (int)m->tensors.size() : 0; }
+
+extern "C" int gpt2_tensor_info(const gpt2_model *m, int id, const char **name, int *ndim, int64_t shape[2]) {
+    if (!m || id < 0 || id >= (int)m->tensors.size()) return GPT2_ERR_BAD_ARG;
+    const TensorInfo &t = m->tensors[id];
+    if (name) *name = t.name.c_str();
+    if (ndim) *ndim = t.ndim;
+    if (shape) {
+        shape[0] = t.shape[0];
+        shape[1] = t.shape[1];
+    }
+    return GPT2_OK;
+}
+
+static int copy_out(gpt2_model *m, const float *base, int id, float *host, size_t n) {
+    if (!m || !host || id < 0 || id >= (int)m->tensors.size()) return GPT2_ERR_BAD_ARG;
+    const TensorInfo &t = m->tensors[id];
+    if (n < (size_t)t.numel) return GPT2_ERR_BAD_ARG;
+    GPT2_CUDA_TRY(cudaMemcpyAsync(host, base + t.offset, t.numel * 4, cudaMemcpyDeviceToHost, m->stream));
+    GPT2_CUDA_TRY(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_get_params(gpt2_model *m, int id, float *host_out, size_t n) {
+    return copy_out(m, m ? m->params : nullptr, id, host_out, n);
+}
+extern "C" int gpt2_get_grads(gpt2_model *m, int id, float *host_out, size_t n) {
+    return copy_out(m, m ? m->grads : nullptr, id, host_out, n);
+}
+extern "C" int gpt2_get_adam_state(gpt2_model *m, int id, float *host_m, float *host_v, size_t n) {
+    TRY(copy_out(m, m ? m->adam_m : nullptr, id, host_m, n));
+    return copy_out(m, m->adam_v, id, host_v, n);
+}
+
+extern "C" int gpt2_set_params(gpt2_model *m, int id, const float *host_in, size_t n) {
+    if (!m || !host_in || id < 0 || id >= (int)m->tensors.size()) return GPT2_ERR_BAD_ARG;
+    const TensorInfo &t = m->tensors[id];
+    if (n < (size_t)t.numel) return GPT2_ERR_BAD_ARG;
+    GPT2_CUDA_TRY(cudaMemcpyAsync(m->params + t.offset, host_in, t.numel * 4, cudaMemcpyHostToDevice, m->stream));
+    if (m->wbf) TRY(k::cast_f32_bf16(m->params + t.offset, m->wbf + t.offset, t.numel, m->stream));
+    GPT2_CUDA_TRY(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_debug_buffer(gpt2_model *m, const char *name, void **dev_ptr, size_t *bytes) {
+    if (!m || !name || !dev_ptr || !bytes) return GPT2_ERR_BAD_ARG;
+    const gpt2_config &c = m->cfg;
+    const size_t es = c.dtype == GPT2_DTYPE_BF16 ? 2 : 4;
+    const size_t BT = (size_t)c.B * c.T;
+    std::string s(name);
+    auto layer_of = [&](const char *prefix, int lim) -> int {
+        const size_t n = strlen(prefix);
+        if (s.compare(0, n, prefix) != 0) return -1;
+        const int l = atoi(s.c_str() + n);
+        return (l >= 0 && l < lim) ? l : -1;
+    };
+    int l;
+    if (s == "logits") { *dev_ptr = m->logits; *bytes = BT * c.Vp * es; }
+    else if (s == "loss_rows") { *dev_ptr = m->loss_rows; *bytes = BT * 4; }
+    else if (s == "lnf") { *dev_ptr = m->lnf; *bytes = BT * c.C * es; }
+    else if ((l = layer_of("qkv.", c.L)) >= 0) { *dev_ptr = m->layers[l].qkv; *bytes = BT * 3 * c.C * es; }
+    else if ((l = layer_of("att.", c.L)) >= 0) { *dev_ptr = m->layers[l].att; *bytes = BT * c.C * es; }
+    else if ((l = layer_of("lse.", c.L)) >= 0) { *dev_ptr = m->layers[l].lse; *bytes = (size_t)c.B * c.H * c.T * 4; }
+    else if ((l = layer_of("resid.", c.L + 1)) >= 0) {
+        *dev_ptr = l < c.L ? m->layers[l].resid : m->resid_final;
+        *bytes = BT * c.C * es;
+    } else return GPT2_ERR_BAD_ARG;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_adam_step(const gpt2_model *m, int *t_out) {
+    if (!m || !t_out) return GPT2_ERR_BAD_ARG;
+    *t_out = m->adam_t;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_profile(gpt2_model *m, int enable) {
+    if (!m) return GPT2_ERR_BAD_ARG;
+    if (enable) {
+        TRY(prof_flush(m));
+        for (int c = 0; c < GPT2_PROF_NCAT; ++c) {
+            m->prof_ms[c] = m->prof_work[c] = 0.0;
+            m->prof_n[c] = 0;
+        }
+    }
+    m->prof_on = enable != 0;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_profile_read(gpt2_model *m, int category, double *total_ms, double *total_work,
+                                 long long *launches) {
+    if (!m || category < 0 || category >= GPT2_PROF_NCAT) return GPT2_ERR_BAD_ARG;
+    TRY(prof_flush(m));
+    if (total_ms) *total_ms = m->prof_ms[category];
+    if (total_work) *total_work = m->prof_work[category];
+    if (launches) *launches = m->prof_n[category];
+    return GPT2_OK;
+}
+
+extern "C" void gpt2_free(gpt2_model *m) {
+    if (!m) return;
+    for (auto &r : m->prof) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    delete m;
+}
+
+// ================================================================== op-level C ABI
+static int op_sms() {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 148;
+    }
+    return sms;
+}
+
+extern "C" int gpt2_op_attention_forward(const void *q, const void *kk, const void *v, int64_t qkv_row_stride,
+                                         void *o, int64_t o_row_stride, float *lse, int B, int T, int H, int hd,
+                                         void *stream) {
+    if (!q || !kk || !v || !o || !lse) return GPT2_ERR_BAD_ARG;
+    if (B <= 0 || T <= 0 || H <= 0 || hd != 64 || qkv_row_stride % 8 || o_row_stride % 8) return GPT2_ERR_BAD_SHAPE;
+    return fa::attention_forward((const bf16 *)q, (const bf16 *)kk, (const bf16 *)v, qkv_row_stride, (bf16 *)o,
+                                 o_row_stride, lse, B, T, H, hd, (cudaStream_t)stream);
+}
+
+extern "C" int gpt2_op_attention_backward(const void *q, const void *kk, const void *v, int64_t qkv_row_stride,
+                                          const void *o, const void *dout, int64_t o_row_stride, const float *lse,
+                                          void *dq, void *dk, void *dv, float *d_scratch, int B, int T, int H, int hd,
+                                          void *stream) {
+    if (!q || !kk || !v || !o || !dout || !lse || !dq || !dk || !dv || !d_scratch) return GPT2_ERR_BAD_ARG;
+    if (B <= 0 || T <= 0 || H <= 0 || hd != 64 || qkv_row_stride % 8 || o_row_stride % 8) return GPT2_ERR_BAD_SHAPE;
+    return fa::attention_backward((const bf16 *)q, (const bf16 *)kk, (const bf16 *)v, qkv_row_stride, (const bf16 *)o,
+                                  (const bf16 *)dout, o_row_stride, lse, (bf16 *)dq, (bf16 *)dk, (bf16 *)dv, d_scratch,
+                                  B, T, H, hd, (cudaStream_t)stream);
+}
+
+extern "C" int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const void *B, int64_t ldb, int b_kmajor,
+                              void *D, void *D2, const void *R, int64_t ldd, const float *bias, int M, int N, int K,
+                              int epilogue, void *stream) {
+    tcg::GemmDesc g;
+    g.A = (const bf16 *)A;
+    g.lda = lda;
+    g.a_kmajor = a_kmajor != 0;
+    g.B = (const bf16 *)B;
+    g.ldb = ldb;
+    g.b_kmajor = b_kmajor != 0;
+    g.D = D;
+    g.D2 = (bf16 *)D2;
+    g.R = (const bf16 *)R;
+    g.ldd = ldd;
+    g.bias = bias;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.epi = epilogue;
+    g.alpha = 1.0f;
+    g.err = nullptr;
+    return tcg::launch_gemm_tc(g, op_sms(), (cudaStream_t)stream);
+}
+
+extern "C" int gpt2_op_classifier(void *logits, const int32_t *targets, float *loss_rows, int N, int V, int Vp,
+                                  float dscale, void *stream) {
+    if (!logits || !targets || !loss_rows) return GPT2_ERR_BAD_ARG;
+    if (N <= 0) return GPT2_ERR_BAD_SHAPE;
+    return k::classifier<bf16>((bf16 *)logits, targets, loss_rows, N, V, Vp, dscale, nullptr, (cudaStream_t)stream);
+}

@@ -1,0 +1,885 @@
+// Memory-bound kernels of the GPT-2 step (embedding, LayerNorm, classifier,
+// bias gradients, fused clip + AdamW) and the fp32-mode SIMT matmul and
+// attention.  Sources, by page title and section:
+//   embedding / position encoding -- "Let's build GPT: from scratch", 01:00:18;
+//   LayerNorm                     -- same page, 01:32:51;
+//   cross-entropy                 -- "Let's reproduce GPT-2 (124M)", §Bölümler 4;
+//   AdamW, clipping               -- same page §Video özeti; "llm.c kullanarak
+//                                    GPT-2 ...", §Eğitim süreci.
+#include <algorithm>
+#include <math.h>
+
+#include "kernels.cuh"
+
+namespace k {
+
+// ============================================================== embedding
+template <typename T> __device__ __forceinline__ void store4(T *p, float a, float b, float c, float d);
+template <> __device__ __forceinline__ void store4<float>(float *p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
+}
+template <> __device__ __forceinline__ void store4<bf16>(bf16 *p, float a, float b, float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t *>(&lo);
+    u.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+template <typename T>
+__global__ void embed_fwd_kernel(const int *__restrict__ tok, const float *__restrict__ wte,
+                                 const float *__restrict__ wpe, T *__restrict__ x, int BT, int Tn, int C, int V,
+                                 int *err) {
+    const int c4 = C >> 2;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)BT * c4) return;
+    const int row = (int)(idx / c4);
+    const int c = (int)(idx - (int64_t)row * c4) * 4;
+    const int t = row % Tn;
+    int tk = tok[row];
+    if (tk < 0 || tk >= V) {
+        raise_device_error(err, DEVERR_BAD_TOKEN);
+        tk = 0;
+    }
+    const float4 a = *reinterpret_cast<const float4 *>(wte + (int64_t)tk * C + c);
+    const float4 p = *reinterpret_cast<const float4 *>(wpe + (int64_t)t * C + c);
+    store4<T>(x + (int64_t)row * C + c, a.x + p.x, a.y + p.y, a.z + p.z, a.w + p.w);
+}
+
+template <typename T>
+int embed_forward(const int *tok, const float *wte, const float *wpe, T *x, int B, int Tn, int C, int V, int *err,
+                  cudaStream_t st) {
+    if (C % 4) return GPT2_ERR_BAD_SHAPE;
+    const int64_t n = (int64_t)B * Tn * (C / 4);
+    embed_fwd_kernel<T><<<ceil_div(n, 256), 256, 0, st>>>(tok, wte, wpe, x, B * Tn, Tn, C, V, err);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+template <typename T>
+__global__ void embed_bwd_wte_kernel(const int *__restrict__ tok, const T *__restrict__ dx, float *__restrict__ dwte,
+                                     int BT, int C, int V) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)BT * C) return;
+    const int row = (int)(idx / C), c = (int)(idx - (int64_t)row * C);
+    int tk = tok[row];
+    if (tk < 0 || tk >= V) tk = 0;
+    atomicAdd(dwte + (int64_t)tk * C + c, to_f32(dx[idx]));
+}
+
+template <typename T>
+__global__ void embed_bwd_wpe_kernel(const T *__restrict__ dx, float *__restrict__ dwpe, int B, int Tn, int C) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)Tn * C) return;
+    float s = 0.f;
+    for (int b = 0; b < B; ++b) s += to_f32(dx[(int64_t)b * Tn * C + idx]);
+    dwpe[idx] += s;
+}
+
+template <typename T>
+int embed_backward(const int *tok, const T *dx, float *dwte, float *dwpe, int B, int Tn, int C, int V,
+                   cudaStream_t st) {
+    const int64_t n = (int64_t)B * Tn * C;
+    embed_bwd_wte_kernel<T><<<ceil_div(n, 256), 256, 0, st>>>(tok, dx, dwte, B * Tn, C, V);
+    embed_bwd_wpe_kernel<T><<<ceil_div((int64_t)Tn * C, 256), 256, 0, st>>>(dx, dwpe, B, Tn, C);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(2);
+    return GPT2_OK;
+}
+
+// ============================================================== LayerNorm
+// One warp per row; the row stays in registers (VPL 16-byte packets per lane).
+template <typename T, int VPL>
+__global__ void ln_fwd_kernel(const T *__restrict__ x, const float *__restrict__ g, const float *__restrict__ b,
+                              T *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd, int N, int C) {
+    constexpr int E = Pack16<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= N) return;
+    const int npk = C / E;
+    const T *xr = x + (int64_t)row * C;
+    Pack16<T> v[VPL];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int p = lane + 32 * i;
+        if (p < npk) {
+            v[i].load(xr + p * E);
+#pragma unroll
+            for (int e = 0; e < E; ++e) s += v[i].get(e);
+        }
+    }
+    const float mu = warp_sum(s) / C;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int p = lane + 32 * i;
+        if (p < npk) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float d = v[i].get(e) - mu;
+                q += d * d;
+            }
+        }
+    }
+    const float rs = rsqrtf(warp_sum(q) / C + 1e-5f);
+    T *yr = y + (int64_t)row * C;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int p = lane + 32 * i;
+        if (p < npk) {
+            Pack16<T> o;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int c = p * E + e;
+                o.set(e, (v[i].get(e) - mu) * rs * g[c] + b[c]);
+            }
+            o.store(yr + p * E);
+        }
+    }
+    if (lane == 0) {
+        mean[row] = mu;
+        rstd[row] = rs;
+    }
+}
+
+template <typename T> static int ln_vpl(int C) {
+    const int npk = C / Pack16<T>::N;
+    const int per_lane = (npk + 31) / 32;
+    return per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 0;
+}
+
+template <typename T>
+int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *mean, float *rstd, int N, int C,
+                      cudaStream_t st) {
+    if (C % Pack16<T>::N) return GPT2_ERR_BAD_SHAPE;
+    const int vpl = ln_vpl<T>(C);
+    const int warps = 8, grid = ceil_div(N, warps);
+    switch (vpl) {
+        case 1: ln_fwd_kernel<T, 1><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C); break;
+        case 2: ln_fwd_kernel<T, 2><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C); break;
+        case 4: ln_fwd_kernel<T, 4><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C); break;
+        case 8: ln_fwd_kernel<T, 8><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C); break;
+        default: return GPT2_ERR_BAD_SHAPE;
+    }
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+template <typename T, int VPL>
+__global__ void ln_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ x, const float *__restrict__ mean,
+                              const float *__restrict__ rstd, const float *__restrict__ g, const T *dres_in,
+                              T *dres_out, float *__restrict__ dg, float *__restrict__ db, int N, int C) {
+    constexpr int E = Pack16<T>::N;
+    extern __shared__ float sh[];  // [2C]: partial dg, partial db
+    for (int i = threadIdx.x; i < 2 * C; i += blockDim.x) sh[i] = 0.f;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+    const int npk = C / E;
+    for (int row = blockIdx.x * warps + (threadIdx.x >> 5); row < N; row += gridDim.x * warps) {
+        const int64_t off = (int64_t)row * C;
+        Pack16<T> vdy[VPL], vx[VPL];
+        const float mu = mean[row], rs = rstd[row];
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
+                vdy[i].load(dy + off + p * E);
+                vx[i].load(x + off + p * E);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int c = p * E + e;
+                    const float dxh = vdy[i].get(e) * g[c];
+                    const float xh = (vx[i].get(e) - mu) * rs;
+                    s1 += dxh;
+                    s2 += dxh * xh;
+                }
+            }
+        }
+        const float m1 = warp_sum(s1) / C, m2 = warp_sum(s2) / C;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
+                Pack16<T> base, o;
+                if (dres_in) base.load(dres_in + off + p * E);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int c = p * E + e;
+                    const float d = vdy[i].get(e);
+                    const float xh = (vx[i].get(e) - mu) * rs;
+                    const float dx = rs * (d * g[c] - m1 - xh * m2);
+                    o.set(e, (dres_in ? base.get(e) : 0.f) + dx);
+                    atomicAdd(&sh[c], d * xh);
+                    atomicAdd(&sh[C + c], d);
+                }
+                o.store(dres_out + off + p * E);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < C; i += blockDim.x) {
+        atomicAdd(dg + i, sh[i]);
+        atomicAdd(db + i, sh[C + i]);
+    }
+}
+
+template <typename T>
+int layernorm_backward(const T *dy, const T *x, const float *mean, const float *rstd, const float *g, const T *dres_in,
+                       T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st) {
+    if (C % Pack16<T>::N) return GPT2_ERR_BAD_SHAPE;
+    const int warps = 8;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int grid = std::max(1, std::min(ceil_div(N, warps), sms * 4));
+    const size_t smem = 2 * C * sizeof(float);
+    switch (ln_vpl<T>(C)) {
+        case 1: ln_bwd_kernel<T, 1><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
+        case 2: ln_bwd_kernel<T, 2><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
+        case 4: ln_bwd_kernel<T, 4><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
+        case 8: ln_bwd_kernel<T, 8><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
+        default: return GPT2_ERR_BAD_SHAPE;
+    }
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+// ============================================================== bias gradient
+// 256 threads: 8 column packets x 32 row lanes; partial sums reduced in shared
+// memory, one atomic per column per block.
+template <typename T>
+__global__ void colsum_kernel(const T *__restrict__ dy, int M, int N, float *__restrict__ db, int rows_per_block) {
+    constexpr int E = Pack16<T>::N;
+    __shared__ float sh[32][8 * E + 1];
+    const int cp = threadIdx.x & 7, rl = threadIdx.x >> 3;
+    const int col = (blockIdx.x * 8 + cp) * E;
+    const int r0 = blockIdx.y * rows_per_block, r1 = min(M, r0 + rows_per_block);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    if (col < N) {
+        for (int r = r0 + rl; r < r1; r += 32) {
+            Pack16<T> v;
+            v.load(dy + (int64_t)r * N + col);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] += v.get(e);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) sh[rl][cp * E + e] = acc[e];
+    __syncthreads();
+    if (threadIdx.x < 8 * E) {
+        const int c = blockIdx.x * 8 * E + threadIdx.x;
+        float s = 0.f;
+        for (int r = 0; r < 32; ++r) s += sh[r][threadIdx.x];
+        if (c < N) atomicAdd(db + c, s);
+    }
+}
+
+template <typename T>
+int column_sum(const T *dy, int M, int N, float *db, cudaStream_t st) {
+    constexpr int E = Pack16<T>::N;
+    if (N % E) return GPT2_ERR_BAD_SHAPE;
+    const int gx = ceil_div(N, 8 * E);
+    const int gy = std::max(1, std::min(ceil_div(M, 256), std::max(1, 592 / gx)));
+    const int rpb = ceil_div(M, gy);
+    colsum_kernel<T><<<dim3(gx, gy), 256, 0, st>>>(dy, M, N, db, rpb);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+// ============================================================== classifier
+__device__ __forceinline__ void lse_merge(float &m, float &s, float om, float os) {
+    if (om == -INFINITY) return;
+    if (m == -INFINITY) {
+        m = om;
+        s = os;
+        return;
+    }
+    const float mn = fmaxf(m, om);
+    s = s * __expf(m - mn) + os * __expf(om - mn);
+    m = mn;
+}
+
+// One block per row (grid-stride): pass 1 online max / sum-exp over v < V,
+// pass 2 writes dz = (softmax - onehot) * dscale in place (0 for v >= V).
+template <typename T>
+__global__ void __launch_bounds__(1024) classifier_kernel(T *logits, const int *__restrict__ targets,
+                                                          float *__restrict__ loss_rows, int N, int V, int Vp,
+                                                          float dscale, int *err) {
+    constexpr int E = Pack16<T>::N;
+    __shared__ float sm_m[32], sm_s[32];
+    __shared__ float sh_lse;
+    __shared__ int sh_tg;
+    const int npk = Vp / E;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int row = blockIdx.x; row < N; row += gridDim.x) {
+        T *z = logits + (int64_t)row * Vp;
+        float m = -INFINITY, s = 0.f;
+        for (int p = threadIdx.x; p < npk; p += blockDim.x) {
+            Pack16<T> v;
+            v.load(z + p * E);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                if (p * E + e < V) {
+                    const float x = v.get(e);
+                    if (x > m) {
+                        s = s * __expf(m - x) + 1.f;
+                        m = x;
+                    } else {
+                        s += __expf(x - m);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float om = __shfl_xor_sync(0xffffffffu, m, o), os = __shfl_xor_sync(0xffffffffu, s, o);
+            lse_merge(m, s, om, os);
+        }
+        if (lane == 0) {
+            sm_m[wid] = m;
+            sm_s[wid] = s;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float M = sm_m[0], S = sm_s[0];
+            for (int w = 1; w < nw; ++w) lse_merge(M, S, sm_m[w], sm_s[w]);
+            const float lse = M + logf(S);
+            int tg = targets[row];
+            if (tg < 0 || tg >= V) {
+                raise_device_error(err, DEVERR_BAD_TOKEN);
+                tg = 0;
+            }
+            loss_rows[row] = lse - to_f32(z[tg]);
+            sh_lse = lse;
+            sh_tg = tg;
+        }
+        __syncthreads();
+        const float lse = sh_lse;
+        const int tg = sh_tg;
+        for (int p = threadIdx.x; p < npk; p += blockDim.x) {
+            Pack16<T> v;
+            v.load(z + p * E);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int c = p * E + e;
+                float d = 0.f;
+                if (c < V) {
+                    d = __expf(v.get(e) - lse);
+                    if (c == tg) d -= 1.f;
+                    d *= dscale;
+                }
+                v.set(e, d);
+            }
+            v.store(z + p * E);
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, int Vp, float dscale, int *err,
+               cudaStream_t st) {
+    if (Vp % Pack16<T>::N || V > Vp || V <= 0) return GPT2_ERR_BAD_SHAPE;
+    const int grid = std::min(N, 148 * 8);
+    classifier_kernel<T><<<grid, 512, 0, st>>>(logits, targets, loss_rows, N, V, Vp, dscale, err);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+__global__ void mean_rows_kernel(const float *__restrict__ rows, int N, float *out) {
+    __shared__ double sh[32];
+    double s = 0.0;
+    for (int i = threadIdx.x; i < N; i += blockDim.x) s += rows[i];
+    s = warp_sum_d(s);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += sh[w];
+        out[0] = (float)(t / N);
+    }
+}
+
+int mean_rows(const float *rows, int N, float *out, cudaStream_t st) {
+    mean_rows_kernel<<<1, 1024, 0, st>>>(rows, N, out);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+// ============================================================== GELU recompute, casts
+template <typename T>
+__global__ void gelu_fwd_kernel(const T *__restrict__ h, T *__restrict__ y, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    constexpr int E = Pack16<T>::N;
+    if (i * E >= n) return;
+    Pack16<T> v;
+    v.load(h + i * E);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v.set(e, gelu_tanh(v.get(e)));
+    v.store(y + i * E);
+}
+
+template <typename T>
+int gelu_forward(const T *h, T *y, int64_t n, cudaStream_t st) {
+    constexpr int E = Pack16<T>::N;
+    if (n % E) return GPT2_ERR_BAD_SHAPE;
+    gelu_fwd_kernel<T><<<ceil_div(n / E, 256), 256, 0, st>>>(h, y, n);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+__global__ void cast_kernel(const float *__restrict__ x, bf16 *__restrict__ y, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) y[i] = __float2bfloat16_rn(x[i]);
+}
+
+int cast_f32_bf16(const float *x, bf16 *y, int64_t n, cudaStream_t st) {
+    cast_kernel<<<ceil_div(n, 256), 256, 0, st>>>(x, y, n);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+// ============================================================== SIMT matmul
+template <typename T>
+__device__ __forceinline__ void simt_epilogue(int epi, float acc, int m, int n, void *D, T *D2, const T *R,
+                                              int64_t ldd, const float *bias) {
+    const int64_t o = (int64_t)m * ldd + n;
+    const float bv = bias ? bias[n] : 0.f;
+    switch (epi) {
+        case GPT2_EPI_STORE: reinterpret_cast<T *>(D)[o] = from_f32<T>(acc + bv); break;
+        case GPT2_EPI_RESIDUAL: reinterpret_cast<T *>(D)[o] = from_f32<T>(acc + bv + to_f32(R[o])); break;
+        case GPT2_EPI_GELU: {
+            const T h = from_f32<T>(acc + bv);
+            reinterpret_cast<T *>(D)[o] = h;
+            D2[o] = from_f32<T>(gelu_tanh(to_f32(h)));
+            break;
+        }
+        case GPT2_EPI_GELU_BWD: reinterpret_cast<T *>(D)[o] = from_f32<T>(acc * gelu_tanh_grad(to_f32(R[o]))); break;
+        case GPT2_EPI_ACCUM_F32: reinterpret_cast<float *>(D)[o] += acc; break;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) matmul_simt_kernel(const T *__restrict__ A, int64_t sam, int64_t sak,
+                                                          const T *__restrict__ Bm, int64_t sbn, int64_t sbk, void *D,
+                                                          T *D2, const T *R, int64_t ldd, const float *bias, int M,
+                                                          int N, int K, int epi, float alpha) {
+    __shared__ float As[16][68], Bs[16][68];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+            const int kk = i & 15, r = i >> 4;
+            const int gk = k0 + kk, gm = m0 + r, gn = n0 + r;
+            As[kk][r] = (gm < M && gk < K) ? to_f32(A[(int64_t)gm * sam + (int64_t)gk * sak]) : 0.f;
+            Bs[kk][r] = (gn < N && gk < K) ? to_f32(Bm[(int64_t)gn * sbn + (int64_t)gk * sbk]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
+            if (m < M && n < N) simt_epilogue<T>(epi, acc[i][j] * alpha, m, n, D, D2, R, ldd, bias);
+        }
+}
+
+template <typename T>
+int matmul_simt(const T *A, int64_t sam, int64_t sak, const T *Bm, int64_t sbn, int64_t sbk, void *D, T *D2,
+                const T *R, int64_t ldd, const float *bias, int M, int N, int K, int epi, float alpha,
+                cudaStream_t st) {
+    if (M <= 0 || N <= 0 || K <= 0) return GPT2_ERR_BAD_SHAPE;
+    matmul_simt_kernel<T><<<dim3(ceil_div(N, 64), ceil_div(M, 64)), 256, 0, st>>>(A, sam, sak, Bm, sbn, sbk, D, D2, R,
+                                                                                 ldd, bias, M, N, K, epi, alpha);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+// ============================================================== SIMT attention
+// Causal, scale 1/sqrt(hd) ("Let's build GPT: from scratch", 01:16:56 and the
+// errata after 01:54:32).  One thread per query row (forward, dQ) or key row
+// (dK, dV); K/V (or Q/dO) tiles staged in shared memory.
+template <typename T, int HD>
+__global__ void attn_fwd_simt_kernel(const T *__restrict__ q, const T *__restrict__ kk, const T *__restrict__ v,
+                                     int64_t rs, T *__restrict__ o, int64_t ors, float *__restrict__ lse, int Tn,
+                                     int H) {
+    constexpr int BQ = 64, BKV = 32;
+    __shared__ float Ks[BKV][HD], Vs[BKV][HD];
+    const int bh = blockIdx.y, b = bh / H, h = bh % H;
+    const int i = blockIdx.x * BQ + threadIdx.x;
+    const bool valid = i < Tn;
+    const float scale = 1.0f / sqrtf((float)HD);
+    float qr[HD], acc[HD];
+#pragma unroll
+    for (int d = 0; d < HD; ++d) {
+        qr[d] = valid ? to_f32(q[((int64_t)b * Tn + i) * rs + h * HD + d]) * scale : 0.f;
+        acc[d] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    const int kv_end = min(Tn, blockIdx.x * BQ + BQ);
+    for (int j0 = 0; j0 < kv_end; j0 += BKV) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < BKV * HD; idx += BQ) {
+            const int jj = idx / HD, d = idx % HD, j = j0 + jj;
+            const int64_t off = ((int64_t)b * Tn + j) * rs + h * HD + d;
+            Ks[jj][d] = j < Tn ? to_f32(kk[off]) : 0.f;
+            Vs[jj][d] = j < Tn ? to_f32(v[off]) : 0.f;
+        }
+        __syncthreads();
+        if (valid) {
+            for (int jj = 0; jj < BKV; ++jj) {
+                const int j = j0 + jj;
+                if (j > i) break;
+                float s = 0.f;
+#pragma unroll
+                for (int d = 0; d < HD; ++d) s = fmaf(qr[d], Ks[jj][d], s);
+                const float mn = fmaxf(m, s);
+                const float corr = expf(m - mn), p = expf(s - mn);
+                l = l * corr + p;
+#pragma unroll
+                for (int d = 0; d < HD; ++d) acc[d] = acc[d] * corr + p * Vs[jj][d];
+                m = mn;
+            }
+        }
+    }
+    if (valid) {
+        const float inv = 1.0f / l;
+#pragma unroll
+        for (int d = 0; d < HD; ++d) o[((int64_t)b * Tn + i) * ors + h * HD + d] = from_f32<T>(acc[d] * inv);
+        lse[(int64_t)bh * Tn + i] = m + logf(l);
+    }
+}
+
+template <typename T, int HD>
+__global__ void attn_bwd_dq_simt_kernel(const T *__restrict__ q, const T *__restrict__ kk, const T *__restrict__ v,
+                                        int64_t rs, const T *__restrict__ o, const T *__restrict__ dout, int64_t ors,
+                                        const float *__restrict__ lse, T *__restrict__ dq, float *__restrict__ Dsc,
+                                        int Tn, int H) {
+    constexpr int BQ = 64, BKV = 32;
+    __shared__ float Ks[BKV][HD], Vs[BKV][HD];
+    const int bh = blockIdx.y, b = bh / H, h = bh % H;
+    const int i = blockIdx.x * BQ + threadIdx.x;
+    const bool valid = i < Tn;
+    const float scale = 1.0f / sqrtf((float)HD);
+    float qr[HD], dor[HD], acc[HD];
+    float Di = 0.f;
+    const int64_t qoff = ((int64_t)b * Tn + i) * rs + h * HD, ooff = ((int64_t)b * Tn + i) * ors + h * HD;
+#pragma unroll
+    for (int d = 0; d < HD; ++d) {
+        qr[d] = valid ? to_f32(q[qoff + d]) : 0.f;
+        dor[d] = valid ? to_f32(dout[ooff + d]) : 0.f;
+        Di += valid ? dor[d] * to_f32(o[ooff + d]) : 0.f;
+        acc[d] = 0.f;
+    }
+    const float li = valid ? lse[(int64_t)bh * Tn + i] : 0.f;
+    if (valid) Dsc[(int64_t)bh * Tn + i] = Di;
+    const int kv_end = min(Tn, blockIdx.x * BQ + BQ);
+    for (int j0 = 0; j0 < kv_end; j0 += BKV) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < BKV * HD; idx += BQ) {
+            const int jj = idx / HD, d = idx % HD, j = j0 + jj;
+            const int64_t off = ((int64_t)b * Tn + j) * rs + h * HD + d;
+            Ks[jj][d] = j < Tn ? to_f32(kk[off]) : 0.f;
+            Vs[jj][d] = j < Tn ? to_f32(v[off]) : 0.f;
+        }
+        __syncthreads();
+        if (valid) {
+            for (int jj = 0; jj < BKV; ++jj) {
+                const int j = j0 + jj;
+                if (j > i) break;
+                float s = 0.f, dp = 0.f;
+#pragma unroll
+                for (int d = 0; d < HD; ++d) {
+                    s = fmaf(qr[d], Ks[jj][d], s);
+                    dp = fmaf(dor[d], Vs[jj][d], dp);
+                }
+                const float p = expf(s * scale - li);
+                const float ds = p * (dp - Di);
+#pragma unroll
+                for (int d = 0; d < HD; ++d) acc[d] = fmaf(ds, Ks[jj][d], acc[d]);
+            }
+        }
+    }
+    if (valid) {
+#pragma unroll
+        for (int d = 0; d < HD; ++d) dq[qoff + d] = from_f32<T>(acc[d] * scale);
+    }
+}
+
+template <typename T, int HD>
+__global__ void attn_bwd_dkv_simt_kernel(const T *__restrict__ q, const T *__restrict__ kk, const T *__restrict__ v,
+                                         int64_t rs, const T *__restrict__ dout, int64_t ors,
+                                         const float *__restrict__ lse, const float *__restrict__ Dsc,
+                                         T *__restrict__ dk, T *__restrict__ dv, int Tn, int H) {
+    constexpr int BKV = 64, BQ = 32;
+    __shared__ float Qs[BQ][HD], Ds[BQ][HD];
+    __shared__ float Ls[BQ], Dd[BQ];
+    const int bh = blockIdx.y, b = bh / H, h = bh % H;
+    const int j = blockIdx.x * BKV + threadIdx.x;
+    const bool valid = j < Tn;
+    const float scale = 1.0f / sqrtf((float)HD);
+    float kr[HD], vr[HD], adk[HD], adv[HD];
+    const int64_t koff = ((int64_t)b * Tn + j) * rs + h * HD;
+#pragma unroll
+    for (int d = 0; d < HD; ++d) {
+        kr[d] = valid ? to_f32(kk[koff + d]) : 0.f;
+        vr[d] = valid ? to_f32(v[koff + d]) : 0.f;
+        adk[d] = 0.f;
+        adv[d] = 0.f;
+    }
+    const int q_start = blockIdx.x * BKV;
+    for (int i0 = q_start; i0 < Tn; i0 += BQ) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < BQ * HD; idx += BKV) {
+            const int ii = idx / HD, d = idx % HD, i = i0 + ii;
+            Qs[ii][d] = i < Tn ? to_f32(q[((int64_t)b * Tn + i) * rs + h * HD + d]) : 0.f;
+            Ds[ii][d] = i < Tn ? to_f32(dout[((int64_t)b * Tn + i) * ors + h * HD + d]) : 0.f;
+        }
+        for (int ii = threadIdx.x; ii < BQ; ii += BKV) {
+            const int i = i0 + ii;
+            Ls[ii] = i < Tn ? lse[(int64_t)bh * Tn + i] : 0.f;
+            Dd[ii] = i < Tn ? Dsc[(int64_t)bh * Tn + i] : 0.f;
+        }
+        __syncthreads();
+        if (valid) {
+            for (int ii = 0; ii < BQ; ++ii) {
+                const int i = i0 + ii;
+                if (i < j || i >= Tn) continue;
+                float s = 0.f, dp = 0.f;
+#pragma unroll
+                for (int d = 0; d < HD; ++d) {
+                    s = fmaf(Qs[ii][d], kr[d], s);
+                    dp = fmaf(Ds[ii][d], vr[d], dp);
+                }
+                const float p = expf(s * scale - Ls[ii]);
+                const float ds = p * (dp - Dd[ii]);
+#pragma unroll
+                for (int d = 0; d < HD; ++d) {
+                    adv[d] = fmaf(p, Ds[ii][d], adv[d]);
+                    adk[d] = fmaf(ds, Qs[ii][d], adk[d]);
+                }
+            }
+        }
+    }
+    if (valid) {
+#pragma unroll
+        for (int d = 0; d < HD; ++d) {
+            dk[koff + d] = from_f32<T>(adk[d] * scale);
+            dv[koff + d] = from_f32<T>(adv[d]);
+        }
+    }
+}
+
+#define ATTN_HD_DISPATCH(HDV, ...)                  \
+    switch (HDV) {                                  \
+        case 8: { constexpr int HD = 8; __VA_ARGS__; } break;   \
+        case 16: { constexpr int HD = 16; __VA_ARGS__; } break; \
+        case 32: { constexpr int HD = 32; __VA_ARGS__; } break; \
+        case 64: { constexpr int HD = 64; __VA_ARGS__; } break; \
+        default: return GPT2_ERR_BAD_SHAPE;         \
+    }
+
+template <typename T>
+int attention_forward_simt(const T *q, const T *kk, const T *v, int64_t rs, T *o, int64_t ors, float *lse, int B,
+                           int Tn, int H, int hd, cudaStream_t st) {
+    const dim3 grid(ceil_div(Tn, 64), B * H);
+    ATTN_HD_DISPATCH(hd, (attn_fwd_simt_kernel<T, HD><<<grid, 64, 0, st>>>(q, kk, v, rs, o, ors, lse, Tn, H)));
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+template <typename T>
+int attention_backward_simt(const T *q, const T *kk, const T *v, int64_t rs, const T *o, const T *dout, int64_t ors,
+                            const float *lse, T *dq, T *dk, T *dv, float *dscratch, int B, int Tn, int H, int hd,
+                            cudaStream_t st) {
+    const dim3 grid(ceil_div(Tn, 64), B * H);
+    ATTN_HD_DISPATCH(hd, (attn_bwd_dq_simt_kernel<T, HD><<<grid, 64, 0, st>>>(q, kk, v, rs, o, dout, ors, lse, dq,
+                                                                                dscratch, Tn, H)));
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    ATTN_HD_DISPATCH(hd, (attn_bwd_dkv_simt_kernel<T, HD><<<grid, 64, 0, st>>>(q, kk, v, rs, dout, ors, lse, dscratch,
+                                                                                 dk, dv, Tn, H)));
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+// ============================================================== clip + AdamW
+constexpr int ADAM_THREADS = 256;
+constexpr int ADAM_BLOCKS_PER_SM = 4;
+
+__device__ __forceinline__ double block_sum_d(double v, double *sh) {
+    v = warp_sum_d(v);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) sh[wid] = v;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += sh[w];
+        sh[0] = t;
+    }
+    __syncthreads();
+    t = sh[0];
+    __syncthreads();
+    return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Phase 1: sum of squares of every gradient (fp32 per thread, fp64 per block);
+// grid barrier (cooperative launch, bounded spin); every block then reduces the
+// block partials in the same fixed order, so all blocks see one norm.
+// Phase 2: clip coefficient and the AdamW update, bf16 copy of the new weights.
+__global__ void __launch_bounds__(ADAM_THREADS) clip_adamw_kernel(float *__restrict__ p, const float *__restrict__ g,
+                                                                  float *__restrict__ m, float *__restrict__ v,
+                                                                  bf16 *__restrict__ shadow, int64_t n,
+                                                                  int64_t n_decay, AdamArgs a,
+                                                                  double *__restrict__ partials, unsigned *counter,
+                                                                  float *norm_out, int *err) {
+    __shared__ double sh[32];
+    __shared__ int ok;
+    const int64_t n4 = n >> 2;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    float s = 0.f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 x = __ldcs(reinterpret_cast<const float4 *>(g) + i);
+        s += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+    }
+    const double bs = block_sum_d((double)s, sh);
+    if (threadIdx.x == 0) {
+        partials[blockIdx.x] = bs;
+        __threadfence();
+        atomicAdd(counter, 1u);
+        ok = 1;
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire(counter) < gridDim.x) {
+            if (global_timer_ns() - t0 > 2000000000ull) {
+                ok = 0;
+                raise_device_error(err, DEVERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(100);
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    if (!ok) return;
+    double t = 0.0;
+    for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) t += __ldcg(partials + i);
+    const double total = block_sum_d(t, sh);
+    const double norm = sqrt(total);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *norm_out = (float)norm;
+    if (!isfinite(norm)) return;
+    const float coef = (float)fmin(1.0, (double)a.clip / (norm + 1e-6));
+    const float decay_mul = 1.0f - a.lr * a.wd;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 gv = __ldcs(reinterpret_cast<const float4 *>(g) + i);
+        float4 pv = reinterpret_cast<float4 *>(p)[i];
+        float4 mv = reinterpret_cast<float4 *>(m)[i];
+        float4 vv = reinterpret_cast<float4 *>(v)[i];
+        const bool decay = i * 4 < n_decay;
+        float *pp = &pv.x, *mp = &mv.x, *vp = &vv.x;
+        const float *gp = &gv.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float gi = gp[e] * coef;
+            mp[e] = a.beta1 * mp[e] + (1.0f - a.beta1) * gi;
+            vp[e] = a.beta2 * vp[e] + (1.0f - a.beta2) * gi * gi;
+            const float mhat = mp[e] / a.bc1, vhat = vp[e] / a.bc2;
+            float pi = pp[e];
+            if (decay) pi *= decay_mul;
+            pp[e] = pi - a.lr * mhat / (sqrtf(vhat) + a.eps);
+        }
+        reinterpret_cast<float4 *>(p)[i] = pv;
+        reinterpret_cast<float4 *>(m)[i] = mv;
+        reinterpret_cast<float4 *>(v)[i] = vv;
+        if (shadow) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(pv.x, pv.y), hi = __floats2bfloat162_rn(pv.z, pv.w);
+            uint2 u;
+            u.x = *reinterpret_cast<uint32_t *>(&lo);
+            u.y = *reinterpret_cast<uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(shadow)[i] = u;
+        }
+    }
+}
+
+int clip_adamw_max_blocks(int num_sms) { return num_sms * ADAM_BLOCKS_PER_SM; }
+
+int clip_adamw(float *p, const float *g, float *m, float *v, bf16 *shadow, int64_t n, int64_t n_decay,
+               const AdamArgs &a, double *partials, unsigned *counter, int max_blocks, float *norm_out, int *err,
+               int num_sms, cudaStream_t st) {
+    if (n % 4 || n_decay % 4) return GPT2_ERR_BAD_SHAPE;
+    int occ = 0;
+    GPT2_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, clip_adamw_kernel, ADAM_THREADS, 0));
+    int grid = std::min(max_blocks, num_sms * std::min(occ, ADAM_BLOCKS_PER_SM));
+    grid = std::max(1, std::min(grid, ceil_div(n / 4, ADAM_THREADS)));
+    GPT2_CUDA_TRY(cudaMemsetAsync(counter, 0, sizeof(unsigned), st));
+    void *args[] = {&p, &g, &m, &v, &shadow, &n, &n_decay, const_cast<AdamArgs *>(&a), &partials, &counter,
+                    &norm_out, &err};
+    GPT2_CUDA_TRY(cudaLaunchCooperativeKernel((void *)clip_adamw_kernel, dim3(grid), dim3(ADAM_THREADS), args, 0, st));
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+// ============================================================== instantiations
+#define INST(T)                                                                                                  \
+    template int embed_forward<T>(const int *, const float *, const float *, T *, int, int, int, int, int *,       \
+                                  cudaStream_t);                                                                 \
+    template int embed_backward<T>(const int *, const T *, float *, float *, int, int, int, int, cudaStream_t);    \
+    template int layernorm_forward<T>(const T *, const float *, const float *, T *, float *, float *, int, int,    \
+                                      cudaStream_t);                                                             \
+    template int layernorm_backward<T>(const T *, const T *, const float *, const float *, const float *,          \
+                                       const T *, T *, float *, float *, int, int, cudaStream_t);                  \
+    template int column_sum<T>(const T *, int, int, float *, cudaStream_t);                                        \
+    template int classifier<T>(T *, const int *, float *, int, int, int, float, int *, cudaStream_t);              \
+    template int gelu_forward<T>(const T *, T *, int64_t, cudaStream_t);                                           \
+    template int matmul_simt<T>(const T *, int64_t, int64_t, const T *, int64_t, int64_t, void *, T *, const T *,  \
+                                int64_t, const float *, int, int, int, int, float, cudaStream_t);                  \
+    template int attention_forward_simt<T>(const T *, const T *, const T *, int64_t, T *, int64_t, float *, int,    \
+                                           int, int, int, cudaStream_t);                                         \
+    template int attention_backward_simt<T>(const T *, const T *, const T *, int64_t, const T *, const T *,        \
+                                            int64_t, const float *, T *, T *, T *, float *, int, int, int, int,    \
+                                            cudaStream_t);
+INST(float)
+INST(bf16)
+#undef INST
+
+}  // namespace k

@@ -1,0 +1,78 @@
+// Launchers of the memory-bound kernels of the step and of the fp32-mode SIMT
+// matmul / attention.  Template parameter T is the activation type: float
+// (fp32 mode) or bf16.  Every launcher only enqueues work on `st`.
+#pragma once
+
+#include "common.cuh"
+
+namespace k {
+
+// x[b,t,:] = wte[tok[b,t]] + wpe[t]   (fp32 master rows, one rounding to T)
+template <typename T>
+int embed_forward(const int *tok, const float *wte, const float *wpe, T *x, int B, int Tn, int C, int V, int *err,
+                  cudaStream_t st);
+
+// dwte[tok[b,t]] += dx[b,t];  dwpe[t] += sum_b dx[b,t]
+template <typename T>
+int embed_backward(const int *tok, const T *dx, float *dwte, float *dwpe, int B, int Tn, int C, int V,
+                   cudaStream_t st);
+
+// y = (x - mean) * rstd * g + b per row of C; mean/rstd fp32 [N]
+template <typename T>
+int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *mean, float *rstd, int N, int C,
+                      cudaStream_t st);
+
+// dres_out = dres_in (may be NULL) + LN'(dy); dg += sum dy*xhat; db += sum dy
+// (dres_in and dres_out may alias)
+template <typename T>
+int layernorm_backward(const T *dy, const T *x, const float *mean, const float *rstd, const float *g, const T *dres_in,
+                       T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st);
+
+// db[n] += sum_m dy[m, n]
+template <typename T>
+int column_sum(const T *dy, int M, int N, float *db, cudaStream_t st);
+
+// fused softmax cross-entropy (in place), see gpt2_op_classifier
+template <typename T>
+int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, int Vp, float dscale, int *err,
+               cudaStream_t st);
+
+// *out = mean(rows[0..N)) with a fixed-order fp64 reduction
+int mean_rows(const float *rows, int N, float *out, cudaStream_t st);
+
+// y = gelu_tanh(h) elementwise (GELU recompute)
+template <typename T>
+int gelu_forward(const T *h, T *y, int64_t n, cudaStream_t st);
+
+int cast_f32_bf16(const float *x, bf16 *y, int64_t n, cudaStream_t st);
+
+// SIMT matmul with the same epilogues as the tensor-core matmul:
+//   acc[m,n] = sum_k A[m*sam + k*sak] * B[n*sbn + k*sbk]
+template <typename T>
+int matmul_simt(const T *A, int64_t sam, int64_t sak, const T *Bm, int64_t sbn, int64_t sbk, void *D, T *D2,
+                const T *R, int64_t ldd, const float *bias, int M, int N, int K, int epi, float alpha,
+                cudaStream_t st);
+
+// SIMT causal attention (any head size <= 64), one thread per query / key row.
+template <typename T>
+int attention_forward_simt(const T *q, const T *kk, const T *v, int64_t rs, T *o, int64_t ors, float *lse, int B,
+                           int Tn, int H, int hd, cudaStream_t st);
+template <typename T>
+int attention_backward_simt(const T *q, const T *kk, const T *v, int64_t rs, const T *o, const T *dout, int64_t ors,
+                            const float *lse, T *dq, T *dk, T *dv, float *dscratch, int B, int Tn, int H, int hd,
+                            cudaStream_t st);
+
+struct AdamArgs {
+    float lr, beta1, beta2, eps, wd, clip;
+    float bc1, bc2;  // 1 - beta^t
+};
+
+// Fused global-norm + clip + AdamW over one flat parameter arena (see
+// gpt2_clip_and_adamw).  Elements [0, n_decay) get weight decay.  `partials`
+// holds >= max_blocks doubles and `counter` one zeroed uint (grid barrier).
+int clip_adamw(float *p, const float *g, float *m, float *v, bf16 *shadow, int64_t n, int64_t n_decay,
+               const AdamArgs &a, double *partials, unsigned *counter, int max_blocks, float *norm_out, int *err,
+               int num_sms, cudaStream_t st);
+int clip_adamw_max_blocks(int num_sms);
+
+}  // namespace k

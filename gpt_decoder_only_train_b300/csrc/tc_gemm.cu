@@ -1,0 +1,112 @@
+// Host side of the tcgen05 GEMM: tensor maps, tile/split choice, dispatch.
+#include <algorithm>
+
+#include "tc_gemm.cuh"
+
+namespace tcg {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map with 128-byte swizzle; OOB elements read as zero.
+int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld_elems, uint32_t box_inner,
+                uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return GPT2_ERR_CUDA;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld_elems * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params &P, int grid, cudaStream_t st) {
+    constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    using Lay = SmemLayout<BN, STAGES>;
+    auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        GPT2_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL));
+        attr_set = true;
+    }
+    kern<<<grid, NUM_THREADS, Lay::TOTAL, st>>>(ta, tb, P);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+template <int BN>
+static int dispatch_major(bool a_mn, bool b_mn, const CUtensorMap &ta, const CUtensorMap &tb, const Params &P,
+                          int grid, cudaStream_t st) {
+    if (!a_mn && !b_mn) return launch_one<BN, false, false>(ta, tb, P, grid, st);
+    if (!a_mn && b_mn) return launch_one<BN, false, true>(ta, tb, P, grid, st);
+    if (a_mn && b_mn) return launch_one<BN, true, true>(ta, tb, P, grid, st);
+    return launch_one<BN, true, false>(ta, tb, P, grid, st);
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
+    if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPT2_ERR_BAD_SHAPE;
+    if (!g.A || !g.B || !g.D) return GPT2_ERR_BAD_ARG;
+    if ((g.lda % 8) || (g.ldb % 8) || (g.ldd % 8) || (g.N % 8)) return GPT2_ERR_BAD_SHAPE;
+    if (!aligned16(g.A) || !aligned16(g.B) || !aligned16(g.D)) return GPT2_ERR_BAD_ARG;
+    if (g.epi < GPT2_EPI_STORE || g.epi > GPT2_EPI_ACCUM_F32) return GPT2_ERR_BAD_ARG;
+    if ((g.epi == GPT2_EPI_RESIDUAL || g.epi == GPT2_EPI_GELU_BWD) && (!g.R || !aligned16(g.R)))
+        return GPT2_ERR_BAD_ARG;
+    if (g.epi == GPT2_EPI_GELU && (!g.D2 || !aligned16(g.D2))) return GPT2_ERR_BAD_ARG;
+    if (g.bias && (reinterpret_cast<uintptr_t>(g.bias) & 15)) return GPT2_ERR_BAD_ARG;
+
+    const int BN = g.N >= 256 ? 256 : (g.N > 64 ? 128 : 64);
+    Params P;
+    P.M = g.M;
+    P.N = g.N;
+    P.K = g.K;
+    P.num_m_blocks = ceil_div(g.M, BM);
+    P.num_n_blocks = ceil_div(g.N, BN);
+    P.num_k_blocks = ceil_div(g.K, BK);
+    P.splits = 1;
+    if (g.epi == GPT2_EPI_ACCUM_F32) {
+        const int tiles = P.num_m_blocks * P.num_n_blocks;
+        if (tiles < num_sms) P.splits = std::max(1, std::min(P.num_k_blocks, num_sms / tiles));
+    }
+    P.k_blocks_per_split = ceil_div(P.num_k_blocks, P.splits);
+    P.splits = ceil_div(P.num_k_blocks, P.k_blocks_per_split);
+    P.epi = g.epi;
+    P.alpha = g.alpha;
+    P.bias = g.bias;
+    P.R = g.R;
+    P.D = g.D;
+    P.D2 = g.D2;
+    P.ldd = g.ldd;
+    P.err = g.err;
+
+    CUtensorMap ta, tb;
+    int rc = g.a_kmajor ? encode_tmap(&ta, g.A, g.K, g.M, g.lda, 64, BM) : encode_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64);
+    if (rc) return rc;
+    rc = g.b_kmajor ? encode_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN) : encode_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64);
+    if (rc) return rc;
+
+    const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;
+    const int grid = std::min(num_work, num_sms);
+    const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
+    if (BN == 256) return dispatch_major<256>(a_mn, b_mn, ta, tb, P, grid, stream);
+    if (BN == 128) return dispatch_major<128>(a_mn, b_mn, ta, tb, P, grid, stream);
+    return dispatch_major<64>(a_mn, b_mn, ta, tb, P, grid, stream);
+}
+
+}  // namespace tcg

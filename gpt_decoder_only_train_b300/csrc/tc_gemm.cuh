@@ -1,0 +1,466 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// Every dense contraction of the GPT-2 step (QKV, attention projection, FC,
+// FC projection and the tied LM head, forward and both backward products) is
+// one call of this kernel ("llm.c kullanarak GPT-2 modelini düşük maliyetle
+// yeniden uygulamak", §Kod yapısı: the Transformer forward/backward is matmuls
+// plus pointwise work; "Let's reproduce GPT-2 (124M)", §Bölümler 5: Tensor
+// Cores).  acc[m, n] = sum_k A(m, k) B(n, k), fp32 accumulation in TMEM.
+//
+// Design (one CTA per SM, persistent over output tiles):
+//   warp 0    one thread issues TMA loads of A/B k-blocks into a STAGES-deep
+//             shared-memory ring (128-byte swizzle);
+//   warp 1    allocates TMEM (2 accumulators x BN columns) and one thread
+//             issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide k slice,
+//             committing each ring slot back to the producer and each finished
+//             accumulator to the epilogue;
+//   warps 2-5 epilogue: tcgen05.ld 32 lanes x 32 columns at a time, fused
+//             bias / residual / GELU / GELU' / fp32 accumulate, 16-byte stores.
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// Operands may be K-major (k contiguous) or MN-major (m or n contiguous), which
+// covers Y = X W^T, dX = dY W and dW = dY^T X without transposes.
+// Every mbarrier wait is bounded (globaltimer); on timeout the CTA records
+// DEVERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace tcg {
+
+constexpr int BM = 128;            // rows of a tile = TMEM lanes
+constexpr int BK = 64;             // 64 bf16 = one 128-byte swizzle row
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN-major TMA box (64 k rows x 128 B)
+constexpr int NUM_THREADS = 192;
+constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s: far above any legitimate wait
+
+struct Params {
+    int M, N, K;
+    int num_m_blocks, num_n_blocks, num_k_blocks;
+    int splits, k_blocks_per_split;
+    int epi;
+    float alpha;
+    const float *bias;
+    const bf16 *R;
+    void *D;
+    bf16 *D2;
+    int64_t ldd;
+    int *err;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity; false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            raise_device_error(err, DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+// Bounded wait used only on the abort path (no abort check).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > 1000000000ull) return;
+}
+
+// ---- TMA --------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, uint64_t *bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+// ---- tcgen05 ------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
+// stride byte offsets (>> 4), descriptor version 1 at bit 46, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B,
+// operand majorness, N >> 3 and M >> 4.
+__host__ __device__ constexpr uint32_t instr_desc(int bn, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+template <int BN, int STAGES>
+struct SmemLayout {
+    static constexpr int B_STAGE_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+    static constexpr int TOTAL = 1024 /*alignment slack*/ + BAR_OFFSET + BAR_BYTES;
+};
+
+// ---- epilogue -----------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// 32 accumulator columns of one row -> global memory.
+__device__ __forceinline__ void epilogue_chunk(const Params &P, int row, int col0, const uint32_t (&r)[32]) {
+    if (row >= P.M) return;
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(r[i]) * P.alpha;
+    if (P.epi == GPT2_EPI_ACCUM_F32) {
+        float *D = reinterpret_cast<float *>(P.D) + (int64_t)row * P.ldd;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const int col = col0 + 4 * g;
+            if (col >= P.N) break;
+            float4 *p = reinterpret_cast<float4 *>(D + col);
+            if (P.splits == 1) {
+                float4 o = *p;
+                o.x += acc[4 * g + 0];
+                o.y += acc[4 * g + 1];
+                o.z += acc[4 * g + 2];
+                o.w += acc[4 * g + 3];
+                *p = o;
+            } else {
+                atomicAdd(D + col + 0, acc[4 * g + 0]);
+                atomicAdd(D + col + 1, acc[4 * g + 1]);
+                atomicAdd(D + col + 2, acc[4 * g + 2]);
+                atomicAdd(D + col + 3, acc[4 * g + 3]);
+            }
+        }
+        return;
+    }
+    bf16 *D = reinterpret_cast<bf16 *>(P.D) + (int64_t)row * P.ldd;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int col = col0 + 8 * g;
+        if (col >= P.N) break;
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = acc[8 * g + i];
+        if (P.bias && P.epi != GPT2_EPI_GELU_BWD) {
+            const float4 b0 = *reinterpret_cast<const float4 *>(P.bias + col);
+            const float4 b1 = *reinterpret_cast<const float4 *>(P.bias + col + 4);
+            x[0] += b0.x; x[1] += b0.y; x[2] += b0.z; x[3] += b0.w;
+            x[4] += b1.x; x[5] += b1.y; x[6] += b1.z; x[7] += b1.w;
+        }
+        if (P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD) {
+            uint4 rv = *reinterpret_cast<const uint4 *>(P.R + (int64_t)row * P.ldd + col);
+            const bf16 *rb = reinterpret_cast<const bf16 *>(&rv);
+            if (P.epi == GPT2_EPI_RESIDUAL) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] += __bfloat162float(rb[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] *= gelu_tanh_grad(__bfloat162float(rb[i]));
+            }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(x[0], x[1]);
+        o.y = pack_bf16x2(x[2], x[3]);
+        o.z = pack_bf16x2(x[4], x[5]);
+        o.w = pack_bf16x2(x[6], x[7]);
+        *reinterpret_cast<uint4 *>(D + col) = o;
+        if (P.epi == GPT2_EPI_GELU) {
+            // GELU of the bf16-rounded pre-activation, so a recompute from the
+            // stored h reproduces the stored output bit for bit.
+            const bf16 *hb = reinterpret_cast<const bf16 *>(&o);
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = gelu_tanh(__bfloat162float(hb[i]));
+            uint4 og;
+            og.x = pack_bf16x2(y[0], y[1]);
+            og.y = pack_bf16x2(y[2], y[3]);
+            og.z = pack_bf16x2(y[4], y[5]);
+            og.w = pack_bf16x2(y[6], y[7]);
+            *reinterpret_cast<uint4 *>(P.D2 + (int64_t)row * P.ldd + col) = og;
+        }
+    }
+}
+
+// ---- the kernel -----------------------------------------------------------------
+template <int BN, int STAGES, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Params P) {
+    using Lay = SmemLayout<BN, STAGES>;
+    constexpr uint32_t IDESC = instr_desc(BN, A_MN, B_MN);
+    constexpr uint32_t TMEM_COLS = 2 * BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::BAR_OFFSET);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < num_work && ok; w += gridDim.x) {
+                const int split = w % P.splits, tile = w / P.splits;
+                const int m0 = (tile % P.num_m_blocks) * BM, n0 = (tile / P.num_m_blocks) * BN;
+                const int kb0 = split * P.k_blocks_per_split;
+                const int kb1 = min(P.num_k_blocks, kb0 + P.k_blocks_per_split);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&full[stage], Lay::STAGE_BYTES);
+                    uint8_t *a_dst = smem + stage * Lay::STAGE_BYTES;
+                    uint8_t *b_dst = a_dst + A_STAGE_BYTES;
+                    const int k0 = kb * BK;
+                    if (!A_MN) {
+                        tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
+                    } else {
+                        tma_load_2d(a_dst, &tmA, &full[stage], m0, k0);
+                        tma_load_2d(a_dst + MN_BLOCK_BYTES, &tmA, &full[stage], m0 + 64, k0);
+                    }
+                    if (!B_MN) {
+                        tma_load_2d(b_dst, &tmB, &full[stage], k0, n0);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < BN / 64; ++i)
+                            tma_load_2d(b_dst + i * MN_BLOCK_BYTES, &tmB, &full[stage], n0 + 64 * i, k0);
+                    }
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {  // abort: let the copies already issued land before the CTA exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            int t = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < num_work && ok; w += gridDim.x, ++t) {
+                const int split = w % P.splits;
+                const int kb0 = split * P.k_blocks_per_split;
+                const int kb1 = min(P.num_k_blocks, kb0 + P.k_blocks_per_split);
+                const int acc = t & 1;
+                const uint32_t aph = (t >> 1) & 1;
+                if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, P.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * Lay::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j) {
+                        const uint64_t ad = A_MN ? smem_desc(a_addr + j * 2048, MN_BLOCK_BYTES, 1024)
+                                                 : smem_desc(a_addr + j * 32, 16, 1024);
+                        const uint64_t bd = B_MN ? smem_desc(b_addr + j * 2048, MN_BLOCK_BYTES, 1024)
+                                                 : smem_desc(b_addr + j * 32, 16, 1024);
+                        tc_mma(d_tmem, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&tfull[acc]);
+            }
+            // all MMAs issued by this thread have completed once `drain` flips
+            tc_commit(drain);
+            mbar_drain(drain, 0);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quad = warp & 3;  // TMEM lanes this warp may access
+        int t = 0;
+        for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++t) {
+            const int tile = w / P.splits;
+            const int m0 = (tile % P.num_m_blocks) * BM, n0 = (tile / P.num_m_blocks) * BN;
+            const int acc = t & 1;
+            const uint32_t aph = (t >> 1) & 1;
+            if (!mbar_wait(&tfull[acc], aph, abort_flag, P.err)) break;
+            tc_fence_after();
+            const int row = m0 + quad * 32 + lane;
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tbase + c0, r);
+                tmem_ld_wait();
+                if (c0 + 32 == BN) {  // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                }
+                if (n0 + c0 < P.N) epilogue_chunk(P, row, n0 + c0, r);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---- host side ---------------------------------------------------------------------
+int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld_elems, uint32_t box_inner,
+                uint32_t box_outer);
+
+struct GemmDesc {
+    const bf16 *A;
+    int64_t lda;
+    bool a_kmajor;
+    const bf16 *B;
+    int64_t ldb;
+    bool b_kmajor;
+    void *D;
+    bf16 *D2;
+    const bf16 *R;
+    int64_t ldd;
+    const float *bias;
+    int M, N, K;
+    int epi;
+    float alpha;  // acc is scaled by alpha before the epilogue
+    int *err;
+};
+
+int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream);
+
+}  // namespace tcg

@@ -1,0 +1,257 @@
+/*
+ * gpt2b300.h -- C ABI of a single-GPU GPT-2 training step for B300 (sm_103a).
+ *
+ * The step is the one the GPT-2 reproduction pages describe: forward and
+ * backward of the pre-LN causal decoder (token + position embedding,
+ * LayerNorm, QKV / projection / FC / FC-projection / LM-head matmuls, causal
+ * multi-head attention, GELU, residuals), the softmax cross-entropy over the
+ * padded vocabulary, global grad-norm clipping and AdamW on fp32 master
+ * weights.  Sources (web pages, by title and section):
+ *   [R]  "Let's reproduce GPT-2 (124M)" -- §Video özeti (mixed precision,
+ *        flash attention, AdamW, warmup+cosine, gradient accumulation),
+ *        §Bölümler 2 (GPT-2 nn.Module), §Bölümler 4 (cross-entropy loss and
+ *        the overfit test).
+ *   [L]  "llm.c kullanarak GPT-2 modelini düşük maliyetle yeniden uygulamak" --
+ *        §Eğitimi çalıştırma (micro-batch -b, sequence length -t, total batch
+ *        -d, recompute -r), §Eğitim süreci (clipping cures the early gradient
+ *        explosion), §Kod yapısı (forward/backward of the Transformer).
+ *   [G]  "Let's build GPT: from scratch" -- chapters 01:00:18 (position
+ *        encoding), 01:02:00 / 01:16:56 (scaled self-attention, scale
+ *        1/sqrt(head_size), errata: future tokens cannot communicate),
+ *        01:21:59 (multi-head), 01:24:25 (feed-forward), 01:26:48 (residual),
+ *        01:32:51 (LayerNorm).
+ *
+ * Conventions for every call
+ *  - Return value: GPT2_OK (0) or a negative GPT2_ERR_* code; no C++ exception
+ *    crosses this boundary.  gpt2_strerror() names a code.
+ *  - Device pointers ("d_" prefix or documented as device) must point to memory
+ *    of the current CUDA device; host pointers ("host_") to ordinary host memory.
+ *  - All matrices are row-major.  Linear weights are [out_features, in_features].
+ *  - bf16 buffers hold IEEE bfloat16 bit patterns (uint16 storage).
+ *  - Work is enqueued on the CUDA stream given at build (model calls) or per call
+ *    (op calls); calls return after enqueueing unless documented otherwise.
+ */
+#ifndef GPT2B300_H
+#define GPT2B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define GPT2_OK                    0
+#define GPT2_ERR_BAD_CONFIG       -1  /* config fields inconsistent or unsupported */
+#define GPT2_ERR_BAD_SHAPE        -2  /* B > cfg.B, T > cfg.T, sizes <= 0 or misaligned */
+#define GPT2_ERR_BAD_TOKEN        -3  /* a token or target outside [0, V) (seen on device) */
+#define GPT2_ERR_ARENA_TOO_SMALL  -4  /* arena_bytes < gpt2_arena_bytes(cfg) */
+#define GPT2_ERR_CUDA             -5  /* a CUDA runtime/driver call failed */
+#define GPT2_ERR_NONFINITE        -6  /* loss or grad norm is NaN/Inf (update skipped) */
+#define GPT2_ERR_TIMEOUT          -7  /* a bounded device wait gave up (no hang) */
+#define GPT2_ERR_BAD_ARG          -8  /* NULL pointer, bad id, bad enum, short buffer */
+#define GPT2_ERR_UNSUPPORTED      -9  /* device is not sm_103 / feature not built */
+#define GPT2_ERR_STATE           -10  /* call order violated (backward without forward) */
+
+/* ---- model configuration -------------------------------------------------- */
+#define GPT2_DTYPE_FP32 0  /* all activations fp32, SIMT fp32 matmuls (no TF32) */
+#define GPT2_DTYPE_BF16 1  /* bf16 activations, tcgen05 bf16 matmuls, fp32 master/grads/state */
+
+typedef struct {
+    int L;              /* layers */
+    int C;              /* channels; head dim = C / H */
+    int H;              /* heads */
+    int V;              /* real vocabulary size: logits v >= V are masked out of the loss */
+    int Vp;             /* padded vocabulary (rows of wte), Vp >= V */
+    int T;              /* maximum sequence length (rows of wpe) */
+    int B;              /* maximum micro-batch */
+    int dtype;          /* GPT2_DTYPE_* */
+    int recompute_gelu; /* 1: do not store GELU(h); recompute it in backward ([L] -r) */
+} gpt2_config;
+
+typedef struct gpt2_model gpt2_model; /* opaque host handle */
+
+/*
+ * Device bytes a model of this config needs: fp32 params, grads, AdamW m and v,
+ * bf16 weight copy (bf16 mode), activations for B*T tokens and scratch.
+ * Returns 0 for an invalid config.
+ */
+size_t gpt2_arena_bytes(const gpt2_config *cfg);
+
+/*
+ * Build a model in a caller-owned device arena (>= gpt2_arena_bytes, 256-byte
+ * aligned) and initialise it from `seed`: every 2-D weight N(0, 0.02^2), the
+ * attention and FC output projections N(0, (0.02/sqrt(2L))^2), biases 0,
+ * LayerNorm gains 1 ([R] §Bölümler 2); wte rows v >= V are 0.  The normal draws
+ * are SplitMix64 counter draws + Box-Muller in double rounded once to fp32
+ * (draw(seed, tensor_id, 2i) / (.., 2i+1)), computed on the host and copied
+ * once.  Grads, m and v are zeroed; the AdamW step counter is 0.
+ * `cuda_stream` (cudaStream_t, may be NULL for the legacy stream) is used by
+ * every later model call.  The arena and stream stay owned by the caller and
+ * must outlive the model; the handle owns only host memory.  Synchronises the
+ * stream before returning.
+ */
+int gpt2_build(const gpt2_config *cfg, uint64_t seed, void *dev_arena, size_t arena_bytes,
+               void *cuda_stream, gpt2_model **out);
+
+/*
+ * Forward pass over d_tokens [B, T] (device int32, B <= cfg.B, T <= cfg.T).
+ * With d_targets (device int32 [B, T]) it also runs the fused classifier: the
+ * loss is the mean over the B*T positions of logsumexp(z[0..V)) - z[target]
+ * ([R] §Bölümler 4) and the logits buffer is overwritten in place by
+ * dloss/dz (for a unit loss weight; backward applies grad_scale), with
+ * dz[v >= V] = 0.  The scalar loss is copied to *loss_out (host), which
+ * synchronises the stream.  With d_targets == NULL only the logits are
+ * computed (no sync; loss_out untouched).  Out-of-range tokens give
+ * GPT2_ERR_BAD_TOKEN (their rows are treated as token 0).
+ */
+int gpt2_forward(gpt2_model *m, const int32_t *d_tokens, const int32_t *d_targets, int B, int T,
+                 float *loss_out);
+
+/*
+ * Backward of grad_scale * loss of the last forward with targets:
+ * grads += d(grad_scale * loss)/d(params).  grad_scale = 1/accumulation_steps
+ * gives the averaged gradient of [R] §Video özeti (gradient accumulation).
+ * GPT2_ERR_STATE if no forward with targets preceded it.
+ */
+int gpt2_backward(gpt2_model *m, float grad_scale);
+
+/* grads = 0 (enqueued). */
+int gpt2_zero_grad(gpt2_model *m);
+
+/*
+ * One fused pass over all parameters ([L] §Eğitim süreci, [R] §Video özeti):
+ *   n = sqrt(sum of all grads^2) (every tensor, fp32 data, fp64 reduction);
+ *   c = min(1, clip / (n + 1e-6));  g = c * grad;
+ *   t += 1;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   p = p (1 - lr wd [2-D weights only]) - lr (m/(1-b1^t)) / (sqrt(v/(1-b2^t)) + eps);
+ *   bf16 weight copy = RN(p).
+ * The pre-clip norm is written to *grad_norm_out (host; synchronises).  If n is
+ * not finite nothing is updated and GPT2_ERR_NONFINITE is returned.  Grads are
+ * left unchanged (call gpt2_zero_grad before the next accumulation).
+ */
+int gpt2_clip_and_adamw(gpt2_model *m, float lr, float beta1, float beta2, float eps, float wd, float clip,
+                        float *grad_norm_out);
+
+/* Number of parameter tensors: 2 + 12 L + 2. */
+int gpt2_num_tensors(const gpt2_model *m);
+
+/*
+ * Name and shape of tensor `id` in the order wte, wpe, per layer
+ * [ln1.g ln1.b qkv.w qkv.b proj.w proj.b ln2.g ln2.b fc.w fc.b fcproj.w fcproj.b], lnf.g, lnf.b.
+ * *name points to static storage owned by the model.
+ */
+int gpt2_tensor_info(const gpt2_model *m, int id, const char **name, int *ndim, int64_t shape[2]);
+
+/* Copy fp32 master params / grads / AdamW m / AdamW v of tensor `id` to host
+ * (n = element count; synchronises). */
+int gpt2_get_params(gpt2_model *m, int id, float *host_out, size_t n);
+int gpt2_get_grads(gpt2_model *m, int id, float *host_out, size_t n);
+int gpt2_get_adam_state(gpt2_model *m, int id, float *host_m, float *host_v, size_t n);
+
+/* Overwrite fp32 master params of tensor `id` from host (and its bf16 copy). */
+int gpt2_set_params(gpt2_model *m, int id, const float *host_in, size_t n);
+
+/*
+ * Device pointer and byte size of an internal activation buffer, for tests:
+ * "logits" ([B*T, Vp], dtype of the model; after a forward with targets it
+ * holds dlogits), "loss_rows" (fp32 [B*T]), "lnf" (final LN output), "qkv.<l>",
+ * "att.<l>", "lse.<l>", "resid.<l>" (input of layer l; resid.L is the final
+ * residual stream).  GPT2_ERR_BAD_ARG for an unknown name.
+ */
+int gpt2_debug_buffer(gpt2_model *m, const char *name, void **dev_ptr, size_t *bytes);
+
+/* Step counter t of AdamW (number of clip_and_adamw calls that updated). */
+int gpt2_adam_step(const gpt2_model *m, int *t_out);
+
+void gpt2_free(gpt2_model *m);
+const char *gpt2_strerror(int status);
+
+/* Text of the last CUDA error seen by this thread (for diagnostics; "" if none). */
+const char *gpt2_last_error_detail(void);
+
+/* Number of kernels this library has launched in this process (all models and op calls). */
+long long gpt2_launch_count(void);
+
+/* ---- per-launch timing (measurement) ---------------------------------------
+ * With profiling enabled, each kernel launch of the model calls is bracketed by
+ * a pair of CUDA events on the model's stream and attributed to a category
+ * together with its algorithmic work (FLOP for matmul and attention, bytes for
+ * the memory-bound kernels).  gpt2_profile(m, 1) clears the totals and starts
+ * recording, gpt2_profile(m, 0) stops; gpt2_profile_read synchronises the
+ * stream and returns the totals of one category.                            */
+#define GPT2_PROF_MATMUL     0  /* tcgen05 / SIMT matmuls: work = 2 M N K FLOP */
+#define GPT2_PROF_ATTENTION  1  /* causal attention: work = 4 hd T(T+1)/2 per head (fwd), 2x that (bwd) FLOP */
+#define GPT2_PROF_CLASSIFIER 2  /* fused classifier: work = bytes read + written */
+#define GPT2_PROF_ADAMW      3  /* clip + AdamW: bytes */
+#define GPT2_PROF_LAYERNORM  4  /* LayerNorm forward/backward: bytes */
+#define GPT2_PROF_OTHER      5  /* embedding, bias sums, GELU recompute, loss mean: bytes */
+#define GPT2_PROF_NCAT       6
+int gpt2_profile(gpt2_model *m, int enable);
+int gpt2_profile_read(gpt2_model *m, int category, double *total_ms, double *total_work, long long *launches);
+
+/* ---- op-level entry points (device pointers; enqueued on `stream`) ------- *
+ * The model calls are built from these kernels; they are exposed for
+ * per-kernel parity tests and for the isolated attention workload.          */
+
+/*
+ * Causal attention forward, flash style: the T x T score matrix is never
+ * stored ([G] 01:02:00, 01:16:56; [R] §Video özeti, flash attention).
+ * For each (b, h): O = softmax(Q K^T / sqrt(hd), j <= i) V and
+ * lse[b,h,i] = logsumexp_j of the scaled scores.
+ * q/k/v/o are bf16 with element (b, t, h, d) at ptr[(b*T + t)*row_stride + h*hd + d]
+ * (row_stride in elements: 3C for a fused qkv buffer, H*hd for separate
+ * tensors).  lse is fp32 [B, H, T].  hd must be 64; row strides multiples of 8.
+ */
+int gpt2_op_attention_forward(const void *q, const void *k, const void *v, int64_t qkv_row_stride, void *o,
+                              int64_t o_row_stride, float *lse, int B, int T, int H, int hd, void *stream);
+
+/*
+ * Causal attention backward from O, dO and lse of the forward:
+ * D = rowsum(dO * O); P = exp(S - lse); dV = P^T dO; dP = dO V^T;
+ * dS = P * (dP - D); dQ = dS K / sqrt(hd); dK = dS^T Q / sqrt(hd).
+ * dq/dk/dv use qkv_row_stride (they may point into one fused dqkv buffer).
+ * d_scratch: caller-owned fp32 workspace of B*H*T floats (holds D).
+ */
+int gpt2_op_attention_backward(const void *q, const void *k, const void *v, int64_t qkv_row_stride,
+                               const void *o, const void *dout, int64_t o_row_stride, const float *lse,
+                               void *dq, void *dk, void *dv, float *d_scratch, int B, int T, int H, int hd,
+                               void *stream);
+
+/* Matmul epilogues of gpt2_op_matmul. */
+#define GPT2_EPI_STORE        0  /* D = acc (+ bias)                      -> bf16 */
+#define GPT2_EPI_RESIDUAL     1  /* D = acc + bias + R[m,n]              -> bf16 */
+#define GPT2_EPI_GELU         2  /* D = acc + bias (h), D2 = gelu_tanh(h) -> bf16, bf16 */
+#define GPT2_EPI_GELU_BWD     3  /* D = acc * gelu_tanh'(R[m,n])          -> bf16 */
+#define GPT2_EPI_ACCUM_F32    4  /* D[m,n] += acc                         -> fp32 */
+
+/*
+ * bf16 matmul on the tcgen05 tensor cores, fp32 accumulation in TMEM:
+ *   acc[m, n] = sum_k A(m, k) * B(n, k)
+ * a_kmajor = 1: A(m,k) = A[m*lda + k]   (row-major [M, K])
+ * a_kmajor = 0: A(m,k) = A[k*lda + m]   (row-major [K, M], i.e. A^T stored)
+ * b_kmajor = 1: B(n,k) = B[n*ldb + k]   (row-major [N, K], a [out,in] weight)
+ * b_kmajor = 0: B(n,k) = B[k*ldb + n]   (row-major [K, N])
+ * D is row-major [M, N] with leading dimension ldd (R uses ldd too); bias is
+ * fp32 [N] or NULL.  Requirements: lda, ldb, ldd multiples of 8, 16-byte
+ * aligned pointers, K >= 1.  M, N, K need not be multiples of the tile.
+ */
+int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const void *B, int64_t ldb, int b_kmajor, void *D,
+                   void *D2, const void *R, int64_t ldd, const float *bias, int M, int N, int K, int epilogue,
+                   void *stream);
+
+/*
+ * Fused classifier over rows of bf16 logits [N, Vp] (in place):
+ * loss_rows[i] = logsumexp(z[i, 0..V)) - z[i, target[i]];
+ * z[i, v] <- (softmax(z[i, 0..V))[v] - [v == target[i]]) * dscale for v < V,
+ * z[i, v] <- 0 for V <= v < Vp.  No probabilities are stored.
+ */
+int gpt2_op_classifier(void *logits, const int32_t *targets, float *loss_rows, int N, int V, int Vp, float dscale,
+                       void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPT2B300_H */

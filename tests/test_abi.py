@@ -1,0 +1,74 @@
+"""The C-ABI library builds, loads without a GPU and exports every declared symbol."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gpt2b300.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(gpt2_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def libh():
+    from gpt_decoder_only_train_b300 import build
+
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_step_calls():
+    names = _declared()
+    for want in ("gpt2_build", "gpt2_forward", "gpt2_backward", "gpt2_clip_and_adamw", "gpt2_get_grads",
+                 "gpt2_get_params", "gpt2_arena_bytes", "gpt2_free"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(libh):
+    missing = [n for n in _declared() if not hasattr(libh, n)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_header():
+    import gpt_decoder_only_train_b300 as g
+
+    assert set(_declared()) <= set(g._SIGS)
+
+
+def test_arena_bytes_and_config_validation(libh):
+    import gpt_decoder_only_train_b300 as g
+
+    L = g.lib()
+    ok = g.make_config(dict(L=12, C=768, H=12, V=50257, Vp=50304, T=1024, B=16, dtype="bf16"))
+    n = L.gpt2_arena_bytes(ctypes.byref(ok))
+    # fp32 params + grads + m + v + bf16 copy alone are ~2.2 GB at 124M
+    assert 2.2e9 < n < 20e9
+    bad = [
+        dict(L=12, C=768, H=11, V=50257, Vp=50304, T=1024, B=16, dtype="bf16"),  # C % H
+        dict(L=12, C=768, H=12, V=50257, Vp=50000, T=1024, B=16, dtype="bf16"),  # Vp < V
+        dict(L=2, C=96, H=3, V=256, Vp=256, T=32, B=2, dtype="bf16"),            # head dim 32 in bf16
+        dict(L=0, C=64, H=4, V=256, Vp=256, T=32, B=2, dtype="fp32"),
+    ]
+    for d in bad:
+        c = g.make_config(d)
+        assert L.gpt2_arena_bytes(ctypes.byref(c)) == 0, d
+
+
+def test_build_rejects_bad_arguments_without_touching_a_gpu(libh):
+    import gpt_decoder_only_train_b300 as g
+
+    L = g.lib()
+    c = g.make_config(dict(L=2, C=64, H=4, V=256, Vp=256, T=32, B=2, dtype="fp32"))
+    h = ctypes.c_void_p()
+    assert L.gpt2_build(ctypes.byref(c), 0, None, 0, None, ctypes.byref(h)) == -8  # NULL arena
+    c.C = 65
+    assert L.gpt2_build(ctypes.byref(c), 0, ctypes.c_void_p(256), 1 << 30, None, ctypes.byref(h)) == -1
+    assert L.gpt2_strerror(-3) == b"token or target out of range"
+    assert L.gpt2_forward(None, None, None, 1, 1, None) == -8

@@ -1,0 +1,236 @@
+"""Whole-step parity of the CUDA library against the oracle, through the C ABI.
+
+fp32 mode: loss and every gradient tensor within max-abs 1e-4 * max|ref|;
+token/target handling and embedding indexing bit-exact (rows that receive no
+gradient are exactly zero).  bf16 mode: |loss - ref| <= 2e-2 and per-tensor
+gradient cosine >= 0.995.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import gpt2 as og
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gpt_decoder_only_train_b300 import build
+
+    build.build()
+    import gpt_decoder_only_train_b300 as mod
+
+    mod.lib()
+    return mod
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def _cos(a, b):
+    a = np.asarray(a, dtype=np.float64).reshape(-1)
+    b = np.asarray(b, dtype=np.float64).reshape(-1)
+    na, nb = np.linalg.norm(a), np.linalg.norm(b)
+    if na == 0 and nb == 0:
+        return 1.0
+    return float(a @ b / (na * nb))
+
+
+SMALL_BF16 = dict(L=2, C=128, H=2, V=500, Vp=512, T=192, B=3, dtype="bf16", recompute_gelu=0)
+RAGGED_BF16 = dict(L=1, C=192, H=3, V=1000, Vp=1024, T=77, B=2, dtype="bf16", recompute_gelu=0)
+
+
+def test_init_is_bit_identical_to_oracle(g):
+    for cfg, seed in ((synthetic.WORKLOADS["tiny_fp32"], 0), (SMALL_BF16, 7)):
+        m = g.GPT2(cfg, seed=seed)
+        P = og.init_params(og.Config.from_dict(cfg), seed)
+        for i, name in enumerate(m.names):
+            a = m.params(i)
+            b = P[name].numpy().astype(np.float32)
+            assert a.tobytes() == b.tobytes(), name
+        m.close()
+
+
+def test_fp32_tiny_step_parity(g):
+    """The tiny fp32 workload: one full step (fwd + bwd + clip + AdamW) vs the oracle."""
+    w = synthetic.WORKLOADS["tiny_fp32"]
+    x, y = synthetic.step_batch(w)
+    m = g.GPT2(w, seed=w["seed"])
+    ref = og.OracleGPT2(og.Config.from_dict(w), w["seed"])
+    loss = m.forward(_dev(x), _dev(y))
+    ref_loss = ref.forward(x, y)
+    assert abs(loss - ref_loss) <= 1e-4 * abs(ref_loss)
+    m.backward(1.0)
+    ref.backward(1.0)
+    for i, name in enumerate(m.names):
+        gg = m.grads(i)
+        rg = ref.grads[name].numpy()
+        assert np.abs(gg - rg).max() <= 1e-4 * np.abs(rg).max() + 1e-12, name
+    # embedding indexing: exactly the rows of tokens present get gradient from the embedding path
+    # (wte rows also get the LM-head gradient); wpe rows >= T are untouched
+    assert (m.grads(1)[x.shape[1]:] == 0).all()
+    lr = 6e-4
+    norm = m.clip_and_adamw(lr, 0.9, 0.95, 1e-8, 0.1, 1.0)
+    ref_norm = ref.clip_and_adamw(lr, 0.9, 0.95, 1e-8, 0.1, 1.0)
+    assert abs(norm - ref_norm) <= 1e-4 * ref_norm
+    for i, name in enumerate(m.names):
+        p = m.params(i)
+        rp = ref.params[name].numpy()
+        assert np.abs(p - rp).max() <= 1e-6 + 0.02 * lr, name
+    assert m.adam_step() == 1
+
+
+def _bf16_step(g, cfg, seed, micro=1):
+    m = g.GPT2(cfg, seed=seed)
+    ref = og.OracleGPT2(og.Config.from_dict(cfg), seed)
+    losses = []
+    for i in range(micro):
+        x, y = synthetic.zipf_window(seed, cfg["B"], cfg["T"], cfg["V"], micro_step=i)
+        loss = m.forward(_dev(x), _dev(y))
+        ref_loss = ref.forward(x, y)
+        losses.append((loss, ref_loss))
+        m.backward(1.0 / micro)
+        ref.backward(1.0 / micro)
+    return m, ref, losses
+
+
+@pytest.mark.parametrize("cfg", [SMALL_BF16, RAGGED_BF16], ids=["small", "ragged"])
+def test_bf16_step_parity(g, cfg):
+    m, ref, losses = _bf16_step(g, cfg, seed=21)
+    loss, ref_loss = losses[0]
+    assert abs(loss - ref_loss) <= 2e-2, (loss, ref_loss)
+    for i, name in enumerate(m.names):
+        c = _cos(m.grads(i), ref.grads[name].numpy())
+        assert c >= 0.995, (name, c)
+    norm = m.clip_and_adamw(6e-4)
+    ref_norm = ref.clip_and_adamw(6e-4)
+    assert abs(norm - ref_norm) <= 0.02 * ref_norm
+    # padded vocabulary rows keep zero gradient and stay exactly zero
+    wte = m.params(0)
+    assert (m.grads(0)[cfg["V"]:] == 0).all()
+    assert (wte[cfg["V"]:] == 0).all()
+
+
+def test_bf16_gradient_accumulation(g):
+    cfg = dict(SMALL_BF16, B=2, T=128)
+    m, ref, losses = _bf16_step(g, cfg, seed=4, micro=3)
+    for loss, ref_loss in losses:
+        assert abs(loss - ref_loss) <= 2e-2
+    for i, name in enumerate(m.names):
+        assert _cos(m.grads(i), ref.grads[name].numpy()) >= 0.995, name
+
+
+def test_gelu_recompute_is_bit_identical(g):
+    """Recomputing GELU from the stored pre-activation changes no bit of loss or grads."""
+    cfg0 = dict(SMALL_BF16, recompute_gelu=0)
+    cfg1 = dict(SMALL_BF16, recompute_gelu=1)
+    x, y = synthetic.zipf_window(8, cfg0["B"], cfg0["T"], cfg0["V"])
+    out = []
+    for cfg in (cfg0, cfg1):
+        m = g.GPT2(cfg, seed=8)
+        loss = m.forward(_dev(x), _dev(y))
+        m.backward(1.0)
+        out.append((loss, [m.grads(i) for i in range(len(m.names)) if m.shapes[i] and len(m.shapes[i]) == 2]))
+        m.close()
+    assert out[0][0] == out[1][0]
+    # 2-D weight grads use split-K atomics; compare to fp32 summation-order noise
+    for a, b in zip(out[0][1], out[1][1]):
+        assert np.abs(a - b).max() <= 1e-5 * max(np.abs(a).max(), 1e-30)
+
+
+def test_padded_logits_get_zero_dlogits(g):
+    cfg = SMALL_BF16
+    m = g.GPT2(cfg, seed=2)
+    x, y = synthetic.zipf_window(2, cfg["B"], cfg["T"], cfg["V"])
+    m.forward(_dev(x), _dev(y))
+    torch.cuda.synchronize()
+    BT = cfg["B"] * cfg["T"]
+    dz = m.debug_tensor("logits", torch.bfloat16, (BT, cfg["Vp"])).float().cpu()
+    assert (dz[:, cfg["V"]:] == 0).all()
+    assert dz[:, : cfg["V"]].sum(1).abs().max().item() < 1e-4  # rows of softmax - onehot sum to 0
+
+
+def _logits(g, m, cfg, x):
+    m.forward(_dev(x), None)
+    torch.cuda.synchronize()
+    return m.debug_tensor("logits", torch.bfloat16, (x.size, cfg["Vp"])).cpu()
+
+
+def test_logits_causal_bitwise(g):
+    cfg = dict(SMALL_BF16, B=1)
+    m = g.GPT2(cfg, seed=3)
+    x, _ = synthetic.zipf_window(3, 1, cfg["T"], cfg["V"])
+    z0 = _logits(g, m, cfg, x)
+    x2 = x.copy()
+    x2[0, 150] = (x2[0, 150] + 1) % cfg["V"]
+    z1 = _logits(g, m, cfg, x2)
+    assert torch.equal(z0[:150], z1[:150])
+    assert not torch.equal(z0[150:], z1[150:])
+
+
+def test_loss_run_to_run_bitwise(g):
+    cfg = SMALL_BF16
+    x, y = synthetic.zipf_window(9, cfg["B"], cfg["T"], cfg["V"])
+    losses = []
+    for _ in range(2):
+        m = g.GPT2(cfg, seed=9)
+        losses.append(m.forward(_dev(x), _dev(y)))
+        m.close()
+    assert losses[0] == losses[1]
+
+
+def test_error_paths_leave_model_usable(g):
+    cfg = SMALL_BF16
+    m = g.GPT2(cfg, seed=1)
+    x, y = synthetic.zipf_window(1, cfg["B"], cfg["T"], cfg["V"])
+    with pytest.raises(g.Gpt2Error) as e:
+        m.backward(1.0)  # no forward yet
+    assert e.value.status == -10
+    with pytest.raises(g.Gpt2Error) as e:
+        m.forward(_dev(np.zeros((cfg["B"] + 1, 4))), _dev(np.zeros((cfg["B"] + 1, 4))))
+    assert e.value.status == -2
+    bad = y.copy()
+    bad[0, 3] = cfg["V"] + 5
+    with pytest.raises(g.Gpt2Error) as e:
+        m.forward(_dev(x), _dev(bad))
+    assert e.value.status == -3
+    bad = x.copy()
+    bad[1, 0] = -1
+    with pytest.raises(g.Gpt2Error) as e:
+        m.forward(_dev(bad), _dev(y))
+    assert e.value.status == -3
+    loss = m.forward(_dev(x), _dev(y))  # next valid call succeeds
+    m.backward(1.0)
+    assert math.isfinite(loss) and math.isfinite(m.clip_and_adamw(6e-4))
+
+
+def test_nonfinite_gradient_skips_update(g):
+    cfg = SMALL_BF16
+    m = g.GPT2(cfg, seed=1)
+    x, y = synthetic.zipf_window(1, cfg["B"], cfg["T"], cfg["V"])
+    m.forward(_dev(x), _dev(y))
+    m.backward(float("nan"))
+    before = m.params(2).copy()
+    with pytest.raises(g.Gpt2Error) as e:
+        m.clip_and_adamw(6e-4)
+    assert e.value.status == -6
+    assert np.array_equal(before, m.params(2))
+    assert m.adam_step() == 0
+
+
+def test_initial_loss_124m(g):
+    """Init loss at the 124M shapes is ln V + 0.02^2 C / 2 (logits ~ N(0, 0.02^2 C))."""
+    w = synthetic.WORKLOADS["gpt2_124m"]
+    m = g.GPT2(w, seed=w["seed"])
+    x, y = synthetic.step_batch(w)
+    loss = m.forward(_dev(x), _dev(y))
+    want = math.log(w["V"]) + 0.02 ** 2 * w["C"] / 2
+    assert abs(loss - want) <= 0.05, (loss, want)
+    m.close()
