@@ -61,6 +61,7 @@ _SIGS = {
     "gpt2_get_grads": (_I, [_P, _I, _P, ctypes.c_size_t]),
     "gpt2_get_adam_state": (_I, [_P, _I, _P, _P, ctypes.c_size_t]),
     "gpt2_set_params": (_I, [_P, _I, _P, ctypes.c_size_t]),
+    "gpt2_set_grads": (_I, [_P, _I, _P, ctypes.c_size_t]),
     "gpt2_debug_buffer": (_I, [_P, ctypes.c_char_p, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
     "gpt2_adam_step": (_I, [_P, ctypes.POINTER(_I)]),
     "gpt2_free": (None, [_P]),
@@ -202,6 +203,10 @@ class GPT2:
     def set_params(self, i, arr):
         a = np.ascontiguousarray(arr, dtype=np.float32)
         check("gpt2_set_params", lib().gpt2_set_params(self.handle, i, a.ctypes.data, a.size))
+
+    def set_grads(self, i, arr):
+        a = np.ascontiguousarray(arr, dtype=np.float32)
+        check("gpt2_set_grads", lib().gpt2_set_grads(self.handle, i, a.ctypes.data, a.size))
 
     def adam_step(self):
         t = ctypes.c_int()

@@ -678,6 +678,15 @@ extern "C" int gpt2_set_params(gpt2_model *m, int id, const float *host_in, size
     return GPT2_OK;
 }
 
+extern "C" int gpt2_set_grads(gpt2_model *m, int id, const float *host_in, size_t n) {
+    if (!m || !host_in || id < 0 || id >= (int)m->tensors.size()) return GPT2_ERR_BAD_ARG;
+    const TensorInfo &t = m->tensors[id];
+    if (n < (size_t)t.numel) return GPT2_ERR_BAD_ARG;
+    GPT2_CUDA_TRY(cudaMemcpyAsync(m->grads + t.offset, host_in, t.numel * 4, cudaMemcpyHostToDevice, m->stream));
+    GPT2_CUDA_TRY(cudaStreamSynchronize(m->stream));
+    return GPT2_OK;
+}
+
 extern "C" int gpt2_debug_buffer(gpt2_model *m, const char *name, void **dev_ptr, size_t *bytes) {
     if (!m || !name || !dev_ptr || !bytes) return GPT2_ERR_BAD_ARG;
     const gpt2_config &c = m->cfg;

@@ -89,7 +89,19 @@ int embed_backward(const int *tok, const T *dx, float *dwte, float *dwpe, int B,
 }
 
 // ============================================================== LayerNorm
-// One warp per row; the row stays in registers (VPL 16-byte packets per lane).
+// One warp per row; the row stays in registers (VPL 16-byte packets per lane,
+// packet p = lane + 32 i covers columns [p*E, p*E + E)).
+template <int E> struct F4x {  // E fp32 values loaded as float4s
+    float v[E];
+    __device__ __forceinline__ void load(const float *p) {
+#pragma unroll
+        for (int i = 0; i < E; i += 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(p + i);
+            v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+        }
+    }
+};
+
 template <typename T, int VPL>
 __global__ void ln_fwd_kernel(const T *__restrict__ x, const float *__restrict__ g, const float *__restrict__ b,
                               T *__restrict__ y, float *__restrict__ mean, float *__restrict__ rstd, int N, int C) {
@@ -105,7 +117,7 @@ __global__ void ln_fwd_kernel(const T *__restrict__ x, const float *__restrict__
     for (int i = 0; i < VPL; ++i) {
         const int p = lane + 32 * i;
         if (p < npk) {
-            v[i].load(xr + p * E);
+            v[i].load_stream(xr + p * E);
 #pragma unroll
             for (int e = 0; e < E; ++e) s += v[i].get(e);
         }
@@ -129,12 +141,12 @@ __global__ void ln_fwd_kernel(const T *__restrict__ x, const float *__restrict__
     for (int i = 0; i < VPL; ++i) {
         const int p = lane + 32 * i;
         if (p < npk) {
+            F4x<E> gg, bb;
+            gg.load(g + p * E);
+            bb.load(b + p * E);
             Pack16<T> o;
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int c = p * E + e;
-                o.set(e, (v[i].get(e) - mu) * rs * g[c] + b[c]);
-            }
+            for (int e = 0; e < E; ++e) o.set(e, (v[i].get(e) - mu) * rs * gg.v[e] + bb.v[e]);
             o.store(yr + p * E);
         }
     }
@@ -168,17 +180,24 @@ int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *m
     return GPT2_OK;
 }
 
+// dx = rstd (dy*g - mean(dy*g) - xhat mean(dy*g*xhat)).  dg/db: every warp
+// accumulates its rows into its own shared-memory slice (layout [e][packet], so
+// a lane owns its columns and the 32 lanes hit 32 banks); at the end the block
+// sums the warp slices in a fixed order and adds them to the fp32 gradients.
 template <typename T, int VPL>
-__global__ void ln_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ x, const float *__restrict__ mean,
-                              const float *__restrict__ rstd, const float *__restrict__ g, const T *dres_in,
-                              T *dres_out, float *__restrict__ dg, float *__restrict__ db, int N, int C) {
+__global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ x,
+                                                        const float *__restrict__ mean,
+                                                        const float *__restrict__ rstd, const float *__restrict__ g,
+                                                        const T *dres_in, T *dres_out, float *__restrict__ dg,
+                                                        float *__restrict__ db, int N, int C) {
     constexpr int E = Pack16<T>::N;
-    extern __shared__ float sh[];  // [2C]: partial dg, partial db
-    for (int i = threadIdx.x; i < 2 * C; i += blockDim.x) sh[i] = 0.f;
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+    extern __shared__ float sh[];  // [warps][2][E][npk]
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, warps = blockDim.x >> 5;
     const int npk = C / E;
-    for (int row = blockIdx.x * warps + (threadIdx.x >> 5); row < N; row += gridDim.x * warps) {
+    for (int i = threadIdx.x; i < warps * 2 * C; i += blockDim.x) sh[i] = 0.f;
+    __syncthreads();
+    float *sdg = sh + wid * 2 * C, *sdb = sdg + C;
+    for (int row = blockIdx.x * warps + wid; row < N; row += gridDim.x * warps) {
         const int64_t off = (int64_t)row * C;
         Pack16<T> vdy[VPL], vx[VPL];
         const float mu = mean[row], rs = rstd[row];
@@ -187,15 +206,19 @@ __global__ void ln_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ x,
         for (int i = 0; i < VPL; ++i) {
             const int p = lane + 32 * i;
             if (p < npk) {
-                vdy[i].load(dy + off + p * E);
-                vx[i].load(x + off + p * E);
+                vdy[i].load_stream(dy + off + p * E);
+                vx[i].load_stream(x + off + p * E);
+                F4x<E> gg;
+                gg.load(g + p * E);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    const int c = p * E + e;
-                    const float dxh = vdy[i].get(e) * g[c];
+                    const float d = vdy[i].get(e);
+                    const float dxh = d * gg.v[e];
                     const float xh = (vx[i].get(e) - mu) * rs;
                     s1 += dxh;
                     s2 += dxh * xh;
+                    sdg[e * npk + p] += d * xh;
+                    sdb[e * npk + p] += d;
                 }
             }
         }
@@ -206,24 +229,28 @@ __global__ void ln_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ x,
             if (p < npk) {
                 Pack16<T> base, o;
                 if (dres_in) base.load(dres_in + off + p * E);
+                F4x<E> gg;
+                gg.load(g + p * E);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    const int c = p * E + e;
-                    const float d = vdy[i].get(e);
                     const float xh = (vx[i].get(e) - mu) * rs;
-                    const float dx = rs * (d * g[c] - m1 - xh * m2);
+                    const float dx = rs * (vdy[i].get(e) * gg.v[e] - m1 - xh * m2);
                     o.set(e, (dres_in ? base.get(e) : 0.f) + dx);
-                    atomicAdd(&sh[c], d * xh);
-                    atomicAdd(&sh[C + c], d);
                 }
                 o.store(dres_out + off + p * E);
             }
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < C; i += blockDim.x) {
-        atomicAdd(dg + i, sh[i]);
-        atomicAdd(db + i, sh[C + i]);
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        const int p = c / E, e = c % E, idx = e * npk + p;
+        float a = 0.f, bsum = 0.f;
+        for (int w = 0; w < warps; ++w) {
+            a += sh[w * 2 * C + idx];
+            bsum += sh[w * 2 * C + C + idx];
+        }
+        atomicAdd(dg + c, a);
+        atomicAdd(db + c, bsum);
     }
 }
 
@@ -232,11 +259,21 @@ int layernorm_backward(const T *dy, const T *x, const float *mean, const float *
                        T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st) {
     if (C % Pack16<T>::N) return GPT2_ERR_BAD_SHAPE;
     const int warps = 8;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = std::max(1, std::min(ceil_div(N, warps), sms * 4));
-    const size_t smem = 2 * C * sizeof(float);
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int grid = std::max(1, std::min(ceil_div(N, warps * 4), sms * 2));
+    const size_t smem = (size_t)warps * 2 * C * sizeof(float);
+    static bool attr = false;
+    if (!attr) {  // up to 2 x 8 x 2 x 2048 floats per SM
+        for (auto fn : {(const void *)ln_bwd_kernel<T, 1>, (const void *)ln_bwd_kernel<T, 2>,
+                        (const void *)ln_bwd_kernel<T, 4>, (const void *)ln_bwd_kernel<T, 8>})
+            GPT2_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * 2 * 2048 * 4));
+        attr = true;
+    }
     switch (ln_vpl<T>(C)) {
         case 1: ln_bwd_kernel<T, 1><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
         case 2: ln_bwd_kernel<T, 2><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
@@ -384,12 +421,100 @@ __global__ void __launch_bounds__(1024) classifier_kernel(T *logits, const int *
     }
 }
 
+// Register-resident variant: the row (NPK packets per thread) is read once,
+// max and sum-exp are block reductions over registers, dz is written once.
+template <typename T, int NPK>
+__global__ void __launch_bounds__(1024) classifier_reg_kernel(T *logits, const int *__restrict__ targets,
+                                                              float *__restrict__ loss_rows, int N, int V, int Vp,
+                                                              float dscale, int *err) {
+    constexpr int E = Pack16<T>::N;
+    __shared__ float red_m[2][32], red_s[2][32];
+    const int npk = Vp / E;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int par = 0;
+    for (int row = blockIdx.x; row < N; row += gridDim.x, par ^= 1) {
+        T *z = logits + (int64_t)row * Vp;
+        int tg = targets[row];
+        const bool bad = tg < 0 || tg >= V;
+        if (bad) tg = 0;
+        Pack16<T> v[NPK];
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NPK; ++i) {
+            const int p = threadIdx.x + i * blockDim.x;
+            if (p < npk) {
+                v[i].load_stream(z + p * E);
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    if (p * E + e < V) m = fmaxf(m, v[i].get(e));
+            }
+        }
+        m = warp_max(m);
+        if (lane == 0) red_m[par][wid] = m;
+        __syncthreads();
+        float M = red_m[par][0];
+        for (int w = 1; w < nw; ++w) M = fmaxf(M, red_m[par][w]);
+        float s = 0.f, zt = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPK; ++i) {
+            const int p = threadIdx.x + i * blockDim.x;
+            if (p < npk) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int c = p * E + e;
+                    if (c < V) s += __expf(v[i].get(e) - M);
+                    if (c == tg) zt = v[i].get(e);
+                }
+            }
+        }
+        s = warp_sum(s);
+        if (lane == 0) red_s[par][wid] = s;
+        __syncthreads();
+        float S = 0.f;
+        for (int w = 0; w < nw; ++w) S += red_s[par][w];
+        const float lse = M + logf(S);
+        if (tg / E % blockDim.x == threadIdx.x) {  // the thread holding the target logit
+            loss_rows[row] = lse - zt;
+            if (bad) raise_device_error(err, DEVERR_BAD_TOKEN);
+        }
+#pragma unroll
+        for (int i = 0; i < NPK; ++i) {
+            const int p = threadIdx.x + i * blockDim.x;
+            if (p < npk) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int c = p * E + e;
+                    float d = 0.f;
+                    if (c < V) {
+                        d = __expf(v[i].get(e) - lse);
+                        if (c == tg) d -= 1.f;
+                        d *= dscale;
+                    }
+                    v[i].set(e, d);
+                }
+                v[i].store(z + p * E);
+            }
+        }
+    }
+}
+
 template <typename T>
 int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, int Vp, float dscale, int *err,
                cudaStream_t st) {
-    if (Vp % Pack16<T>::N || V > Vp || V <= 0) return GPT2_ERR_BAD_SHAPE;
-    const int grid = std::min(N, 148 * 8);
-    classifier_kernel<T><<<grid, 512, 0, st>>>(logits, targets, loss_rows, N, V, Vp, dscale, err);
+    constexpr int E = Pack16<T>::N;
+    if (Vp % E || V > Vp || V <= 0) return GPT2_ERR_BAD_SHAPE;
+    const int npk = Vp / E;
+    const int threads = std::min(1024, (npk + 31) / 32 * 32);
+    const int npt = ceil_div(npk, threads);
+    const int grid = std::min(N, 148 * 2);
+    switch (npt <= 1 ? 1 : npt <= 2 ? 2 : npt <= 4 ? 4 : npt <= 8 ? 8 : 0) {
+        case 1: classifier_reg_kernel<T, 1><<<grid, threads, 0, st>>>(logits, targets, loss_rows, N, V, Vp, dscale, err); break;
+        case 2: classifier_reg_kernel<T, 2><<<grid, threads, 0, st>>>(logits, targets, loss_rows, N, V, Vp, dscale, err); break;
+        case 4: classifier_reg_kernel<T, 4><<<grid, threads, 0, st>>>(logits, targets, loss_rows, N, V, Vp, dscale, err); break;
+        case 8: classifier_reg_kernel<T, 8><<<grid, threads, 0, st>>>(logits, targets, loss_rows, N, V, Vp, dscale, err); break;
+        default: classifier_kernel<T><<<std::min(N, 148 * 8), 512, 0, st>>>(logits, targets, loss_rows, N, V, Vp,
+                                                                            dscale, err);
+    }
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;

@@ -1,0 +1,136 @@
+"""Time single kernels of the library through the op-level C ABI.
+
+    python -m gpt_decoder_only_train_b300.kernel_bench matmul --M 16384 --N 50304 --K 768
+    python -m gpt_decoder_only_train_b300.kernel_bench matmul --M 768 --N 768 --K 16384 --a-mn --b-mn --epi accum
+    python -m gpt_decoder_only_train_b300.kernel_bench attention --B 16 --T 1024 --H 12 [--bwd]
+    python -m gpt_decoder_only_train_b300.kernel_bench classifier --N 16384 --V 50257 --Vp 50304
+    python -m gpt_decoder_only_train_b300.kernel_bench attention-sweep
+
+Inputs are seeded random bf16 on the device; each line reports the mean time
+per launch (CUDA events, after warm-up) and the algorithmic FLOP/s or bytes/s.
+Operands larger than L2 are rotated through copies so that a launch does not
+find its inputs in L2 (``--rotate``).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import sys
+
+import torch
+
+import gpt_decoder_only_train_b300 as g
+
+EPIS = {"store": g.EPI_STORE, "residual": g.EPI_RESIDUAL, "gelu": g.EPI_GELU, "gelu_bwd": g.EPI_GELU_BWD,
+        "accum": g.EPI_ACCUM_F32}
+
+
+def _time(fn, iters, warmup):
+    for _ in range(warmup):
+        fn(0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(iters):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def bench_matmul(a):
+    M, N, K = a.M, a.N, a.K
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    A = torch.randn(K if a.a_mn else M, M if a.a_mn else K, device="cuda", generator=gen).to(torch.bfloat16)
+    B = torch.randn(K if a.b_mn else N, N if a.b_mn else K, device="cuda", generator=gen).to(torch.bfloat16)
+    epi = EPIS[a.epi]
+    D = torch.zeros(M, N, device="cuda", dtype=torch.float32 if epi == g.EPI_ACCUM_F32 else torch.bfloat16)
+    D2 = torch.empty(M, N, device="cuda", dtype=torch.bfloat16) if epi == g.EPI_GELU else None
+    R = torch.randn(M, N, device="cuda", generator=gen).to(torch.bfloat16) if epi in (g.EPI_RESIDUAL,
+                                                                                        g.EPI_GELU_BWD) else None
+    bias = torch.randn(N, device="cuda", generator=gen) if epi in (g.EPI_STORE, g.EPI_RESIDUAL, g.EPI_GELU) else None
+    lda = M if a.a_mn else K
+    ldb = N if a.b_mn else K
+
+    def run(i):
+        g.matmul(A, lda, not a.a_mn, B, ldb, not a.b_mn, D, N, M, N, K, epi, D2=D2, R=R, bias=bias)
+
+    ms = _time(run, a.iters, a.warmup)
+    flops = 2.0 * M * N * K
+    return {"op": "matmul", "M": M, "N": N, "K": K, "a_major": "mn" if a.a_mn else "k",
+            "b_major": "mn" if a.b_mn else "k", "epi": a.epi, "ms": ms, "TFLOP/s": flops / ms / 1e9}
+
+
+def attn_flops(B, T, H, hd=64):
+    return 4.0 * hd * (T * (T + 1) / 2) * B * H
+
+
+def bench_attention(B, T, H, bwd, iters, warmup):
+    hd = 64
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    mk = lambda: torch.randn(B, T, H, hd, device="cuda", generator=gen).to(torch.bfloat16)
+    q, k, v, do = mk(), mk(), mk(), mk()
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, T, device="cuda")
+    g.attention_forward(q, k, v, o, lse, B, T, H)
+    if not bwd:
+        ms = _time(lambda i: g.attention_forward(q, k, v, o, lse, B, T, H), iters, warmup)
+        fl = attn_flops(B, T, H)
+    else:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        sc = torch.empty(B * H * T, device="cuda")
+        ms = _time(lambda i: g.attention_backward(q, k, v, o, do, lse, dq, dk, dv, sc, B, T, H), iters, warmup)
+        fl = 2.0 * attn_flops(B, T, H)
+    return {"op": "attention_" + ("bwd" if bwd else "fwd"), "B": B, "T": T, "H": H, "ms": ms,
+            "TFLOP/s": fl / ms / 1e9}
+
+
+def bench_classifier(a):
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    z0 = torch.randn(a.N, a.Vp, device="cuda", generator=gen).to(torch.bfloat16)
+    z = z0.clone()
+    t = torch.randint(0, a.V, (a.N,), device="cuda", dtype=torch.int32, generator=gen)
+    rows = torch.empty(a.N, device="cuda")
+    ms = _time(lambda i: g.classifier(z, t, rows, a.N, a.V, a.Vp, 1.0 / a.N), a.iters, a.warmup)
+    nbytes = 2.0 * a.N * a.Vp * 2
+    return {"op": "classifier", "N": a.N, "Vp": a.Vp, "ms": ms, "GB/s": nbytes / ms / 1e6}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=["matmul", "attention", "classifier", "attention-sweep"])
+    ap.add_argument("--M", type=int, default=16384)
+    ap.add_argument("--N", type=int, default=2304)
+    ap.add_argument("--K", type=int, default=768)
+    ap.add_argument("--a-mn", action="store_true")
+    ap.add_argument("--b-mn", action="store_true")
+    ap.add_argument("--epi", default="store", choices=sorted(EPIS))
+    ap.add_argument("--B", type=int, default=16)
+    ap.add_argument("--T", type=int, default=1024)
+    ap.add_argument("--H", type=int, default=12)
+    ap.add_argument("--bwd", action="store_true")
+    ap.add_argument("--V", type=int, default=50257)
+    ap.add_argument("--Vp", type=int, default=50304)
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    a = ap.parse_args(argv)
+    from gpt_decoder_only_train_b300 import build
+
+    build.build()
+    if a.op == "matmul":
+        out = [bench_matmul(a)]
+    elif a.op == "attention":
+        out = [bench_attention(a.B, a.T, a.H, a.bwd, a.iters, a.warmup)]
+    elif a.op == "classifier":
+        out = [bench_classifier(a)]
+    else:
+        out = []
+        for T, B in ((256, 256), (1024, 64), (2048, 32), (4096, 16)):
+            for bwd in (False, True):
+                out.append(bench_attention(B, T, 12, bwd, a.iters, a.warmup))
+    for r in out:
+        print(json.dumps(r), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -153,6 +153,10 @@ int gpt2_get_adam_state(gpt2_model *m, int id, float *host_m, float *host_v, siz
 /* Overwrite fp32 master params of tensor `id` from host (and its bf16 copy). */
 int gpt2_set_params(gpt2_model *m, int id, const float *host_in, size_t n);
 
+/* Overwrite the fp32 gradient of tensor `id` from host (tests of the optimizer
+ * on given gradients; synchronises). */
+int gpt2_set_grads(gpt2_model *m, int id, const float *host_in, size_t n);
+
 /*
  * Device pointer and byte size of an internal activation buffer, for tests:
  * "logits" ([B*T, Vp], dtype of the model; after a forward with targets it

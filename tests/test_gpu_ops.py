@@ -50,10 +50,17 @@ def _close(out, ref, rel_elem=1e-2, rel_fro=4e-3):
 # ------------------------------------------------------------------ matmul
 
 def _operand(M, K, kmajor, seed):
-    """Logical [M, K] matrix and its storage (K-major: [M, K]; MN-major: [K, M])."""
+    """Logical [M, K] matrix and its storage (K-major: [M, ld]; MN-major: [K, ld]).
+
+    The leading dimension is rounded up to a multiple of 8 (the 16-byte row
+    pitch rule of the tensor maps); the padding columns hold garbage that the
+    kernel must not read."""
     a = _bf16((M, K), seed)
-    store = a.contiguous() if kmajor else a.t().contiguous()
-    ld = K if kmajor else M
+    inner = K if kmajor else M
+    ld = (inner + 7) // 8 * 8
+    rows = M if kmajor else K
+    store = torch.full((rows, ld), float("nan"), dtype=torch.bfloat16)
+    store[:, :inner] = a if kmajor else a.t()
     return a, store, ld
 
 
