@@ -73,6 +73,8 @@ _SIGS = {
                                ctypes.POINTER(ctypes.c_longlong)]),
     "gpt2_op_attention_forward": (_I, [_P, _P, _P, _I64, _P, _I64, _P, _I, _I, _I, _I, _P]),
     "gpt2_op_attention_backward": (_I, [_P, _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "gpt2_op_attention_backward_noalloc": (_I, [_P, _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I,
+                                                _P]),
     "gpt2_op_matmul": (_I, [_P, _I64, _I, _P, _I64, _I, _P, _P, _P, _I64, _P, _I, _I, _I, _I, _P]),
     "gpt2_op_classifier": (_I, [_P, _P, _P, _I, _I, _I, _F, _P]),
 }
@@ -263,6 +265,19 @@ def attention_backward(q, k, v, o, do, lse, dq, dk, dv, scratch, B, T, H, hd=64,
     check("gpt2_op_attention_backward", lib().gpt2_op_attention_backward(
         _ptr(q), _ptr(k), _ptr(v), rs, _ptr(o), _ptr(do), ors, _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         _ptr(scratch), B, T, H, hd, _stream(stream)))
+
+
+NOALLOC_ATTN_MAX_ROWS = 1 << 20
+
+
+def attention_backward_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, T, H, hd=64, qkv_row_stride=None,
+                               o_row_stride=None, stream=None):
+    """Attention backward without a caller workspace (the library's fixed array holds it)."""
+    rs = qkv_row_stride if qkv_row_stride is not None else H * hd
+    ors = o_row_stride if o_row_stride is not None else H * hd
+    check("gpt2_op_attention_backward_noalloc", lib().gpt2_op_attention_backward_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), rs, _ptr(o), _ptr(do), ors, _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        B, T, H, hd, _stream(stream)))
 
 
 def matmul(A, lda, a_kmajor, B, ldb, b_kmajor, D, ldd, M, N, K, epilogue=EPI_STORE, D2=None, R=None, bias=None,

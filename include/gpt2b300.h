@@ -223,6 +223,32 @@ int gpt2_op_attention_backward(const void *q, const void *k, const void *v, int6
                                void *dq, void *dk, void *dv, float *d_scratch, int B, int T, int H, int hd,
                                void *stream);
 
+/*
+ * Attention backward that allocates nothing.  The source pages have no
+ * counterpart to this entry point; it exists for callers of this library that
+ * cannot allocate device memory when they call it (for example, when a
+ * memory-pool owner has already reserved the device's memory, or when the
+ * hosting runtime forbids allocation after start-up) and so cannot supply the
+ * d_scratch workspace of gpt2_op_attention_backward.
+ *
+ * Same arguments and results as gpt2_op_attention_backward, without
+ * d_scratch: the B*H*T-float workspace is a fixed array inside the library,
+ * GPT2_NOALLOC_ATTN_MAX_ROWS floats (4 MiB) that every GPU loading the
+ * library holds until the process exits.  B*H*T above that limit returns
+ * GPT2_ERR_BAD_SHAPE.  The call makes no cudaMalloc / cudaFree and uses no
+ * allocating library routine.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls on a device
+ * share the one array, which keeps the previous call's contents (the kernels
+ * overwrite the part they read before reading it): calls that can overlap on
+ * the GPU (different streams, or different host threads) race on it and must
+ * be serialised by the caller.
+ */
+#define GPT2_NOALLOC_ATTN_MAX_ROWS (1 << 20)
+int gpt2_op_attention_backward_noalloc(const void *q, const void *k, const void *v, int64_t qkv_row_stride,
+                                       const void *o, const void *dout, int64_t o_row_stride, const float *lse,
+                                       void *dq, void *dk, void *dv, int B, int T, int H, int hd, void *stream);
+
 /* Matmul epilogues of gpt2_op_matmul. */
 #define GPT2_EPI_STORE        0  /* D = acc (+ bias)                      -> bf16 */
 #define GPT2_EPI_RESIDUAL     1  /* D = acc + bias + R[m,n]              -> bf16 */
