@@ -1,10 +1,9 @@
-// Flash-style causal attention (head dim 64) on mma.sync bf16 tensor cores.
+// Flash-style causal attention backward (head dim 64) on mma.sync bf16 tensor
+// cores; the forward runs on tcgen05 (attn_tc.cu).
 //
-// Forward: one CTA per (64-query block, b*h); 4 warps x 16 query rows.  K/V
-// 64-row tiles stream through a double-buffered cp.async ring (XOR-swizzled
-// shared memory read by ldmatrix); scores, the running max / sum and the
-// output accumulator stay in registers (online softmax in the log2 domain).
-// Backward: two kernels without atomics --
+// K/V and Q/dO 64-row tiles stream through double-buffered cp.async rings
+// (XOR-swizzled shared memory read by ldmatrix); scores and the softmax
+// recompute stay in registers.  Two kernels without atomics --
 //   dQ kernel   (per query block): D = rowsum(dO*O), then for each key block
 //               S, P = exp(S - lse), dP = dO V^T, dS = P (dP - D), dQ += dS K;
 //   dK/dV kernel (per key block): for each query block S^T, P^T, dP^T,
@@ -115,95 +114,6 @@ __device__ __forceinline__ void zero(float (&a)[8][4]) {
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int e = 0; e < 4; ++e) a[i][e] = 0.f;
-}
-
-// ----------------------------------------------------------------- forward
-__global__ void __launch_bounds__(NT) fwd_kernel(const bf16 *__restrict__ q, const bf16 *__restrict__ k,
-                                                 const bf16 *__restrict__ v, int64_t rs, bf16 *__restrict__ o,
-                                                 int64_t ors, float *__restrict__ lse, int T, int H, float sl2) {
-    extern __shared__ __align__(1024) uint8_t sm[];
-    const int nqb = (T + 63) / 64;
-    const int qb = nqb - 1 - blockIdx.x;
-    const int bh = blockIdx.y, b = bh / H, h = bh % H;
-    const int64_t hoff = (int64_t)b * T * rs + h * HD;
-    const bf16 *qg = q + hoff, *kg = k + hoff, *vg = v + hoff;
-    const uint32_t sQ = su32(sm), sK = sQ + TILE, sV = sQ + 3 * TILE;  // K, V double-buffered
-    load_tile(sQ, qg, rs, qb * 64, T);
-    load_tile(sK, kg, rs, 0, T);
-    load_tile(sV, vg, rs, 0, T);
-    cp_commit();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
-    const int row0 = qb * 64 + warp * 16 + gid;
-    float oacc[8][4], s[8][4];
-    zero(oacc);
-    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-    uint32_t qf[4][4];
-    for (int j = 0; j <= qb; ++j) {
-        const int buf = j & 1;
-        if (j < qb) {
-            load_tile(sK + (buf ^ 1) * TILE, kg, rs, (j + 1) * 64, T);
-            load_tile(sV + (buf ^ 1) * TILE, vg, rs, (j + 1) * 64, T);
-        }
-        cp_commit();
-        cp_wait1();
-        __syncthreads();
-        if (j == 0)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) ld_a(sQ, warp * 16, kk, qf[kk]);
-        zero(s);
-        mm_rows(s, qf, sK + buf * TILE);
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = j * 64 + nt * 8 + 2 * t4 + (e & 1), row = row0 + (e >> 1) * 8;
-                float x = s[nt][e] * sl2;
-                if (key > row || key >= T) x = -INFINITY;
-                s[nt][e] = x;
-                mx[e >> 1] = fmaxf(mx[e >> 1], x);
-            }
-        float muse[2], corr[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-            const float mn = fmaxf(mrow[r], mx[r]);
-            muse[r] = mn == -INFINITY ? 0.f : mn;
-            corr[r] = exp2f(mrow[r] - muse[r]);
-            mrow[r] = mn;
-        }
-        float ls[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float p = exp2f(s[nt][e] - muse[e >> 1]);
-                s[nt][e] = p;
-                ls[e >> 1] += p;
-                oacc[nt][e] *= corr[e >> 1];
-            }
-        lrow[0] = lrow[0] * corr[0] + ls[0];
-        lrow[1] = lrow[1] * corr[1] + ls[1];
-        mm_cols(oacc, s, sV + buf * TILE);
-        __syncthreads();
-    }
-    bf16 *og = o + (int64_t)b * T * ors + h * HD;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        float l = lrow[r];
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        const int row = row0 + r * 8;
-        if (row < T) {
-            const float inv = 1.0f / l;
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-                *reinterpret_cast<uint32_t *>(og + (int64_t)row * ors + nt * 8 + 2 * t4) =
-                    pk(oacc[nt][2 * r] * inv, oacc[nt][2 * r + 1] * inv);
-            if (t4 == 0) lse[(int64_t)bh * T + row] = (mrow[r] + log2f(l)) * LN2;
-        }
-    }
 }
 
 // ----------------------------------------------------------------- backward: dQ (+ D)
@@ -389,17 +299,7 @@ static int smem_opt_in(const void *fn, int bytes) {
 int attention_forward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, bf16 *o, int64_t ors, float *lse,
                       int B, int T, int H, int hd, cudaStream_t st) {
     if (hd != HD || rs % 8 || ors % 8) return GPT2_ERR_BAD_SHAPE;
-    static bool init = false;
-    const int smem = 5 * TILE;
-    if (!init) {
-        if (int rc = smem_opt_in((const void *)fwd_kernel, smem)) return rc;
-        init = true;
-    }
-    const float sl2 = LOG2E / sqrtf((float)HD);
-    fwd_kernel<<<dim3((T + 63) / 64, B * H), NT, smem, st>>>(q, k, v, rs, o, ors, lse, T, H, sl2);
-    GPT2_CUDA_TRY(cudaGetLastError());
-    gpt2_note_launches(1);
-    return GPT2_OK;
+    return attention_forward_tc(q, k, v, rs, o, ors, lse, B, T, H, st);
 }
 
 int attention_backward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,

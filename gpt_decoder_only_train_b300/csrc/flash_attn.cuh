@@ -14,6 +14,10 @@ namespace fa {
 int attention_forward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, bf16 *o, int64_t ors, float *lse,
                       int B, int T, int H, int hd, cudaStream_t st);
 
+// tcgen05 implementation of attention_forward (attn_tc.cu).
+int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, bf16 *o, int64_t ors, float *lse,
+                         int B, int T, int H, cudaStream_t st);
+
 // dq/dk/dv (row stride rs) from O, dO (row stride ors) and lse; Dscr holds
 // D = rowsum(dO * O) as fp32 [B, H, T].
 int attention_backward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,

@@ -159,31 +159,38 @@ __global__ void ln_fwd_kernel(const T *__restrict__ x, const float *__restrict__
 template <typename T> static int ln_vpl(int C) {
     const int npk = C / Pack16<T>::N;
     const int per_lane = (npk + 31) / 32;
-    return per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 0;
+    return per_lane <= 8 ? per_lane : 0;
 }
+
+#define LN_VPL_SWITCH(VPLV, ...)                                         \
+    switch (VPLV) {                                                      \
+        case 1: { constexpr int V_ = 1; __VA_ARGS__; } break;            \
+        case 2: { constexpr int V_ = 2; __VA_ARGS__; } break;            \
+        case 3: { constexpr int V_ = 3; __VA_ARGS__; } break;            \
+        case 4: { constexpr int V_ = 4; __VA_ARGS__; } break;            \
+        case 5: { constexpr int V_ = 5; __VA_ARGS__; } break;            \
+        case 6: { constexpr int V_ = 6; __VA_ARGS__; } break;            \
+        case 7: { constexpr int V_ = 7; __VA_ARGS__; } break;            \
+        case 8: { constexpr int V_ = 8; __VA_ARGS__; } break;            \
+        default: return GPT2_ERR_BAD_SHAPE;                              \
+    }
 
 template <typename T>
 int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *mean, float *rstd, int N, int C,
                       cudaStream_t st) {
     if (C % Pack16<T>::N) return GPT2_ERR_BAD_SHAPE;
-    const int vpl = ln_vpl<T>(C);
     const int warps = 8, grid = ceil_div(N, warps);
-    switch (vpl) {
-        case 1: ln_fwd_kernel<T, 1><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C); break;
-        case 2: ln_fwd_kernel<T, 2><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C); break;
-        case 4: ln_fwd_kernel<T, 4><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C); break;
-        case 8: ln_fwd_kernel<T, 8><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C); break;
-        default: return GPT2_ERR_BAD_SHAPE;
-    }
+    LN_VPL_SWITCH(ln_vpl<T>(C), ln_fwd_kernel<T, V_><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C))
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
 }
 
-// dx = rstd (dy*g - mean(dy*g) - xhat mean(dy*g*xhat)).  dg/db: every warp
-// accumulates its rows into its own shared-memory slice (layout [e][packet], so
-// a lane owns its columns and the 32 lanes hit 32 banks); at the end the block
-// sums the warp slices in a fixed order and adds them to the fp32 gradients.
+// dx = rstd (dy*g - mean(dy*g) - xhat mean(dy*g*xhat)).  Each lane keeps the
+// dg/db partial sums of its columns in registers over the rows its warp
+// handles (VPL is the exact packet count per lane); at the end the warps add
+// their partials into shared memory and the block adds those to the fp32
+// gradients.
 template <typename T, int VPL>
 __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ x,
                                                         const float *__restrict__ mean,
@@ -191,12 +198,15 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
                                                         const T *dres_in, T *dres_out, float *__restrict__ dg,
                                                         float *__restrict__ db, int N, int C) {
     constexpr int E = Pack16<T>::N;
-    extern __shared__ float sh[];  // [warps][2][E][npk]
+    extern __shared__ float sh[];  // [2C]
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, warps = blockDim.x >> 5;
     const int npk = C / E;
-    for (int i = threadIdx.x; i < warps * 2 * C; i += blockDim.x) sh[i] = 0.f;
-    __syncthreads();
-    float *sdg = sh + wid * 2 * C, *sdb = sdg + C;
+    for (int i = threadIdx.x; i < 2 * C; i += blockDim.x) sh[i] = 0.f;
+    float adg[VPL][E], adb[VPL][E];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+#pragma unroll
+        for (int e = 0; e < E; ++e) adg[i][e] = adb[i][e] = 0.f;
     for (int row = blockIdx.x * warps + wid; row < N; row += gridDim.x * warps) {
         const int64_t off = (int64_t)row * C;
         Pack16<T> vdy[VPL], vx[VPL];
@@ -208,17 +218,23 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
             if (p < npk) {
                 vdy[i].load_stream(dy + off + p * E);
                 vx[i].load_stream(x + off + p * E);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
                 F4x<E> gg;
                 gg.load(g + p * E);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const float d = vdy[i].get(e);
-                    const float dxh = d * gg.v[e];
                     const float xh = (vx[i].get(e) - mu) * rs;
+                    const float dxh = d * gg.v[e];
                     s1 += dxh;
                     s2 += dxh * xh;
-                    sdg[e * npk + p] += d * xh;
-                    sdb[e * npk + p] += d;
+                    adg[i][e] = fmaf(d, xh, adg[i][e]);
+                    adb[i][e] += d;
                 }
             }
         }
@@ -242,15 +258,20 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
         }
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < C; c += blockDim.x) {
-        const int p = c / E, e = c % E, idx = e * npk + p;
-        float a = 0.f, bsum = 0.f;
-        for (int w = 0; w < warps; ++w) {
-            a += sh[w * 2 * C + idx];
-            bsum += sh[w * 2 * C + C + idx];
-        }
-        atomicAdd(dg + c, a);
-        atomicAdd(db + c, bsum);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int p = lane + 32 * i;
+        if (p < npk)
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                atomicAdd(&sh[p * E + e], adg[i][e]);
+                atomicAdd(&sh[C + p * E + e], adb[i][e]);
+            }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < C; i += blockDim.x) {
+        atomicAdd(dg + i, sh[i]);
+        atomicAdd(db + i, sh[C + i]);
     }
 }
 
@@ -266,21 +287,9 @@ int layernorm_backward(const T *dy, const T *x, const float *mean, const float *
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     }
     const int grid = std::max(1, std::min(ceil_div(N, warps * 4), sms * 2));
-    const size_t smem = (size_t)warps * 2 * C * sizeof(float);
-    static bool attr = false;
-    if (!attr) {  // up to 2 x 8 x 2 x 2048 floats per SM
-        for (auto fn : {(const void *)ln_bwd_kernel<T, 1>, (const void *)ln_bwd_kernel<T, 2>,
-                        (const void *)ln_bwd_kernel<T, 4>, (const void *)ln_bwd_kernel<T, 8>})
-            GPT2_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 8 * 2 * 2048 * 4));
-        attr = true;
-    }
-    switch (ln_vpl<T>(C)) {
-        case 1: ln_bwd_kernel<T, 1><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
-        case 2: ln_bwd_kernel<T, 2><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
-        case 4: ln_bwd_kernel<T, 4><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
-        case 8: ln_bwd_kernel<T, 8><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C); break;
-        default: return GPT2_ERR_BAD_SHAPE;
-    }
+    const size_t smem = 2 * C * sizeof(float);
+    LN_VPL_SWITCH(ln_vpl<T>(C), ln_bwd_kernel<T, V_><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in,
+                                                                                    dres_out, dg, db, N, C))
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
@@ -498,6 +507,116 @@ __global__ void __launch_bounds__(1024) classifier_reg_kernel(T *logits, const i
     }
 }
 
+// bf16 specialisation tuned for instruction count: bf16 pairs are unpacked
+// with integer shifts, only the packet that straddles V takes per-element
+// checks, and exp is evaluated once per logit: e = 2^(x log2e - M log2e) is
+// summed in fp32 and kept as bf16 in the row registers, then
+// dz = e * dscale / S.  The target logit's dz is recomputed in fp32 from the
+// logit itself (p_t - 1 loses no precision when p_t is close to 1).
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ uint32_t bf_pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <int NPK>
+__global__ void __launch_bounds__(1024) classifier_bf16_kernel(bf16 *logits, const int *__restrict__ targets,
+                                                               float *__restrict__ loss_rows, int N, int V, int Vp,
+                                                               float dscale, int *err) {
+    __shared__ float red_m[2][32], red_s[2][32];
+    const int npk = Vp >> 3;
+    const int full_pk = V >> 3;  // packets entirely below V
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const float L2E = 1.4426950408889634f;
+    int par = 0;
+    for (int row = blockIdx.x; row < N; row += gridDim.x, par ^= 1) {
+        bf16 *z = logits + (int64_t)row * Vp;
+        int tg = targets[row];
+        const bool bad = tg < 0 || tg >= V;
+        if (bad) tg = 0;
+        uint4 v[NPK];
+        float m = -INFINITY, zt = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPK; ++i) {
+            const int p = threadIdx.x + i * blockDim.x;
+            if (p < npk) {
+                v[i] = __ldcs(reinterpret_cast<const uint4 *>(z) + p);
+                const uint32_t *u = &v[i].x;
+                if (p == (tg >> 3)) {  // keep the target logit itself (fp32 of its bf16 value)
+                    const int k = (tg & 7) >> 1;
+                    const uint32_t w = k == 0 ? v[i].x : k == 1 ? v[i].y : k == 2 ? v[i].z : v[i].w;
+                    zt = (tg & 1) ? bf_hi(w) : bf_lo(w);
+                }
+                if (p < full_pk) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) m = fmaxf(m, fmaxf(bf_lo(u[k]), bf_hi(u[k])));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (p * 8 + 2 * k < V) m = fmaxf(m, bf_lo(u[k]));
+                        if (p * 8 + 2 * k + 1 < V) m = fmaxf(m, bf_hi(u[k]));
+                    }
+                }
+            }
+        }
+        m = warp_max(m);
+        if (lane == 0) red_m[par][wid] = m;
+        __syncthreads();
+        float M = red_m[par][0];
+        for (int w = 1; w < nw; ++w) M = fmaxf(M, red_m[par][w]);
+        const float Mc = M * L2E;
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPK; ++i) {
+            const int p = threadIdx.x + i * blockDim.x;
+            if (p < npk) {
+                uint32_t *u = &v[i].x;
+                if (p < full_pk) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float a = exp2f(fmaf(bf_lo(u[k]), L2E, -Mc));
+                        const float b = exp2f(fmaf(bf_hi(u[k]), L2E, -Mc));
+                        s += a + b;
+                        u[k] = bf_pack(a, b);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = p * 8 + 2 * k;
+                        const float a = c < V ? exp2f(fmaf(bf_lo(u[k]), L2E, -Mc)) : 0.f;
+                        const float b = c + 1 < V ? exp2f(fmaf(bf_hi(u[k]), L2E, -Mc)) : 0.f;
+                        s += a + b;
+                        u[k] = bf_pack(a, b);
+                    }
+                }
+            }
+        }
+        s = warp_sum(s);
+        if (lane == 0) red_s[par][wid] = s;
+        __syncthreads();
+        float S = 0.f;
+        for (int w = 0; w < nw; ++w) S += red_s[par][w];
+        const float lse = M + logf(S);
+        const float scale = dscale / S;
+#pragma unroll
+        for (int i = 0; i < NPK; ++i) {
+            const int p = threadIdx.x + i * blockDim.x;
+            if (p < npk) {
+                uint32_t *u = &v[i].x;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) u[k] = bf_pack(bf_lo(u[k]) * scale, bf_hi(u[k]) * scale);
+                reinterpret_cast<uint4 *>(z)[p] = v[i];
+            }
+        }
+        if (threadIdx.x == (tg >> 3) % blockDim.x) {  // this thread loaded and stored the target's packet
+            loss_rows[row] = lse - zt;
+            z[tg] = __float2bfloat16_rn((__expf(zt - lse) - 1.0f) * dscale);
+            if (bad) raise_device_error(err, DEVERR_BAD_TOKEN);
+        }
+    }
+}
+
 template <typename T>
 int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, int Vp, float dscale, int *err,
                cudaStream_t st) {
@@ -507,6 +626,21 @@ int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, in
     const int threads = std::min(1024, (npk + 31) / 32 * 32);
     const int npt = ceil_div(npk, threads);
     const int grid = std::min(N, 148 * 2);
+    if constexpr (sizeof(T) == 2) {
+        bf16 *lg = reinterpret_cast<bf16 *>(logits);
+        switch (npt <= 1 ? 1 : npt <= 2 ? 2 : npt <= 4 ? 4 : npt <= 7 ? 7 : npt <= 8 ? 8 : 0) {
+            case 1: classifier_bf16_kernel<1><<<grid, threads, 0, st>>>(lg, targets, loss_rows, N, V, Vp, dscale, err); break;
+            case 2: classifier_bf16_kernel<2><<<grid, threads, 0, st>>>(lg, targets, loss_rows, N, V, Vp, dscale, err); break;
+            case 4: classifier_bf16_kernel<4><<<grid, threads, 0, st>>>(lg, targets, loss_rows, N, V, Vp, dscale, err); break;
+            case 7: classifier_bf16_kernel<7><<<grid, threads, 0, st>>>(lg, targets, loss_rows, N, V, Vp, dscale, err); break;
+            case 8: classifier_bf16_kernel<8><<<grid, threads, 0, st>>>(lg, targets, loss_rows, N, V, Vp, dscale, err); break;
+            default: classifier_kernel<T><<<std::min(N, 148 * 8), 512, 0, st>>>(logits, targets, loss_rows, N, V, Vp,
+                                                                               dscale, err);
+        }
+        GPT2_CUDA_TRY(cudaGetLastError());
+        gpt2_note_launches(1);
+        return GPT2_OK;
+    }
     switch (npt <= 1 ? 1 : npt <= 2 ? 2 : npt <= 4 ? 4 : npt <= 8 ? 8 : 0) {
         case 1: classifier_reg_kernel<T, 1><<<grid, threads, 0, st>>>(logits, targets, loss_rows, N, V, Vp, dscale, err); break;
         case 2: classifier_reg_kernel<T, 2><<<grid, threads, 0, st>>>(logits, targets, loss_rows, N, V, Vp, dscale, err); break;

@@ -14,8 +14,10 @@
 //             issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide k slice,
 //             committing each ring slot back to the producer and each finished
 //             accumulator to the epilogue;
-//   warps 2-5 epilogue: tcgen05.ld 32 lanes x 32 columns at a time, fused
-//             bias / residual / GELU / GELU' / fp32 accumulate, 16-byte stores.
+//   warps 2-9 epilogue: two warps per TMEM lane quadrant, each reading half of
+//             the tile's columns with tcgen05.ld (32 lanes x 32 columns, two
+//             loads in flight), fused bias / residual / GELU / GELU' / fp32
+//             accumulate, 16-byte stores.
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
 // Operands may be K-major (k contiguous) or MN-major (m or n contiguous), which
 // covers Y = X W^T, dX = dY W and dW = dY^T X without transposes.
@@ -34,7 +36,8 @@ constexpr int BM = 128;            // rows of a tile = TMEM lanes
 constexpr int BK = 64;             // 64 bf16 = one 128-byte swizzle row
 constexpr int A_STAGE_BYTES = BM * BK * 2;
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN-major TMA box (64 k rows x 128 B)
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quadrant, each owning half the tile's columns
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s: far above any legitimate wait
 
 struct Params {
@@ -106,6 +109,13 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, uint64_t *bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 4);
+            mbar_init(&tempty[a], EPI_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -405,8 +415,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_drain(drain, 0);
         }
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
-        const int quad = warp & 3;  // TMEM lanes this warp may access
+        // ---------------- epilogue (warps 2..9) ----------------
+        const int quad = warp & 3;                        // TMEM lanes this warp may access
+        const int col_half = (warp - 2) >> 2;             // which half of the tile's columns
+        constexpr int HALF = BN / 2;
         int t = 0;
         for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++t) {
             const int tile = w / P.splits;
@@ -416,18 +428,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!mbar_wait(&tfull[acc], aph, abort_flag, P.err)) break;
             tc_fence_after();
             const int row = m0 + quad * 32 + lane;
-            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+            const int c_begin = col_half * HALF;
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + c_begin);
+            if constexpr (HALF >= 64) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(tbase + c0, r);
-                tmem_ld_wait();
-                if (c0 + 32 == BN) {  // accumulator fully read: hand it back to the MMA warp
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                for (int c0 = 0; c0 < HALF; c0 += 64) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tbase + c0, r0);
+                    tmem_ld32(tbase + c0 + 32, r1);
+                    tmem_ld_wait();
+                    if (c0 + 64 == HALF) {  // this warp's part of the accumulator is read: release it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[acc]);
+                    }
+                    const int col = n0 + c_begin + c0;
+                    if (col < P.N) epilogue_chunk(P, row, col, r0);
+                    if (col + 32 < P.N) epilogue_chunk(P, row, col + 32, r1);
                 }
-                if (n0 + c0 < P.N) epilogue_chunk(P, row, n0 + c0, r);
+            } else {
+                uint32_t r0[32];
+                tmem_ld32(tbase, r0);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+                const int col = n0 + c_begin;
+                if (col < P.N) epilogue_chunk(P, row, col, r0);
             }
         }
     }
