@@ -1,6 +1,6 @@
 // Flash-style causal attention for head dimension 64, bf16 in / out, fp32
-// softmax statistics.  The T x T score matrix is never stored: scores live in
-// registers one 64 x 64 block at a time ("Let's reproduce GPT-2 (124M)",
+// softmax statistics, on the tcgen05 tensor cores.  The T x T score matrix is
+// never stored: scores live in TMEM one block at a time ("Let's reproduce GPT-2 (124M)",
 // §Video özeti: flash attention; "Let's build GPT: from scratch", 01:02:00 and
 // 01:16:56: causal self-attention scaled by 1/sqrt(head_size)).
 #pragma once
@@ -17,6 +17,11 @@ int attention_forward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, b
 // tcgen05 implementation of attention_forward (attn_tc.cu).
 int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, bf16 *o, int64_t ors, float *lse,
                          int B, int T, int H, cudaStream_t st);
+
+// tcgen05 implementation of attention_backward (attn_tc.cu).
+int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
+                          int64_t ors, const float *lse, bf16 *dq, bf16 *dk, bf16 *dv, float *Dscr, int B, int T,
+                          int H, cudaStream_t st);
 
 // dq/dk/dv (row stride rs) from O, dO (row stride ors) and lse; Dscr holds
 // D = rowsum(dO * O) as fp32 [B, H, T].
