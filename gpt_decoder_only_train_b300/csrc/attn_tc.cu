@@ -47,6 +47,14 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&f)[32]) {
     for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
 }
 
+// 2^x with the hardware approximation (MUFU.EX2, flush-to-zero): the results
+// feed bf16 operands and fp32 sums whose error budget is far above its ~2 ulp.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 struct Bars {
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(NT, 2)
         auto fold_o = [&](int j) -> bool {   // acc = acc * 2^(m_acc - m_pend) + O_j (this thread's 32 columns)
             if (!mbar_wait(&bar->o_full, j & 1, abort_flag, nullptr)) return false;
             tc_fence_after();
-            const float c = exp2f(m_acc - m_pend);
+            const float c = ex2(m_acc - m_pend);
             float f[32];
             tmem_ld32f(tO + lane_off + half * 32, f);
 #pragma unroll
@@ -229,7 +237,7 @@ __global__ void __launch_bounds__(NT, 2)
             if (!ok) continue;
             const float m_new = fmaxf(m, mx);
             const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-            const float corr = exp2f(m - mu);
+            const float corr = ex2(m - mu);
             // O_{j-1} is complete once PV_{j-1} has finished reading P: fold it
             // before P is overwritten.
             if (j > 0 && !(ok = fold_o(j - 1))) continue;
@@ -243,8 +251,8 @@ __global__ void __launch_bounds__(NT, 2)
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    float p0 = exp2f(fmaf(f[i], sl2, -mu));
-                    float p1 = exp2f(fmaf(f[i + 1], sl2, -mu));
+                    float p0 = ex2(fmaf(f[i], sl2, -mu));
+                    float p1 = ex2(fmaf(f[i + 1], sl2, -mu));
                     if (masked_block) {
                         p0 = c0 + i <= lim ? p0 : 0.f;
                         p1 = c0 + i + 1 <= lim ? p1 : 0.f;
@@ -471,6 +479,9 @@ __global__ void __launch_bounds__(NT, 2)
             if (!(ok = mbar_wait(&bar->sp_full, j & 1, abort_flag, nullptr))) break;
             tc_fence_after();
             uint32_t w[2][8];
+            // visible keys of this thread's 32: columns c <= lim (key <= q and key < T; none if q >= T)
+            const int lim = q < T ? min(q, T - 1) - (j * dq::BK + half * 32) : -1;
+            const bool full = lim >= 31;
 #pragma unroll
             for (int c0 = 0; c0 < 32; c0 += 16) {
                 float sv[16], dp[16];
@@ -478,10 +489,12 @@ __global__ void __launch_bounds__(NT, 2)
                 tmem_ld16f(tdP + lane_off + half * 32 + c0, dp);
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
-                    const int key = j * dq::BK + half * 32 + c0 + i;
-                    const bool v0 = key <= q && key < T && q < T, v1 = key + 1 <= q && key + 1 < T && q < T;
-                    const float p0 = v0 ? exp2f(fmaf(sv[i], sl2, -l2)) : 0.f;
-                    const float p1 = v1 ? exp2f(fmaf(sv[i + 1], sl2, -l2)) : 0.f;
+                    float p0 = ex2(fmaf(sv[i], sl2, -l2));
+                    float p1 = ex2(fmaf(sv[i + 1], sl2, -l2));
+                    if (!full) {
+                        p0 = c0 + i <= lim ? p0 : 0.f;
+                        p1 = c0 + i + 1 <= lim ? p1 : 0.f;
+                    }
                     w[c0 >> 4][i >> 1] = pack_bf16x2(p0 * (dp[i] - Dq), p1 * (dp[i + 1] - Dq));
                 }
             }
@@ -674,20 +687,33 @@ __global__ void __launch_bounds__(NT, 2)
             if (!ok) continue;
             tc_fence_after();
             uint32_t wp[2][8], wd[2][8];
-            const int qbase = (q0blk + it) * dkv::BQ;
+            const int qbase = (q0blk + it) * dkv::BQ + half * 32;
+            // visible queries of this thread's 32: lo <= c <= hi (q >= key, q < T; none if key >= T)
+            const int lo = key - qbase, hi = key < T ? T - 1 - qbase : -1;
+            const bool full = lo <= 0 && hi >= 31;
 #pragma unroll
             for (int c0 = 0; c0 < 32; c0 += 16) {
-                float st[16], dpt[16];
+                float st[16], dpt[16], lv[16], dv[16];
                 tmem_ld16f(tSt + lane_off + half * 32 + c0, st);
                 tmem_ld16f(tdPt + lane_off + half * 32 + c0, dpt);
 #pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(L + half * 32 + c0 + i);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(Dv + half * 32 + c0 + i);
+                    lv[i] = a.x; lv[i + 1] = a.y; lv[i + 2] = a.z; lv[i + 3] = a.w;
+                    dv[i] = d4.x; dv[i + 1] = d4.y; dv[i + 2] = d4.z; dv[i + 3] = d4.w;
+                }
+#pragma unroll
                 for (int i = 0; i < 16; i += 2) {
-                    const int c = half * 32 + c0 + i, q = qbase + c;
-                    const bool v0 = q >= key && q < T && key < T, v1 = q + 1 >= key && q + 1 < T && key < T;
-                    const float p0 = v0 ? exp2f(fmaf(st[i], sl2, -L[c])) : 0.f;
-                    const float p1 = v1 ? exp2f(fmaf(st[i + 1], sl2, -L[c + 1])) : 0.f;
+                    float p0 = ex2(fmaf(st[i], sl2, -lv[i]));
+                    float p1 = ex2(fmaf(st[i + 1], sl2, -lv[i + 1]));
+                    if (!full) {
+                        const int c = c0 + i;
+                        p0 = (c >= lo && c <= hi) ? p0 : 0.f;
+                        p1 = (c + 1 >= lo && c + 1 <= hi) ? p1 : 0.f;
+                    }
                     wp[c0 >> 4][i >> 1] = pack_bf16x2(p0, p1);
-                    wd[c0 >> 4][i >> 1] = pack_bf16x2(p0 * (dpt[i] - Dv[c]), p1 * (dpt[i + 1] - Dv[c + 1]));
+                    wd[c0 >> 4][i >> 1] = pack_bf16x2(p0 * (dpt[i] - dv[i]), p1 * (dpt[i + 1] - dv[i + 1]));
                 }
             }
             tc_fence_before();

@@ -86,6 +86,10 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     }
     P.k_blocks_per_split = ceil_div(P.num_k_blocks, P.splits);
     P.splits = ceil_div(P.num_k_blocks, P.k_blocks_per_split);
+    // raster: share the A block across concurrent tiles when A is far larger than L2
+    // and B is not (A would otherwise stream from HBM once per N block)
+    const double a_bytes = 2.0 * g.M * g.K, b_bytes = 2.0 * g.N * g.K;
+    P.n_fastest = (P.num_n_blocks <= 8 && a_bytes > 256e6 && b_bytes < 96e6) ? 1 : 0;
     P.epi = g.epi;
     P.alpha = g.alpha;
     P.bias = g.bias;

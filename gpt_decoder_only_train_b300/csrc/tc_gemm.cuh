@@ -44,6 +44,7 @@ struct Params {
     int M, N, K;
     int num_m_blocks, num_n_blocks, num_k_blocks;
     int splits, k_blocks_per_split;
+    int n_fastest;  // tile raster: 1 = consecutive tiles share the A block (A is the large operand)
     int epi;
     float alpha;
     const float *bias;
@@ -191,6 +192,16 @@ struct SmemLayout {
     static constexpr int TOTAL = 1024 /*alignment slack*/ + BAR_OFFSET + BAR_BYTES;
 };
 
+// Tile raster: m-fastest keeps one B block shared by the concurrently running
+// tiles; n-fastest keeps one A block shared (used when A is the operand too
+// large for L2 and N has few blocks, e.g. the LM-head backward over dlogits).
+__device__ __forceinline__ int tile_m(const Params &P, int tile) {
+    return P.n_fastest ? tile / P.num_n_blocks : tile % P.num_m_blocks;
+}
+__device__ __forceinline__ int tile_n(const Params &P, int tile) {
+    return P.n_fastest ? tile % P.num_n_blocks : tile / P.num_m_blocks;
+}
+
 // ---- epilogue -----------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -328,7 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int w = blockIdx.x; w < num_work && ok; w += gridDim.x) {
                 const int split = w % P.splits, tile = w / P.splits;
-                const int m0 = (tile % P.num_m_blocks) * BM, n0 = (tile / P.num_m_blocks) * BN;
+                const int m0 = tile_m(P, tile) * BM, n0 = tile_n(P, tile) * BN;
                 const int kb0 = split * P.k_blocks_per_split;
                 const int kb1 = min(P.num_k_blocks, kb0 + P.k_blocks_per_split);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -422,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int t = 0;
         for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++t) {
             const int tile = w / P.splits;
-            const int m0 = (tile % P.num_m_blocks) * BM, n0 = (tile / P.num_m_blocks) * BN;
+            const int m0 = tile_m(P, tile) * BM, n0 = tile_n(P, tile) * BN;
             const int acc = t & 1;
             const uint32_t aph = (t >> 1) & 1;
             if (!mbar_wait(&tfull[acc], aph, abort_flag, P.err)) break;
