@@ -183,11 +183,14 @@ __host__ __device__ constexpr uint32_t instr_desc(int bn, bool a_mn, bool b_mn) 
            ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
+constexpr int EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16
+
 template <int BN, int STAGES>
 struct SmemLayout {
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_WARPS * EPI_STAGE_BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
     static constexpr int TOTAL = 1024 /*alignment slack*/ + BAR_OFFSET + BAR_BYTES;
 };
@@ -282,6 +285,96 @@ __device__ __forceinline__ void epilogue_chunk(const Params &P, int row, int col
             og.w = pack_bf16x2(y[6], y[7]);
             *reinterpret_cast<uint4 *>(P.D2 + (int64_t)row * P.ldd + col) = og;
         }
+    }
+}
+
+// ---- staged bf16 epilogue: 32 rows x 64 columns per warp ------------------------
+// Each lane owns one row in TMEM order; the warp's tile passes through a
+// swizzled shared-memory block so that global loads (residual / h) and stores
+// are whole 128-byte row segments instead of 16 bytes from 32 different rows.
+__device__ __forceinline__ uint4 *stage_at(uint8_t *stage, int row, int chunk) {
+    return reinterpret_cast<uint4 *>(stage + row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void stage_load(uint8_t *stage, const bf16 *g, int64_t ld, int row0, int col0, int M, int N,
+                                           int lane) {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int rr = it * 4 + (lane >> 3), ch = lane & 7;
+        const int row = row0 + rr, col = col0 + ch * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < M && col < N) v = *reinterpret_cast<const uint4 *>(g + (int64_t)row * ld + col);
+        *stage_at(stage, rr, ch) = v;
+    }
+}
+
+__device__ __forceinline__ void stage_store(uint8_t *stage, bf16 *g, int64_t ld, int row0, int col0, int M, int N,
+                                            int lane) {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int rr = it * 4 + (lane >> 3), ch = lane & 7;
+        const int row = row0 + rr, col = col0 + ch * 8;
+        if (row < M && col < N) *reinterpret_cast<uint4 *>(g + (int64_t)row * ld + col) = *stage_at(stage, rr, ch);
+    }
+}
+
+// 64 accumulator columns (two 32-column TMEM loads) of the warp's 32 rows -> bf16
+// outputs with the fused epilogue; row0 is the warp's first row, col0 the group's
+// first column.
+__device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage, int row0, int col0, int lane,
+                                                 const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+    float x[64];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        x[i] = __uint_as_float(r0[i]) * P.alpha;
+        x[32 + i] = __uint_as_float(r1[i]) * P.alpha;
+    }
+    if (P.bias && P.epi != GPT2_EPI_GELU_BWD) {
+#pragma unroll
+        for (int i = 0; i < 64; i += 4) {
+            float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (col0 + i < P.N) b = *reinterpret_cast<const float4 *>(P.bias + col0 + i);
+            x[i] += b.x; x[i + 1] += b.y; x[i + 2] += b.z; x[i + 3] += b.w;
+        }
+    }
+    if (P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD) {
+        stage_load(stage, P.R, P.ldd, row0, col0, P.M, P.N, lane);
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v = *stage_at(stage, lane, c);
+            const bf16 *rb = reinterpret_cast<const bf16 *>(&v);
+            if (P.epi == GPT2_EPI_RESIDUAL) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[c * 8 + i] += __bfloat162float(rb[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[c * 8 + i] *= gelu_tanh_grad(__bfloat162float(rb[i]));
+            }
+        }
+        __syncwarp();
+    }
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) *stage_at(stage, lane, c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    __syncwarp();
+    stage_store(stage, reinterpret_cast<bf16 *>(P.D), P.ldd, row0, col0, P.M, P.N, lane);
+    __syncwarp();
+    if (P.epi == GPT2_EPI_GELU) {
+        // GELU of the bf16-rounded pre-activation (a recompute from stored h matches bit for bit)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+            w[i] = pack_bf16x2(gelu_tanh(__low2float(hv)), gelu_tanh(__high2float(hv)));
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *stage_at(stage, lane, c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        __syncwarp();
+        stage_store(stage, P.D2, P.ldd, row0, col0, P.M, P.N, lane);
+        __syncwarp();
     }
 }
 
@@ -429,6 +522,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------- epilogue (warps 2..9) ----------------
         const int quad = warp & 3;                        // TMEM lanes this warp may access
         const int col_half = (warp - 2) >> 2;             // which half of the tile's columns
+        uint8_t *stage = smem + Lay::EPI_OFFSET + (warp - 2) * EPI_STAGE_BYTES;
         constexpr int HALF = BN / 2;
         int t = 0;
         for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++t) {
@@ -454,8 +548,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (lane == 0) mbar_arrive(&tempty[acc]);
                     }
                     const int col = n0 + c_begin + c0;
-                    if (col < P.N) epilogue_chunk(P, row, col, r0);
-                    if (col + 32 < P.N) epilogue_chunk(P, row, col + 32, r1);
+                    if (P.epi == GPT2_EPI_ACCUM_F32) {
+                        if (col < P.N) epilogue_chunk(P, row, col, r0);
+                        if (col + 32 < P.N) epilogue_chunk(P, row, col + 32, r1);
+                    } else if (col < P.N) {
+                        epilogue_group64(P, stage, m0 + quad * 32, col, lane, r0, r1);
+                    }
                 }
             } else {
                 uint32_t r0[32];
