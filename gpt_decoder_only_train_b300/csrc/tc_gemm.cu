@@ -33,9 +33,8 @@ int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer
     return r == CUDA_SUCCESS ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, int STAGES, bool A_MN, bool B_MN>
 static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params &P, int grid, cudaStream_t st) {
-    constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
     using Lay = SmemLayout<BN, STAGES>;
     auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN>;
     static bool attr_set = false;
@@ -49,13 +48,13 @@ static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params
     return GPT2_OK;
 }
 
-template <int BN>
+template <int BN, int STAGES>
 static int dispatch_major(bool a_mn, bool b_mn, const CUtensorMap &ta, const CUtensorMap &tb, const Params &P,
                           int grid, cudaStream_t st) {
-    if (!a_mn && !b_mn) return launch_one<BN, false, false>(ta, tb, P, grid, st);
-    if (!a_mn && b_mn) return launch_one<BN, false, true>(ta, tb, P, grid, st);
-    if (a_mn && b_mn) return launch_one<BN, true, true>(ta, tb, P, grid, st);
-    return launch_one<BN, true, false>(ta, tb, P, grid, st);
+    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false>(ta, tb, P, grid, st);
+    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true>(ta, tb, P, grid, st);
+    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true>(ta, tb, P, grid, st);
+    return launch_one<BN, STAGES, true, false>(ta, tb, P, grid, st);
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -108,9 +107,15 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;
     const int grid = std::min(num_work, num_sms);
     const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
-    if (BN == 256) return dispatch_major<256>(a_mn, b_mn, ta, tb, P, grid, stream);
-    if (BN == 128) return dispatch_major<128>(a_mn, b_mn, ta, tb, P, grid, stream);
-    return dispatch_major<64>(a_mn, b_mn, ta, tb, P, grid, stream);
+    const bool reads_r = g.epi == GPT2_EPI_RESIDUAL || g.epi == GPT2_EPI_GELU_BWD;
+    if (BN == 256) {
+        // operand-reading epilogues (only K-major A, as the model uses them) trade a ring stage for prefetch
+        if (reads_r && !a_mn) return b_mn ? launch_one<256, 3, false, true>(ta, tb, P, grid, stream)
+                                          : launch_one<256, 3, false, false>(ta, tb, P, grid, stream);
+        return dispatch_major<256, 4>(a_mn, b_mn, ta, tb, P, grid, stream);
+    }
+    if (BN == 128) return dispatch_major<128, 6>(a_mn, b_mn, ta, tb, P, grid, stream);
+    return dispatch_major<64, 8>(a_mn, b_mn, ta, tb, P, grid, stream);
 }
 
 }  // namespace tcg

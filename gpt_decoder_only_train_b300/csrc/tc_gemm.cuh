@@ -185,12 +185,17 @@ __host__ __device__ constexpr uint32_t instr_desc(int bn, bool a_mn, bool b_mn) 
 
 constexpr int EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16
 
+// Epilogues that read a second operand (residual, GELU input) run with a
+// 3-deep ring so that each epilogue warp gets a second staging block: the next
+// 32 x 64 block of that operand is fetched (cp.async) while the current one is
+// being computed and stored.
 template <int BN, int STAGES>
 struct SmemLayout {
     static constexpr int B_STAGE_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int EPI_BUFS = STAGES == 3 ? 2 : 1;
     static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
-    static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_WARPS * EPI_STAGE_BYTES;
+    static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_WARPS * EPI_BUFS * EPI_STAGE_BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
     static constexpr int TOTAL = 1024 /*alignment slack*/ + BAR_OFFSET + BAR_BYTES;
 };
@@ -318,11 +323,31 @@ __device__ __forceinline__ void stage_store(uint8_t *stage, bf16 *g, int64_t ld,
     }
 }
 
+// Asynchronous version of stage_load (cp.async, 16 bytes per lane per step,
+// zero fill outside [M, N)); complete it with cp_async_wait_all + __syncwarp.
+__device__ __forceinline__ void stage_prefetch(uint8_t *stage, const bf16 *g, int64_t ld, int row0, int col0, int M,
+                                               int N, int lane) {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int rr = it * 4 + (lane >> 3), ch = lane & 7;
+        const int row = row0 + rr, col = col0 + ch * 8;
+        const bool ok = row < M && col < N;
+        const bf16 *src = ok ? g + (int64_t)row * ld + col : g;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(stage_at(stage, rr, ch))),
+                     "l"(src), "r"(ok ? 16 : 0)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // 64 accumulator columns (two 32-column TMEM loads) of the warp's 32 rows -> bf16
 // outputs with the fused epilogue; row0 is the warp's first row, col0 the group's
 // first column.
-__device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage, int row0, int col0, int lane,
-                                                 const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+// rstage: if non-null, the block of R for this group is already being fetched
+// there (stage_prefetch); otherwise R is loaded through `stage`.
+__device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage, uint8_t *rstage, int row0, int col0,
+                                                 int lane, const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
     float x[64];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -338,11 +363,17 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage
         }
     }
     if (P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD) {
-        stage_load(stage, P.R, P.ldd, row0, col0, P.M, P.N, lane);
+        uint8_t *rs = rstage;
+        if (rs) {
+            cp_async_wait_all();
+        } else {
+            rs = stage;
+            stage_load(rs, P.R, P.ldd, row0, col0, P.M, P.N, lane);
+        }
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const uint4 v = *stage_at(stage, lane, c);
+            const uint4 v = *stage_at(rs, lane, c);
             const bf16 *rb = reinterpret_cast<const bf16 *>(&v);
             if (P.epi == GPT2_EPI_RESIDUAL) {
 #pragma unroll
@@ -522,8 +553,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------- epilogue (warps 2..9) ----------------
         const int quad = warp & 3;                        // TMEM lanes this warp may access
         const int col_half = (warp - 2) >> 2;             // which half of the tile's columns
-        uint8_t *stage = smem + Lay::EPI_OFFSET + (warp - 2) * EPI_STAGE_BYTES;
+        uint8_t *stage = smem + Lay::EPI_OFFSET + (warp - 2) * Lay::EPI_BUFS * EPI_STAGE_BYTES;
         constexpr int HALF = BN / 2;
+        if (Lay::EPI_BUFS > 1 && (P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD) &&
+            (int)blockIdx.x < num_work) {
+            const int t0 = blockIdx.x / P.splits;
+            const int ncol = tile_n(P, t0) * BN + col_half * HALF;
+            if (ncol < P.N)
+                stage_prefetch(stage + EPI_STAGE_BYTES, P.R, P.ldd, tile_m(P, t0) * BM + quad * 32, ncol, P.M, P.N,
+                               lane);
+        }
         int t = 0;
         for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++t) {
             const int tile = w / P.splits;
@@ -536,8 +575,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int c_begin = col_half * HALF;
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + c_begin);
             if constexpr (HALF >= 64) {
+                const bool need_r = P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD;
+                uint8_t *rstage = (Lay::EPI_BUFS > 1 && need_r) ? stage + EPI_STAGE_BYTES : nullptr;
+                const int row0 = m0 + quad * 32;
 #pragma unroll 1
                 for (int c0 = 0; c0 < HALF; c0 += 64) {
+                    const int col = n0 + c_begin + c0;
                     uint32_t r0[32], r1[32];
                     tmem_ld32(tbase + c0, r0);
                     tmem_ld32(tbase + c0 + 32, r1);
@@ -547,12 +590,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&tempty[acc]);
                     }
-                    const int col = n0 + c_begin + c0;
                     if (P.epi == GPT2_EPI_ACCUM_F32) {
                         if (col < P.N) epilogue_chunk(P, row, col, r0);
                         if (col + 32 < P.N) epilogue_chunk(P, row, col + 32, r1);
                     } else if (col < P.N) {
-                        epilogue_group64(P, stage, m0 + quad * 32, col, lane, r0, r1);
+                        epilogue_group64(P, stage, rstage, row0, col, lane, r0, r1);
+                    }
+                    // fetch the operand block of the next group (this tile or the next one)
+                    if (rstage) {
+                        __syncwarp();
+                        int nrow0 = row0, ncol = col + 64;
+                        if (c0 + 64 == HALF) {
+                            const int wn = w + gridDim.x;
+                            if (wn < num_work) {
+                                const int tn = wn / P.splits;
+                                nrow0 = tile_m(P, tn) * BM + quad * 32;
+                                ncol = tile_n(P, tn) * BN + c_begin;
+                            } else {
+                                ncol = P.N;  // nothing left: no fetch
+                            }
+                        }
+                        if (ncol < P.N) stage_prefetch(rstage, P.R, P.ldd, nrow0, ncol, P.M, P.N, lane);
                     }
                 }
             } else {
