@@ -77,6 +77,8 @@ _SIGS = {
                                                 _P]),
     "gpt2_op_matmul": (_I, [_P, _I64, _I, _P, _I64, _I, _P, _P, _P, _I64, _P, _I, _I, _I, _I, _P]),
     "gpt2_op_classifier": (_I, [_P, _P, _P, _I, _I, _I, _F, _P]),
+    "gpt2_op_layernorm_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
+    "gpt2_op_layernorm_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
 }
 
 
@@ -285,6 +287,17 @@ def matmul(A, lda, a_kmajor, B, ldb, b_kmajor, D, ldd, M, N, K, epilogue=EPI_STO
     check("gpt2_op_matmul", lib().gpt2_op_matmul(
         _ptr(A), lda, int(a_kmajor), _ptr(B), ldb, int(b_kmajor), _ptr(D), _ptr(D2), _ptr(R), ldd, _ptr(bias),
         M, N, K, epilogue, _stream(stream)))
+
+
+def layernorm_forward(x, g, b, y, mean, rstd, N, C, stream=None):
+    check("gpt2_op_layernorm_forward", lib().gpt2_op_layernorm_forward(
+        _ptr(x), _ptr(g), _ptr(b), _ptr(y), _ptr(mean), _ptr(rstd), N, C, _stream(stream)))
+
+
+def layernorm_backward(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C, stream=None):
+    check("gpt2_op_layernorm_backward", lib().gpt2_op_layernorm_backward(
+        _ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(g), _ptr(dres_in), _ptr(dres_out), _ptr(dg), _ptr(db),
+        N, C, _stream(stream)))
 
 
 def classifier(logits, targets, loss_rows, N, V, Vp, dscale, stream=None):

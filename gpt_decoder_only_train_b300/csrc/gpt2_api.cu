@@ -807,6 +807,22 @@ extern "C" int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const vo
     return tcg::launch_gemm_tc(g, op_sms(), (cudaStream_t)stream);
 }
 
+extern "C" int gpt2_op_layernorm_forward(const void *x, const float *g, const float *b, void *y, float *mean,
+                                         float *rstd, int N, int C, void *stream) {
+    if (!x || !g || !b || !y || !mean || !rstd) return GPT2_ERR_BAD_ARG;
+    if (N <= 0 || C <= 0 || C % 8 || C > 2048) return GPT2_ERR_BAD_SHAPE;
+    return k::layernorm_forward<bf16>((const bf16 *)x, g, b, (bf16 *)y, mean, rstd, N, C, (cudaStream_t)stream);
+}
+
+extern "C" int gpt2_op_layernorm_backward(const void *dy, const void *x, const float *mean, const float *rstd,
+                                          const float *g, const void *dres_in, void *dres_out, float *dg, float *db,
+                                          int N, int C, void *stream) {
+    if (!dy || !x || !mean || !rstd || !g || !dres_out || !dg || !db) return GPT2_ERR_BAD_ARG;
+    if (N <= 0 || C <= 0 || C % 8 || C > 2048) return GPT2_ERR_BAD_SHAPE;
+    return k::layernorm_backward<bf16>((const bf16 *)dy, (const bf16 *)x, mean, rstd, g, (const bf16 *)dres_in,
+                                       (bf16 *)dres_out, dg, db, N, C, (cudaStream_t)stream);
+}
+
 extern "C" int gpt2_op_classifier(void *logits, const int32_t *targets, float *loss_rows, int N, int V, int Vp,
                                   float dscale, void *stream) {
     if (!logits || !targets || !loss_rows) return GPT2_ERR_BAD_ARG;

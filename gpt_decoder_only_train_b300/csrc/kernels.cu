@@ -617,6 +617,142 @@ __global__ void __launch_bounds__(1024) classifier_bf16_kernel(bf16 *logits, con
     }
 }
 
+// Shared-memory pipelined variant for large vocabularies: each row (Vp bf16)
+// arrives by one bulk asynchronous copy into one of two shared-memory
+// buffers, so the next row streams in while this one is reduced and written.
+// Per row: max (block reduction), e = 2^(x log2e - M log2e) summed in fp32 and
+// stored back as bf16 in place, then dz = e * dscale / S written with 16-byte
+// stores; the target logit is read before the overwrite and its dz recomputed
+// in fp32.
+constexpr int CLS_SMEM_THREADS = 1024;
+
+// 2^x with the hardware approximation (MUFU.EX2, flush-to-zero); the values
+// are stored as bf16 and summed in fp32, far above its error.
+__device__ __forceinline__ float ex2_hw(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t cls_su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__global__ void __launch_bounds__(CLS_SMEM_THREADS, 1)
+    classifier_smem_kernel(bf16 *logits, const int *__restrict__ targets, float *__restrict__ loss_rows, int N, int V,
+                           int Vp, int row_bytes_padded, float dscale, int *err) {
+    extern __shared__ __align__(128) uint8_t cls_smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(cls_smem + 2 * row_bytes_padded);
+    __shared__ float red_m[2][32], red_s[2][32];
+    const int npk = Vp >> 3;
+    const int full_pk = V >> 3;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const float L2E = 1.4426950408889634f;
+    const uint32_t row_bytes = (uint32_t)Vp * 2;
+    auto issue = [&](int row, int buf) {
+        const uint32_t b = cls_su32(&bar[buf]);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(row_bytes) : "memory");
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                cls_su32(cls_smem + buf * row_bytes_padded)),
+            "l"(logits + (int64_t)row * Vp), "r"(row_bytes), "r"(b)
+            : "memory");
+    };
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(cls_su32(&bar[0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(cls_su32(&bar[1])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if ((int)blockIdx.x < N) issue(blockIdx.x, 0);
+        if ((int)(blockIdx.x + gridDim.x) < N) issue(blockIdx.x + gridDim.x, 1);
+    }
+    __syncthreads();
+    int i = 0;
+    for (int row = blockIdx.x; row < N; row += gridDim.x, ++i) {
+        const int buf = i & 1;
+        uint4 *zs = reinterpret_cast<uint4 *>(cls_smem + buf * row_bytes_padded);
+        // wait for this row's copy (bounded: a copy that never lands flags a timeout)
+        {
+            const uint32_t b = cls_su32(&bar[buf]), par = (i >> 1) & 1;
+            uint32_t done = 0;
+            const uint64_t t0 = global_timer_ns();
+            while (true) {
+                asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                             "selp.u32 %0, 1, 0, p;\n\t}\n"
+                             : "=r"(done)
+                             : "r"(b), "r"(par)
+                             : "memory");
+                if (done) break;
+                if (global_timer_ns() - t0 > 2000000000ull) {
+                    raise_device_error(err, DEVERR_TIMEOUT);
+                    return;  // every thread of the block times out on the same copy
+                }
+            }
+        }
+        int tg = targets[row];
+        const bool bad = tg < 0 || tg >= V;
+        if (bad) tg = 0;
+        float m = -INFINITY;
+        for (int p = threadIdx.x; p < npk; p += blockDim.x) {
+            const uint4 v = zs[p];
+            const uint32_t *u = &v.x;
+            if (p < full_pk) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) m = fmaxf(m, fmaxf(bf_lo(u[k]), bf_hi(u[k])));
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (p * 8 + 2 * k < V) m = fmaxf(m, bf_lo(u[k]));
+                    if (p * 8 + 2 * k + 1 < V) m = fmaxf(m, bf_hi(u[k]));
+                }
+            }
+        }
+        const float zt = __bfloat162float(reinterpret_cast<const bf16 *>(zs)[tg]);
+        m = warp_max(m);
+        if (lane == 0) red_m[buf][wid] = m;
+        __syncthreads();  // (also: everyone has read zt before the in-place overwrite)
+        float M = red_m[buf][0];
+        for (int w = 1; w < nw; ++w) M = fmaxf(M, red_m[buf][w]);
+        const float Mc = M * L2E;
+        float sacc = 0.f;
+        for (int p = threadIdx.x; p < npk; p += blockDim.x) {
+            uint4 v = zs[p];
+            uint32_t *u = &v.x;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = p * 8 + 2 * k;
+                const float a = (p < full_pk || c < V) ? ex2_hw(fmaf(bf_lo(u[k]), L2E, -Mc)) : 0.f;
+                const float b2 = (p < full_pk || c + 1 < V) ? ex2_hw(fmaf(bf_hi(u[k]), L2E, -Mc)) : 0.f;
+                sacc += a + b2;
+                u[k] = bf_pack(a, b2);
+            }
+            zs[p] = v;
+        }
+        sacc = warp_sum(sacc);
+        if (lane == 0) red_s[buf][wid] = sacc;
+        __syncthreads();
+        float S = 0.f;
+        for (int w = 0; w < nw; ++w) S += red_s[buf][w];
+        const float lse = M + logf(S);
+        const float scale = dscale / S;
+        uint4 *zg = reinterpret_cast<uint4 *>(logits + (int64_t)row * Vp);
+        for (int p = threadIdx.x; p < npk; p += blockDim.x) {
+            uint4 v = zs[p];
+            uint32_t *u = &v.x;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) u[k] = bf_pack(bf_lo(u[k]) * scale, bf_hi(u[k]) * scale);
+            if (p == (tg >> 3)) {  // the target's dz from the logit itself, in fp32
+                bf16 *e8 = reinterpret_cast<bf16 *>(&v);
+                e8[tg & 7] = __float2bfloat16_rn((__expf(zt - lse) - 1.0f) * dscale);
+            }
+            zg[p] = v;
+        }
+        if (threadIdx.x == 0) {
+            loss_rows[row] = lse - zt;
+            if (bad) raise_device_error(err, DEVERR_BAD_TOKEN);
+        }
+        __syncthreads();  // the buffer is free again
+        if (threadIdx.x == 0 && row + 2 * (int)gridDim.x < N) issue(row + 2 * gridDim.x, buf);
+    }
+}
+
 template <typename T>
 int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, int Vp, float dscale, int *err,
                cudaStream_t st) {
@@ -628,6 +764,25 @@ int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, in
     const int grid = std::min(N, 148 * 2);
     if constexpr (sizeof(T) == 2) {
         bf16 *lg = reinterpret_cast<bf16 *>(logits);
+        // large rows: shared-memory pipeline (two rows of Vp bf16 in flight per SM)
+        const int row_pad = (Vp * 2 + 127) / 128 * 128;
+        const size_t cls_smem_bytes = 2 * (size_t)row_pad + 64;
+        if (Vp >= 8192 && cls_smem_bytes <= 200 * 1024) {
+            static bool attr = false;
+            if (!attr) {
+                GPT2_CUDA_TRY(cudaFuncSetAttribute(classifier_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   200 * 1024 + 64));
+                attr = true;
+            }
+            int dev = 0, sms = 148;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            classifier_smem_kernel<<<std::min(N, sms), CLS_SMEM_THREADS, cls_smem_bytes, st>>>(
+                lg, targets, loss_rows, N, V, Vp, row_pad, dscale, err);
+            GPT2_CUDA_TRY(cudaGetLastError());
+            gpt2_note_launches(1);
+            return GPT2_OK;
+        }
         switch (npt <= 1 ? 1 : npt <= 2 ? 2 : npt <= 4 ? 4 : npt <= 7 ? 7 : npt <= 8 ? 8 : 0) {
             case 1: classifier_bf16_kernel<1><<<grid, threads, 0, st>>>(lg, targets, loss_rows, N, V, Vp, dscale, err); break;
             case 2: classifier_bf16_kernel<2><<<grid, threads, 0, st>>>(lg, targets, loss_rows, N, V, Vp, dscale, err); break;

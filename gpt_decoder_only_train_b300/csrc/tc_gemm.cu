@@ -80,8 +80,10 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     P.num_k_blocks = ceil_div(g.K, BK);
     P.splits = 1;
     if (g.epi == GPT2_EPI_ACCUM_F32) {
+        // split K so that the work units fill about two waves of the persistent grid
         const int tiles = P.num_m_blocks * P.num_n_blocks;
-        if (tiles < num_sms) P.splits = std::max(1, std::min(P.num_k_blocks, num_sms / tiles));
+        if (tiles < 2 * num_sms)
+            P.splits = std::max(1, std::min(P.num_k_blocks / 4, (2 * num_sms + tiles - 1) / tiles));
     }
     P.k_blocks_per_split = ceil_div(P.num_k_blocks, P.splits);
     P.splits = ceil_div(P.num_k_blocks, P.k_blocks_per_split);

@@ -236,11 +236,10 @@ __device__ __forceinline__ void epilogue_chunk(const Params &P, int row, int col
                 o.z += acc[4 * g + 2];
                 o.w += acc[4 * g + 3];
                 *p = o;
-            } else {
-                atomicAdd(D + col + 0, acc[4 * g + 0]);
-                atomicAdd(D + col + 1, acc[4 * g + 1]);
-                atomicAdd(D + col + 2, acc[4 * g + 2]);
-                atomicAdd(D + col + 3, acc[4 * g + 3]);
+            } else {  // split-K partial: one 16-byte vector reduction
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(D + col), "f"(acc[4 * g + 0]),
+                             "f"(acc[4 * g + 1]), "f"(acc[4 * g + 2]), "f"(acc[4 * g + 3])
+                             : "memory");
             }
         }
         return;

@@ -249,6 +249,24 @@ int gpt2_op_attention_backward_noalloc(const void *q, const void *k, const void 
                                        const void *o, const void *dout, int64_t o_row_stride, const float *lse,
                                        void *dq, void *dk, void *dv, int B, int T, int H, int hd, void *stream);
 
+/*
+ * LayerNorm over rows of C bf16 values ("Let's build GPT: from scratch",
+ * 01:32:51): y = (x - mean) / sqrt(var + 1e-5) * g + b with biased variance;
+ * mean and rstd (fp32 [N]) are written for the backward.  g, b fp32 [C];
+ * C a multiple of 8 and at most 2048.
+ */
+int gpt2_op_layernorm_forward(const void *x, const float *g, const float *b, void *y, float *mean, float *rstd,
+                              int N, int C, void *stream);
+
+/*
+ * LayerNorm backward: dres_out = dres_in + dx with
+ * dx = rstd (dy*g - mean(dy*g) - xhat mean(dy*g*xhat)); dg += sum_rows dy*xhat,
+ * db += sum_rows dy (fp32 [C], accumulated).  dres_in may be NULL (then dres_out
+ * = dx) or equal dres_out (in place).  All bf16 [N, C] except the fp32 stats.
+ */
+int gpt2_op_layernorm_backward(const void *dy, const void *x, const float *mean, const float *rstd, const float *g,
+                               const void *dres_in, void *dres_out, float *dg, float *db, int N, int C, void *stream);
+
 /* Matmul epilogues of gpt2_op_matmul. */
 #define GPT2_EPI_STORE        0  /* D = acc (+ bias)                      -> bf16 */
 #define GPT2_EPI_RESIDUAL     1  /* D = acc + bias + R[m,n]              -> bf16 */

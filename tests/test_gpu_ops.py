@@ -216,3 +216,33 @@ def test_classifier_parity(g, N, V, Vp):
     out = zd.double().cpu()
     assert torch.all(out[:, V:] == 0)
     _close(out[:, :V], dz * (dscale * N), rel_elem=1e-2, rel_fro=6e-3)
+
+
+# ------------------------------------------------------------------ layernorm
+
+@pytest.mark.parametrize("N,C", [(37, 768), (300, 64), (16, 1024), (5, 2048)])
+def test_layernorm_forward_backward_parity(g, N, C):
+    gen = torch.Generator().manual_seed(C)
+    x = (torch.randn(N, C, generator=gen) * 2 + 0.5).to(torch.bfloat16)
+    dy = torch.randn(N, C, generator=gen).to(torch.bfloat16)
+    dres = torch.randn(N, C, generator=gen).to(torch.bfloat16)
+    gg = (1 + 0.1 * torch.randn(C, generator=gen)).float()
+    bb = (0.1 * torch.randn(C, generator=gen)).float()
+    y = torch.empty(N, C, dtype=torch.bfloat16, device="cuda")
+    mean = torch.empty(N, device="cuda")
+    rstd = torch.empty(N, device="cuda")
+    xd = x.cuda()
+    g.layernorm_forward(xd, gg.cuda(), bb.cuda(), y, mean, rstd, N, C)
+    out = dres.clone().cuda()
+    dg = torch.full((C,), 0.25, device="cuda")
+    db = torch.full((C,), -0.5, device="cuda")
+    g.layernorm_backward(dy.cuda(), xd, mean, rstd, gg.cuda(), out, out, dg, db, N, C)  # in place
+    torch.cuda.synchronize()
+    ry, rm, rr = og.layernorm_forward(x.double(), gg.double(), bb.double())
+    _close(y, ry)
+    assert (mean.cpu().double() - rm.squeeze(-1)).abs().max() < 1e-5 * max(1.0, rm.abs().max().item())
+    assert ((rstd.cpu().double() - rr.squeeze(-1)) / rr.squeeze(-1)).abs().max() < 1e-5
+    dx, rdg, rdb = og.layernorm_backward(dy.double(), x.double(), rm, rr, gg.double())
+    _close(out, dres.double() + dx)
+    assert ((dg.cpu().double() - 0.25 - rdg).norm() / rdg.norm()).item() < 1e-5
+    assert ((db.cpu().double() + 0.5 - rdb).norm() / rdb.norm()).item() < 1e-5
