@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(NT, 2)
                   const __grid_constant__ CUtensorMap tv, bf16 *__restrict__ o, int64_t ors, float *__restrict__ lse,
                   int T, int H, float sl2) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = align_smem_1024(smem_raw);
     Bars *bar = reinterpret_cast<Bars *>(sm + BAR_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + BAR_OFF + sizeof(Bars));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -323,6 +323,18 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&f)[16]) {
     for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(r[i]);
 }
 
+// tcgen05.ld of 32 lanes x 16 columns without the wait (batch several loads,
+// then one tmem_ld_wait)
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // 16 bf16 values (8 words) of row r into a swizzled 128-row x 128-byte atom at 16-byte chunks cc, cc+1
 __device__ __forceinline__ void store_row_chunks(uint8_t *atom, int r, int cc, const uint32_t (&w)[8]) {
     uint8_t *row = atom + r * 128;
@@ -334,7 +346,7 @@ __device__ __forceinline__ void store_row_chunks(uint8_t *atom, int r, int cc, c
 // One CTA per (128-query block, b*h); key blocks of 64.  TMEM: S [0,64),
 // dP [64,128), dQ [128,192).  Softmax threads: two per query row, 32 keys each.
 namespace dq {
-constexpr int BQ = 128, BK = 64, SLOTS = 4;
+constexpr int BQ = 128, BK = 64, SLOTS = 7;
 constexpr int TQ = BQ * HD * 2;      // 16 KB
 constexpr int TK = BK * HD * 2;      // 8 KB
 constexpr int OFF_DO = TQ, OFF_RING = 2 * TQ, OFF_DS = OFF_RING + SLOTS * TK, OFF_RED = OFF_DS + TQ;
@@ -353,7 +365,7 @@ __global__ void __launch_bounds__(NT, 2)
                      const float *__restrict__ lse, bf16 *__restrict__ dqo, int64_t rs, float *__restrict__ Dscr,
                      int T, int H, float sl2, float scale) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = align_smem_1024(smem_raw);
     dq::Bars *bar = reinterpret_cast<dq::Bars *>(sm + dq::OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + dq::OFF_BAR + sizeof(dq::Bars));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -485,8 +497,17 @@ __global__ void __launch_bounds__(NT, 2)
 #pragma unroll
             for (int c0 = 0; c0 < 32; c0 += 16) {
                 float sv[16], dp[16];
-                tmem_ld16f(tS + lane_off + half * 32 + c0, sv);
-                tmem_ld16f(tdP + lane_off + half * 32 + c0, dp);
+                {
+                    uint32_t ra[16], rb[16];
+                    tmem_ld16_nowait(tS + lane_off + half * 32 + c0, ra);
+                    tmem_ld16_nowait(tdP + lane_off + half * 32 + c0, rb);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        sv[i] = __uint_as_float(ra[i]);
+                        dp[i] = __uint_as_float(rb[i]);
+                    }
+                }
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
                     float p0 = ex2(fmaf(sv[i], sl2, -l2));
@@ -533,208 +554,290 @@ __global__ void __launch_bounds__(NT, 2)
 }
 
 // ---------------------------------------------------------------- dK/dV kernel
-// One CTA per (128-key block, b*h); query blocks of 64 from the key block on.
-// TMEM: S^T [0,64), dP^T [64,128), dV [128,192), dK [192,256).  Softmax
-// threads: two per key row, 32 queries each.
+// One CTA per (128-key block, b*h), one CTA per SM; query blocks of 64 from the
+// key block on.  Every GEMM takes its A operand from TMEM, so shared memory only
+// carries the Q / dO tiles (B operands) and lse / D:
+//   S^T  = K Q^T      A = K (TMEM, loaded once)   B = Q  (K-major tile)
+//   dP^T = V dO^T     A = V (TMEM, loaded once)   B = dO (K-major tile)
+//   dV  += P^T dO     A = P^T (TMEM)              B = dO (MN-major view)
+//   dK  += dS^T Q     A = dS^T (TMEM)             B = Q  (MN-major view)
+// S^T / dP^T are double-buffered.  The softmax warps read their 16 columns of
+// S^T and dP^T and write P^T / dS^T as bf16 back over the first 8 of those
+// columns, so that K-step kk of the dV / dK products reads columns
+// [16 kk, 16 kk + 8) of the buffer.  tcgen05.mma operations issued by one
+// thread execute in order, so S^T of block it+2 (issued after the dV / dK
+// products of block it) never overwrites P^T / dS^T before they are read.
+// TMEM columns: S^T[b] [64b, 64b+64), dP^T[b] [128+64b, ...), dV [256,320),
+// dK [320,384), K [384,416), V [416,448) (bf16 pairs).
+// Warps: 0 loads Q / dO (TMA) and lse / D (cp.async) through a ring, 1 issues
+// the MMAs, 2-17 are the softmax warps: four per TMEM lane quadrant, each
+// owning 16 of the 64 queries of a block.
 namespace dkv {
-constexpr int BKY = 128, BQ = 64, SLOTS = 4;
-constexpr int TKY = BKY * HD * 2;  // 16 KB
-constexpr int TQ = BQ * HD * 2;    // 8 KB
-constexpr int OFF_V = TKY, OFF_RING = 2 * TKY, OFF_P = OFF_RING + SLOTS * TQ, OFF_DS = OFF_P + TKY;
-constexpr int OFF_LD = OFF_DS + TKY;  // [2 buffers][lse 64 | D 64] floats
-constexpr int OFF_BAR = OFF_LD + 2 * 128 * 4;
-constexpr int SMEM = 1024 + OFF_BAR + 256;
+constexpr int BKY = 128, BQ = 64, SLOTS = 12, SWARPS = 16, NLD = SLOTS / 2;
+constexpr int NTH = 64 + 32 * SWARPS;
+constexpr int TQ = BQ * HD * 2;                  // 8 KB
+constexpr int OFF_LD = SLOTS * TQ;               // [NLD][lse 64 | D 64] floats
+constexpr int OFF_BAR = OFF_LD + NLD * 2 * BQ * 4;
+constexpr int SMEM = 1024 + OFF_BAR + 512;
+constexpr uint32_t TCOLS = 512;
+constexpr uint32_t C_ST = 0, C_DPT = 128, C_DV = 256, C_DK = 320, C_K = 384, C_V = 416;
 struct Bars {
-    uint64_t kv_full, st_full, pds_full, pds_free, dkv_done, drain;
-    uint64_t full[SLOTS], empty[SLOTS];
+    uint64_t kv_full, dkv_done, drain;
+    uint64_t st_full[2], pds_full[2];
+    uint64_t full[SLOTS], empty[SLOTS], ld_full[NLD];
 };
 }  // namespace dkv
 
-__global__ void __launch_bounds__(NT, 2)
-    bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                      const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
-                      const float *__restrict__ lse, const float *__restrict__ Dscr, bf16 *__restrict__ dko,
-                      bf16 *__restrict__ dvo, int64_t rs, int T, int H, float sl2, float scale) {
+// tcgen05.mma with the A operand in TMEM (kind::f16, fp32 accumulate)
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 32 lanes x 8 columns of 32-bit words from registers into TMEM
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 4-byte asynchronous global -> shared copy; src_bytes 0 stores a zero
+__device__ __forceinline__ void cp_async4(float *dst, const float *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// the mbarrier counts one arrival when this thread's earlier cp.async copies have landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__global__ void __launch_bounds__(dkv::NTH, 1)
+    bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                      const bf16 *__restrict__ kg, const bf16 *__restrict__ vg, const float *__restrict__ lse,
+                      const float *__restrict__ Dscr, bf16 *__restrict__ dko, bf16 *__restrict__ dvo, int64_t rs,
+                      int T, int H, float sl2, float scale) {
+    constexpr int BKY = dkv::BKY, BQ = dkv::BQ, SLOTS = dkv::SLOTS, SWARPS = dkv::SWARPS, NLD = dkv::NLD;
+    constexpr int TQ = dkv::TQ, OFF_LD = dkv::OFF_LD, OFF_BAR = dkv::OFF_BAR;
+    constexpr uint32_t TCOLS = dkv::TCOLS, C_ST = dkv::C_ST, C_DPT = dkv::C_DPT, C_DV = dkv::C_DV, C_DK = dkv::C_DK,
+                       C_K = dkv::C_K, C_V = dkv::C_V;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    dkv::Bars *bar = reinterpret_cast<dkv::Bars *>(sm + dkv::OFF_BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + dkv::OFF_BAR + sizeof(dkv::Bars));
+    uint8_t *sm = align_smem_1024(smem_raw);
+    dkv::Bars *bar = reinterpret_cast<dkv::Bars *>(sm + OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + sizeof(dkv::Bars));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *ldbuf = reinterpret_cast<float *>(sm + OFF_LD);
     const int kb = blockIdx.x;  // key block 0 sees every query block: launch first
     const int bh = blockIdx.y, b = bh / H, h = bh % H;
-    const int q0blk = kb * (dkv::BKY / dkv::BQ);
-    const int nit = (T + dkv::BQ - 1) / dkv::BQ - q0blk;
+    const int q0blk = kb * (BKY / BQ);
+    const int nit = (T + BQ - 1) / BQ - q0blk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        mbar_init(&bar->kv_full, 1);
-        mbar_init(&bar->st_full, 1);
-        mbar_init(&bar->pds_full, SOFTMAX_WARPS);
-        mbar_init(&bar->pds_free, 1);
+        mbar_init(&bar->kv_full, SWARPS);
         mbar_init(&bar->dkv_done, 1);
         mbar_init(&bar->drain, 1);
-        for (int i = 0; i < dkv::SLOTS; ++i) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar->st_full[i], 1);
+            mbar_init(&bar->pds_full[i], SWARPS);
+        }
+        for (int i = 0; i < SLOTS; ++i) {
             mbar_init(&bar->full[i], 1);
             mbar_init(&bar->empty[i], 1);
         }
+        for (int i = 0; i < NLD; ++i) mbar_init(&bar->ld_full[i], 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tdo);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_alloc(tmem_slot, TCOLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tSt = tmem, tdPt = tmem + 64, tdV = tmem + 128, tdK = tmem + 192;
 
     if (warp == 0) {
-        if (lane == 0) {
-            mbar_expect_tx(&bar->kv_full, 2 * dkv::TKY);
-            tma_load_3d(sm, &tk, &bar->kv_full, h * HD, kb * dkv::BKY, b);
-            tma_load_3d(sm + dkv::OFF_V, &tv, &bar->kv_full, h * HD, kb * dkv::BKY, b);
-            uint32_t issued = 0, iph = 0;
-            bool ok = true;
-            for (int i = 0; i < 2 * nit && ok; ++i) {
-                const int sl = i % dkv::SLOTS;
-                const uint32_t ph = (i / dkv::SLOTS) & 1;
-                if (!(ok = mbar_wait(&bar->empty[sl], ph ^ 1, abort_flag, nullptr))) break;
-                mbar_expect_tx(&bar->full[sl], dkv::TQ);
-                tma_load_3d(sm + dkv::OFF_RING + sl * dkv::TQ, (i & 1) ? &tdo : &tq, &bar->full[sl], h * HD,
-                            (q0blk + (i >> 1)) * dkv::BQ, b);
-                issued |= 1u << sl;
-                iph = (iph & ~(1u << sl)) | (ph << sl);
+        // Query block i uses ring slots 2i, 2i+1 (mod SLOTS) for Q and dO and
+        // lse / D entry i mod NLD; both are refilled once the dV / dK products
+        // of the block that last used them have completed.
+        bool ok = true;
+        int nissued = 0;
+        for (int i = 0; i < nit; ++i) {
+            const int sq = (2 * i) % SLOTS, sd = sq + 1, e = sq >> 1;
+            const uint32_t ph = ((2 * i) / SLOTS) & 1;
+            if (!(ok = mbar_wait(&bar->empty[sq], ph ^ 1, abort_flag, nullptr))) break;
+            if (!(ok = mbar_wait(&bar->empty[sd], ph ^ 1, abort_flag, nullptr))) break;
+            const int q0 = (q0blk + i) * BQ;
+            if (lane == 0) {
+                mbar_expect_tx(&bar->full[sq], TQ);
+                tma_load_3d(sm + sq * TQ, &tq, &bar->full[sq], h * HD, q0, b);
+                mbar_expect_tx(&bar->full[sd], TQ);
+                tma_load_3d(sm + sd * TQ, &tdo, &bar->full[sd], h * HD, q0, b);
             }
-            if (!ok) {
-                mbar_drain(&bar->kv_full, 0);
-                for (int sl = 0; sl < dkv::SLOTS; ++sl)
-                    if (issued & (1u << sl)) mbar_drain(&bar->full[sl], (iph >> sl) & 1);
+            // lanes 0-15: lse of queries q0 + 4 lane + j; lanes 16-31: D
+            const float *src = (lane < 16 ? lse : Dscr) + (int64_t)bh * T;
+            float *dst = ldbuf + e * 128 + lane * 4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int q = q0 + (lane & 15) * 4 + j;
+                cp_async4(dst + j, src + (q < T ? q : 0), q < T ? 4u : 0u);
+            }
+            cp_async_arrive_noinc(&bar->ld_full[e]);
+            nissued = i + 1;
+        }
+        if (!ok && lane == 0) {
+            for (int i = nissued > NLD ? nissued - NLD : 0; i < nissued; ++i) {
+                const int sq = (2 * i) % SLOTS;
+                const uint32_t ph = ((2 * i) / SLOTS) & 1;
+                mbar_drain(&bar->full[sq], ph);
+                mbar_drain(&bar->full[sq + 1], ph);
             }
         }
+        cp_async_wait_all();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t ID_ST = instr_desc(dkv::BQ, false, false);  // 128 x 64: K/V K-major x Q/dO K-major
-            constexpr uint32_t ID_G = instr_desc(HD, false, true);    // 128 x 64: P^T/dS^T K-major x dO/Q MN-major
-            const uint32_t aK = smem_u32(sm), aV = smem_u32(sm + dkv::OFF_V);
-            const uint32_t aP = smem_u32(sm + dkv::OFF_P), aDS = smem_u32(sm + dkv::OFF_DS);
+            constexpr uint32_t ID_ST = instr_desc(BQ, false, false);  // 128 x 64, B = Q / dO K-major
+            constexpr uint32_t ID_G = instr_desc(HD, false, true);    // 128 x 64, B = dO / Q MN-major
+            const uint64_t ring_k = smem_desc(smem_u32(sm), 16, 1024);    // K-major view of slot 0
+            const uint64_t ring_mn = smem_desc(smem_u32(sm), 8192, 1024); // MN-major view of slot 0
             bool ok = mbar_wait(&bar->kv_full, 0, abort_flag, nullptr);
-            auto issue_st = [&](int it) -> bool {
-                const int sq = (2 * it) % dkv::SLOTS, sd = (2 * it + 1) % dkv::SLOTS;
-                if (!mbar_wait(&bar->full[sq], ((2 * it) / dkv::SLOTS) & 1, abort_flag, nullptr)) return false;
-                if (!mbar_wait(&bar->full[sd], ((2 * it + 1) / dkv::SLOTS) & 1, abort_flag, nullptr)) return false;
-                tc_fence_after();
-                const uint32_t aQ = smem_u32(sm + dkv::OFF_RING + sq * dkv::TQ), aDO = smem_u32(sm + dkv::OFF_RING + sd * dkv::TQ);
+            tc_fence_after();
+            for (int it = 0; it <= nit && ok; ++it) {
+                if (it < nit) {
+                    const int bb = it & 1, sq = (2 * it) % SLOTS, sd = sq + 1;
+                    const uint32_t ph = ((2 * it) / SLOTS) & 1;
+                    if (!(ok = mbar_wait(&bar->full[sq], ph, abort_flag, nullptr))) break;
+                    if (!(ok = mbar_wait(&bar->full[sd], ph, abort_flag, nullptr))) break;
+                    tc_fence_after();
+                    const uint64_t bq = ring_k + (uint64_t)(sq * (TQ >> 4)), bd = ring_k + (uint64_t)(sd * (TQ >> 4));
+                    const uint32_t ts = tmem + C_ST + bb * 64, td = tmem + C_DPT + bb * 64;
+                    tc_mma_ts(ts, tmem + C_K, bq, ID_ST, 0u);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    tc_mma(tSt, smem_desc(aK + kk * 32, 16, 1024), smem_desc(aQ + kk * 32, 16, 1024), ID_ST,
-                           kk > 0 ? 1u : 0u);
+                    for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(ts, tmem + C_K + 8 * kk, bq + 2 * kk, ID_ST, 1u);
+                    tc_mma_ts(td, tmem + C_V, bd, ID_ST, 0u);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    tc_mma(tdPt, smem_desc(aV + kk * 32, 16, 1024), smem_desc(aDO + kk * 32, 16, 1024), ID_ST,
-                           kk > 0 ? 1u : 0u);
-                tc_commit(&bar->st_full);
-                return true;
-            };
-            if (ok) ok = issue_st(0);
-            for (int it = 0; it < nit && ok; ++it) {
-                if (!(ok = mbar_wait(&bar->pds_full, it & 1, abort_flag, nullptr))) break;
-                if (it + 1 < nit && !(ok = issue_st(it + 1))) break;
-                const int sq = (2 * it) % dkv::SLOTS, sd = (2 * it + 1) % dkv::SLOTS;
-                const uint32_t aQ = smem_u32(sm + dkv::OFF_RING + sq * dkv::TQ), aDO = smem_u32(sm + dkv::OFF_RING + sd * dkv::TQ);
-                tc_fence_after();
+                    for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(td, tmem + C_V + 8 * kk, bd + 2 * kk, ID_ST, 1u);
+                    tc_commit(&bar->st_full[bb]);
+                }
+                if (it >= 1) {  // dV and dK products of the previous block
+                    const int pi = it - 1, pb = pi & 1, sq = (2 * pi) % SLOTS, sd = sq + 1;
+                    if (!(ok = mbar_wait(&bar->pds_full[pb], (pi >> 1) & 1, abort_flag, nullptr))) break;
+                    tc_fence_after();
+                    const uint64_t bq = ring_mn + (uint64_t)(sq * (TQ >> 4)), bd = ring_mn + (uint64_t)(sd * (TQ >> 4));
+                    const uint32_t pa = tmem + C_ST + pb * 64, da = tmem + C_DPT + pb * 64;
+                    const uint32_t acc0 = pi > 0 ? 1u : 0u;
+                    tc_mma_ts(tmem + C_DV, pa, bd, ID_G, acc0);
 #pragma unroll
-                for (int kk = 0; kk < dkv::BQ / 16; ++kk)
-                    tc_mma(tdV, smem_desc(aP + kk * 32, 16, 1024), smem_desc(aDO + kk * 2048, 8192, 1024), ID_G,
-                           (it > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 1; kk < BQ / 16; ++kk) tc_mma_ts(tmem + C_DV, pa + 16 * kk, bd + 128 * kk, ID_G, 1u);
+                    tc_mma_ts(tmem + C_DK, da, bq, ID_G, acc0);
 #pragma unroll
-                for (int kk = 0; kk < dkv::BQ / 16; ++kk)
-                    tc_mma(tdK, smem_desc(aDS + kk * 32, 16, 1024), smem_desc(aQ + kk * 2048, 8192, 1024), ID_G,
-                           (it > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&bar->empty[sq]);
-                tc_commit(&bar->empty[sd]);
-                tc_commit(&bar->pds_free);
+                    for (int kk = 1; kk < BQ / 16; ++kk) tc_mma_ts(tmem + C_DK, da + 16 * kk, bq + 128 * kk, ID_G, 1u);
+                    tc_commit(&bar->empty[sq]);
+                    tc_commit(&bar->empty[sd]);
+                }
             }
             tc_commit(&bar->dkv_done);
             tc_commit(&bar->drain);
             mbar_drain(&bar->drain, 0);
         }
     } else {
-        const int quad = warp & 3, half = (warp - 2) >> 2;
-        const int r = quad * 32 + lane, key = kb * dkv::BKY + r;
-        const int sidx = threadIdx.x - 64;  // 0..255 over the softmax warps
+        const int quad = warp & 3, sub = (warp - 2) >> 2;  // sub: queries [16 sub, 16 sub + 16) of each block
+        const int r = quad * 32 + lane, key = kb * BKY + r;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        float *ld = reinterpret_cast<float *>(sm + dkv::OFF_LD);  // [buf][0..63 lse*log2e | 64..127 D]
-        auto load_ld = [&](int it, int buf) {
-            if (sidx < 128 && it < nit) {
-                const int q = (q0blk + it) * dkv::BQ + (sidx & 63);
-                float v = 0.f;
-                if (q < T) v = sidx < 64 ? lse[(int64_t)bh * T + q] * LOG2E : Dscr[(int64_t)bh * T + q];
-                ld[buf * 128 + sidx] = v;
+        // Row `key` of K and V, elements [16 sub, 16 sub + 16), into TMEM as A operands.
+        {
+            uint32_t kr[8], vr[8];
+            if (key < T) {
+                const int64_t off = ((int64_t)b * T + key) * rs + h * HD + sub * 16;
+                const uint4 k0 = *reinterpret_cast<const uint4 *>(kg + off);
+                const uint4 k1 = *reinterpret_cast<const uint4 *>(kg + off + 8);
+                const uint4 v0 = *reinterpret_cast<const uint4 *>(vg + off);
+                const uint4 v1 = *reinterpret_cast<const uint4 *>(vg + off + 8);
+                kr[0] = k0.x, kr[1] = k0.y, kr[2] = k0.z, kr[3] = k0.w, kr[4] = k1.x, kr[5] = k1.y, kr[6] = k1.z,
+                kr[7] = k1.w;
+                vr[0] = v0.x, vr[1] = v0.y, vr[2] = v0.z, vr[3] = v0.w, vr[4] = v1.x, vr[5] = v1.y, vr[6] = v1.z,
+                vr[7] = v1.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) kr[i] = vr[i] = 0u;
             }
-        };
-        auto group_sync = [&]() { asm volatile("bar.sync 5, 256;" ::: "memory"); };
-        load_ld(0, 0);
-        uint8_t *sP = sm + dkv::OFF_P, *sDS = sm + dkv::OFF_DS;
+            tmem_st8(tmem + lane_off + C_K + sub * 8, kr);
+            tmem_st8(tmem + lane_off + C_V + sub * 8, vr);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->kv_full);
+        }
         bool ok = true;
-        // A failed (timed-out) wait clears `ok`; the loop still runs to the end
-        // so that every thread reaches every group barrier (bar.sync has no timeout).
         for (int it = 0; it < nit; ++it) {
-            group_sync();               // buffer it&1 is filled; buffer (it+1)&1 is no longer read
-            load_ld(it + 1, (it + 1) & 1);
-            const float *L = ld + (it & 1) * 128, *Dv = L + 64;
-            if (ok) ok = mbar_wait(&bar->st_full, it & 1, abort_flag, nullptr);
-            if (!ok) continue;
+            const int bb = it & 1, e = it % NLD;
+            if (!(ok = mbar_wait(&bar->st_full[bb], (it >> 1) & 1, abort_flag, nullptr))) break;
+            if (!(ok = mbar_wait(&bar->ld_full[e], (it / NLD) & 1, abort_flag, nullptr))) break;
             tc_fence_after();
-            uint32_t wp[2][8], wd[2][8];
-            const int qbase = (q0blk + it) * dkv::BQ + half * 32;
-            // visible queries of this thread's 32: lo <= c <= hi (q >= key, q < T; none if key >= T)
+            const uint32_t cs = tmem + lane_off + C_ST + bb * 64 + sub * 16;
+            const uint32_t cd = tmem + lane_off + C_DPT + bb * 64 + sub * 16;
+            uint32_t ra[16], rb[16];
+            tmem_ld16_nowait(cs, ra);
+            tmem_ld16_nowait(cd, rb);
+            tmem_ld_wait();
+            const float *L = ldbuf + e * 128 + sub * 16, *Dv = ldbuf + e * 128 + 64 + sub * 16;
+            const int qbase = (q0blk + it) * BQ + sub * 16;
+            // visible queries of this thread's 16: lo <= c <= hi (q >= key, q < T; none if key >= T)
             const int lo = key - qbase, hi = key < T ? T - 1 - qbase : -1;
-            const bool full = lo <= 0 && hi >= 31;
+            const bool full = lo <= 0 && hi >= 15;
+            uint32_t wp[8], wd[8];
 #pragma unroll
-            for (int c0 = 0; c0 < 32; c0 += 16) {
-                float st[16], dpt[16], lv[16], dv[16];
-                tmem_ld16f(tSt + lane_off + half * 32 + c0, st);
-                tmem_ld16f(tdPt + lane_off + half * 32 + c0, dpt);
+            for (int i = 0; i < 16; i += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(L + i);
+                const float4 d4 = *reinterpret_cast<const float4 *>(Dv + i);
+                const float lv[4] = {a4.x * LOG2E, a4.y * LOG2E, a4.z * LOG2E, a4.w * LOG2E};
+                const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-                for (int i = 0; i < 16; i += 4) {
-                    const float4 a = *reinterpret_cast<const float4 *>(L + half * 32 + c0 + i);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(Dv + half * 32 + c0 + i);
-                    lv[i] = a.x; lv[i + 1] = a.y; lv[i + 2] = a.z; lv[i + 3] = a.w;
-                    dv[i] = d4.x; dv[i + 1] = d4.y; dv[i + 2] = d4.z; dv[i + 3] = d4.w;
-                }
-#pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    float p0 = ex2(fmaf(st[i], sl2, -lv[i]));
-                    float p1 = ex2(fmaf(st[i + 1], sl2, -lv[i + 1]));
+                for (int e2 = 0; e2 < 4; e2 += 2) {
+                    const int c = i + e2;
+                    float p0 = ex2(fmaf(__uint_as_float(ra[c]), sl2, -lv[e2]));
+                    float p1 = ex2(fmaf(__uint_as_float(ra[c + 1]), sl2, -lv[e2 + 1]));
                     if (!full) {
-                        const int c = c0 + i;
                         p0 = (c >= lo && c <= hi) ? p0 : 0.f;
                         p1 = (c + 1 >= lo && c + 1 <= hi) ? p1 : 0.f;
                     }
-                    wp[c0 >> 4][i >> 1] = pack_bf16x2(p0, p1);
-                    wd[c0 >> 4][i >> 1] = pack_bf16x2(p0 * (dpt[i] - dv[i]), p1 * (dpt[i + 1] - dv[i + 1]));
+                    wp[c >> 1] = pack_bf16x2(p0, p1);
+                    wd[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(rb[c]) - dv4[e2]),
+                                             p1 * (__uint_as_float(rb[c + 1]) - dv4[e2 + 1]));
                 }
             }
+            tmem_st8(cs, wp);  // P^T over the first 8 of this thread's S^T columns
+            tmem_st8(cd, wd);  // dS^T over the first 8 of its dP^T columns
+            tmem_st_wait();
             tc_fence_before();
-            if (it > 0 && !(ok = mbar_wait(&bar->pds_free, (it - 1) & 1, abort_flag, nullptr))) continue;
-            store_row_chunks(sP, r, half * 4, wp[0]);
-            store_row_chunks(sP, r, half * 4 + 2, wp[1]);
-            store_row_chunks(sDS, r, half * 4, wd[0]);
-            store_row_chunks(sDS, r, half * 4 + 2, wd[1]);
-            fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->pds_full);
+            if (lane == 0) mbar_arrive(&bar->pds_full[bb]);
         }
         if (ok && mbar_wait(&bar->dkv_done, 0, abort_flag, nullptr)) {
             tc_fence_after();
-            float fv[32], fk[32];
-            tmem_ld32f(tdV + lane_off + half * 32, fv);
-            tmem_ld32f(tdK + lane_off + half * 32, fk);
-            if (key < T) {
-                const int64_t off = ((int64_t)b * T + key) * rs + h * HD + half * 32;
+            float fv[16], fk[16];
+            {
+                uint32_t ra[16], rb[16];
+                tmem_ld16_nowait(tmem + lane_off + C_DV + sub * 16, ra);
+                tmem_ld16_nowait(tmem + lane_off + C_DK + sub * 16, rb);
+                tmem_ld_wait();
 #pragma unroll
-                for (int d = 0; d < 32; d += 8) {
+                for (int i = 0; i < 16; ++i) {
+                    fv[i] = __uint_as_float(ra[i]);
+                    fk[i] = __uint_as_float(rb[i]);
+                }
+            }
+            if (key < T) {
+                const int64_t off = ((int64_t)b * T + key) * rs + h * HD + sub * 16;
+#pragma unroll
+                for (int d = 0; d < 16; d += 8) {
                     uint4 u, w;
                     u.x = pack_bf16x2(fv[d], fv[d + 1]);
                     u.y = pack_bf16x2(fv[d + 2], fv[d + 3]);
@@ -754,7 +857,7 @@ __global__ void __launch_bounds__(NT, 2)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, TCOLS);
     }
 }
 
@@ -814,13 +917,11 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
          reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq_out) |
          reinterpret_cast<uintptr_t>(dk_out) | reinterpret_cast<uintptr_t>(dv_out)) & 15)
         return GPT2_ERR_BAD_ARG;
-    CUtensorMap q128, do128, k64, v64, k128, v128, q64, do64;
+    CUtensorMap q128, do128, k64, v64, q64, do64;
     if (int rc = encode_qkv_map(&q128, q, rs, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&do128, dout, ors, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&k64, k, rs, T, B, H, 64)) return rc;
     if (int rc = encode_qkv_map(&v64, v, rs, T, B, H, 64)) return rc;
-    if (int rc = encode_qkv_map(&k128, k, rs, T, B, H, 128)) return rc;
-    if (int rc = encode_qkv_map(&v128, v, rs, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&q64, q, rs, T, B, H, 64)) return rc;
     if (int rc = encode_qkv_map(&do64, dout, ors, T, B, H, 64)) return rc;
     static bool init = false;
@@ -833,8 +934,8 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
     bwd_dq_tc_kernel<<<dim3((T + dq::BQ - 1) / dq::BQ, B * H), NT, dq::SMEM, st>>>(
         q128, do128, k64, v64, o, dout, ors, lse, dq_out, rs, Dscr, T, H, sl2, scale);
     GPT2_CUDA_TRY(cudaGetLastError());
-    bwd_dkv_tc_kernel<<<dim3((T + dkv::BKY - 1) / dkv::BKY, B * H), NT, dkv::SMEM, st>>>(
-        k128, v128, q64, do64, lse, Dscr, dk_out, dv_out, rs, T, H, sl2, scale);
+    bwd_dkv_tc_kernel<<<dim3((T + dkv::BKY - 1) / dkv::BKY, B * H), dkv::NTH, dkv::SMEM, st>>>(
+        q64, do64, k, v, lse, Dscr, dk_out, dv_out, rs, T, H, sl2, scale);
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(2);
     return GPT2_OK;

@@ -59,6 +59,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 1024-byte aligned base inside the dynamic shared-memory array.  The offset is
+// added to the array pointer itself (no round trip through an integer), so the
+// compiler still knows the result points to shared memory and emits
+// shared-memory loads and stores for it rather than generic ones.
+__device__ __forceinline__ uint8_t *align_smem_1024(uint8_t *raw) {
+    return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 // ---- mbarrier ---------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -417,7 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr uint32_t IDESC = instr_desc(BN, A_MN, B_MN);
     constexpr uint32_t TMEM_COLS = 2 * BN;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = align_smem_1024(smem_raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::BAR_OFFSET);
     uint64_t *empty = full + STAGES;
     uint64_t *tfull = empty + STAGES;
