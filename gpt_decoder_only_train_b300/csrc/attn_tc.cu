@@ -74,8 +74,10 @@ __global__ void __launch_bounds__(NT, 2)
     uint8_t *sQ = sm, *sP = sm + P_OFF;
 
     const int nqb = (T + BQ - 1) / BQ;
-    const int qb = nqb - 1 - blockIdx.x;  // heaviest query blocks first
-    const int bh = blockIdx.y, b = bh / H, h = bh % H;
+    // blockIdx.x (fastest in launch order) runs over b*h, so every head's
+    // heaviest query block is launched before any lighter one
+    const int qb = nqb - 1 - blockIdx.y;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int nkv = qb + 1;               // causal: key blocks 0..qb
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -370,8 +372,8 @@ __global__ void __launch_bounds__(NT, 2)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + dq::OFF_BAR + sizeof(dq::Bars));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int nqb = (T + dq::BQ - 1) / dq::BQ;
-    const int qb = nqb - 1 - blockIdx.x;
-    const int bh = blockIdx.y, b = bh / H, h = bh % H;
+    const int qb = nqb - 1 - blockIdx.y;  // heaviest query blocks launched first
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int nkv = min((T + dq::BK - 1) / dq::BK, (qb + 1) * (dq::BQ / dq::BK));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -584,7 +586,7 @@ constexpr uint32_t C_ST = 0, C_DPT = 128, C_DV = 256, C_DK = 320, C_K = 384, C_V
 struct Bars {
     uint64_t kv_full, dkv_done, drain;
     uint64_t st_full[2], pds_full[2];
-    uint64_t full[SLOTS], empty[SLOTS], ld_full[NLD];
+    uint64_t full[NLD], empty[NLD], ld_full[NLD];  // per ring entry: Q and dO slots + lse / D
 };
 }  // namespace dkv
 
@@ -631,8 +633,8 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + sizeof(dkv::Bars));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *ldbuf = reinterpret_cast<float *>(sm + OFF_LD);
-    const int kb = blockIdx.x;  // key block 0 sees every query block: launch first
-    const int bh = blockIdx.y, b = bh / H, h = bh % H;
+    const int kb = blockIdx.y;  // key block 0 sees every query block: launched first
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int q0blk = kb * (BKY / BQ);
     const int nit = (T + BQ - 1) / BQ - q0blk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -644,11 +646,11 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
             mbar_init(&bar->st_full[i], 1);
             mbar_init(&bar->pds_full[i], SWARPS);
         }
-        for (int i = 0; i < SLOTS; ++i) {
+        for (int i = 0; i < NLD; ++i) {
             mbar_init(&bar->full[i], 1);
             mbar_init(&bar->empty[i], 1);
+            mbar_init(&bar->ld_full[i], 32);
         }
-        for (int i = 0; i < NLD; ++i) mbar_init(&bar->ld_full[i], 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tq);
@@ -664,22 +666,20 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // Query block i uses ring slots 2i, 2i+1 (mod SLOTS) for Q and dO and
-        // lse / D entry i mod NLD; both are refilled once the dV / dK products
-        // of the block that last used them have completed.
+        // Query block i uses ring entry e = i mod NLD: shared-memory slots 2e
+        // (Q) and 2e+1 (dO) and lse / D entry e.  The entry is refilled once the
+        // dV / dK products of the block that last used it have completed.
         bool ok = true;
         int nissued = 0;
         for (int i = 0; i < nit; ++i) {
-            const int sq = (2 * i) % SLOTS, sd = sq + 1, e = sq >> 1;
-            const uint32_t ph = ((2 * i) / SLOTS) & 1;
-            if (!(ok = mbar_wait(&bar->empty[sq], ph ^ 1, abort_flag, nullptr))) break;
-            if (!(ok = mbar_wait(&bar->empty[sd], ph ^ 1, abort_flag, nullptr))) break;
+            const int e = i % NLD, sq = 2 * e, sd = sq + 1;
+            const uint32_t ph = (i / NLD) & 1;
+            if (!(ok = mbar_wait(&bar->empty[e], ph ^ 1, abort_flag, nullptr))) break;
             const int q0 = (q0blk + i) * BQ;
             if (lane == 0) {
-                mbar_expect_tx(&bar->full[sq], TQ);
-                tma_load_3d(sm + sq * TQ, &tq, &bar->full[sq], h * HD, q0, b);
-                mbar_expect_tx(&bar->full[sd], TQ);
-                tma_load_3d(sm + sd * TQ, &tdo, &bar->full[sd], h * HD, q0, b);
+                mbar_expect_tx(&bar->full[e], 2 * TQ);
+                tma_load_3d(sm + sq * TQ, &tq, &bar->full[e], h * HD, q0, b);
+                tma_load_3d(sm + sd * TQ, &tdo, &bar->full[e], h * HD, q0, b);
             }
             // lanes 0-15: lse of queries q0 + 4 lane + j; lanes 16-31: D
             const float *src = (lane < 16 ? lse : Dscr) + (int64_t)bh * T;
@@ -693,12 +693,8 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
             nissued = i + 1;
         }
         if (!ok && lane == 0) {
-            for (int i = nissued > NLD ? nissued - NLD : 0; i < nissued; ++i) {
-                const int sq = (2 * i) % SLOTS;
-                const uint32_t ph = ((2 * i) / SLOTS) & 1;
-                mbar_drain(&bar->full[sq], ph);
-                mbar_drain(&bar->full[sq + 1], ph);
-            }
+            for (int i = nissued > NLD ? nissued - NLD : 0; i < nissued; ++i)
+                mbar_drain(&bar->full[i % NLD], (i / NLD) & 1);
         }
         cp_async_wait_all();
     } else if (warp == 1) {
@@ -711,10 +707,8 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
             tc_fence_after();
             for (int it = 0; it <= nit && ok; ++it) {
                 if (it < nit) {
-                    const int bb = it & 1, sq = (2 * it) % SLOTS, sd = sq + 1;
-                    const uint32_t ph = ((2 * it) / SLOTS) & 1;
-                    if (!(ok = mbar_wait(&bar->full[sq], ph, abort_flag, nullptr))) break;
-                    if (!(ok = mbar_wait(&bar->full[sd], ph, abort_flag, nullptr))) break;
+                    const int bb = it & 1, e = it % NLD, sq = 2 * e, sd = sq + 1;
+                    if (!(ok = mbar_wait(&bar->full[e], (it / NLD) & 1, abort_flag, nullptr))) break;
                     tc_fence_after();
                     const uint64_t bq = ring_k + (uint64_t)(sq * (TQ >> 4)), bd = ring_k + (uint64_t)(sd * (TQ >> 4));
                     const uint32_t ts = tmem + C_ST + bb * 64, td = tmem + C_DPT + bb * 64;
@@ -727,7 +721,7 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
                     tc_commit(&bar->st_full[bb]);
                 }
                 if (it >= 1) {  // dV and dK products of the previous block
-                    const int pi = it - 1, pb = pi & 1, sq = (2 * pi) % SLOTS, sd = sq + 1;
+                    const int pi = it - 1, pb = pi & 1, pe = pi % NLD, sq = 2 * pe, sd = sq + 1;
                     if (!(ok = mbar_wait(&bar->pds_full[pb], (pi >> 1) & 1, abort_flag, nullptr))) break;
                     tc_fence_after();
                     const uint64_t bq = ring_mn + (uint64_t)(sq * (TQ >> 4)), bd = ring_mn + (uint64_t)(sd * (TQ >> 4));
@@ -739,8 +733,7 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
                     tc_mma_ts(tmem + C_DK, da, bq, ID_G, acc0);
 #pragma unroll
                     for (int kk = 1; kk < BQ / 16; ++kk) tc_mma_ts(tmem + C_DK, da + 16 * kk, bq + 128 * kk, ID_G, 1u);
-                    tc_commit(&bar->empty[sq]);
-                    tc_commit(&bar->empty[sd]);
+                    tc_commit(&bar->empty[pe]);
                 }
             }
             tc_commit(&bar->dkv_done);
@@ -903,7 +896,7 @@ int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs
         init = true;
     }
     const float sl2 = LOG2E / sqrtf((float)HD);
-    fwd_tc_kernel<<<dim3((T + BQ - 1) / BQ, B * H), NT, SMEM, st>>>(mq, mk, mv, o, ors, lse, T, H, sl2);
+    fwd_tc_kernel<<<dim3(B * H, (T + BQ - 1) / BQ), NT, SMEM, st>>>(mq, mk, mv, o, ors, lse, T, H, sl2);
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
@@ -931,10 +924,10 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
         init = true;
     }
     const float scale = 1.0f / sqrtf((float)HD), sl2 = LOG2E * scale;
-    bwd_dq_tc_kernel<<<dim3((T + dq::BQ - 1) / dq::BQ, B * H), NT, dq::SMEM, st>>>(
+    bwd_dq_tc_kernel<<<dim3(B * H, (T + dq::BQ - 1) / dq::BQ), NT, dq::SMEM, st>>>(
         q128, do128, k64, v64, o, dout, ors, lse, dq_out, rs, Dscr, T, H, sl2, scale);
     GPT2_CUDA_TRY(cudaGetLastError());
-    bwd_dkv_tc_kernel<<<dim3((T + dkv::BKY - 1) / dkv::BKY, B * H), dkv::NTH, dkv::SMEM, st>>>(
+    bwd_dkv_tc_kernel<<<dim3(B * H, (T + dkv::BKY - 1) / dkv::BKY), dkv::NTH, dkv::SMEM, st>>>(
         q64, do64, k, v, lse, Dscr, dk_out, dv_out, rs, T, H, sl2, scale);
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(2);

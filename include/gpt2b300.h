@@ -206,7 +206,9 @@ int gpt2_profile_read(gpt2_model *m, int category, double *total_ms, double *tot
  * lse[b,h,i] = logsumexp_j of the scaled scores.
  * q/k/v/o are bf16 with element (b, t, h, d) at ptr[(b*T + t)*row_stride + h*hd + d]
  * (row_stride in elements: 3C for a fused qkv buffer, H*hd for separate
- * tensors).  lse is fp32 [B, H, T].  hd must be 64; row strides multiples of 8.
+ * tensors).  lse is fp32 [B, H, T].  hd must be 64; row strides multiples of 8;
+ * all pointers 16-byte aligned; B*H <= 2^31-1 and T <= 4194240 (65535 blocks
+ * of 64), else GPT2_ERR_BAD_SHAPE.
  */
 int gpt2_op_attention_forward(const void *q, const void *k, const void *v, int64_t qkv_row_stride, void *o,
                               int64_t o_row_stride, float *lse, int B, int T, int H, int hd, void *stream);
@@ -217,6 +219,7 @@ int gpt2_op_attention_forward(const void *q, const void *k, const void *v, int64
  * dS = P * (dP - D); dQ = dS K / sqrt(hd); dK = dS^T Q / sqrt(hd).
  * dq/dk/dv use qkv_row_stride (they may point into one fused dqkv buffer).
  * d_scratch: caller-owned fp32 workspace of B*H*T floats (holds D).
+ * Shape, stride and alignment limits are those of gpt2_op_attention_forward.
  */
 int gpt2_op_attention_backward(const void *q, const void *k, const void *v, int64_t qkv_row_stride,
                                const void *o, const void *dout, int64_t o_row_stride, const float *lse,

@@ -72,3 +72,23 @@ def test_build_rejects_bad_arguments_without_touching_a_gpu(libh):
     assert L.gpt2_build(ctypes.byref(c), 0, ctypes.c_void_p(256), 1 << 30, None, ctypes.byref(h)) == -1
     assert L.gpt2_strerror(-3) == b"token or target out of range"
     assert L.gpt2_forward(None, None, None, 1, 1, None) == -8
+
+
+def test_attention_entries_check_shapes_before_any_device_work(libh):
+    """The op-level attention calls return an error code for shapes their
+    kernels cannot launch; the checks run before any pointer is touched."""
+    import gpt_decoder_only_train_b300 as g
+
+    L = g.lib()
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its checks first
+    f = ctypes.cast(p, ctypes.POINTER(ctypes.c_float))
+    fwd = lambda B, T, H, hd, rs=192: L.gpt2_op_attention_forward(p, p, p, rs, p, 64, f, B, T, H, hd, None)
+    bwd = lambda B, T, H, hd, rs=192: L.gpt2_op_attention_backward(p, p, p, rs, p, p, 64, f, p, p, p, f, B, T, H,
+                                                                   hd, None)
+    bad_shape = -2  # GPT2_ERR_BAD_SHAPE
+    for call in (fwd, bwd):
+        assert call(2, 65535 * 64 + 1, 1, 64) == bad_shape  # more than 65535 blocks of 64 rows
+        assert call(2, 128, 1, 32) == bad_shape  # head dim other than 64
+        assert call(2, 128, 1, 64, rs=100) == bad_shape  # row stride not a multiple of 8
+        assert call(0, 128, 1, 64) == bad_shape
+    assert L.gpt2_op_attention_forward(None, p, p, 192, p, 64, f, 2, 128, 1, 64, None) == -8  # NULL pointer
