@@ -80,10 +80,27 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     P.num_k_blocks = ceil_div(g.K, BK);
     P.splits = 1;
     if (g.epi == GPT2_EPI_ACCUM_F32) {
-        // split K so that the work units fill about two waves of the persistent grid
+        // Split K (partial products are added into D) so that the work units
+        // fill whole waves of the persistent grid: the smallest split count
+        // whose last wave is at least 95% busy, else the best one found.  Each
+        // split keeps at least 4 K blocks.
         const int tiles = P.num_m_blocks * P.num_n_blocks;
-        if (tiles < 2 * num_sms)
-            P.splits = std::max(1, std::min(P.num_k_blocks / 4, (2 * num_sms + tiles - 1) / tiles));
+        if (tiles < 2 * num_sms) {
+            const int max_splits = std::max(1, P.num_k_blocks / 4);
+            int best = 1;
+            double best_eff = 0.0;
+            for (int sp = 1; sp <= max_splits; ++sp) {
+                const int kbps = ceil_div(P.num_k_blocks, sp), real = ceil_div(P.num_k_blocks, kbps);
+                const long long units = (long long)tiles * real;
+                const double eff = (double)units / ((double)ceil_div((int)units, num_sms) * num_sms);
+                if (eff > best_eff + 1e-9) {
+                    best_eff = eff;
+                    best = real;
+                }
+                if (eff >= 0.95) break;
+            }
+            P.splits = best;
+        }
     }
     P.k_blocks_per_split = ceil_div(P.num_k_blocks, P.splits);
     P.splits = ceil_div(P.num_k_blocks, P.k_blocks_per_split);
