@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
         for (int e = 0; e < E; ++e) adg[i][e] = adb[i][e] = 0.f;
     for (int row = blockIdx.x * warps + wid; row < N; row += gridDim.x * warps) {
         const int64_t off = (int64_t)row * C;
-        Pack16<T> vdy[VPL], vx[VPL];
+        // all three input rows are requested before any is used: one memory
+        // round trip per row (dres_in may alias dres_out; rows are disjoint)
+        Pack16<T> vdy[VPL], vx[VPL], vr[VPL];
         const float mu = mean[row], rs = rstd[row];
         float s1 = 0.f, s2 = 0.f;
 #pragma unroll
@@ -218,6 +220,7 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
             if (p < npk) {
                 vdy[i].load_stream(dy + off + p * E);
                 vx[i].load_stream(x + off + p * E);
+                if (dres_in) vr[i].load_stream(dres_in + off + p * E);
             }
         }
 #pragma unroll
@@ -243,15 +246,14 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
         for (int i = 0; i < VPL; ++i) {
             const int p = lane + 32 * i;
             if (p < npk) {
-                Pack16<T> base, o;
-                if (dres_in) base.load(dres_in + off + p * E);
+                Pack16<T> o;
                 F4x<E> gg;
                 gg.load(g + p * E);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const float xh = (vx[i].get(e) - mu) * rs;
                     const float dx = rs * (vdy[i].get(e) * gg.v[e] - m1 - xh * m2);
-                    o.set(e, (dres_in ? base.get(e) : 0.f) + dx);
+                    o.set(e, (dres_in ? vr[i].get(e) : 0.f) + dx);
                 }
                 o.store(dres_out + off + p * E);
             }
