@@ -556,38 +556,51 @@ __global__ void __launch_bounds__(NT, 2)
 }
 
 // ---------------------------------------------------------------- dK/dV kernel
-// One CTA per (128-key block, b*h), one CTA per SM; query blocks of 64 from the
-// key block on.  Every GEMM takes its A operand from TMEM, so shared memory only
-// carries the Q / dO tiles (B operands) and lse / D:
-//   S^T  = K Q^T      A = K (TMEM, loaded once)   B = Q  (K-major tile)
-//   dP^T = V dO^T     A = V (TMEM, loaded once)   B = dO (K-major tile)
-//   dV  += P^T dO     A = P^T (TMEM)              B = dO (MN-major view)
-//   dK  += dS^T Q     A = dS^T (TMEM)             B = Q  (MN-major view)
+// Persistent: one CTA per SM walks a list of work items (128-key block, b*h),
+// heaviest first, each CTA taking every gridDim.x-th item in alternating
+// direction.  An item iterates over the query blocks of 64 from its key
+// block on.  Every GEMM takes its A operand from TMEM, so shared memory only
+// carries K / V (staging), the Q / dO tiles (B operands) and lse / D:
+//   S^T  = K Q^T      A = K (TMEM)      B = Q  (K-major tile)
+//   dP^T = V dO^T     A = V (TMEM)      B = dO (K-major tile)
+//   dV  += P^T dO     A = P^T (TMEM)    B = dO (MN-major view)
+//   dK  += dS^T Q     A = dS^T (TMEM)   B = Q  (MN-major view)
 // S^T / dP^T are double-buffered.  The softmax warps read their 16 columns of
 // S^T and dP^T and write P^T / dS^T as bf16 back over the first 8 of those
 // columns, so that K-step kk of the dV / dK products reads columns
 // [16 kk, 16 kk + 8) of the buffer.  tcgen05.mma operations issued by one
-// thread execute in order, so S^T of block it+2 (issued after the dV / dK
-// products of block it) never overwrites P^T / dS^T before they are read.
+// thread execute in order, so S^T of block g+2 (issued after the dV / dK
+// products of block g) never overwrites P^T / dS^T before they are read.
+// K / V of the next item are staged (TMA) and copied into the second TMEM
+// slot while the current item runs, and the dV / dK read-out of an item
+// overlaps the first score products of the next one.
 // TMEM columns: S^T[b] [64b, 64b+64), dP^T[b] [128+64b, ...), dV [256,320),
-// dK [320,384), K [384,416), V [416,448) (bf16 pairs).
-// Warps: 0 loads Q / dO (TMA) and lse / D (cp.async) through a ring, 1 issues
-// the MMAs, 2-17 are the softmax warps: four per TMEM lane quadrant, each
-// owning 16 of the 64 queries of a block.
+// dK [320,384), K[s] [384+64s, +32), V[s] [416+64s, +32) (bf16 pairs).
+// Warps: 0 loads (TMA, cp.async), 1 issues the MMAs, 2-17 are the softmax
+// warps: four per TMEM lane quadrant, each owning 16 of a block's 64 queries.
 namespace dkv {
 constexpr int BKY = 128, BQ = 64, SLOTS = 12, SWARPS = 16, NLD = SLOTS / 2;
 constexpr int NTH = 64 + 32 * SWARPS;
-constexpr int TQ = BQ * HD * 2;                  // 8 KB
-constexpr int OFF_LD = SLOTS * TQ;               // [NLD][lse 64 | D 64] floats
+constexpr int TQ = BQ * HD * 2;    // 8 KB
+constexpr int TKV = BKY * HD * 2;  // 16 KB: a K or V tile
+constexpr int OFF_KV = SLOTS * TQ;  // [2 item slots][K | V]
+constexpr int OFF_LD = OFF_KV + 4 * TKV;  // [NLD][lse 64 | D 64] floats
 constexpr int OFF_BAR = OFF_LD + NLD * 2 * BQ * 4;
 constexpr int SMEM = 1024 + OFF_BAR + 512;
 constexpr uint32_t TCOLS = 512;
-constexpr uint32_t C_ST = 0, C_DPT = 128, C_DV = 256, C_DK = 320, C_K = 384, C_V = 416;
+constexpr uint32_t C_ST = 0, C_DPT = 128, C_DV = 256, C_DK = 320, C_KV = 384;
 struct Bars {
-    uint64_t kv_full, dkv_done, drain;
+    uint64_t dkv_done, dkv_free, drain;
+    uint64_t kv_sfull[2], kv_sempty[2], kv_tfull[2];
     uint64_t st_full[2], pds_full[2];
     uint64_t full[NLD], empty[NLD], ld_full[NLD];  // per ring entry: Q and dO slots + lse / D
 };
+// Item j of this CTA (snake order over the heaviest-first list), or -1.
+__device__ __forceinline__ int item_of(int j, int nitems) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long p = (long long)j * G + ((j & 1) ? G - 1 - c : c);
+    return p < nitems ? (int)p : -1;
+}
 }  // namespace dkv
 
 // tcgen05.mma with the A operand in TMEM (kind::f16, fp32 accumulate)
@@ -620,29 +633,29 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 __global__ void __launch_bounds__(dkv::NTH, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
-                      const bf16 *__restrict__ kg, const bf16 *__restrict__ vg, const float *__restrict__ lse,
-                      const float *__restrict__ Dscr, bf16 *__restrict__ dko, bf16 *__restrict__ dvo, int64_t rs,
-                      int T, int H, float sl2, float scale) {
-    constexpr int BKY = dkv::BKY, BQ = dkv::BQ, SLOTS = dkv::SLOTS, SWARPS = dkv::SWARPS, NLD = dkv::NLD;
-    constexpr int TQ = dkv::TQ, OFF_LD = dkv::OFF_LD, OFF_BAR = dkv::OFF_BAR;
+                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                      const float *__restrict__ lse, const float *__restrict__ Dscr, bf16 *__restrict__ dko,
+                      bf16 *__restrict__ dvo, int64_t rs, int T, int H, int nitems, float sl2, float scale) {
+    constexpr int BKY = dkv::BKY, BQ = dkv::BQ, SWARPS = dkv::SWARPS, NLD = dkv::NLD;
+    constexpr int TQ = dkv::TQ, TKV = dkv::TKV, OFF_KV = dkv::OFF_KV, OFF_LD = dkv::OFF_LD, OFF_BAR = dkv::OFF_BAR;
     constexpr uint32_t TCOLS = dkv::TCOLS, C_ST = dkv::C_ST, C_DPT = dkv::C_DPT, C_DV = dkv::C_DV, C_DK = dkv::C_DK,
-                       C_K = dkv::C_K, C_V = dkv::C_V;
+                       C_KV = dkv::C_KV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align_smem_1024(smem_raw);
     dkv::Bars *bar = reinterpret_cast<dkv::Bars *>(sm + OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + sizeof(dkv::Bars));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *ldbuf = reinterpret_cast<float *>(sm + OFF_LD);
-    const int kb = blockIdx.y;  // key block 0 sees every query block: launched first
-    const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int q0blk = kb * (BKY / BQ);
-    const int nit = (T + BQ - 1) / BQ - q0blk;
+    const int nqb = (T + BQ - 1) / BQ, BH = nitems / ((T + BKY - 1) / BKY);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        mbar_init(&bar->kv_full, SWARPS);
         mbar_init(&bar->dkv_done, 1);
+        mbar_init(&bar->dkv_free, SWARPS);
         mbar_init(&bar->drain, 1);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar->kv_sfull[i], 1);
+            mbar_init(&bar->kv_sempty[i], SWARPS);
+            mbar_init(&bar->kv_tfull[i], SWARPS);
             mbar_init(&bar->st_full[i], 1);
             mbar_init(&bar->pds_full[i], SWARPS);
         }
@@ -655,6 +668,8 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tdo);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TCOLS);
@@ -666,180 +681,217 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // Query block i uses ring entry e = i mod NLD: shared-memory slots 2e
-        // (Q) and 2e+1 (dO) and lse / D entry e.  The entry is refilled once the
+        // K / V of item j go to staging slot j & 1 one item ahead; query block g
+        // (counted over all items) uses ring entry g mod NLD: shared-memory
+        // slots 2e (Q) and 2e+1 (dO) and lse / D entry e, refilled once the
         // dV / dK products of the block that last used it have completed.
         bool ok = true;
-        int nissued = 0;
-        for (int i = 0; i < nit; ++i) {
-            const int e = i % NLD, sq = 2 * e, sd = sq + 1;
-            const uint32_t ph = (i / NLD) & 1;
-            if (!(ok = mbar_wait(&bar->empty[e], ph ^ 1, abort_flag, nullptr))) break;
-            const int q0 = (q0blk + i) * BQ;
+        int g = 0, nring = 0, nkv = 0;
+        auto load_kv = [&](int j) -> bool {
+            const int p = dkv::item_of(j, nitems);
+            if (p < 0) return true;
+            const int s = j & 1, kb = p / BH, bh = p % BH;
+            if (!mbar_wait(&bar->kv_sempty[s], ((j >> 1) & 1) ^ 1, abort_flag, nullptr)) return false;
             if (lane == 0) {
-                mbar_expect_tx(&bar->full[e], 2 * TQ);
-                tma_load_3d(sm + sq * TQ, &tq, &bar->full[e], h * HD, q0, b);
-                tma_load_3d(sm + sd * TQ, &tdo, &bar->full[e], h * HD, q0, b);
+                mbar_expect_tx(&bar->kv_sfull[s], 2 * TKV);
+                tma_load_3d(sm + OFF_KV + s * 2 * TKV, &tk, &bar->kv_sfull[s], (bh % H) * HD, kb * BKY, bh / H);
+                tma_load_3d(sm + OFF_KV + s * 2 * TKV + TKV, &tv, &bar->kv_sfull[s], (bh % H) * HD, kb * BKY, bh / H);
             }
-            // lanes 0-15: lse of queries q0 + 4 lane + j; lanes 16-31: D
-            const float *src = (lane < 16 ? lse : Dscr) + (int64_t)bh * T;
-            float *dst = ldbuf + e * 128 + lane * 4;
+            nkv = j + 1;
+            return true;
+        };
+        ok = load_kv(0);
+        for (int j = 0; ok; ++j) {
+            const int p = dkv::item_of(j, nitems);
+            if (p < 0) break;
+            if (!(ok = load_kv(j + 1))) break;
+            const int kb = p / BH, bh = p % BH, b = bh / H, h = bh % H, nit = nqb - 2 * kb;
+            for (int i = 0; i < nit; ++i, ++g) {
+                const int e = g % NLD;
+                const uint32_t ph = (g / NLD) & 1;
+                if (!(ok = mbar_wait(&bar->empty[e], ph ^ 1, abort_flag, nullptr))) break;
+                const int q0 = (2 * kb + i) * BQ;
+                if (lane == 0) {
+                    mbar_expect_tx(&bar->full[e], 2 * TQ);
+                    tma_load_3d(sm + 2 * e * TQ, &tq, &bar->full[e], h * HD, q0, b);
+                    tma_load_3d(sm + (2 * e + 1) * TQ, &tdo, &bar->full[e], h * HD, q0, b);
+                }
+                // lanes 0-15: lse of queries q0 + 4 lane + jj; lanes 16-31: D
+                const float *src = (lane < 16 ? lse : Dscr) + (int64_t)bh * T;
+                float *dst = ldbuf + e * 128 + lane * 4;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int q = q0 + (lane & 15) * 4 + j;
-                cp_async4(dst + j, src + (q < T ? q : 0), q < T ? 4u : 0u);
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int q = q0 + (lane & 15) * 4 + jj;
+                    cp_async4(dst + jj, src + (q < T ? q : 0), q < T ? 4u : 0u);
+                }
+                cp_async_arrive_noinc(&bar->ld_full[e]);
+                nring = g + 1;
             }
-            cp_async_arrive_noinc(&bar->ld_full[e]);
-            nissued = i + 1;
         }
-        if (!ok && lane == 0) {
-            for (int i = nissued > NLD ? nissued - NLD : 0; i < nissued; ++i)
-                mbar_drain(&bar->full[i % NLD], (i / NLD) & 1);
+        if (!ok && lane == 0) {  // let the copies already issued land before the CTA exits
+            for (int i = nring > NLD ? nring - NLD : 0; i < nring; ++i) mbar_drain(&bar->full[i % NLD], (i / NLD) & 1);
+            for (int j = nkv > 2 ? nkv - 2 : 0; j < nkv; ++j) mbar_drain(&bar->kv_sfull[j & 1], (j >> 1) & 1);
         }
         cp_async_wait_all();
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t ID_ST = instr_desc(BQ, false, false);  // 128 x 64, B = Q / dO K-major
             constexpr uint32_t ID_G = instr_desc(HD, false, true);    // 128 x 64, B = dO / Q MN-major
-            const uint64_t ring_k = smem_desc(smem_u32(sm), 16, 1024);    // K-major view of slot 0
-            const uint64_t ring_mn = smem_desc(smem_u32(sm), 8192, 1024); // MN-major view of slot 0
-            bool ok = mbar_wait(&bar->kv_full, 0, abort_flag, nullptr);
-            tc_fence_after();
-            for (int it = 0; it <= nit && ok; ++it) {
-                if (it < nit) {
-                    const int bb = it & 1, e = it % NLD, sq = 2 * e, sd = sq + 1;
-                    if (!(ok = mbar_wait(&bar->full[e], (it / NLD) & 1, abort_flag, nullptr))) break;
+            const uint64_t ring_k = smem_desc(smem_u32(sm), 16, 1024);     // K-major view of slot 0
+            const uint64_t ring_mn = smem_desc(smem_u32(sm), 8192, 1024);  // MN-major view of slot 0
+            bool ok = true;
+            // dV / dK products of query block gp, the it-th block of item j
+            auto grads = [&](int gp, int j, int it, bool last) -> bool {
+                const int pb = gp & 1, pe = gp % NLD;
+                if (!mbar_wait(&bar->pds_full[pb], (gp >> 1) & 1, abort_flag, nullptr)) return false;
+                if (it == 0 && j > 0 && !mbar_wait(&bar->dkv_free, (j - 1) & 1, abort_flag, nullptr)) return false;
+                tc_fence_after();
+                const uint64_t bq = ring_mn + (uint64_t)(2 * pe * (TQ >> 4));
+                const uint64_t bd = ring_mn + (uint64_t)((2 * pe + 1) * (TQ >> 4));
+                const uint32_t pa = tmem + C_ST + pb * 64, da = tmem + C_DPT + pb * 64;
+                const uint32_t acc0 = it > 0 ? 1u : 0u;
+                tc_mma_ts(tmem + C_DV, pa, bd, ID_G, acc0);
+#pragma unroll
+                for (int kk = 1; kk < BQ / 16; ++kk) tc_mma_ts(tmem + C_DV, pa + 16 * kk, bd + 128 * kk, ID_G, 1u);
+                tc_mma_ts(tmem + C_DK, da, bq, ID_G, acc0);
+#pragma unroll
+                for (int kk = 1; kk < BQ / 16; ++kk) tc_mma_ts(tmem + C_DK, da + 16 * kk, bq + 128 * kk, ID_G, 1u);
+                tc_commit(&bar->empty[pe]);
+                if (last) tc_commit(&bar->dkv_done);
+                return true;
+            };
+            int g = 0, pj = 0, pit = 0;
+            bool plast = false;
+            for (int j = 0; ok; ++j) {
+                const int p = dkv::item_of(j, nitems);
+                if (p < 0) break;
+                const int nit = nqb - 2 * (p / BH);
+                if (!(ok = mbar_wait(&bar->kv_tfull[j & 1], (j >> 1) & 1, abort_flag, nullptr))) break;
+                const uint32_t tK = tmem + C_KV + 64 * (j & 1), tV = tK + 32;
+                for (int it = 0; it < nit; ++it, ++g) {
+                    const int bb = g & 1, e = g % NLD;
+                    if (!(ok = mbar_wait(&bar->full[e], (g / NLD) & 1, abort_flag, nullptr))) break;
                     tc_fence_after();
-                    const uint64_t bq = ring_k + (uint64_t)(sq * (TQ >> 4)), bd = ring_k + (uint64_t)(sd * (TQ >> 4));
+                    const uint64_t bq = ring_k + (uint64_t)(2 * e * (TQ >> 4));
+                    const uint64_t bd = ring_k + (uint64_t)((2 * e + 1) * (TQ >> 4));
                     const uint32_t ts = tmem + C_ST + bb * 64, td = tmem + C_DPT + bb * 64;
-                    tc_mma_ts(ts, tmem + C_K, bq, ID_ST, 0u);
+                    tc_mma_ts(ts, tK, bq, ID_ST, 0u);
 #pragma unroll
-                    for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(ts, tmem + C_K + 8 * kk, bq + 2 * kk, ID_ST, 1u);
-                    tc_mma_ts(td, tmem + C_V, bd, ID_ST, 0u);
+                    for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(ts, tK + 8 * kk, bq + 2 * kk, ID_ST, 1u);
+                    tc_mma_ts(td, tV, bd, ID_ST, 0u);
 #pragma unroll
-                    for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(td, tmem + C_V + 8 * kk, bd + 2 * kk, ID_ST, 1u);
+                    for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(td, tV + 8 * kk, bd + 2 * kk, ID_ST, 1u);
                     tc_commit(&bar->st_full[bb]);
-                }
-                if (it >= 1) {  // dV and dK products of the previous block
-                    const int pi = it - 1, pb = pi & 1, pe = pi % NLD, sq = 2 * pe, sd = sq + 1;
-                    if (!(ok = mbar_wait(&bar->pds_full[pb], (pi >> 1) & 1, abort_flag, nullptr))) break;
-                    tc_fence_after();
-                    const uint64_t bq = ring_mn + (uint64_t)(sq * (TQ >> 4)), bd = ring_mn + (uint64_t)(sd * (TQ >> 4));
-                    const uint32_t pa = tmem + C_ST + pb * 64, da = tmem + C_DPT + pb * 64;
-                    const uint32_t acc0 = pi > 0 ? 1u : 0u;
-                    tc_mma_ts(tmem + C_DV, pa, bd, ID_G, acc0);
-#pragma unroll
-                    for (int kk = 1; kk < BQ / 16; ++kk) tc_mma_ts(tmem + C_DV, pa + 16 * kk, bd + 128 * kk, ID_G, 1u);
-                    tc_mma_ts(tmem + C_DK, da, bq, ID_G, acc0);
-#pragma unroll
-                    for (int kk = 1; kk < BQ / 16; ++kk) tc_mma_ts(tmem + C_DK, da + 16 * kk, bq + 128 * kk, ID_G, 1u);
-                    tc_commit(&bar->empty[pe]);
+                    if (g > 0 && !(ok = grads(g - 1, pj, pit, plast))) break;
+                    pj = j, pit = it, plast = it == nit - 1;
                 }
             }
-            tc_commit(&bar->dkv_done);
+            if (ok && g > 0) grads(g - 1, pj, pit, plast);
             tc_commit(&bar->drain);
             mbar_drain(&bar->drain, 0);
         }
     } else {
         const int quad = warp & 3, sub = (warp - 2) >> 2;  // sub: queries [16 sub, 16 sub + 16) of each block
-        const int r = quad * 32 + lane, key = kb * BKY + r;
+        const int r = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        // Row `key` of K and V, elements [16 sub, 16 sub + 16), into TMEM as A operands.
-        {
-            uint32_t kr[8], vr[8];
-            if (key < T) {
-                const int64_t off = ((int64_t)b * T + key) * rs + h * HD + sub * 16;
-                const uint4 k0 = *reinterpret_cast<const uint4 *>(kg + off);
-                const uint4 k1 = *reinterpret_cast<const uint4 *>(kg + off + 8);
-                const uint4 v0 = *reinterpret_cast<const uint4 *>(vg + off);
-                const uint4 v1 = *reinterpret_cast<const uint4 *>(vg + off + 8);
-                kr[0] = k0.x, kr[1] = k0.y, kr[2] = k0.z, kr[3] = k0.w, kr[4] = k1.x, kr[5] = k1.y, kr[6] = k1.z,
-                kr[7] = k1.w;
-                vr[0] = v0.x, vr[1] = v0.y, vr[2] = v0.z, vr[3] = v0.w, vr[4] = v1.x, vr[5] = v1.y, vr[6] = v1.z,
-                vr[7] = v1.w;
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) kr[i] = vr[i] = 0u;
-            }
-            tmem_st8(tmem + lane_off + C_K + sub * 8, kr);
-            tmem_st8(tmem + lane_off + C_V + sub * 8, vr);
+        // Row r of the staged K and V tiles of item j, elements [16 sub, 16 sub + 16)
+        // (128-byte swizzle: chunk c of row r sits at chunk c ^ (r & 7)), into TMEM slot j & 1.
+        auto copy_kv = [&](int j) -> bool {
+            const int s = j & 1;
+            if (!mbar_wait(&bar->kv_sfull[s], (j >> 1) & 1, abort_flag, nullptr)) return false;
+            const uint8_t *kt = sm + OFF_KV + s * 2 * TKV + r * 128, *vt = kt + TKV;
+            const int c0 = ((2 * sub) ^ (r & 7)) << 4, c1 = ((2 * sub + 1) ^ (r & 7)) << 4;
+            const uint4 k0 = *reinterpret_cast<const uint4 *>(kt + c0), k1 = *reinterpret_cast<const uint4 *>(kt + c1);
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(vt + c0), v1 = *reinterpret_cast<const uint4 *>(vt + c1);
+            const uint32_t kr[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+            const uint32_t vr[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            tmem_st8(tmem + lane_off + C_KV + 64 * s + sub * 8, kr);
+            tmem_st8(tmem + lane_off + C_KV + 64 * s + 32 + sub * 8, vr);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->kv_full);
-        }
-        bool ok = true;
-        for (int it = 0; it < nit; ++it) {
-            const int bb = it & 1, e = it % NLD;
-            if (!(ok = mbar_wait(&bar->st_full[bb], (it >> 1) & 1, abort_flag, nullptr))) break;
-            if (!(ok = mbar_wait(&bar->ld_full[e], (it / NLD) & 1, abort_flag, nullptr))) break;
-            tc_fence_after();
-            const uint32_t cs = tmem + lane_off + C_ST + bb * 64 + sub * 16;
-            const uint32_t cd = tmem + lane_off + C_DPT + bb * 64 + sub * 16;
-            uint32_t ra[16], rb[16];
-            tmem_ld16_nowait(cs, ra);
-            tmem_ld16_nowait(cd, rb);
-            tmem_ld_wait();
-            const float *L = ldbuf + e * 128 + sub * 16, *Dv = ldbuf + e * 128 + 64 + sub * 16;
-            const int qbase = (q0blk + it) * BQ + sub * 16;
-            // visible queries of this thread's 16: lo <= c <= hi (q >= key, q < T; none if key >= T)
-            const int lo = key - qbase, hi = key < T ? T - 1 - qbase : -1;
-            const bool full = lo <= 0 && hi >= 15;
-            uint32_t wp[8], wd[8];
-#pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(L + i);
-                const float4 d4 = *reinterpret_cast<const float4 *>(Dv + i);
-                const float lv[4] = {a4.x * LOG2E, a4.y * LOG2E, a4.z * LOG2E, a4.w * LOG2E};
-                const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                for (int e2 = 0; e2 < 4; e2 += 2) {
-                    const int c = i + e2;
-                    float p0 = ex2(fmaf(__uint_as_float(ra[c]), sl2, -lv[e2]));
-                    float p1 = ex2(fmaf(__uint_as_float(ra[c + 1]), sl2, -lv[e2 + 1]));
-                    if (!full) {
-                        p0 = (c >= lo && c <= hi) ? p0 : 0.f;
-                        p1 = (c + 1 >= lo && c + 1 <= hi) ? p1 : 0.f;
-                    }
-                    wp[c >> 1] = pack_bf16x2(p0, p1);
-                    wd[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(rb[c]) - dv4[e2]),
-                                             p1 * (__uint_as_float(rb[c + 1]) - dv4[e2 + 1]));
-                }
+            if (lane == 0) {
+                mbar_arrive(&bar->kv_tfull[s]);
+                mbar_arrive(&bar->kv_sempty[s]);
             }
-            tmem_st8(cs, wp);  // P^T over the first 8 of this thread's S^T columns
-            tmem_st8(cd, wd);  // dS^T over the first 8 of its dP^T columns
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->pds_full[bb]);
-        }
-        if (ok && mbar_wait(&bar->dkv_done, 0, abort_flag, nullptr)) {
-            tc_fence_after();
-            float fv[16], fk[16];
-            {
+            return true;
+        };
+        bool ok = copy_kv(0);
+        int g = 0;
+        for (int j = 0; ok; ++j) {
+            const int p = dkv::item_of(j, nitems);
+            if (p < 0) break;
+            const int kb = p / BH, bh = p % BH, b = bh / H, h = bh % H, nit = nqb - 2 * kb;
+            const int key = kb * BKY + r;
+            for (int it = 0; it < nit; ++it, ++g) {
+                const int bb = g & 1, e = g % NLD;
+                if (!(ok = mbar_wait(&bar->st_full[bb], (g >> 1) & 1, abort_flag, nullptr))) break;
+                if (!(ok = mbar_wait(&bar->ld_full[e], (g / NLD) & 1, abort_flag, nullptr))) break;
+                tc_fence_after();
+                const uint32_t cs = tmem + lane_off + C_ST + bb * 64 + sub * 16;
+                const uint32_t cd = tmem + lane_off + C_DPT + bb * 64 + sub * 16;
                 uint32_t ra[16], rb[16];
-                tmem_ld16_nowait(tmem + lane_off + C_DV + sub * 16, ra);
-                tmem_ld16_nowait(tmem + lane_off + C_DK + sub * 16, rb);
+                tmem_ld16_nowait(cs, ra);
+                tmem_ld16_nowait(cd, rb);
                 tmem_ld_wait();
+                const float *L = ldbuf + e * 128 + sub * 16, *Dv = ldbuf + e * 128 + 64 + sub * 16;
+                const int qbase = (2 * kb + it) * BQ + sub * 16;
+                // visible queries of this thread's 16: lo <= c <= hi (q >= key, q < T; none if key >= T)
+                const int lo = key - qbase, hi = key < T ? T - 1 - qbase : -1;
+                const bool full = lo <= 0 && hi >= 15;
+                uint32_t wp[8], wd[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    fv[i] = __uint_as_float(ra[i]);
-                    fk[i] = __uint_as_float(rb[i]);
+                for (int i = 0; i < 16; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(L + i);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(Dv + i);
+                    const float lv[4] = {a4.x * LOG2E, a4.y * LOG2E, a4.z * LOG2E, a4.w * LOG2E};
+                    const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; e2 += 2) {
+                        const int c = i + e2;
+                        float p0 = ex2(fmaf(__uint_as_float(ra[c]), sl2, -lv[e2]));
+                        float p1 = ex2(fmaf(__uint_as_float(ra[c + 1]), sl2, -lv[e2 + 1]));
+                        if (!full) {
+                            p0 = (c >= lo && c <= hi) ? p0 : 0.f;
+                            p1 = (c + 1 >= lo && c + 1 <= hi) ? p1 : 0.f;
+                        }
+                        wp[c >> 1] = pack_bf16x2(p0, p1);
+                        wd[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(rb[c]) - dv4[e2]),
+                                                 p1 * (__uint_as_float(rb[c + 1]) - dv4[e2 + 1]));
+                    }
                 }
+                tmem_st8(cs, wp);  // P^T over the first 8 of this thread's S^T columns
+                tmem_st8(cd, wd);  // dS^T over the first 8 of its dP^T columns
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->pds_full[bb]);
+                if (it == 0 && dkv::item_of(j + 1, nitems) >= 0 && !(ok = copy_kv(j + 1))) break;
             }
+            if (!ok) break;
+            // dV / dK of the item: read out of TMEM, release the accumulators, store
+            if (!(ok = mbar_wait(&bar->dkv_done, j & 1, abort_flag, nullptr))) break;
+            tc_fence_after();
+            uint32_t ra[16], rb[16];
+            tmem_ld16_nowait(tmem + lane_off + C_DV + sub * 16, ra);
+            tmem_ld16_nowait(tmem + lane_off + C_DK + sub * 16, rb);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->dkv_free);
             if (key < T) {
                 const int64_t off = ((int64_t)b * T + key) * rs + h * HD + sub * 16;
 #pragma unroll
                 for (int d = 0; d < 16; d += 8) {
                     uint4 u, w;
-                    u.x = pack_bf16x2(fv[d], fv[d + 1]);
-                    u.y = pack_bf16x2(fv[d + 2], fv[d + 3]);
-                    u.z = pack_bf16x2(fv[d + 4], fv[d + 5]);
-                    u.w = pack_bf16x2(fv[d + 6], fv[d + 7]);
-                    w.x = pack_bf16x2(fk[d] * scale, fk[d + 1] * scale);
-                    w.y = pack_bf16x2(fk[d + 2] * scale, fk[d + 3] * scale);
-                    w.z = pack_bf16x2(fk[d + 4] * scale, fk[d + 5] * scale);
-                    w.w = pack_bf16x2(fk[d + 6] * scale, fk[d + 7] * scale);
+                    u.x = pack_bf16x2(__uint_as_float(ra[d]), __uint_as_float(ra[d + 1]));
+                    u.y = pack_bf16x2(__uint_as_float(ra[d + 2]), __uint_as_float(ra[d + 3]));
+                    u.z = pack_bf16x2(__uint_as_float(ra[d + 4]), __uint_as_float(ra[d + 5]));
+                    u.w = pack_bf16x2(__uint_as_float(ra[d + 6]), __uint_as_float(ra[d + 7]));
+                    w.x = pack_bf16x2(__uint_as_float(rb[d]) * scale, __uint_as_float(rb[d + 1]) * scale);
+                    w.y = pack_bf16x2(__uint_as_float(rb[d + 2]) * scale, __uint_as_float(rb[d + 3]) * scale);
+                    w.z = pack_bf16x2(__uint_as_float(rb[d + 4]) * scale, __uint_as_float(rb[d + 5]) * scale);
+                    w.w = pack_bf16x2(__uint_as_float(rb[d + 6]) * scale, __uint_as_float(rb[d + 7]) * scale);
                     *reinterpret_cast<uint4 *>(dvo + off + d) = u;
                     *reinterpret_cast<uint4 *>(dko + off + d) = w;
                 }
@@ -910,12 +962,14 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
          reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq_out) |
          reinterpret_cast<uintptr_t>(dk_out) | reinterpret_cast<uintptr_t>(dv_out)) & 15)
         return GPT2_ERR_BAD_ARG;
-    CUtensorMap q128, do128, k64, v64, q64, do64;
+    CUtensorMap q128, do128, k64, v64, q64, do64, k128, v128;
     if (int rc = encode_qkv_map(&q128, q, rs, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&do128, dout, ors, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&k64, k, rs, T, B, H, 64)) return rc;
     if (int rc = encode_qkv_map(&v64, v, rs, T, B, H, 64)) return rc;
     if (int rc = encode_qkv_map(&q64, q, rs, T, B, H, 64)) return rc;
+    if (int rc = encode_qkv_map(&k128, k, rs, T, B, H, 128)) return rc;
+    if (int rc = encode_qkv_map(&v128, v, rs, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&do64, dout, ors, T, B, H, 64)) return rc;
     static bool init = false;
     if (!init) {
@@ -927,8 +981,13 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
     bwd_dq_tc_kernel<<<dim3(B * H, (T + dq::BQ - 1) / dq::BQ), NT, dq::SMEM, st>>>(
         q128, do128, k64, v64, o, dout, ors, lse, dq_out, rs, Dscr, T, H, sl2, scale);
     GPT2_CUDA_TRY(cudaGetLastError());
-    bwd_dkv_tc_kernel<<<dim3(B * H, (T + dkv::BKY - 1) / dkv::BKY), dkv::NTH, dkv::SMEM, st>>>(
-        q64, do64, k, v, lse, Dscr, dk_out, dv_out, rs, T, H, sl2, scale);
+    // persistent dK/dV grid: one CTA per SM over (key block, b*h) items, heaviest first
+    const int nitems = ((T + dkv::BKY - 1) / dkv::BKY) * B * H;
+    int dev = 0, sms = 0;
+    GPT2_CUDA_TRY(cudaGetDevice(&dev));
+    GPT2_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    bwd_dkv_tc_kernel<<<std::min(nitems, sms), dkv::NTH, dkv::SMEM, st>>>(q64, do64, k128, v128, lse, Dscr, dk_out,
+                                                                          dv_out, rs, T, H, nitems, sl2, scale);
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(2);
     return GPT2_OK;
