@@ -835,29 +835,35 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
                 tmem_ld16_nowait(cd, rb);
                 tmem_ld_wait();
                 const float *L = ldbuf + e * 128 + sub * 16, *Dv = ldbuf + e * 128 + 64 + sub * 16;
-                const int qbase = (2 * kb + it) * BQ + sub * 16;
-                // visible queries of this thread's 16: lo <= c <= hi (q >= key, q < T; none if key >= T)
+                const int q0 = (2 * kb + it) * BQ, qbase = q0 + sub * 16;
+                // Blocks past the diagonal with all keys and queries below T need no
+                // mask (the same answer for the whole CTA).  Otherwise the visible
+                // queries of this thread's 16 are lo <= c <= hi (q >= key, q < T;
+                // none if key >= T).
+                const bool block_full = q0 >= kb * BKY + BKY - 1 && q0 + BQ <= T && kb * BKY + BKY <= T;
                 const int lo = key - qbase, hi = key < T ? T - 1 - qbase : -1;
-                const bool full = lo <= 0 && hi >= 15;
+                const F2 sl2x2 = f2(sl2, sl2), nlog2e = f2(-LOG2E, -LOG2E);
                 uint32_t wp[8], wd[8];
 #pragma unroll
                 for (int i = 0; i < 16; i += 4) {
                     const float4 a4 = *reinterpret_cast<const float4 *>(L + i);
                     const float4 d4 = *reinterpret_cast<const float4 *>(Dv + i);
-                    const float lv[4] = {a4.x * LOG2E, a4.y * LOG2E, a4.z * LOG2E, a4.w * LOG2E};
-                    const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                    const F2 nl[2] = {f2_mul(f2(a4.x, a4.y), nlog2e), f2_mul(f2(a4.z, a4.w), nlog2e)};
+                    const F2 dd[2] = {f2(d4.x, d4.y), f2(d4.z, d4.w)};
 #pragma unroll
-                    for (int e2 = 0; e2 < 4; e2 += 2) {
-                        const int c = i + e2;
-                        float p0 = ex2(fmaf(__uint_as_float(ra[c]), sl2, -lv[e2]));
-                        float p1 = ex2(fmaf(__uint_as_float(ra[c + 1]), sl2, -lv[e2 + 1]));
-                        if (!full) {
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int c = i + 2 * h2;
+                        // s * scale * log2(e) - lse * log2(e), two columns per instruction
+                        const F2 t = f2_fma(f2(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sl2x2, nl[h2]);
+                        float p0 = ex2(f2_lo(t)), p1 = ex2(f2_hi(t));
+                        if (!block_full) {
                             p0 = (c >= lo && c <= hi) ? p0 : 0.f;
                             p1 = (c + 1 >= lo && c + 1 <= hi) ? p1 : 0.f;
                         }
                         wp[c >> 1] = pack_bf16x2(p0, p1);
-                        wd[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(rb[c]) - dv4[e2]),
-                                                 p1 * (__uint_as_float(rb[c + 1]) - dv4[e2 + 1]));
+                        const F2 ds = f2_mul(f2(p0, p1),
+                                             f2_sub(f2(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), dd[h2]));
+                        wd[c >> 1] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
                     }
                 }
                 tmem_st8(cs, wp);  // P^T over the first 8 of this thread's S^T columns

@@ -60,6 +60,43 @@ template <typename T> struct Pack16 {
     __device__ __forceinline__ void store(T *ptr) const { *reinterpret_cast<uint4 *>(ptr) = raw; }
 };
 
+// Two fp32 values packed in one 64-bit register: the .f32x2 forms of
+// fma / mul / add / sub (sm_100 and later) do the work of two scalar
+// instructions with one issue slot.  Rounding is that of the scalar forms.
+struct F2 {
+    unsigned long long u;
+};
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.u) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2_lo(F2 v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v.u));
+    return lo;
+}
+__device__ __forceinline__ float f2_hi(F2 v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v.u));
+    return hi;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
+    F2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.u) : "l"(a.u), "l"(b.u), "l"(c.u));
+    return d;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+    F2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.u) : "l"(a.u), "l"(b.u));
+    return d;
+}
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+    F2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d.u) : "l"(a.u), "l"(b.u));
+    return d;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
