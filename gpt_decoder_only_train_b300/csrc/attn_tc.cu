@@ -344,204 +344,344 @@ __device__ __forceinline__ void store_row_chunks(uint8_t *atom, int r, int cc, c
     *reinterpret_cast<uint4 *>(row + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// tcgen05.mma with the A operand in TMEM (kind::f16, fp32 accumulate)
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// 32 lanes x 8 columns of 32-bit words from registers into TMEM
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 4-byte asynchronous global -> shared copy; src_bytes 0 stores a zero
+__device__ __forceinline__ void cp_async4(float *dst, const float *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+// the mbarrier counts one arrival when this thread's earlier cp.async copies have landed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// 16 bf16 of row r, elements [16 sub, 16 sub + 16), from a 128-byte-swizzled tile (chunk c of
+// row r at chunk c ^ (r & 7)) as 8 packed words
+__device__ __forceinline__ void tile_row16(const uint8_t *tile, int r, int sub, uint32_t (&w)[8]) {
+    const uint8_t *row = tile + r * 128;
+    const uint4 a = *reinterpret_cast<const uint4 *>(row + (((2 * sub) ^ (r & 7)) << 4));
+    const uint4 c = *reinterpret_cast<const uint4 *>(row + (((2 * sub + 1) ^ (r & 7)) << 4));
+    w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w, w[4] = c.x, w[5] = c.y, w[6] = c.z, w[7] = c.w;
+}
+// Item j of this CTA in a persistent grid: every gridDim.x-th entry of a
+// heaviest-first list, in alternating direction, or -1 past the end.
+__device__ __forceinline__ int item_of(int j, int nitems) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long p = (long long)j * G + ((j & 1) ? G - 1 - c : c);
+    return p < nitems ? (int)p : -1;
+}
+
 // ---------------------------------------------------------------- dQ kernel
-// One CTA per (128-query block, b*h); key blocks of 64.  TMEM: S [0,64),
-// dP [64,128), dQ [128,192).  Softmax threads: two per query row, 32 keys each.
+// Persistent: one CTA per SM walks the (128-query block, b*h) items, heaviest
+// first; an item iterates over the key blocks of 64 up to the diagonal.
+//   S  = Q K^T      A = Q (TMEM)     B = K (K-major tile)
+//   dP = dO V^T     A = dO (TMEM)    B = V (K-major tile)
+//   dQ += dS K      A = dS (TMEM)    B = K (MN-major view)
+// S / dP are double-buffered; the softmax warps write dS as bf16 over the
+// first 8 of their 16 dP columns (K-step kk of the dQ product reads columns
+// [16 kk, 16 kk + 8)).  Q, dO and O of the next item are staged by TMA while
+// the current item runs; D = rowsum(dO * O) is computed from the staged tiles
+// (every thread sums its own row in full) and written for the dK/dV kernel.
+// TMEM columns: S[b] [64b, +64), dP[b] [128+64b, +64), dQ [256,320),
+// Q[s] [320+64s, +32), dO[s] [352+64s, +32).
 namespace dq {
-constexpr int BQ = 128, BK = 64, SLOTS = 7;
-constexpr int TQ = BQ * HD * 2;      // 16 KB
-constexpr int TK = BK * HD * 2;      // 8 KB
-constexpr int OFF_DO = TQ, OFF_RING = 2 * TQ, OFF_DS = OFF_RING + SLOTS * TK, OFF_RED = OFF_DS + TQ;
-constexpr int OFF_BAR = OFF_RED + 2 * 128 * 4;
-constexpr int SMEM = 1024 + OFF_BAR + 256;
+constexpr int BQ = 128, BK = 64, NST = 6, SWARPS = 16;
+constexpr int NTH = 64 + 32 * SWARPS;
+constexpr int TQ = BQ * HD * 2;   // 16 KB: a Q, dO or O tile
+constexpr int TK = BK * HD * 2;   // 8 KB: a K or V tile
+constexpr int OFF_ITEM = NST * 2 * TK;      // [2 item slots][Q | dO | O]
+constexpr int OFF_LSE = OFF_ITEM + 6 * TQ;  // [2][128] floats
+constexpr int OFF_BAR = OFF_LSE + 2 * BQ * 4;
+constexpr int SMEM = 1024 + OFF_BAR + 512;
+constexpr uint32_t TCOLS = 512;
+constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256, C_QD = 320;
 struct Bars {
-    uint64_t qd_full, sp_full, ds_full, ds_free, dq_done, drain;
-    uint64_t full[SLOTS], empty[SLOTS];
+    uint64_t dq_done, dq_free, drain;
+    uint64_t it_sfull[2], it_lfull[2], it_sempty[2], it_tfull[2];
+    uint64_t sp_full[2], ds_full[2];
+    uint64_t full[NST], empty[NST];  // per ring entry: K and V tiles of one key block
 };
 }  // namespace dq
 
-__global__ void __launch_bounds__(NT, 2)
+__global__ void __launch_bounds__(dq::NTH, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
-                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                     const bf16 *__restrict__ o, const bf16 *__restrict__ dout, int64_t ors,
-                     const float *__restrict__ lse, bf16 *__restrict__ dqo, int64_t rs, float *__restrict__ Dscr,
-                     int T, int H, float sl2, float scale) {
+                     const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv, const float *__restrict__ lse,
+                     bf16 *__restrict__ dqo, int64_t rs, float *__restrict__ Dscr, int T, int H, int nitems,
+                     float sl2, float scale) {
+    constexpr int BQ = dq::BQ, BK = dq::BK, NST = dq::NST, SWARPS = dq::SWARPS;
+    constexpr int TQ = dq::TQ, TK = dq::TK, OFF_ITEM = dq::OFF_ITEM, OFF_LSE = dq::OFF_LSE, OFF_BAR = dq::OFF_BAR;
+    constexpr uint32_t TCOLS = dq::TCOLS, C_S = dq::C_S, C_DP = dq::C_DP, C_DQ = dq::C_DQ, C_QD = dq::C_QD;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = align_smem_1024(smem_raw);
-    dq::Bars *bar = reinterpret_cast<dq::Bars *>(sm + dq::OFF_BAR);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + dq::OFF_BAR + sizeof(dq::Bars));
+    dq::Bars *bar = reinterpret_cast<dq::Bars *>(sm + OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + sizeof(dq::Bars));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    const int nqb = (T + dq::BQ - 1) / dq::BQ;
-    const int qb = nqb - 1 - blockIdx.y;  // heaviest query blocks launched first
-    const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int nkv = min((T + dq::BK - 1) / dq::BK, (qb + 1) * (dq::BQ / dq::BK));
+    float *lsebuf = reinterpret_cast<float *>(sm + OFF_LSE);
+    const int nqb = (T + BQ - 1) / BQ, nkb = (T + BK - 1) / BK, BH = nitems / nqb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // item p: query block nqb - 1 - p / BH (heaviest first), b*h = p % BH
+    auto item_qb = [&](int p) { return nqb - 1 - p / BH; };
+    auto item_nkv = [&](int qb) { return min(nkb, (qb + 1) * (BQ / BK)); };
     if (threadIdx.x == 0) {
-        mbar_init(&bar->qd_full, 1);
-        mbar_init(&bar->sp_full, 1);
-        mbar_init(&bar->ds_full, SOFTMAX_WARPS);
-        mbar_init(&bar->ds_free, 1);
         mbar_init(&bar->dq_done, 1);
+        mbar_init(&bar->dq_free, SWARPS);
         mbar_init(&bar->drain, 1);
-        for (int i = 0; i < dq::SLOTS; ++i) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar->it_sfull[i], 1);
+            mbar_init(&bar->it_lfull[i], 32);
+            mbar_init(&bar->it_sempty[i], SWARPS);
+            mbar_init(&bar->it_tfull[i], SWARPS);
+            mbar_init(&bar->sp_full[i], 1);
+            mbar_init(&bar->ds_full[i], SWARPS);
+        }
+        for (int i = 0; i < NST; ++i) {
             mbar_init(&bar->full[i], 1);
             mbar_init(&bar->empty[i], 1);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tdo);
+        tma_prefetch_desc(&to);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_alloc(tmem_slot, TCOLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tdP = tmem + 64, tdQ = tmem + 128;
 
     if (warp == 0) {
-        if (lane == 0) {
-            mbar_expect_tx(&bar->qd_full, 2 * dq::TQ);
-            tma_load_3d(sm, &tq, &bar->qd_full, h * HD, qb * dq::BQ, b);
-            tma_load_3d(sm + dq::OFF_DO, &tdo, &bar->qd_full, h * HD, qb * dq::BQ, b);
-            uint32_t issued = 0, iph = 0;
-            bool ok = true;
-            for (int i = 0; i < 2 * nkv && ok; ++i) {
-                const int sl = i % dq::SLOTS;
-                const uint32_t ph = (i / dq::SLOTS) & 1;
-                if (!(ok = mbar_wait(&bar->empty[sl], ph ^ 1, abort_flag, nullptr))) break;
-                mbar_expect_tx(&bar->full[sl], dq::TK);
-                tma_load_3d(sm + dq::OFF_RING + sl * dq::TK, (i & 1) ? &tv : &tk, &bar->full[sl], h * HD, (i >> 1) * dq::BK, b);
-                issued |= 1u << sl;
-                iph = (iph & ~(1u << sl)) | (ph << sl);
+        // Q / dO / O / lse of item j go to staging slot j & 1 one item ahead; key
+        // block g (counted over all items) uses ring entry g mod NST (K and V
+        // tiles), refilled once the dQ product of the block that last used it
+        // has completed.
+        bool ok = true;
+        int g = 0, nring = 0, nstage = 0;
+        auto stage_item = [&](int j) -> bool {
+            const int p = item_of(j, nitems);
+            if (p < 0) return true;
+            const int s = j & 1, qb = item_qb(p), bh = p % BH, b = bh / H, h = bh % H;
+            if (!mbar_wait(&bar->it_sempty[s], ((j >> 1) & 1) ^ 1, abort_flag, nullptr)) return false;
+            uint8_t *dst = sm + OFF_ITEM + s * 3 * TQ;
+            if (lane == 0) {
+                mbar_expect_tx(&bar->it_sfull[s], 3 * TQ);
+                tma_load_3d(dst, &tq, &bar->it_sfull[s], h * HD, qb * BQ, b);
+                tma_load_3d(dst + TQ, &tdo, &bar->it_sfull[s], h * HD, qb * BQ, b);
+                tma_load_3d(dst + 2 * TQ, &to, &bar->it_sfull[s], h * HD, qb * BQ, b);
             }
-            if (!ok) {
-                mbar_drain(&bar->qd_full, 0);
-                for (int sl = 0; sl < dq::SLOTS; ++sl)
-                    if (issued & (1u << sl)) mbar_drain(&bar->full[sl], (iph >> sl) & 1);
+            const float *src = lse + (int64_t)bh * T;
+            float *ld = lsebuf + s * BQ + lane * 4;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int q = qb * BQ + lane * 4 + jj;
+                cp_async4(ld + jj, src + (q < T ? q : 0), q < T ? 4u : 0u);
+            }
+            cp_async_arrive_noinc(&bar->it_lfull[s]);
+            nstage = j + 1;
+            return true;
+        };
+        ok = stage_item(0);
+        for (int j = 0; ok; ++j) {
+            const int p = item_of(j, nitems);
+            if (p < 0) break;
+            if (!(ok = stage_item(j + 1))) break;
+            const int qb = item_qb(p), bh = p % BH, b = bh / H, h = bh % H, nkv = item_nkv(qb);
+            for (int i = 0; i < nkv; ++i, ++g) {
+                const int e = g % NST;
+                if (!(ok = mbar_wait(&bar->empty[e], ((g / NST) & 1) ^ 1, abort_flag, nullptr))) break;
+                if (lane == 0) {
+                    mbar_expect_tx(&bar->full[e], 2 * TK);
+                    tma_load_3d(sm + 2 * e * TK, &tk, &bar->full[e], h * HD, i * BK, b);
+                    tma_load_3d(sm + (2 * e + 1) * TK, &tv, &bar->full[e], h * HD, i * BK, b);
+                }
+                nring = g + 1;
             }
         }
+        if (!ok && lane == 0) {  // let the copies already issued land before the CTA exits
+            for (int i = nring > NST ? nring - NST : 0; i < nring; ++i) mbar_drain(&bar->full[i % NST], (i / NST) & 1);
+            for (int j = nstage > 2 ? nstage - 2 : 0; j < nstage; ++j) mbar_drain(&bar->it_sfull[j & 1], (j >> 1) & 1);
+        }
+        cp_async_wait_all();
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t ID_S = instr_desc(dq::BK, false, false);   // 128 x 64, K-major x K-major
-            constexpr uint32_t ID_DQ = instr_desc(HD, false, true);   // 128 x 64, dS K-major, K MN-major
-            const uint32_t aQ = smem_u32(sm), aDO = smem_u32(sm + dq::OFF_DO), aDS = smem_u32(sm + dq::OFF_DS);
-            bool ok = mbar_wait(&bar->qd_full, 0, abort_flag, nullptr);
-            auto issue_sp = [&](int j) -> bool {
-                const int sk = (2 * j) % dq::SLOTS, sv = (2 * j + 1) % dq::SLOTS;
-                if (!mbar_wait(&bar->full[sk], ((2 * j) / dq::SLOTS) & 1, abort_flag, nullptr)) return false;
-                if (!mbar_wait(&bar->full[sv], ((2 * j + 1) / dq::SLOTS) & 1, abort_flag, nullptr)) return false;
+            constexpr uint32_t ID_S = instr_desc(BK, false, false);  // 128 x 64, B = K / V K-major
+            constexpr uint32_t ID_DQ = instr_desc(HD, false, true);  // 128 x 64, B = K MN-major
+            const uint64_t ring_k = smem_desc(smem_u32(sm), 16, 1024);     // K-major view of ring slot 0
+            const uint64_t ring_mn = smem_desc(smem_u32(sm), 8192, 1024);  // MN-major view of ring slot 0
+            bool ok = true;
+            // dQ product of key block gp, the it-th block of item j
+            auto dq_mma = [&](int gp, int j, int it, bool last) -> bool {
+                const int pb = gp & 1, pe = gp % NST;
+                if (!mbar_wait(&bar->ds_full[pb], (gp >> 1) & 1, abort_flag, nullptr)) return false;
+                if (it == 0 && j > 0 && !mbar_wait(&bar->dq_free, (j - 1) & 1, abort_flag, nullptr)) return false;
                 tc_fence_after();
-                const uint32_t aK = smem_u32(sm + dq::OFF_RING + sk * dq::TK), aV = smem_u32(sm + dq::OFF_RING + sv * dq::TK);
+                const uint64_t bk = ring_mn + (uint64_t)(2 * pe * (TK >> 4));
+                const uint32_t da = tmem + C_DP + pb * 64;
+                tc_mma_ts(tmem + C_DQ, da, bk, ID_DQ, it > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    tc_mma(tS, smem_desc(aQ + kk * 32, 16, 1024), smem_desc(aK + kk * 32, 16, 1024), ID_S,
-                           kk > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    tc_mma(tdP, smem_desc(aDO + kk * 32, 16, 1024), smem_desc(aV + kk * 32, 16, 1024), ID_S,
-                           kk > 0 ? 1u : 0u);
-                tc_commit(&bar->sp_full);
+                for (int kk = 1; kk < BK / 16; ++kk) tc_mma_ts(tmem + C_DQ, da + 16 * kk, bk + 128 * kk, ID_DQ, 1u);
+                tc_commit(&bar->empty[pe]);
+                if (last) tc_commit(&bar->dq_done);
                 return true;
             };
-            if (ok) ok = issue_sp(0);
-            for (int j = 0; j < nkv && ok; ++j) {
-                if (!(ok = mbar_wait(&bar->ds_full, j & 1, abort_flag, nullptr))) break;
-                if (j + 1 < nkv && !(ok = issue_sp(j + 1))) break;
-                const int sk = (2 * j) % dq::SLOTS, sv = (2 * j + 1) % dq::SLOTS;
-                const uint32_t aK = smem_u32(sm + dq::OFF_RING + sk * dq::TK);
-                tc_fence_after();
+            int g = 0, pj = 0, pit = 0;
+            bool plast = false;
+            for (int j = 0; ok; ++j) {
+                const int p = item_of(j, nitems);
+                if (p < 0) break;
+                const int nkv = item_nkv(item_qb(p));
+                if (!(ok = mbar_wait(&bar->it_tfull[j & 1], (j >> 1) & 1, abort_flag, nullptr))) break;
+                const uint32_t tQ = tmem + C_QD + 64 * (j & 1), tDO = tQ + 32;
+                for (int it = 0; it < nkv; ++it, ++g) {
+                    const int bb = g & 1, e = g % NST;
+                    if (!(ok = mbar_wait(&bar->full[e], (g / NST) & 1, abort_flag, nullptr))) break;
+                    tc_fence_after();
+                    const uint64_t bk = ring_k + (uint64_t)(2 * e * (TK >> 4));
+                    const uint64_t bv = ring_k + (uint64_t)((2 * e + 1) * (TK >> 4));
+                    const uint32_t ts = tmem + C_S + bb * 64, tp = tmem + C_DP + bb * 64;
+                    tc_mma_ts(ts, tQ, bk, ID_S, 0u);
 #pragma unroll
-                for (int kk = 0; kk < dq::BK / 16; ++kk)
-                    tc_mma(tdQ, smem_desc(aDS + kk * 32, 16, 1024), smem_desc(aK + kk * 2048, 8192, 1024), ID_DQ,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&bar->empty[sk]);
-                tc_commit(&bar->empty[sv]);
-                tc_commit(&bar->ds_free);
+                    for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(ts, tQ + 8 * kk, bk + 2 * kk, ID_S, 1u);
+                    tc_mma_ts(tp, tDO, bv, ID_S, 0u);
+#pragma unroll
+                    for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(tp, tDO + 8 * kk, bv + 2 * kk, ID_S, 1u);
+                    tc_commit(&bar->sp_full[bb]);
+                    if (g > 0 && !(ok = dq_mma(g - 1, pj, pit, plast))) break;
+                    pj = j, pit = it, plast = it == nkv - 1;
+                }
             }
-            tc_commit(&bar->dq_done);
+            if (ok && g > 0) dq_mma(g - 1, pj, pit, plast);
             tc_commit(&bar->drain);
             mbar_drain(&bar->drain, 0);
         }
     } else {
-        const int quad = warp & 3, half = (warp - 2) >> 2;
-        const int r = quad * 32 + lane, q = qb * dq::BQ + r;
+        const int quad = warp & 3, sub = (warp - 2) >> 2;  // sub: keys [16 sub, 16 sub + 16) of each block
+        const int r = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        float *red = reinterpret_cast<float *>(sm + dq::OFF_RED);
-        // D = rowsum(dO * O): each thread sums 32 of the 64 columns, partners exchange
-        float part = 0.f;
-        if (q < T) {
-            const int64_t off = ((int64_t)b * T + q) * ors + h * HD + half * 32;
+        // Q / dO rows of item j (elements [16 sub, +16)) into TMEM slot j & 1,
+        // plus lse * log2(e) and D = rowsum(dO * O) of row r
+        auto stage_in = [&](int j, float &l2, float &Dr) -> bool {
+            const int s = j & 1, p = item_of(j, nitems);
+            if (!mbar_wait(&bar->it_sfull[s], (j >> 1) & 1, abort_flag, nullptr)) return false;
+            if (!mbar_wait(&bar->it_lfull[s], (j >> 1) & 1, abort_flag, nullptr)) return false;
+            const uint8_t *tile = sm + OFF_ITEM + s * 3 * TQ;
+            uint32_t wq[8], wd[8];
+            tile_row16(tile, r, sub, wq);
+            tile_row16(tile + TQ, r, sub, wd);
+            tmem_st8(tmem + lane_off + C_QD + 64 * s + sub * 8, wq);
+            tmem_st8(tmem + lane_off + C_QD + 64 * s + 32 + sub * 8, wd);
+            float acc = 0.f;
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-                Pack16<bf16> a, gd;
-                a.load(o + off + c);
-                gd.load(dout + off + c);
+            for (int c = 0; c < 4; ++c) {  // the whole row: 64 elements of dO and O
+                uint32_t a[8], o8[8];
+                tile_row16(tile + TQ, r, c, a);
+                tile_row16(tile + 2 * TQ, r, c, o8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) part = fmaf(a.get(e), gd.get(e), part);
-            }
-        }
-        red[half * 128 + r] = part;
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
-        const float Dq = red[r] + red[128 + r];
-        if (half == 0 && q < T) Dscr[(int64_t)bh * T + q] = Dq;
-        const float l2 = q < T ? lse[(int64_t)bh * T + q] * LOG2E : 0.f;
-        uint8_t *sDS = sm + dq::OFF_DS;
-        bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            if (!(ok = mbar_wait(&bar->sp_full, j & 1, abort_flag, nullptr))) break;
-            tc_fence_after();
-            uint32_t w[2][8];
-            // visible keys of this thread's 32: columns c <= lim (key <= q and key < T; none if q >= T)
-            const int lim = q < T ? min(q, T - 1) - (j * dq::BK + half * 32) : -1;
-            const bool full = lim >= 31;
-#pragma unroll
-            for (int c0 = 0; c0 < 32; c0 += 16) {
-                float sv[16], dp[16];
-                {
-                    uint32_t ra[16], rb[16];
-                    tmem_ld16_nowait(tS + lane_off + half * 32 + c0, ra);
-                    tmem_ld16_nowait(tdP + lane_off + half * 32 + c0, rb);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        sv[i] = __uint_as_float(ra[i]);
-                        dp[i] = __uint_as_float(rb[i]);
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    float p0 = ex2(fmaf(sv[i], sl2, -l2));
-                    float p1 = ex2(fmaf(sv[i + 1], sl2, -l2));
-                    if (!full) {
-                        p0 = c0 + i <= lim ? p0 : 0.f;
-                        p1 = c0 + i + 1 <= lim ? p1 : 0.f;
-                    }
-                    w[c0 >> 4][i >> 1] = pack_bf16x2(p0 * (dp[i] - Dq), p1 * (dp[i + 1] - Dq));
+                for (int w = 0; w < 8; ++w) {
+                    acc = fmaf(bf16_lo(a[w]), bf16_lo(o8[w]), acc);
+                    acc = fmaf(bf16_hi(a[w]), bf16_hi(o8[w]), acc);
                 }
             }
+            Dr = acc;
+            l2 = lsebuf[s * BQ + r] * LOG2E;
+            const int q = item_qb(p) * BQ + r;
+            if (sub == 0 && q < T) Dscr[(int64_t)(p % BH) * T + q] = acc;
+            tmem_st_wait();
             tc_fence_before();
-            if (j > 0 && !(ok = mbar_wait(&bar->ds_free, (j - 1) & 1, abort_flag, nullptr))) break;
-            store_row_chunks(sDS, r, half * 4, w[0]);
-            store_row_chunks(sDS, r, half * 4 + 2, w[1]);
-            fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->ds_full);
-        }
-        if (ok && mbar_wait(&bar->dq_done, 0, abort_flag, nullptr)) {
-            tc_fence_after();
-            float f[32];
-            tmem_ld32f(tdQ + lane_off + half * 32, f);
-            if (q < T) {
-                bf16 *row = dqo + ((int64_t)b * T + q) * rs + h * HD + half * 32;
+            if (lane == 0) {
+                mbar_arrive(&bar->it_tfull[s]);
+                mbar_arrive(&bar->it_sempty[s]);
+            }
+            return true;
+        };
+        float l2 = 0.f, Dr = 0.f, l2n = 0.f, Drn = 0.f;
+        bool ok = stage_in(0, l2, Dr);
+        int g = 0;
+        for (int j = 0; ok; ++j) {
+            const int p = item_of(j, nitems);
+            if (p < 0) break;
+            const int qb = item_qb(p), bh = p % BH, b = bh / H, h = bh % H, nkv = item_nkv(qb);
+            const int q = qb * BQ + r;
+            const F2 sl2x2 = f2(sl2, sl2), nl2 = f2(-l2, -l2), dd = f2(Dr, Dr);
+            for (int it = 0; it < nkv; ++it, ++g) {
+                const int bb = g & 1;
+                if (!(ok = mbar_wait(&bar->sp_full[bb], (g >> 1) & 1, abort_flag, nullptr))) break;
+                tc_fence_after();
+                const uint32_t cs = tmem + lane_off + C_S + bb * 64 + sub * 16;
+                const uint32_t cp = tmem + lane_off + C_DP + bb * 64 + sub * 16;
+                uint32_t ra[16], rb[16];
+                tmem_ld16_nowait(cs, ra);
+                tmem_ld16_nowait(cp, rb);
+                tmem_ld_wait();
+                const int k0 = it * BK, kbase = k0 + sub * 16;
+                // Blocks wholly below the diagonal with every query below T need no
+                // mask (same answer for the whole CTA); otherwise the visible keys of
+                // this thread's 16 are columns c <= lim (key <= q, key < T; none if q >= T).
+                const bool block_full = k0 + BK - 1 <= qb * BQ && qb * BQ + BQ <= T;
+                const int lim = q < T ? min(q, T - 1) - kbase : -1;
+                uint32_t wd[8];
 #pragma unroll
-                for (int d = 0; d < 32; d += 8) {
+                for (int c = 0; c < 16; c += 2) {
+                    const F2 t = f2_fma(f2(__uint_as_float(ra[c]), __uint_as_float(ra[c + 1])), sl2x2, nl2);
+                    float p0 = ex2(f2_lo(t)), p1 = ex2(f2_hi(t));
+                    if (!block_full) {
+                        p0 = c <= lim ? p0 : 0.f;
+                        p1 = c + 1 <= lim ? p1 : 0.f;
+                    }
+                    const F2 ds =
+                        f2_mul(f2(p0, p1), f2_sub(f2(__uint_as_float(rb[c]), __uint_as_float(rb[c + 1])), dd));
+                    wd[c >> 1] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
+                }
+                tmem_st8(cp, wd);  // dS over the first 8 of this thread's dP columns
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->ds_full[bb]);
+                if (it == 0 && item_of(j + 1, nitems) >= 0 && !(ok = stage_in(j + 1, l2n, Drn))) break;
+            }
+            if (!ok) break;
+            l2 = l2n, Dr = Drn;
+            // dQ of the item: read out of TMEM, release the accumulator, store
+            if (!(ok = mbar_wait(&bar->dq_done, j & 1, abort_flag, nullptr))) break;
+            tc_fence_after();
+            uint32_t ra[16];
+            tmem_ld16_nowait(tmem + lane_off + C_DQ + sub * 16, ra);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->dq_free);
+            if (q < T) {
+                bf16 *row = dqo + ((int64_t)b * T + q) * rs + h * HD + sub * 16;
+#pragma unroll
+                for (int d = 0; d < 16; d += 8) {
                     uint4 u;
-                    u.x = pack_bf16x2(f[d] * scale, f[d + 1] * scale);
-                    u.y = pack_bf16x2(f[d + 2] * scale, f[d + 3] * scale);
-                    u.z = pack_bf16x2(f[d + 4] * scale, f[d + 5] * scale);
-                    u.w = pack_bf16x2(f[d + 6] * scale, f[d + 7] * scale);
+                    u.x = pack_bf16x2(__uint_as_float(ra[d]) * scale, __uint_as_float(ra[d + 1]) * scale);
+                    u.y = pack_bf16x2(__uint_as_float(ra[d + 2]) * scale, __uint_as_float(ra[d + 3]) * scale);
+                    u.z = pack_bf16x2(__uint_as_float(ra[d + 4]) * scale, __uint_as_float(ra[d + 5]) * scale);
+                    u.w = pack_bf16x2(__uint_as_float(ra[d + 6]) * scale, __uint_as_float(ra[d + 7]) * scale);
                     *reinterpret_cast<uint4 *>(row + d) = u;
                 }
             }
@@ -551,7 +691,7 @@ __global__ void __launch_bounds__(NT, 2)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, TCOLS);
     }
 }
 
@@ -595,41 +735,8 @@ struct Bars {
     uint64_t st_full[2], pds_full[2];
     uint64_t full[NLD], empty[NLD], ld_full[NLD];  // per ring entry: Q and dO slots + lse / D
 };
-// Item j of this CTA (snake order over the heaviest-first list), or -1.
-__device__ __forceinline__ int item_of(int j, int nitems) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const long long p = (long long)j * G + ((j & 1) ? G - 1 - c : c);
-    return p < nitems ? (int)p : -1;
-}
 }  // namespace dkv
 
-// tcgen05.mma with the A operand in TMEM (kind::f16, fp32 accumulate)
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// 32 lanes x 8 columns of 32-bit words from registers into TMEM
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-// 4-byte asynchronous global -> shared copy; src_bytes 0 stores a zero
-__device__ __forceinline__ void cp_async4(float *dst, const float *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-// the mbarrier counts one arrival when this thread's earlier cp.async copies have landed
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __global__ void __launch_bounds__(dkv::NTH, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
@@ -688,7 +795,7 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
         bool ok = true;
         int g = 0, nring = 0, nkv = 0;
         auto load_kv = [&](int j) -> bool {
-            const int p = dkv::item_of(j, nitems);
+            const int p = item_of(j, nitems);
             if (p < 0) return true;
             const int s = j & 1, kb = p / BH, bh = p % BH;
             if (!mbar_wait(&bar->kv_sempty[s], ((j >> 1) & 1) ^ 1, abort_flag, nullptr)) return false;
@@ -702,7 +809,7 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
         };
         ok = load_kv(0);
         for (int j = 0; ok; ++j) {
-            const int p = dkv::item_of(j, nitems);
+            const int p = item_of(j, nitems);
             if (p < 0) break;
             if (!(ok = load_kv(j + 1))) break;
             const int kb = p / BH, bh = p % BH, b = bh / H, h = bh % H, nit = nqb - 2 * kb;
@@ -763,7 +870,7 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
             int g = 0, pj = 0, pit = 0;
             bool plast = false;
             for (int j = 0; ok; ++j) {
-                const int p = dkv::item_of(j, nitems);
+                const int p = item_of(j, nitems);
                 if (p < 0) break;
                 const int nit = nqb - 2 * (p / BH);
                 if (!(ok = mbar_wait(&bar->kv_tfull[j & 1], (j >> 1) & 1, abort_flag, nullptr))) break;
@@ -819,7 +926,7 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
         bool ok = copy_kv(0);
         int g = 0;
         for (int j = 0; ok; ++j) {
-            const int p = dkv::item_of(j, nitems);
+            const int p = item_of(j, nitems);
             if (p < 0) break;
             const int kb = p / BH, bh = p % BH, b = bh / H, h = bh % H, nit = nqb - 2 * kb;
             const int key = kb * BKY + r;
@@ -872,7 +979,7 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar->pds_full[bb]);
-                if (it == 0 && dkv::item_of(j + 1, nitems) >= 0 && !(ok = copy_kv(j + 1))) break;
+                if (it == 0 && item_of(j + 1, nitems) >= 0 && !(ok = copy_kv(j + 1))) break;
             }
             if (!ok) break;
             // dV / dK of the item: read out of TMEM, release the accumulators, store
@@ -968,9 +1075,10 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
          reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq_out) |
          reinterpret_cast<uintptr_t>(dk_out) | reinterpret_cast<uintptr_t>(dv_out)) & 15)
         return GPT2_ERR_BAD_ARG;
-    CUtensorMap q128, do128, k64, v64, q64, do64, k128, v128;
+    CUtensorMap q128, do128, o128, k64, v64, q64, do64, k128, v128;
     if (int rc = encode_qkv_map(&q128, q, rs, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&do128, dout, ors, T, B, H, 128)) return rc;
+    if (int rc = encode_qkv_map(&o128, o, ors, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&k64, k, rs, T, B, H, 64)) return rc;
     if (int rc = encode_qkv_map(&v64, v, rs, T, B, H, 64)) return rc;
     if (int rc = encode_qkv_map(&q64, q, rs, T, B, H, 64)) return rc;
@@ -984,14 +1092,16 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
         init = true;
     }
     const float scale = 1.0f / sqrtf((float)HD), sl2 = LOG2E * scale;
-    bwd_dq_tc_kernel<<<dim3(B * H, (T + dq::BQ - 1) / dq::BQ), NT, dq::SMEM, st>>>(
-        q128, do128, k64, v64, o, dout, ors, lse, dq_out, rs, Dscr, T, H, sl2, scale);
-    GPT2_CUDA_TRY(cudaGetLastError());
-    // persistent dK/dV grid: one CTA per SM over (key block, b*h) items, heaviest first
-    const int nitems = ((T + dkv::BKY - 1) / dkv::BKY) * B * H;
     int dev = 0, sms = 0;
     GPT2_CUDA_TRY(cudaGetDevice(&dev));
     GPT2_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    // persistent dQ grid: one CTA per SM over (query block, b*h) items, heaviest first
+    const int nq_items = ((T + dq::BQ - 1) / dq::BQ) * B * H;
+    bwd_dq_tc_kernel<<<std::min(nq_items, sms), dq::NTH, dq::SMEM, st>>>(q128, do128, o128, k64, v64, lse, dq_out, rs,
+                                                                         Dscr, T, H, nq_items, sl2, scale);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    // persistent dK/dV grid: one CTA per SM over (key block, b*h) items, heaviest first
+    const int nitems = ((T + dkv::BKY - 1) / dkv::BKY) * B * H;
     bwd_dkv_tc_kernel<<<std::min(nitems, sms), dkv::NTH, dkv::SMEM, st>>>(q64, do64, k128, v128, lse, Dscr, dk_out,
                                                                           dv_out, rs, T, H, nitems, sl2, scale);
     GPT2_CUDA_TRY(cudaGetLastError());

@@ -60,6 +60,10 @@ template <typename T> struct Pack16 {
     __device__ __forceinline__ void store(T *ptr) const { *reinterpret_cast<uint4 *>(ptr) = raw; }
 };
 
+// The two bf16 halves of a packed word as fp32 (exact: a bf16 is the top half of an fp32)
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
 // Two fp32 values packed in one 64-bit register: the .f32x2 forms of
 // fma / mul / add / sub (sm_100 and later) do the work of two scalar
 // instructions with one issue slot.  Rounding is that of the scalar forms.
