@@ -101,6 +101,12 @@ __device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
     return d;
 }
 
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+    F2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.u) : "l"(a.u), "l"(b.u));
+    return d;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -126,17 +132,40 @@ __device__ __forceinline__ float tanh_hw(float x) {
     return y;
 }
 
-// GPT-2's tanh GELU and its derivative (the tanh form of "Let's reproduce
-// GPT-2 (124M)", §Bölümler 2; the constant is sqrt(2/pi)).
+// GELU, tanh form: gelu(h) = h/2 (1 + tanh(k (h + c h^3))), k = sqrt(2/pi),
+// c = 0.044715, written as u = k + k c h^2, t = tanh(h u), gelu = h/2 + (h/2) t.
+// Its derivative 1/2 (1 + t) + a (1 - t^2) with a = (k h / 2)(1 + 3 c h^2) is
+// evaluated as 1/2 + t/2 - na + (na t) t with na = -a.  The scalar and paired
+// versions run the same operations in the same order, so every kernel that
+// uses them produces the same bits.
+constexpr float GELU_K = 0.7978845608028654f, GELU_KC = 0.035677408136300125f;  // k, k c
+constexpr float GELU_NA1 = -0.05351611220445019f, GELU_NA0 = -0.3989422804014327f;  // -3 k c / 2, -k / 2
 __device__ __forceinline__ float gelu_tanh(float h) {
-    const float k = 0.7978845608028654f, c = 0.044715f;
-    return 0.5f * h * (1.0f + tanh_hw(k * (h + c * h * h * h)));
+    const float h2 = h * h, u = fmaf(h2, GELU_KC, GELU_K), t = tanh_hw(h * u), hh = 0.5f * h;
+    return fmaf(hh, t, hh);
 }
 __device__ __forceinline__ float gelu_tanh_grad(float h) {
-    const float k = 0.7978845608028654f, c = 0.044715f;
-    float t = tanh_hw(k * (h + c * h * h * h));
-    return 0.5f * (1.0f + t) + 0.5f * h * (1.0f - t * t) * k * (1.0f + 3.0f * c * h * h);
+    const float h2 = h * h, u = fmaf(h2, GELU_KC, GELU_K), t = tanh_hw(h * u);
+    const float na = h * fmaf(h2, GELU_NA1, GELU_NA0);
+    const float base = fmaf(t, 0.5f, 0.5f) - na;
+    return fmaf(na * t, t, base);
 }
+__device__ __forceinline__ F2 gelu_tanh2(F2 h) {
+    const F2 h2 = f2_mul(h, h), u = f2_fma(h2, f2(GELU_KC, GELU_KC), f2(GELU_K, GELU_K));
+    const F2 a = f2_mul(h, u), t = f2(tanh_hw(f2_lo(a)), tanh_hw(f2_hi(a))), hh = f2_mul(h, f2(0.5f, 0.5f));
+    return f2_fma(hh, t, hh);
+}
+__device__ __forceinline__ F2 gelu_tanh_grad2(F2 h) {
+    const F2 h2 = f2_mul(h, h), u = f2_fma(h2, f2(GELU_KC, GELU_KC), f2(GELU_K, GELU_K));
+    const F2 a = f2_mul(h, u), t = f2(tanh_hw(f2_lo(a)), tanh_hw(f2_hi(a)));
+    const F2 na = f2_mul(h, f2_fma(h2, f2(GELU_NA1, GELU_NA1), f2(GELU_NA0, GELU_NA0)));
+    const F2 base = f2_sub(f2_fma(t, f2(0.5f, 0.5f), f2(0.5f, 0.5f)), na);
+    return f2_fma(f2_mul(na, t), t, base);
+}
+
+// GPT-2's tanh GELU and its derivative (the tanh form of "Let's reproduce
+// GPT-2 (124M)", §Bölümler 2; the constant is sqrt(2/pi)).
+
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;

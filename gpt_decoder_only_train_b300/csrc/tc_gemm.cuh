@@ -367,18 +367,25 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // there (stage_prefetch); otherwise R is loaded through `stage`.
 __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage, uint8_t *rstage, int row0, int col0,
                                                  int lane, const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
-    float x[64];
+    // x[i] holds columns 2i, 2i+1; the arithmetic runs on pairs (.f32x2)
+    F2 x[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        x[i] = __uint_as_float(r0[i]) * P.alpha;
-        x[32 + i] = __uint_as_float(r1[i]) * P.alpha;
+    for (int i = 0; i < 16; ++i) {
+        x[i] = f2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+        x[16 + i] = f2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+    }
+    if (P.alpha != 1.0f) {
+        const F2 al = f2(P.alpha, P.alpha);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = f2_mul(x[i], al);
     }
     if (P.bias && P.epi != GPT2_EPI_GELU_BWD) {
 #pragma unroll
         for (int i = 0; i < 64; i += 4) {
             float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
             if (col0 + i < P.N) b = *reinterpret_cast<const float4 *>(P.bias + col0 + i);
-            x[i] += b.x; x[i + 1] += b.y; x[i + 2] += b.z; x[i + 3] += b.w;
+            x[i / 2] = f2_add(x[i / 2], f2(b.x, b.y));
+            x[i / 2 + 1] = f2_add(x[i / 2 + 1], f2(b.z, b.w));
         }
     }
     if (P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD) {
@@ -393,20 +400,18 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const uint4 v = *stage_at(rs, lane, c);
-            const bf16 *rb = reinterpret_cast<const bf16 *>(&v);
-            if (P.epi == GPT2_EPI_RESIDUAL) {
+            const uint32_t rw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x[c * 8 + i] += __bfloat162float(rb[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[c * 8 + i] *= gelu_tanh_grad(__bfloat162float(rb[i]));
+            for (int k = 0; k < 4; ++k) {
+                const F2 r = f2(bf16_lo(rw[k]), bf16_hi(rw[k]));
+                x[4 * c + k] = P.epi == GPT2_EPI_RESIDUAL ? f2_add(x[4 * c + k], r) : f2_mul(x[4 * c + k], gelu_tanh_grad2(r));
             }
         }
         __syncwarp();
     }
     uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(f2_lo(x[i]), f2_hi(x[i]));
 #pragma unroll
     for (int c = 0; c < 8; ++c) *stage_at(stage, lane, c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
     __syncwarp();
@@ -416,8 +421,8 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage
         // GELU of the bf16-rounded pre-activation (a recompute from stored h matches bit for bit)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
-            w[i] = pack_bf16x2(gelu_tanh(__low2float(hv)), gelu_tanh(__high2float(hv)));
+            const F2 y = gelu_tanh2(f2(bf16_lo(w[i]), bf16_hi(w[i])));
+            w[i] = pack_bf16x2(f2_lo(y), f2_hi(y));
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c)
