@@ -458,9 +458,12 @@ int backward_impl(gpt2_model *m, float grad_scale) {
               GPT2_EPI_STORE, grad_scale));
     TRY(mm<T>(m, m->logits, Vp, false, m->lnf, C, false, Gf(m, 0), nullptr, nullptr, C, nullptr, Vp, C, BT,
               GPT2_EPI_ACCUM_F32, grad_scale));
+    // The LayerNorm backward kernels also add the column sums of the residual
+    // gradient they produce into the bias gradient of the projection that
+    // consumes it (the last block's MLP output projection here).
     TIMED(GPT2_PROF_LAYERNORM, 3 * act + stats,
           k::layernorm_backward<T>(dsmall, (T *)m->resid_final, m->lnf_mean, m->lnf_rstd, Pf(m, nt - 2), nullptr, dres,
-                                   Gf(m, nt - 2), Gf(m, nt - 1), BT, C, st));
+                                   Gf(m, nt - 2), Gf(m, nt - 1), BT, C, st, Gf(m, m->lp[c.L - 1].fcprojb)));
     for (int l = c.L - 1; l >= 0; --l) {
         LayerBuf &y = m->layers[l];
         const LayerParams &p = m->lp[l];
@@ -472,7 +475,6 @@ int backward_impl(gpt2_model *m, float grad_scale) {
         // FC projection: x' = x1 + g Wfcproj^T + b
         TRY(mm<T>(m, dres, C, false, g_in, 4 * C, false, Gf(m, p.fcprojw), nullptr, nullptr, 4 * C, nullptr, C, 4 * C,
                   BT, GPT2_EPI_ACCUM_F32));
-        TIMED(GPT2_PROF_OTHER, act, k::column_sum<T>(dres, BT, C, Gf(m, p.fcprojb), st));
         TRY(mm<T>(m, dres, C, true, W<T>(m, p.fcprojw), 4 * C, false, dbig, nullptr, y.fch, 4 * C, nullptr, BT, 4 * C,
                   C, GPT2_EPI_GELU_BWD));
         // FC: h = y2 Wfc^T + b
@@ -483,11 +485,10 @@ int backward_impl(gpt2_model *m, float grad_scale) {
                   GPT2_EPI_STORE));
         TIMED(GPT2_PROF_LAYERNORM, 4 * act + stats,
               k::layernorm_backward<T>(dsmall, (T *)y.resid_mid, y.ln2_mean, y.ln2_rstd, Pf(m, p.ln2g), dres, dres,
-                                       Gf(m, p.ln2g), Gf(m, p.ln2b), BT, C, st));
+                                       Gf(m, p.ln2g), Gf(m, p.ln2b), BT, C, st, Gf(m, p.projb)));
         // attention projection: x1 = x + O Wproj^T + b
         TRY(mm<T>(m, dres, C, false, y.att, C, false, Gf(m, p.projw), nullptr, nullptr, C, nullptr, C, C, BT,
                   GPT2_EPI_ACCUM_F32));
-        TIMED(GPT2_PROF_OTHER, act, k::column_sum<T>(dres, BT, C, Gf(m, p.projb), st));
         TRY(mm<T>(m, dres, C, true, W<T>(m, p.projw), C, false, datt, nullptr, nullptr, C, nullptr, BT, C, C,
                   GPT2_EPI_STORE));
         TRY(attn_bwd<T>(m, (T *)y.qkv, (T *)y.att, datt, y.lse, dqkv, B, Tn));
@@ -499,7 +500,8 @@ int backward_impl(gpt2_model *m, float grad_scale) {
                   GPT2_EPI_STORE));
         TIMED(GPT2_PROF_LAYERNORM, 4 * act + stats,
               k::layernorm_backward<T>(dsmall, (T *)y.resid, y.ln1_mean, y.ln1_rstd, Pf(m, p.ln1g), dres, dres,
-                                       Gf(m, p.ln1g), Gf(m, p.ln1b), BT, C, st));
+                                       Gf(m, p.ln1g), Gf(m, p.ln1b), BT, C, st,
+                                       l > 0 ? Gf(m, m->lp[l - 1].fcprojb) : nullptr));
     }
     TIMED(GPT2_PROF_OTHER, act + 8.0 * BT * C + 4.0 * BT,
           k::embed_backward<T>(m->tokens, dres, Gf(m, 0), Gf(m, 1), B, Tn, C, c.V, st));

@@ -186,34 +186,37 @@ int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *m
     return GPT2_OK;
 }
 
-// dx = rstd (dy*g - mean(dy*g) - xhat mean(dy*g*xhat)).  Each lane keeps the
-// dg/db partial sums of its columns in registers over the rows its warp
-// handles (VPL is the exact packet count per lane); at the end the warps add
-// their partials into shared memory and the block adds those to the fp32
-// gradients.
+// dx = rstd (dy*g - mean(dy*g) - xhat mean(dy*g*xhat)).  One block of 16
+// warps per SM; each warp takes one row at a time with its three input rows
+// requested together.  Each lane keeps the dg / db / column-sum partials of
+// its columns in registers over the rows its warp handles (VPL is the exact
+// packet count per lane).  At the end every warp writes its partials to its
+// own shared-memory row, the block sums the rows column by column (no shared
+// atomics) and adds the result to the fp32 gradients with one atomic per
+// column.
 template <typename T, int VPL>
-__global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ x,
+__global__ void __launch_bounds__(512, 1) ln_bwd_kernel(const T *__restrict__ dy, const T *__restrict__ x,
                                                         const float *__restrict__ mean,
                                                         const float *__restrict__ rstd, const float *__restrict__ g,
                                                         const T *dres_in, T *dres_out, float *__restrict__ dg,
-                                                        float *__restrict__ db, int N, int C) {
-    constexpr int E = Pack16<T>::N;
-    extern __shared__ float sh[];  // [2C]
+                                                        float *__restrict__ db, float *__restrict__ dsum, int N,
+                                                        int C) {
+    constexpr int E = Pack16<T>::N, E2 = E / 2;  // elements per packet, element pairs per packet
+    extern __shared__ float sh[];  // [warps][3C]: dg, db, column sums of dres_out
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, warps = blockDim.x >> 5;
     const int npk = C / E;
-    for (int i = threadIdx.x; i < 2 * C; i += blockDim.x) sh[i] = 0.f;
-    float adg[VPL][E], adb[VPL][E];
+    // the arithmetic runs on element pairs (.f32x2)
+    F2 adg[VPL][E2], adb[VPL][E2], ads[VPL][E2];
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
 #pragma unroll
-        for (int e = 0; e < E; ++e) adg[i][e] = adb[i][e] = 0.f;
+        for (int k = 0; k < E2; ++k) adg[i][k] = adb[i][k] = ads[i][k] = f2(0.f, 0.f);
     for (int row = blockIdx.x * warps + wid; row < N; row += gridDim.x * warps) {
         const int64_t off = (int64_t)row * C;
         // all three input rows are requested before any is used: one memory
         // round trip per row (dres_in may alias dres_out; rows are disjoint)
         Pack16<T> vdy[VPL], vx[VPL], vr[VPL];
         const float mu = mean[row], rs = rstd[row];
-        float s1 = 0.f, s2 = 0.f;
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const int p = lane + 32 * i;
@@ -223,6 +226,8 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
                 if (dres_in) vr[i].load_stream(dres_in + off + p * E);
             }
         }
+        const F2 rs2 = f2(rs, rs), nmr = f2(-mu * rs, -mu * rs);  // xhat = x rs - mu rs
+        F2 s1 = f2(0.f, 0.f), s2 = f2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const int p = lane + 32 * i;
@@ -230,18 +235,19 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
                 F4x<E> gg;
                 gg.load(g + p * E);
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float d = vdy[i].get(e);
-                    const float xh = (vx[i].get(e) - mu) * rs;
-                    const float dxh = d * gg.v[e];
-                    s1 += dxh;
-                    s2 += dxh * xh;
-                    adg[i][e] = fmaf(d, xh, adg[i][e]);
-                    adb[i][e] += d;
+                for (int k = 0; k < E2; ++k) {
+                    const F2 d = f2(vdy[i].get(2 * k), vdy[i].get(2 * k + 1));
+                    const F2 xh = f2_fma(f2(vx[i].get(2 * k), vx[i].get(2 * k + 1)), rs2, nmr);
+                    const F2 dxh = f2_mul(d, f2(gg.v[2 * k], gg.v[2 * k + 1]));
+                    s1 = f2_add(s1, dxh);
+                    s2 = f2_fma(dxh, xh, s2);
+                    adg[i][k] = f2_fma(d, xh, adg[i][k]);
+                    adb[i][k] = f2_add(adb[i][k], d);
                 }
             }
         }
-        const float m1 = warp_sum(s1) / C, m2 = warp_sum(s2) / C;
+        const float m1 = warp_sum(f2_lo(s1) + f2_hi(s1)) / C, m2 = warp_sum(f2_lo(s2) + f2_hi(s2)) / C;
+        const F2 nm1 = f2(-m1, -m1), nm2 = f2(-m2, -m2);
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
             const int p = lane + 32 * i;
@@ -250,48 +256,61 @@ __global__ void __launch_bounds__(256, 2) ln_bwd_kernel(const T *__restrict__ dy
                 F4x<E> gg;
                 gg.load(g + p * E);
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float xh = (vx[i].get(e) - mu) * rs;
-                    const float dx = rs * (vdy[i].get(e) * gg.v[e] - m1 - xh * m2);
-                    o.set(e, (dres_in ? vr[i].get(e) : 0.f) + dx);
+                for (int k = 0; k < E2; ++k) {
+                    const F2 xh = f2_fma(f2(vx[i].get(2 * k), vx[i].get(2 * k + 1)), rs2, nmr);
+                    // dx = rs (dy g - m1 - xhat m2)
+                    const F2 t = f2_fma(xh, nm2, f2_fma(f2(vdy[i].get(2 * k), vdy[i].get(2 * k + 1)),
+                                                         f2(gg.v[2 * k], gg.v[2 * k + 1]), nm1));
+                    F2 ov = f2_mul(t, rs2);
+                    if (dres_in) ov = f2_add(ov, f2(vr[i].get(2 * k), vr[i].get(2 * k + 1)));
+                    o.set(2 * k, f2_lo(ov));
+                    o.set(2 * k + 1, f2_hi(ov));
+                    // column sums of the stored (rounded) output
+                    ads[i][k] = f2_add(ads[i][k], f2(o.get(2 * k), o.get(2 * k + 1)));
                 }
                 o.store(dres_out + off + p * E);
             }
         }
     }
-    __syncthreads();
+    float *my = sh + wid * 3 * C;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int p = lane + 32 * i;
         if (p < npk)
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                atomicAdd(&sh[p * E + e], adg[i][e]);
-                atomicAdd(&sh[C + p * E + e], adb[i][e]);
+            for (int k = 0; k < E2; ++k) {
+                my[p * E + 2 * k] = f2_lo(adg[i][k]);
+                my[p * E + 2 * k + 1] = f2_hi(adg[i][k]);
+                my[C + p * E + 2 * k] = f2_lo(adb[i][k]);
+                my[C + p * E + 2 * k + 1] = f2_hi(adb[i][k]);
+                my[2 * C + p * E + 2 * k] = f2_lo(ads[i][k]);
+                my[2 * C + p * E + 2 * k + 1] = f2_hi(ads[i][k]);
             }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < C; i += blockDim.x) {
-        atomicAdd(dg + i, sh[i]);
-        atomicAdd(db + i, sh[C + i]);
+    const int ncol = dsum ? 3 * C : 2 * C;
+    for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
+        float sum = 0.f;
+        for (int w = 0; w < warps; ++w) sum += sh[w * 3 * C + c];
+        atomicAdd(c < C ? dg + c : c < 2 * C ? db + (c - C) : dsum + (c - 2 * C), sum);
     }
 }
 
 template <typename T>
 int layernorm_backward(const T *dy, const T *x, const float *mean, const float *rstd, const float *g, const T *dres_in,
-                       T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st) {
+                       T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st, float *dsum) {
     if (C % Pack16<T>::N) return GPT2_ERR_BAD_SHAPE;
-    const int warps = 8;
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    }
-    const int grid = std::max(1, std::min(ceil_div(N, warps * 4), sms * 2));
-    const size_t smem = 2 * C * sizeof(float);
-    LN_VPL_SWITCH(ln_vpl<T>(C), ln_bwd_kernel<T, V_><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in,
-                                                                                    dres_out, dg, db, N, C))
+    // 16 warps per block unless the per-warp partial rows (3C floats each) do not fit in shared memory
+    const int warps = std::max(1, std::min(16, (int)((227 * 1024) / (3 * C * sizeof(float)))));
+    int dev = 0, sms = 0;
+    GPT2_CUDA_TRY(cudaGetDevice(&dev));
+    GPT2_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int grid = std::max(1, std::min(ceil_div(N, warps), sms));
+    const size_t smem = (size_t)warps * 3 * C * sizeof(float);
+    LN_VPL_SWITCH(ln_vpl<T>(C), {
+        GPT2_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_kernel<T, V_>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        ln_bwd_kernel<T, V_><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, dsum, N, C);
+    })
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
@@ -311,9 +330,20 @@ __global__ void colsum_kernel(const T *__restrict__ dy, int M, int N, float *__r
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     if (col < N) {
-        for (int r = r0 + rl; r < r1; r += 32) {
+        // four rows in flight per thread (the loads do not depend on each other)
+        int r = r0 + rl;
+        for (; r + 96 < r1; r += 128) {
+            Pack16<T> v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u].load_stream(dy + (int64_t)(r + 32 * u) * N + col);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] += v[u].get(e);
+        }
+        for (; r < r1; r += 32) {
             Pack16<T> v;
-            v.load(dy + (int64_t)r * N + col);
+            v.load_stream(dy + (int64_t)r * N + col);
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[e] += v.get(e);
         }
@@ -1283,7 +1313,7 @@ int clip_adamw(float *p, const float *g, float *m, float *v, bf16 *shadow, int64
     template int layernorm_forward<T>(const T *, const float *, const float *, T *, float *, float *, int, int,    \
                                       cudaStream_t);                                                             \
     template int layernorm_backward<T>(const T *, const T *, const float *, const float *, const float *,          \
-                                       const T *, T *, float *, float *, int, int, cudaStream_t);                  \
+                                       const T *, T *, float *, float *, int, int, cudaStream_t, float *);         \
     template int column_sum<T>(const T *, int, int, float *, cudaStream_t);                                        \
     template int classifier<T>(T *, const int *, float *, int, int, int, float, int *, cudaStream_t);              \
     template int gelu_forward<T>(const T *, T *, int64_t, cudaStream_t);                                           \

@@ -22,11 +22,13 @@ template <typename T>
 int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *mean, float *rstd, int N, int C,
                       cudaStream_t st);
 
-// dres_out = dres_in (may be NULL) + LN'(dy); dg += sum dy*xhat; db += sum dy
-// (dres_in and dres_out may alias)
+// dres_out = dres_in (may be NULL) + LN'(dy); dg += sum dy*xhat; db += sum dy;
+// dsum (may be NULL) += column sums of dres_out as stored, i.e. the bias
+// gradient of a layer whose output gradient is dres_out (dres_in and dres_out
+// may alias)
 template <typename T>
 int layernorm_backward(const T *dy, const T *x, const float *mean, const float *rstd, const float *g, const T *dres_in,
-                       T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st);
+                       T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st, float *dsum = nullptr);
 
 // db[n] += sum_m dy[m, n]
 template <typename T>
