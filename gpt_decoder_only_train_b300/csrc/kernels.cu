@@ -721,37 +721,59 @@ __global__ void __launch_bounds__(CLS_SMEM_THREADS, 1)
         int tg = targets[row];
         const bool bad = tg < 0 || tg >= V;
         if (bad) tg = 0;
+        // Pass 1: row max.  Packets below full_pk hold only real columns; the
+        // max of bf16 values is exact in bf16, two per instruction.
+        uint32_t m2 = 0xff80ff80u;  // (-inf, -inf)
         float m = -INFINITY;
-        for (int p = threadIdx.x; p < npk; p += blockDim.x) {
+        for (int p = threadIdx.x; p < full_pk; p += blockDim.x) {
+            const uint4 v = zs[p];
+            asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v.x));
+            asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v.y));
+            asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v.z));
+            asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v.w));
+        }
+        for (int p = full_pk + threadIdx.x; p < npk; p += blockDim.x) {  // the padded tail
             const uint4 v = zs[p];
             const uint32_t *u = &v.x;
-            if (p < full_pk) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) m = fmaxf(m, fmaxf(bf_lo(u[k]), bf_hi(u[k])));
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (p * 8 + 2 * k < V) m = fmaxf(m, bf_lo(u[k]));
-                    if (p * 8 + 2 * k + 1 < V) m = fmaxf(m, bf_hi(u[k]));
-                }
+            for (int k = 0; k < 4; ++k) {
+                if (p * 8 + 2 * k < V) m = fmaxf(m, bf_lo(u[k]));
+                if (p * 8 + 2 * k + 1 < V) m = fmaxf(m, bf_hi(u[k]));
             }
         }
+        m = fmaxf(m, fmaxf(bf_lo(m2), bf_hi(m2)));
         const float zt = __bfloat162float(reinterpret_cast<const bf16 *>(zs)[tg]);
         m = warp_max(m);
         if (lane == 0) red_m[buf][wid] = m;
         __syncthreads();  // (also: everyone has read zt before the in-place overwrite)
         float M = red_m[buf][0];
         for (int w = 1; w < nw; ++w) M = fmaxf(M, red_m[buf][w]);
+        // Pass 2: e = 2^(x log2e - M log2e), summed in fp32 and stored back as
+        // bf16 in place; the arithmetic runs on column pairs (.f32x2).
+        const F2 l2e2 = f2(L2E, L2E), nmc2 = f2(-M * L2E, -M * L2E);
+        F2 sacc2 = f2(0.f, 0.f);
+        for (int p = threadIdx.x; p < full_pk; p += blockDim.x) {
+            uint4 v = zs[p];
+            uint32_t *u = &v.x;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const F2 t = f2_fma(f2(bf_lo(u[k]), bf_hi(u[k])), l2e2, nmc2);
+                const float a = ex2_hw(f2_lo(t)), b2 = ex2_hw(f2_hi(t));
+                sacc2 = f2_add(sacc2, f2(a, b2));
+                u[k] = bf_pack(a, b2);
+            }
+            zs[p] = v;
+        }
+        float sacc = f2_lo(sacc2) + f2_hi(sacc2);
         const float Mc = M * L2E;
-        float sacc = 0.f;
-        for (int p = threadIdx.x; p < npk; p += blockDim.x) {
+        for (int p = full_pk + threadIdx.x; p < npk; p += blockDim.x) {  // the padded tail: 0 past V
             uint4 v = zs[p];
             uint32_t *u = &v.x;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int c = p * 8 + 2 * k;
-                const float a = (p < full_pk || c < V) ? ex2_hw(fmaf(bf_lo(u[k]), L2E, -Mc)) : 0.f;
-                const float b2 = (p < full_pk || c + 1 < V) ? ex2_hw(fmaf(bf_hi(u[k]), L2E, -Mc)) : 0.f;
+                const float a = c < V ? ex2_hw(fmaf(bf_lo(u[k]), L2E, -Mc)) : 0.f;
+                const float b2 = c + 1 < V ? ex2_hw(fmaf(bf_hi(u[k]), L2E, -Mc)) : 0.f;
                 sacc += a + b2;
                 u[k] = bf_pack(a, b2);
             }
@@ -764,12 +786,17 @@ __global__ void __launch_bounds__(CLS_SMEM_THREADS, 1)
         for (int w = 0; w < nw; ++w) S += red_s[buf][w];
         const float lse = M + logf(S);
         const float scale = dscale / S;
+        const F2 scale2 = f2(scale, scale);
+        // Pass 3: dz = e dscale / S, 16-byte stores
         uint4 *zg = reinterpret_cast<uint4 *>(logits + (int64_t)row * Vp);
         for (int p = threadIdx.x; p < npk; p += blockDim.x) {
             uint4 v = zs[p];
             uint32_t *u = &v.x;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) u[k] = bf_pack(bf_lo(u[k]) * scale, bf_hi(u[k]) * scale);
+            for (int k = 0; k < 4; ++k) {
+                const F2 y = f2_mul(f2(bf_lo(u[k]), bf_hi(u[k])), scale2);
+                u[k] = bf_pack(f2_lo(y), f2_hi(y));
+            }
             if (p == (tg >> 3)) {  // the target's dz from the logit itself, in fp32
                 bf16 *e8 = reinterpret_cast<bf16 *>(&v);
                 e8[tg & 7] = __float2bfloat16_rn((__expf(zt - lse) - 1.0f) * dscale);
