@@ -1,19 +1,10 @@
 // Causal flash attention forward and backward on the tcgen05 tensor cores
 // (head dim 64).
 //
-// Forward: one CTA per (128-query block, b*h), heaviest blocks first; two CTAs
-// per SM.
-//   warp 0     TMA: Q once, then K_j / V_j of each 128-key block through a
-//              3-slot shared-memory ring (128-byte swizzle);
-//   warp 1     one thread issues tcgen05.mma: S = Q K_j^T into TMEM
-//              (128 x 128 fp32), then O_j = P_j V_j into TMEM (128 x 64 fp32);
-//   warps 2-9  softmax: two threads per query row (= TMEM lane), each owning
-//              64 of the block's 128 keys and 32 of the 64 output columns.
-//              They read S with tcgen05.ld, mask, exchange the row max through
-//              shared memory, compute P in the log2 domain and write it as
-//              bf16 into shared memory in the MMA's swizzled K-major layout,
-//              then fold O_j into a register accumulator with the running
-//              rescale.  O = acc / l and lse are written at the end.
+// The forward, dQ and dK/dV kernels are persistent (one CTA per SM over a
+// heaviest-first list of work items) and keep their fixed operand (Q, or K
+// and V) in TMEM as the A operand of tcgen05.mma; each kernel's layout is
+// described above it.
 // The T x T matrix is never stored ("Let's reproduce GPT-2 (124M)", §Video
 // özeti: flash attention); the mask lets a query see itself and the past
 // ("Let's build GPT: from scratch", 00:57:00 erratum; scale 1/sqrt(head_size),
@@ -25,16 +16,7 @@ namespace fatc {
 
 using namespace tcg;
 
-constexpr int BQ = 128, BKV = 128, HD = 64;
-constexpr int TILE = 128 * HD * 2;   // 16 KB: 128 rows of 128 B
-constexpr int SLOTS = 3;             // K/V ring slots (K_j, V_j alternate)
-constexpr int P_OFF = TILE * (1 + SLOTS);
-constexpr int RED_OFF = P_OFF + 2 * TILE;          // exchange buffers [3][2 halves][128 rows] floats:
-constexpr int BAR_OFF = RED_OFF + 3 * 2 * 128 * 4; // two alternate for the row max, the third for the row sum
-constexpr int SMEM = 1024 + BAR_OFF + 256;
-constexpr int SOFTMAX_WARPS = 8;                   // two per TMEM lane quadrant, one per half of the keys
-constexpr int NT = 64 + 32 * SOFTMAX_WARPS;
-constexpr uint32_t TMEM_COLS = 256;  // S: columns [0,128), O: [128,192)
+constexpr int HD = 64;  // head dimension
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -53,295 +35,6 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-struct Bars {
-    uint64_t q_full, s_full, p_full, o_full, o_free, drain;
-    uint64_t full[SLOTS], empty[SLOTS];
-};
-
-__global__ void __launch_bounds__(NT, 2)
-    fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, bf16 *__restrict__ o, int64_t ors, float *__restrict__ lse,
-                  int T, int H, float sl2) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = align_smem_1024(smem_raw);
-    Bars *bar = reinterpret_cast<Bars *>(sm + BAR_OFF);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + BAR_OFF + sizeof(Bars));
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    uint8_t *sQ = sm, *sP = sm + P_OFF;
-
-    const int nqb = (T + BQ - 1) / BQ;
-    // blockIdx.x (fastest in launch order) runs over b*h, so every head's
-    // heaviest query block is launched before any lighter one
-    const int qb = nqb - 1 - blockIdx.y;
-    const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int nkv = qb + 1;               // causal: key blocks 0..qb
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        mbar_init(&bar->q_full, 1);
-        mbar_init(&bar->s_full, 1);
-        mbar_init(&bar->p_full, SOFTMAX_WARPS);
-        mbar_init(&bar->o_full, 1);
-        mbar_init(&bar->o_free, SOFTMAX_WARPS);
-        mbar_init(&bar->drain, 1);
-        for (int s = 0; s < SLOTS; ++s) {
-            mbar_init(&bar->full[s], 1);
-            mbar_init(&bar->empty[s], 1);
-        }
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        tma_prefetch_desc(&tq);
-        tma_prefetch_desc(&tk);
-        tma_prefetch_desc(&tv);
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 128;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer ----------------
-            mbar_expect_tx(&bar->q_full, TILE);
-            tma_load_3d(sQ, &tq, &bar->q_full, h * HD, qb * BQ, b);
-            uint32_t issued = 0, issued_phase = 0;
-            bool ok = true;
-            for (int i = 0; i < 2 * nkv && ok; ++i) {
-                const int s = i % SLOTS;
-                const uint32_t ph = (i / SLOTS) & 1;
-                if (!mbar_wait(&bar->empty[s], ph ^ 1, abort_flag, nullptr)) {
-                    ok = false;
-                    break;
-                }
-                mbar_expect_tx(&bar->full[s], TILE);
-                uint8_t *dst = sm + TILE * (1 + s);
-                const int j = i >> 1;
-                if ((i & 1) == 0)
-                    tma_load_3d(dst, &tk, &bar->full[s], h * HD, j * BKV, b);
-                else
-                    tma_load_3d(dst, &tv, &bar->full[s], h * HD, j * BKV, b);
-                issued |= 1u << s;
-                issued_phase = (issued_phase & ~(1u << s)) | (ph << s);
-            }
-            if (!ok) {
-                mbar_drain(&bar->q_full, 0);
-                for (int s = 0; s < SLOTS; ++s)
-                    if (issued & (1u << s)) mbar_drain(&bar->full[s], (issued_phase >> s) & 1);
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            constexpr uint32_t IDESC_S = instr_desc(BKV, false, false);  // 128 x 128, K-major x K-major
-            constexpr uint32_t IDESC_O = instr_desc(HD, false, true);    // 128 x 64, P K-major, V MN-major
-            const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP);
-            bool ok = mbar_wait(&bar->q_full, 0, abort_flag, nullptr);
-            auto issue_s = [&](int j) -> bool {
-                const int s = (2 * j) % SLOTS;
-                if (!mbar_wait(&bar->full[s], ((2 * j) / SLOTS) & 1, abort_flag, nullptr)) return false;
-                tc_fence_after();
-                const uint32_t aK = smem_u32(sm + TILE * (1 + s));
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    tc_mma(tS, smem_desc(aQ + kk * 32, 16, 1024), smem_desc(aK + kk * 32, 16, 1024), IDESC_S,
-                           kk > 0 ? 1u : 0u);
-                tc_commit(&bar->empty[s]);
-                tc_commit(&bar->s_full);
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; j < nkv && ok; ++j) {
-                // softmax has turned S_j into P_j (and is done reading S)
-                if (!(ok = mbar_wait(&bar->p_full, j & 1, abort_flag, nullptr))) break;
-                if (j + 1 < nkv && !(ok = issue_s(j + 1))) break;
-                if (j > 0 && !(ok = mbar_wait(&bar->o_free, (j - 1) & 1, abort_flag, nullptr))) break;
-                const int s = (2 * j + 1) % SLOTS;
-                if (!(ok = mbar_wait(&bar->full[s], ((2 * j + 1) / SLOTS) & 1, abort_flag, nullptr))) break;
-                tc_fence_after();
-                const uint32_t aV = smem_u32(sm + TILE * (1 + s));
-#pragma unroll
-                for (int kk = 0; kk < BKV / 16; ++kk)
-                    tc_mma(tO, smem_desc(aP + (kk >> 2) * TILE + (kk & 3) * 32, 16, 1024),
-                           smem_desc(aV + kk * 2048, 8192, 1024), IDESC_O, kk > 0 ? 1u : 0u);
-                tc_commit(&bar->empty[s]);
-                tc_commit(&bar->o_full);
-            }
-            tc_commit(&bar->drain);
-            mbar_drain(&bar->drain, 0);
-        }
-    } else {
-        // ---------------- softmax (warps 2..9): two threads per query row ----------------
-        const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;    // keys [64 half, 64 half + 64), O columns [32 half, 32 half + 32)
-        const int r = quad * 32 + lane;      // row within the block = TMEM lane
-        const int q = qb * BQ + r;           // query index
-        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        float *red = reinterpret_cast<float *>(sm + RED_OFF);  // [3 buffers][2 halves][128 rows]
-        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory"); };
-        float acc[32];
-#pragma unroll
-        for (int d = 0; d < 32; ++d) acc[d] = 0.f;
-        float m = -INFINITY, l = 0.f, m_acc = -INFINITY, m_pend = -INFINITY;
-        bool ok = true;
-        auto fold_o = [&](int j) -> bool {   // acc = acc * 2^(m_acc - m_pend) + O_j (this thread's 32 columns)
-            if (!mbar_wait(&bar->o_full, j & 1, abort_flag, nullptr)) return false;
-            tc_fence_after();
-            const float c = ex2(m_acc - m_pend);
-            float f[32];
-            tmem_ld32f(tO + lane_off + half * 32, f);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = fmaf(acc[i], c, f[i]);
-            m_acc = m_pend;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->o_free);
-            return true;
-        };
-        // A failed (timed-out) wait clears `ok`; the loop still runs to the end
-        // so that every thread reaches every named barrier (bar.sync has no timeout).
-        for (int j = 0; j < nkv; ++j) {
-            if (ok) ok = mbar_wait(&bar->s_full, j & 1, abort_flag, nullptr);
-            tc_fence_after();
-            const int kbase = j * BKV + half * 64;
-            // keys of this thread's half that need a mask: causal diagonal block or past T
-            const bool masked_block = (j == qb) || (kbase + 63 >= T);
-            const int lim = min(T - 1 - kbase, (j == qb) ? r - half * 64 : 63);  // last visible column
-            // pass 1: row max of the scaled, masked scores (two 32-column loads)
-            float mx = -INFINITY;
-            if (ok) {
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 32) {
-                    float f[32];
-                    tmem_ld32f(tS + lane_off + half * 64 + c0, f);
-                    if (!masked_block) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, f[i]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, c0 + i <= lim ? f[i] : -INFINITY);
-                    }
-                }
-            }
-            mx *= sl2;
-            float *rb = red + (j & 1) * 256;
-            rb[half * 128 + r] = mx;
-            pair_sync();
-            mx = fmaxf(rb[r], rb[128 + r]);
-            if (!ok) continue;
-            const float m_new = fmaxf(m, mx);
-            const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-            const float corr = ex2(m - mu);
-            // O_{j-1} is complete once PV_{j-1} has finished reading P: fold it
-            // before P is overwritten.
-            if (j > 0 && !(ok = fold_o(j - 1))) continue;
-            // pass 2: P = 2^(s*sl2 - m_new) as bf16 into this half's 64-key atom of the P tile
-            float ls = 0.f;
-            uint8_t *atom = sP + half * TILE + r * 128;
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                float f[32];
-                tmem_ld32f(tS + lane_off + half * 64 + c0, f);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float p0 = ex2(fmaf(f[i], sl2, -mu));
-                    float p1 = ex2(fmaf(f[i + 1], sl2, -mu));
-                    if (masked_block) {
-                        p0 = c0 + i <= lim ? p0 : 0.f;
-                        p1 = c0 + i + 1 <= lim ? p1 : 0.f;
-                    }
-                    ls += p0 + p1;
-                    __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
-                    pk[i >> 1] = *reinterpret_cast<uint32_t *>(&v2);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int cc = (c0 >> 3) + k;
-                    *reinterpret_cast<uint4 *>(atom + ((cc ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                }
-            }
-            l = l * corr + ls;
-            m = m_new;
-            tc_fence_before();
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar->p_full);
-            m_pend = m_new;
-        }
-        if (ok) ok = fold_o(nkv - 1);
-        // the row sum is split over the two halves
-        float *rs2 = red + 2 * 256;
-        rs2[half * 128 + r] = l;
-        pair_sync();
-        const float lt = rs2[r] + rs2[128 + r];
-        if (ok && q < T) {
-            const float inv = 1.0f / lt;
-            bf16 *orow = o + ((int64_t)b * T + q) * ors + h * HD + half * 32;
-#pragma unroll
-            for (int d = 0; d < 32; d += 8) {
-                uint4 w;
-                w.x = pack_bf16x2(acc[d] * inv, acc[d + 1] * inv);
-                w.y = pack_bf16x2(acc[d + 2] * inv, acc[d + 3] * inv);
-                w.z = pack_bf16x2(acc[d + 4] * inv, acc[d + 5] * inv);
-                w.w = pack_bf16x2(acc[d + 6] * inv, acc[d + 7] * inv);
-                *reinterpret_cast<uint4 *>(orow + d) = w;
-            }
-            if (half == 0) lse[(int64_t)bh * T + q] = (m + log2f(lt)) * LN2;
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
-    }
-}
-
-// ===================================================================== backward
-// Two kernels, no atomics.  D = rowsum(dO * O) is written by the dQ kernel and
-// read by the dK/dV kernel, so the dQ kernel runs first.
-
-__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&f)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(r[i]);
-}
-
-// tcgen05.ld of 32 lanes x 16 columns without the wait (batch several loads,
-// then one tmem_ld_wait)
-__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
-
-// 16 bf16 values (8 words) of row r into a swizzled 128-row x 128-byte atom at 16-byte chunks cc, cc+1
-__device__ __forceinline__ void store_row_chunks(uint8_t *atom, int r, int cc, const uint32_t (&w)[8]) {
-    uint8_t *row = atom + r * 128;
-    *reinterpret_cast<uint4 *>(row + ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4 *>(row + (((cc + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // tcgen05.mma with the A operand in TMEM (kind::f16, fp32 accumulate)
@@ -385,6 +78,363 @@ __device__ __forceinline__ int item_of(int j, int nitems) {
     const int G = gridDim.x, c = blockIdx.x;
     const long long p = (long long)j * G + ((j & 1) ? G - 1 - c : c);
     return p < nitems ? (int)p : -1;
+}
+
+namespace fwd {
+constexpr int BQ = 128, BKV = 128, SLOTS = 6, SWARPS = 8;
+constexpr int NTH = 64 + 32 * SWARPS;
+constexpr int TILE = 128 * HD * 2;         // 16 KB: a Q, K or V tile
+constexpr int OFF_Q = SLOTS * TILE;        // [2 item slots] staged Q tiles
+constexpr int OFF_RED = OFF_Q + 2 * TILE;  // [2 parities][2 halves][128 rows] row maxima, then [2][128] row sums
+constexpr int OFF_BAR = OFF_RED + 3 * 2 * 128 * 4;
+constexpr int SMEM = 1024 + OFF_BAR + 512;
+constexpr uint32_t TCOLS = 512;
+constexpr uint32_t C_S = 0, C_O = 256, C_Q = 384;  // S[b] [128b, +128), O[b] [256+64b, +64), Q[s] [384+32s, +32)
+struct Bars {
+    uint64_t drain;
+    uint64_t q_sfull[2], q_sempty[2], q_tfull[2];
+    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+    uint64_t xmax[4][2], xsum[4];  // exchanges between the two softmax warps of a TMEM lane quadrant
+    uint64_t full[SLOTS], empty[SLOTS];
+};
+}  // namespace fwd
+
+// Forward.  Persistent: one CTA per SM walks the (128-query block, b*h)
+// items, heaviest first; an item runs over the key blocks of 128 up to the
+// diagonal.
+//   warp 0     TMA: Q of the next item into a staging slot, K_j / V_j through
+//              a ring of SLOTS shared-memory tiles (128-byte swizzle);
+//   warp 1     one thread issues tcgen05.mma: S_j = Q K_j^T (A = Q in TMEM)
+//              two key blocks ahead into a double-buffered S, and
+//              O_j = P_j V_j (A = P_j in TMEM) into a double-buffered O;
+//   warps 2-9  softmax: two threads per query row (= TMEM lane), each owning
+//              64 of a block's 128 keys and 32 of the 64 output columns.  They
+//              read S with tcgen05.ld, mask, exchange the row max, write
+//              P = 2^(s - m) as bf16 over the first 32 of their own 64 S
+//              columns, and fold O_{j-1} into a register accumulator with the
+//              running rescale.  O = acc / l and lse are written per item.
+// The T x T matrix is never stored ("Let's reproduce GPT-2 (124M)", §Video
+// özeti: flash attention); the mask lets a query see itself and the past
+// ("Let's build GPT: from scratch", 00:57:00 erratum; scale 1/sqrt(head_size),
+// 01:20:05 erratum).  Every mbarrier wait is bounded (see tc_gemm.cuh).
+__global__ void __launch_bounds__(fwd::NTH, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, bf16 *__restrict__ o, int64_t ors, float *__restrict__ lse,
+                  int T, int H, int nitems, float sl2) {
+    constexpr int BQ = fwd::BQ, BKV = fwd::BKV, SLOTS = fwd::SLOTS, SWARPS = fwd::SWARPS, TILE = fwd::TILE;
+    constexpr int OFF_Q = fwd::OFF_Q, OFF_RED = fwd::OFF_RED, OFF_BAR = fwd::OFF_BAR;
+    constexpr uint32_t TCOLS = fwd::TCOLS, C_S = fwd::C_S, C_O = fwd::C_O, C_Q = fwd::C_Q;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align_smem_1024(smem_raw);
+    fwd::Bars *bar = reinterpret_cast<fwd::Bars *>(sm + OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + sizeof(fwd::Bars));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int nqb = (T + BQ - 1) / BQ, BH = nitems / nqb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto item_qb = [&](int p) { return nqb - 1 - p / BH; };  // heaviest query blocks first
+    if (threadIdx.x == 0) {
+        mbar_init(&bar->drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar->q_sfull[i], 1);
+            mbar_init(&bar->q_sempty[i], SWARPS);
+            mbar_init(&bar->q_tfull[i], SWARPS);
+            mbar_init(&bar->s_full[i], 1);
+            mbar_init(&bar->p_full[i], SWARPS);
+            mbar_init(&bar->o_full[i], 1);
+            mbar_init(&bar->o_free[i], SWARPS);
+        }
+        for (int qd = 0; qd < 4; ++qd) {
+            mbar_init(&bar->xmax[qd][0], 2);
+            mbar_init(&bar->xmax[qd][1], 2);
+            mbar_init(&bar->xsum[qd], 2);
+        }
+        for (int s = 0; s < SLOTS; ++s) {
+            mbar_init(&bar->full[s], 1);
+            mbar_init(&bar->empty[s], 1);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TCOLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // Q of item j goes to staging slot j & 1 one item ahead; key block g
+            // (counted over all items) puts K in ring tile 2g and V in 2g+1 (mod SLOTS).
+            bool ok = true;
+            int t = 0, nq = 0;
+            auto stage_q = [&](int j) -> bool {
+                const int p = item_of(j, nitems);
+                if (p < 0) return true;
+                const int s = j & 1, bh = p % BH;
+                if (!mbar_wait(&bar->q_sempty[s], ((j >> 1) & 1) ^ 1, abort_flag, nullptr)) return false;
+                mbar_expect_tx(&bar->q_sfull[s], TILE);
+                tma_load_3d(sm + OFF_Q + s * TILE, &tq, &bar->q_sfull[s], (bh % H) * HD, item_qb(p) * BQ, bh / H);
+                nq = j + 1;
+                return true;
+            };
+            ok = stage_q(0);
+            for (int j = 0; ok; ++j) {
+                const int p = item_of(j, nitems);
+                if (p < 0) break;
+                if (!(ok = stage_q(j + 1))) break;
+                const int bh = p % BH, b = bh / H, h = bh % H, nkv = item_qb(p) + 1;
+                for (int i = 0; i < 2 * nkv && ok; ++i, ++t) {
+                    const int s = t % SLOTS;
+                    if (!(ok = mbar_wait(&bar->empty[s], ((t / SLOTS) & 1) ^ 1, abort_flag, nullptr))) break;
+                    mbar_expect_tx(&bar->full[s], TILE);
+                    tma_load_3d(sm + s * TILE, (i & 1) ? &tv : &tk, &bar->full[s], h * HD, (i >> 1) * BKV, b);
+                }
+            }
+            if (!ok) {  // let the copies already issued land before the CTA exits
+                for (int i = t > SLOTS ? t - SLOTS : 0; i < t; ++i) mbar_drain(&bar->full[i % SLOTS], (i / SLOTS) & 1);
+                for (int j = nq > 2 ? nq - 2 : 0; j < nq; ++j) mbar_drain(&bar->q_sfull[j & 1], (j >> 1) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // S runs two key blocks ahead of O = P V: after PV_g the next score
+            // block g+2 reuses S buffer g & 1 (the in-order pipe has read P_g).
+            constexpr uint32_t ID_S = instr_desc(BKV, false, false);  // 128 x 128, B = K K-major
+            constexpr uint32_t ID_O = instr_desc(HD, false, true);    // 128 x 64, B = V MN-major
+            const uint64_t ring_k = smem_desc(smem_u32(sm), 16, 1024);     // K-major view of ring tile 0
+            const uint64_t ring_mn = smem_desc(smem_u32(sm), 8192, 1024);  // MN-major view of ring tile 0
+            auto item_len = [&](int j, int &n) -> bool {
+                const int p = item_of(j, nitems);
+                if (p < 0) return false;
+                n = item_qb(p) + 1;
+                return true;
+            };
+            int sj = 0, sit = 0, sn = 0, gs = 0, gj = 0, git = 0, gn = 0, go = 0;
+            bool s_on = item_len(0, sn), o_on = s_on;
+            gn = sn;
+            auto issue_s = [&]() -> bool {  // S_gs = Q K^T into S[gs & 1]
+                if (sit == 0 && !mbar_wait(&bar->q_tfull[sj & 1], (sj >> 1) & 1, abort_flag, nullptr)) return false;
+                const int tk_ = 2 * gs, s = tk_ % SLOTS;
+                if (!mbar_wait(&bar->full[s], (tk_ / SLOTS) & 1, abort_flag, nullptr)) return false;
+                tc_fence_after();
+                const uint32_t tQ = tmem + C_Q + 32 * (sj & 1), ts = tmem + C_S + 128 * (gs & 1);
+                const uint64_t bk = ring_k + (uint64_t)(s * (TILE >> 4));
+                tc_mma_ts(ts, tQ, bk, ID_S, 0u);
+#pragma unroll
+                for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(ts, tQ + 8 * kk, bk + 2 * kk, ID_S, 1u);
+                tc_commit(&bar->empty[s]);
+                tc_commit(&bar->s_full[gs & 1]);
+                ++gs;
+                if (++sit == sn) sit = 0, s_on = item_len(++sj, sn);
+                return true;
+            };
+            auto issue_o = [&]() -> bool {  // O_go = P V into O[go & 1]
+                const int b2 = go & 1, tv_ = 2 * go + 1, s = tv_ % SLOTS;
+                if (!mbar_wait(&bar->p_full[b2], (go >> 1) & 1, abort_flag, nullptr)) return false;
+                if (go >= 2 && !mbar_wait(&bar->o_free[b2], ((go - 2) >> 1) & 1, abort_flag, nullptr)) return false;
+                if (!mbar_wait(&bar->full[s], (tv_ / SLOTS) & 1, abort_flag, nullptr)) return false;
+                tc_fence_after();
+                const uint32_t pa = tmem + C_S + 128 * b2, to = tmem + C_O + 64 * b2;
+                const uint64_t bv = ring_mn + (uint64_t)(s * (TILE >> 4));
+                // K-step kk (keys 16kk..16kk+15): P columns 64 (kk / 4) + 8 (kk % 4)
+                tc_mma_ts(to, pa, bv, ID_O, 0u);
+#pragma unroll
+                for (int kk = 1; kk < BKV / 16; ++kk)
+                    tc_mma_ts(to, pa + 64 * (kk >> 2) + 8 * (kk & 3), bv + 128 * kk, ID_O, 1u);
+                tc_commit(&bar->empty[s]);
+                tc_commit(&bar->o_full[b2]);
+                ++go;
+                if (++git == gn) git = 0, o_on = item_len(++gj, gn);
+                return true;
+            };
+            bool ok = true;
+            for (int i = 0; i < 2 && ok && s_on; ++i) ok = issue_s();
+            while (ok && o_on) {
+                if ((ok = issue_o()) && s_on) ok = issue_s();
+            }
+            tc_commit(&bar->drain);
+            mbar_drain(&bar->drain, 0);
+        }
+    } else {
+        const int quad = warp & 3, half = (warp - 2) >> 2;  // keys [64 half, +64), O columns [32 half, +32)
+        const int r = quad * 32 + lane;                      // row within the block = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        float *red = reinterpret_cast<float *>(sm + OFF_RED);
+        // exchange a per-row value with the other warp of this quadrant (mbarrier, bounded)
+        auto exchange = [&](float *buf, uint64_t *xb, uint32_t parity, float v, bool &ok) -> float {
+            buf[half * 128 + r] = v;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xb);
+            if (ok) ok = mbar_wait(xb, parity, abort_flag, nullptr);
+            return buf[(half ^ 1) * 128 + r];
+        };
+        // Q rows of item j (this thread's 32 of the 64 head dims) into TMEM slot j & 1
+        auto stage_in = [&](int j) -> bool {
+            const int s = j & 1;
+            if (!mbar_wait(&bar->q_sfull[s], (j >> 1) & 1, abort_flag, nullptr)) return false;
+            const uint8_t *tile = sm + OFF_Q + s * TILE;
+            uint32_t w0[8], w1[8];
+            tile_row16(tile, r, 2 * half, w0);
+            tile_row16(tile, r, 2 * half + 1, w1);
+            tmem_st8(tmem + lane_off + C_Q + 32 * s + 16 * half, w0);
+            tmem_st8(tmem + lane_off + C_Q + 32 * s + 16 * half + 8, w1);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bar->q_tfull[s]);
+                mbar_arrive(&bar->q_sempty[s]);
+            }
+            return true;
+        };
+        bool ok = stage_in(0);
+        int g = 0;
+        const F2 sl2x2 = f2(sl2, sl2);
+        for (int j = 0; ok; ++j) {
+            const int p = item_of(j, nitems);
+            if (p < 0) break;
+            const int qb = item_qb(p), bh = p % BH, b = bh / H, h = bh % H, nkv = qb + 1;
+            const int q = qb * BQ + r;
+            float acc[32];
+#pragma unroll
+            for (int d = 0; d < 32; ++d) acc[d] = 0.f;
+            float m = -INFINITY, l = 0.f, m_acc = -INFINITY, m_pend = -INFINITY;
+            // fold O_gp (block gp of this item) into acc with the running rescale
+            auto fold_o = [&](int gp) -> bool {
+                const int b2 = gp & 1;
+                if (!mbar_wait(&bar->o_full[b2], (gp >> 1) & 1, abort_flag, nullptr)) return false;
+                tc_fence_after();
+                const float c = ex2(m_acc - m_pend);
+                float f[32];
+                tmem_ld32f(tmem + lane_off + C_O + 64 * b2 + 32 * half, f);
+                const F2 c2 = f2(c, c);
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const F2 a = f2_fma(f2(acc[i], acc[i + 1]), c2, f2(f[i], f[i + 1]));
+                    acc[i] = f2_lo(a);
+                    acc[i + 1] = f2_hi(a);
+                }
+                m_acc = m_pend;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->o_free[b2]);
+                return true;
+            };
+            for (int jj = 0; jj < nkv; ++jj, ++g) {
+                const int bb = g & 1;
+                if (ok) ok = mbar_wait(&bar->s_full[bb], (g >> 1) & 1, abort_flag, nullptr);
+                tc_fence_after();
+                const uint32_t ts = tmem + lane_off + C_S + 128 * bb + 64 * half;
+                const int kbase = jj * BKV + half * 64;
+                // blocks below the diagonal and inside T need no mask (same for the whole CTA)
+                const bool block_full = jj < qb && (jj + 1) * BKV <= T;
+                const int lim = min(T - 1 - kbase, jj == qb ? r - half * 64 : 63);  // last visible column
+                // pass 1: row max of the masked scores
+                float mx = -INFINITY;
+                if (ok) {
+#pragma unroll
+                    for (int c0 = 0; c0 < 64; c0 += 32) {
+                        float f[32];
+                        tmem_ld32f(ts + c0, f);
+                        if (block_full) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, f[i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, c0 + i <= lim ? f[i] : -INFINITY);
+                        }
+                    }
+                }
+                mx *= sl2;
+                mx = fmaxf(mx, exchange(red + bb * 256, &bar->xmax[quad][bb], (g >> 1) & 1, mx, ok));
+                if (!ok) break;
+                const float m_new = fmaxf(m, mx);
+                const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+                const float corr = ex2(m - mu);
+                const F2 nmu = f2(-mu, -mu);
+                // pass 2: P = 2^(s sl2 - m) as bf16 over the first 32 of this thread's 64 S columns
+                F2 ls2 = f2(0.f, 0.f);
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    float f[32];
+                    tmem_ld32f(ts + c0, f);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const F2 t = f2_fma(f2(f[i], f[i + 1]), sl2x2, nmu);
+                        float p0 = ex2(f2_lo(t)), p1 = ex2(f2_hi(t));
+                        if (!block_full) {
+                            p0 = c0 + i <= lim ? p0 : 0.f;
+                            p1 = c0 + i + 1 <= lim ? p1 : 0.f;
+                        }
+                        ls2 = f2_add(ls2, f2(p0, p1));
+                        pk[i >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    uint32_t w0[8], w1[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) w0[k] = pk[k], w1[k] = pk[8 + k];
+                    tmem_st8(ts + c0 / 2, w0);
+                    tmem_st8(ts + c0 / 2 + 8, w1);
+                }
+                l = l * corr + (f2_lo(ls2) + f2_hi(ls2));
+                m = m_new;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar->p_full[bb]);
+                if (jj > 0 && !(ok = fold_o(g - 1))) break;
+                m_pend = m_new;
+                if (jj == 0 && item_of(j + 1, nitems) >= 0 && !(ok = stage_in(j + 1))) break;
+            }
+            if (!ok) break;
+            if (!(ok = fold_o(g - 1))) break;
+            // the row sum is split over the two halves
+            const float lt = l + exchange(red + 2 * 256, &bar->xsum[quad], j & 1, l, ok);
+            if (!ok) break;
+            if (q < T) {
+                const float inv = 1.0f / lt;
+                bf16 *orow = o + ((int64_t)b * T + q) * ors + h * HD + half * 32;
+#pragma unroll
+                for (int d = 0; d < 32; d += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(acc[d] * inv, acc[d + 1] * inv);
+                    w.y = pack_bf16x2(acc[d + 2] * inv, acc[d + 3] * inv);
+                    w.z = pack_bf16x2(acc[d + 4] * inv, acc[d + 5] * inv);
+                    w.w = pack_bf16x2(acc[d + 6] * inv, acc[d + 7] * inv);
+                    *reinterpret_cast<uint4 *>(orow + d) = w;
+                }
+                if (half == 0) lse[(int64_t)bh * T + q] = (m + log2f(lt)) * LN2;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TCOLS);
+    }
+}
+
+// ===================================================================== backward
+// Two kernels, no atomics.  D = rowsum(dO * O) is written by the dQ kernel and
+// read by the dK/dV kernel, so the dQ kernel runs first.
+
+// tcgen05.ld of 32 lanes x 16 columns without the wait (batch several loads,
+// then one tmem_ld_wait)
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
 }
 
 // ---------------------------------------------------------------- dQ kernel
@@ -1057,11 +1107,16 @@ int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs
     if (int rc = encode_qkv_map(&mv, v, rs, T, B, H)) return rc;
     static bool init = false;
     if (!init) {
-        GPT2_CUDA_TRY(cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM));
+        GPT2_CUDA_TRY(cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::SMEM));
         init = true;
     }
     const float sl2 = LOG2E / sqrtf((float)HD);
-    fwd_tc_kernel<<<dim3(B * H, (T + BQ - 1) / BQ), NT, SMEM, st>>>(mq, mk, mv, o, ors, lse, T, H, sl2);
+    int dev = 0, sms = 0;
+    GPT2_CUDA_TRY(cudaGetDevice(&dev));
+    GPT2_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    // persistent grid: one CTA per SM over (query block, b*h) items, heaviest first
+    const int nitems = ((T + fwd::BQ - 1) / fwd::BQ) * B * H;
+    fwd_tc_kernel<<<std::min(nitems, sms), fwd::NTH, fwd::SMEM, st>>>(mq, mk, mv, o, ors, lse, T, H, nitems, sl2);
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
