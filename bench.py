@@ -103,6 +103,31 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# DRAM traffic of the GEMM launches of one step, from one ncu capture of the
+# 147 GEMM launches of a bench step (dram__bytes_read.sum + dram__bytes_write.sum,
+# a single-pass metric set; profiles/gemm_tcgen05_gpt2_124m_shapes.md).  It is
+# reported only while the GEMM sources are the ones that were measured.
+GEMM_TRAFFIC = {
+    "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
+                "gpt_decoder_only_train_b300/csrc/common.cuh"],
+    "sha256": "1bfe1fbe555f6e9fe403e696227a2d7246b29cf6c0ad4474b6c65dcf917f3294",
+    "bytes_per_launch": 26.690e9 / 147,
+}
+
+
+def gemm_traffic():
+    import hashlib
+
+    h = hashlib.sha256()
+    try:
+        for f in GEMM_TRAFFIC["sources"]:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return GEMM_TRAFFIC["bytes_per_launch"] if h.hexdigest() == GEMM_TRAFFIC["sha256"] else None
+
+
 def cpu_baseline(w, budget_s=25.0):
     """The oracle, as it stands, on a bounded sample: the 124M step on B=1 x T=256 tokens."""
     import torch
@@ -298,7 +323,8 @@ def main():
                     "vs_measured_bf16_burst": per_gpu * fpt / (peaks["bf16_tflops"] * 1e12)},
             "roofline": {"kernel": "tcgen05 bf16 GEMM (all matmuls of the step)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "frac": (achieved / peak) if achieved else None, "traffic": gemm_traffic(),
+                         "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
                          "peak_source": "%s bf16_tflops_sustained" % peak_src,
                          "launches_per_step": mm_n / args.steps,
                          "timing": "CUDA events around each launch, second pass over the same steps"},
