@@ -33,28 +33,54 @@ int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer
     return r == CUDA_SUCCESS ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN>
-static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params &P, int grid, cudaStream_t st) {
-    using Lay = SmemLayout<BN, STAGES>;
-    auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN>;
+// units: work units (tiles x splits); the grid is one CTA per SM (or one pair
+// of CTAs per two SMs) up to that count.
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR>
+static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params &P, int units, int num_sms,
+                      cudaStream_t st) {
+    using Lay = SmemLayout<BN, STAGES, PAIR>;
+    auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, PAIR>;
     static bool attr_set = false;
+    static int max_pairs = 0;
     if (!attr_set) {
         GPT2_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL));
         attr_set = true;
     }
-    kern<<<grid, NUM_THREADS, Lay::TOTAL, st>>>(ta, tb, P);
+    if constexpr (PAIR) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = Lay::TOTAL;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (!max_pairs) {  // how many CTA pairs can be resident at once (about half the SMs)
+            cfg.gridDim = dim3(2 * (num_sms / 2));
+            int n = 0;
+            GPT2_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+            max_pairs = n > 0 ? n : 1;
+        }
+        cfg.gridDim = dim3(2 * std::min(units, max_pairs));
+        GPT2_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, P));
+    } else {
+        kern<<<std::min(units, num_sms), NUM_THREADS, Lay::TOTAL, st>>>(ta, tb, P);
+    }
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool PAIR>
 static int dispatch_major(bool a_mn, bool b_mn, const CUtensorMap &ta, const CUtensorMap &tb, const Params &P,
-                          int grid, cudaStream_t st) {
-    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false>(ta, tb, P, grid, st);
-    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true>(ta, tb, P, grid, st);
-    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true>(ta, tb, P, grid, st);
-    return launch_one<BN, STAGES, true, false>(ta, tb, P, grid, st);
+                          int units, int num_sms, cudaStream_t st) {
+    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false, PAIR>(ta, tb, P, units, num_sms, st);
+    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true, PAIR>(ta, tb, P, units, num_sms, st);
+    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true, PAIR>(ta, tb, P, units, num_sms, st);
+    return launch_one<BN, STAGES, true, false, PAIR>(ta, tb, P, units, num_sms, st);
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -71,11 +97,21 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     if (g.bias && (reinterpret_cast<uintptr_t>(g.bias) & 15)) return GPT2_ERR_BAD_ARG;
 
     const int BN = g.N >= 256 ? 256 : (g.N > 64 ? 128 : 64);
+    // CTA pairs on 256 x 256 tiles (cta_group::2): each SM reads half of the B
+    // tile per stage, which keeps shared-memory traffic per MMA within what the
+    // SM delivers, at the cost of pair synchronisation per tile.  Measured on
+    // the model's shapes, pairs pay off for long K, for large plain outputs and
+    // for weight gradients with enough tiles; short-K products with a heavy
+    // epilogue (GELU, residual) or few tiles stay on single CTAs.
+    const int pair_tiles = ceil_div(g.M, 2 * BM) * ceil_div(g.N, 256);
+    const bool pair = BN == 256 && (g.epi == GPT2_EPI_ACCUM_F32 ? pair_tiles >= 16
+                                                                : (g.K >= 1024 || (g.epi == GPT2_EPI_STORE && g.N >= 2048)));
+    const int conc = pair ? num_sms / 2 : num_sms;  // work units that run at once
     Params P;
     P.M = g.M;
     P.N = g.N;
     P.K = g.K;
-    P.num_m_blocks = ceil_div(g.M, BM);
+    P.num_m_blocks = ceil_div(g.M, pair ? 2 * BM : BM);
     P.num_n_blocks = ceil_div(g.N, BN);
     P.num_k_blocks = ceil_div(g.K, BK);
     P.splits = 1;
@@ -85,14 +121,14 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
         // whose last wave is at least 95% busy, else the best one found.  Each
         // split keeps at least 4 K blocks.
         const int tiles = P.num_m_blocks * P.num_n_blocks;
-        if (tiles < 2 * num_sms) {
+        if (tiles < 2 * conc) {
             const int max_splits = std::max(1, P.num_k_blocks / 4);
             int best = 1;
             double best_eff = 0.0;
             for (int sp = 1; sp <= max_splits; ++sp) {
                 const int kbps = ceil_div(P.num_k_blocks, sp), real = ceil_div(P.num_k_blocks, kbps);
                 const long long units = (long long)tiles * real;
-                const double eff = (double)units / ((double)ceil_div((int)units, num_sms) * num_sms);
+                const double eff = (double)units / ((double)ceil_div((int)units, conc) * conc);
                 if (eff > best_eff + 1e-9) {
                     best_eff = eff;
                     best = real;
@@ -120,21 +156,26 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     CUtensorMap ta, tb;
     int rc = g.a_kmajor ? encode_tmap(&ta, g.A, g.K, g.M, g.lda, 64, BM) : encode_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64);
     if (rc) return rc;
-    rc = g.b_kmajor ? encode_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN) : encode_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64);
+    rc = g.b_kmajor ? encode_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, pair ? BN / 2 : BN)
+                    : encode_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64);
     if (rc) return rc;
 
     const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;
-    const int grid = std::min(num_work, num_sms);
     const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
     const bool reads_r = g.epi == GPT2_EPI_RESIDUAL || g.epi == GPT2_EPI_GELU_BWD;
-    if (BN == 256) {
+    if (BN == 256 && pair) {
         // operand-reading epilogues (only K-major A, as the model uses them) trade a ring stage for prefetch
-        if (reads_r && !a_mn) return b_mn ? launch_one<256, 3, false, true>(ta, tb, P, grid, stream)
-                                          : launch_one<256, 3, false, false>(ta, tb, P, grid, stream);
-        return dispatch_major<256, 4>(a_mn, b_mn, ta, tb, P, grid, stream);
+        if (reads_r && !a_mn) return b_mn ? launch_one<256, 5, false, true, true>(ta, tb, P, num_work, num_sms, stream)
+                                          : launch_one<256, 5, false, false, true>(ta, tb, P, num_work, num_sms, stream);
+        return dispatch_major<256, 6, true>(a_mn, b_mn, ta, tb, P, num_work, num_sms, stream);
     }
-    if (BN == 128) return dispatch_major<128, 6>(a_mn, b_mn, ta, tb, P, grid, stream);
-    return dispatch_major<64, 8>(a_mn, b_mn, ta, tb, P, grid, stream);
+    if (BN == 256) {
+        if (reads_r && !a_mn) return b_mn ? launch_one<256, 3, false, true, false>(ta, tb, P, num_work, num_sms, stream)
+                                          : launch_one<256, 3, false, false, false>(ta, tb, P, num_work, num_sms, stream);
+        return dispatch_major<256, 4, false>(a_mn, b_mn, ta, tb, P, num_work, num_sms, stream);
+    }
+    if (BN == 128) return dispatch_major<128, 6, false>(a_mn, b_mn, ta, tb, P, num_work, num_sms, stream);
+    return dispatch_major<64, 8, false>(a_mn, b_mn, ta, tb, P, num_work, num_sms, stream);
 }
 
 }  // namespace tcg

@@ -203,17 +203,70 @@ __host__ __device__ constexpr uint32_t instr_desc(int bn, bool a_mn, bool b_mn) 
            ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
+// Instruction descriptor for a CTA-pair MMA (cta_group::2): M = 256.
+__host__ __device__ constexpr uint32_t instr_desc_pair(int bn, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+// ---- CTA pairs (cluster of two, cta_group::2) ------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of the same shared-memory object in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t smem_in_rank(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+// TMA load into this CTA's shared memory, completion counted on an mbarrier of either CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *tm, uint32_t bar_cluster, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive (when the MMAs issued so far complete) on the mbarrier at this offset in the CTAs of `mask`
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 constexpr int EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16
 
 // Epilogues that read a second operand (residual, GELU input) run with a
 // 3-deep ring so that each epilogue warp gets a second staging block: the next
 // 32 x 64 block of that operand is fetched (cp.async) while the current one is
 // being computed and stored.
-template <int BN, int STAGES>
+// PAIR: a CTA pair shares one 256 x BN tile (cta_group::2), each CTA holding
+// 128 rows of A and BN / 2 rows of B per stage; the R-reading variant of the
+// pair kernel has 5 stages.
+template <int BN, int STAGES, bool PAIR = false>
 struct SmemLayout {
-    static constexpr int B_STAGE_BYTES = BN * BK * 2;
+    static constexpr int B_STAGE_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int EPI_BUFS = STAGES == 3 ? 2 : 1;
+    static constexpr int EPI_BUFS = (PAIR ? STAGES == 5 : STAGES == 3) ? 2 : 1;
     static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_WARPS * EPI_BUFS * EPI_STAGE_BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
@@ -434,13 +487,19 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage
 }
 
 // ---- the kernel -----------------------------------------------------------------
-template <int BN, int STAGES, bool A_MN, bool B_MN>
+// PAIR: launched as clusters of two CTAs sharing 256 x BN tiles; the even CTA
+// issues the cta_group::2 MMAs for both, each CTA loads its own 128 rows of A
+// and BN / 2 rows of B (completions counted on the even CTA's barriers) and
+// runs the epilogue of its own 128 rows.
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params P) {
-    using Lay = SmemLayout<BN, STAGES>;
-    constexpr uint32_t IDESC = instr_desc(BN, A_MN, B_MN);
+    using Lay = SmemLayout<BN, STAGES, PAIR>;
+    constexpr uint32_t IDESC = PAIR ? instr_desc_pair(BN, A_MN, B_MN) : instr_desc(BN, A_MN, B_MN);
     constexpr uint32_t TMEM_COLS = 2 * BN;
+    constexpr int TM = PAIR ? 2 * BM : BM;        // rows of a tile
+    constexpr int BN_CTA = PAIR ? BN / 2 : BN;    // rows of B this CTA loads per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_smem_1024(smem_raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::BAR_OFFSET);
@@ -452,6 +511,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_rank() : 0;               // CTA within the pair
+    const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // first work unit
+    const int ustep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;    // units run concurrently
+    const int row_off = PAIR ? (int)rank * BM : 0;                 // this CTA's rows within a tile
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -459,7 +522,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], EPI_WARPS);
+            mbar_init(&tempty[a], PAIR ? 2 * EPI_WARPS : EPI_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -468,11 +531,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {  // one warp of each CTA of the pair allocates collectively
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the even CTA's barriers exist before the odd CTA's copies signal them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -485,9 +556,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < num_work && ok; w += gridDim.x) {
+            for (int w = unit0; w < num_work && ok; w += ustep) {
                 const int split = w % P.splits, tile = w / P.splits;
-                const int m0 = tile_m(P, tile) * BM, n0 = tile_n(P, tile) * BN;
+                const int m0 = tile_m(P, tile) * TM + row_off, n0 = tile_n(P, tile) * BN + (PAIR ? (int)rank * BN_CTA : 0);
                 const int kb0 = split * P.k_blocks_per_split;
                 const int kb1 = min(P.num_k_blocks, kb0 + P.k_blocks_per_split);
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -495,22 +566,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(&full[stage], Lay::STAGE_BYTES);
                     uint8_t *a_dst = smem + stage * Lay::STAGE_BYTES;
                     uint8_t *b_dst = a_dst + A_STAGE_BYTES;
                     const int k0 = kb * BK;
-                    if (!A_MN) {
-                        tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
-                    } else {
-                        tma_load_2d(a_dst, &tmA, &full[stage], m0, k0);
-                        tma_load_2d(a_dst + MN_BLOCK_BYTES, &tmA, &full[stage], m0 + 64, k0);
-                    }
-                    if (!B_MN) {
-                        tma_load_2d(b_dst, &tmB, &full[stage], k0, n0);
-                    } else {
+                    if constexpr (PAIR) {
+                        // both CTAs' bytes are counted on the even CTA's barrier, which it arms
+                        if (rank == 0) mbar_expect_tx(&full[stage], 2 * Lay::STAGE_BYTES);
+                        const uint32_t fb = smem_in_rank(&full[stage], 0);
+                        if (!A_MN) {
+                            tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
+                        } else {
+                            tma_load_2d_pair(a_dst, &tmA, fb, m0, k0);
+                            tma_load_2d_pair(a_dst + MN_BLOCK_BYTES, &tmA, fb, m0 + 64, k0);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d_pair(b_dst, &tmB, fb, k0, n0);
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)
-                            tma_load_2d(b_dst + i * MN_BLOCK_BYTES, &tmB, &full[stage], n0 + 64 * i, k0);
+                            for (int i = 0; i < BN_CTA / 64; ++i)
+                                tma_load_2d_pair(b_dst + i * MN_BLOCK_BYTES, &tmB, fb, n0 + 64 * i, k0);
+                        }
+                    } else {
+                        mbar_expect_tx(&full[stage], Lay::STAGE_BYTES);
+                        if (!A_MN) {
+                            tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
+                        } else {
+                            tma_load_2d(a_dst, &tmA, &full[stage], m0, k0);
+                            tma_load_2d(a_dst + MN_BLOCK_BYTES, &tmA, &full[stage], m0 + 64, k0);
+                        }
+                        if (!B_MN) {
+                            tma_load_2d(b_dst, &tmB, &full[stage], k0, n0);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < BN / 64; ++i)
+                                tma_load_2d(b_dst + i * MN_BLOCK_BYTES, &tmB, &full[stage], n0 + 64 * i, k0);
+                        }
                     }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -520,19 +610,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (!ok) {  // abort: let the copies already issued land before the CTA exits
+            if (!ok && rank == 0) {  // abort: let the copies already issued land before the CTA exits
                 for (int s = 0; s < STAGES; ++s)
                     if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (the even CTA of a pair issues for both) ----------------
             int stage = 0;
             uint32_t phase = 0;
             int t = 0;
             bool ok = true;
-            for (int w = blockIdx.x; w < num_work && ok; w += gridDim.x, ++t) {
+            for (int w = unit0; w < num_work && ok; w += ustep, ++t) {
                 const int split = w % P.splits;
                 const int kb0 = split * P.k_blocks_per_split;
                 const int kb1 = min(P.num_k_blocks, kb0 + P.k_blocks_per_split);
@@ -558,19 +648,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                  : smem_desc(a_addr + j * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc(b_addr + j * 2048, MN_BLOCK_BYTES, 1024)
                                                  : smem_desc(b_addr + j * 32, 16, 1024);
-                        tc_mma(d_tmem, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+                        if constexpr (PAIR)
+                            tc_mma_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+                        else
+                            tc_mma(d_tmem, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
                     }
-                    tc_commit(&empty[stage]);
+                    if constexpr (PAIR)
+                        tc_commit_pair(&empty[stage], 3);
+                    else
+                        tc_commit(&empty[stage]);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&tfull[acc]);
+                if constexpr (PAIR)
+                    tc_commit_pair(&tfull[acc], 3);
+                else
+                    tc_commit(&tfull[acc]);
             }
             // all MMAs issued by this thread have completed once `drain` flips
-            tc_commit(drain);
+            if constexpr (PAIR)
+                tc_commit_pair(drain, 1);
+            else
+                tc_commit(drain);
             mbar_drain(drain, 0);
         }
     } else {
@@ -580,17 +682,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t *stage = smem + Lay::EPI_OFFSET + (warp - 2) * Lay::EPI_BUFS * EPI_STAGE_BYTES;
         constexpr int HALF = BN / 2;
         if (Lay::EPI_BUFS > 1 && (P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD) &&
-            (int)blockIdx.x < num_work) {
-            const int t0 = blockIdx.x / P.splits;
+            unit0 < num_work) {
+            const int t0 = unit0 / P.splits;
             const int ncol = tile_n(P, t0) * BN + col_half * HALF;
             if (ncol < P.N)
-                stage_prefetch(stage + EPI_STAGE_BYTES, P.R, P.ldd, tile_m(P, t0) * BM + quad * 32, ncol, P.M, P.N,
+                stage_prefetch(stage + EPI_STAGE_BYTES, P.R, P.ldd, tile_m(P, t0) * TM + row_off + quad * 32, ncol, P.M, P.N,
                                lane);
         }
         int t = 0;
-        for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++t) {
+        for (int w = unit0; w < num_work; w += ustep, ++t) {
             const int tile = w / P.splits;
-            const int m0 = tile_m(P, tile) * BM, n0 = tile_n(P, tile) * BN;
+            const int m0 = tile_m(P, tile) * TM + row_off, n0 = tile_n(P, tile) * BN;
             const int acc = t & 1;
             const uint32_t aph = (t >> 1) & 1;
             if (!mbar_wait(&tfull[acc], aph, abort_flag, P.err)) break;
@@ -612,7 +714,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (c0 + 64 == HALF) {  // this warp's part of the accumulator is read: release it
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty[acc]);
+                        if (lane == 0) {
+                            if constexpr (PAIR)
+                                mbar_arrive_cluster(smem_in_rank(&tempty[acc], 0));
+                            else
+                                mbar_arrive(&tempty[acc]);
+                        }
                     }
                     if (P.epi == GPT2_EPI_ACCUM_F32) {
                         if (col < P.N) epilogue_chunk(P, row, col, r0);
@@ -625,10 +732,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __syncwarp();
                         int nrow0 = row0, ncol = col + 64;
                         if (c0 + 64 == HALF) {
-                            const int wn = w + gridDim.x;
+                            const int wn = w + ustep;
                             if (wn < num_work) {
                                 const int tn = wn / P.splits;
-                                nrow0 = tile_m(P, tn) * BM + quad * 32;
+                                nrow0 = tile_m(P, tn) * TM + row_off + quad * 32;
                                 ncol = tile_n(P, tn) * BN + c_begin;
                             } else {
                                 ncol = P.N;  // nothing left: no fetch
@@ -643,7 +750,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(smem_in_rank(&tempty[acc], 0));
+                    else
+                        mbar_arrive(&tempty[acc]);
+                }
                 const int col = n0 + c_begin;
                 if (col < P.N) epilogue_chunk(P, row, col, r0);
             }
@@ -651,9 +763,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the pair's MMAs and both epilogues are done with TMEM
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                         : "memory");
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
