@@ -110,8 +110,8 @@ class ClockSampler:
 GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
-    "sha256": "1bfe1fbe555f6e9fe403e696227a2d7246b29cf6c0ad4474b6c65dcf917f3294",
-    "bytes_per_launch": 26.690e9 / 147,
+    "sha256": "64b1ab090b0cb3b5bc990960cd11829e71a749b86ae2cc179f15001604a4cbdd",
+    "bytes_per_launch": 27.5776e9 / 147,
 }
 
 
@@ -128,8 +128,9 @@ def gemm_traffic():
     return GEMM_TRAFFIC["bytes_per_launch"] if h.hexdigest() == GEMM_TRAFFIC["sha256"] else None
 
 
-def cpu_baseline(w, budget_s=25.0):
-    """The oracle, as it stands, on a bounded sample: the 124M step on B=1 x T=256 tokens."""
+def cpu_baseline(w, min_s=12.0, budget_s=30.0):
+    """The oracle, as it stands, on a bounded sample: the 124M step on B=1 x T=256 tokens, repeated
+    until at least min_s seconds of CPU work (and at most budget_s) have elapsed."""
     import torch
 
     from oracle import gpt2 as og
@@ -148,7 +149,7 @@ def cpu_baseline(w, budget_s=25.0):
         m.clip_and_adamw(6e-4)
         steps += 1
         el = time.perf_counter() - t0
-        if el > budget_s * 0.5 or steps >= 3:
+        if el >= min_s or el + el / steps > budget_s:
             break
     return {"value": steps * B * T / el, "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
             "sample": "GPT-2 124M fp64 oracle step (fwd+bwd+clip+AdamW) on %d x %d Zipf tokens, %d step(s), %.1f s"
@@ -159,7 +160,7 @@ def run_reference(args, w, rank, world):
     """The CPU oracle timed as the reference arm (rank 0 only)."""
     if rank != 0:
         return
-    base = cpu_baseline(w, budget_s=max(10.0, 20.0 * max(1, args.steps) / 20.0))
+    base = cpu_baseline(w)
     fpt = flops_per_token(w)
     line = {
         "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tokens/s", "n_gpus": args.gpus,

@@ -249,8 +249,17 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t mask) {
         "h"(mask)
         : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+// Release of a TMEM accumulator to the even CTA of a pair.  The even CTA arrives
+// on its own barrier; the odd CTA arrives remotely with relaxed semantics: its
+// tcgen05.ld reads have completed (tcgen05.wait::ld) and are ordered before the
+// arrive by tcgen05.fence::before_thread_sync, and there is no memory write
+// that the MMA side has to observe, so a cluster-scope release is not needed.
+__device__ __forceinline__ void release_accumulator(uint64_t *bar, uint32_t rank) {
+    if (rank == 0)
+        mbar_arrive(bar);
+    else
+        asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(smem_in_rank(bar, 0))
+                     : "memory");
 }
 
 constexpr int EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16
@@ -716,7 +725,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __syncwarp();
                         if (lane == 0) {
                             if constexpr (PAIR)
-                                mbar_arrive_cluster(smem_in_rank(&tempty[acc], 0));
+                                release_accumulator(&tempty[acc], rank);
                             else
                                 mbar_arrive(&tempty[acc]);
                         }
@@ -752,7 +761,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if constexpr (PAIR)
-                        mbar_arrive_cluster(smem_in_rank(&tempty[acc], 0));
+                        release_accumulator(&tempty[acc], rank);
                     else
                         mbar_arrive(&tempty[acc]);
                 }
