@@ -100,12 +100,15 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     // CTA pairs on 256 x 256 tiles (cta_group::2): each SM reads half of the B
     // tile per stage, which keeps shared-memory traffic per MMA within what the
     // SM delivers, at the cost of pair synchronisation per tile.  Measured on
-    // the model's shapes, pairs pay off for long K, for large plain outputs and
-    // for weight gradients with enough tiles; short-K products with a heavy
-    // epilogue (GELU, residual) or few tiles stay on single CTAs.
+    // the model's shapes, pairs pay off for long K, for large plain outputs, for
+    // the GELU forward and for weight gradients with enough tiles; short-K
+    // products that read a second operand (residual, GELU backward) or have few
+    // tiles stay on single CTAs.
     const int pair_tiles = ceil_div(g.M, 2 * BM) * ceil_div(g.N, 256);
-    const bool pair = BN == 256 && (g.epi == GPT2_EPI_ACCUM_F32 ? pair_tiles >= 16
-                                                                : (g.K >= 1024 || (g.epi == GPT2_EPI_STORE && g.N >= 2048)));
+    const bool pair = BN == 256 && (g.epi == GPT2_EPI_ACCUM_F32
+                                        ? pair_tiles >= 16
+                                        : (g.K >= 1024 || g.epi == GPT2_EPI_GELU ||
+                                           (g.epi == GPT2_EPI_STORE && g.N >= 2048)));
     const int conc = pair ? num_sms / 2 : num_sms;  // work units that run at once
     Params P;
     P.M = g.M;
@@ -140,10 +143,11 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     }
     P.k_blocks_per_split = ceil_div(P.num_k_blocks, P.splits);
     P.splits = ceil_div(P.num_k_blocks, P.k_blocks_per_split);
-    // raster: share the A block across concurrent tiles when A is far larger than L2
-    // and B is not (A would otherwise stream from HBM once per N block)
+    // raster: share the A block across concurrent tiles when A is not small next
+    // to L2 and B is (with m fastest, A would stream from HBM once per N block:
+    // measured 2.3x the A bytes for 100 MB operands and N = 768)
     const double a_bytes = 2.0 * g.M * g.K, b_bytes = 2.0 * g.N * g.K;
-    P.n_fastest = (P.num_n_blocks <= 8 && a_bytes > 256e6 && b_bytes < 96e6) ? 1 : 0;
+    P.n_fastest = (P.num_n_blocks <= 8 && a_bytes > 32e6 && b_bytes < 96e6) ? 1 : 0;
     P.epi = g.epi;
     P.alpha = g.alpha;
     P.bias = g.bias;
