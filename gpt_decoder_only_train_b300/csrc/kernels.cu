@@ -156,6 +156,76 @@ __global__ void ln_fwd_kernel(const T *__restrict__ x, const float *__restrict__
     }
 }
 
+// bf16 rows (forward and backward): the computation of the generic kernels with the packets handled as 32-bit words
+// (a bf16 is the top half of an fp32, so unpacking is one shift or mask) and the
+// output rounded two elements at a time.
+__device__ __forceinline__ F2 bf16x2_f2(uint32_t w) { return f2(bf16_lo(w), bf16_hi(w)); }
+__device__ __forceinline__ uint32_t f2_bf16x2(F2 v) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f2_lo(v), f2_hi(v));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int VPL>
+__global__ void ln_fwd_bf16_kernel(const bf16 *__restrict__ x, const float *__restrict__ g,
+                                   const float *__restrict__ b, bf16 *__restrict__ y, float *__restrict__ mean,
+                                   float *__restrict__ rstd, int N, int C) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= N) return;
+    const int npk = C / 8;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + (int64_t)row * C);
+    uint4 v[VPL];
+    F2 s = f2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int p = lane + 32 * i;
+        if (p < npk) {
+            v[i] = __ldcs(xr + p);
+            s = f2_add(s, f2_add(f2_add(bf16x2_f2(v[i].x), bf16x2_f2(v[i].y)),
+                                 f2_add(bf16x2_f2(v[i].z), bf16x2_f2(v[i].w))));
+        }
+    }
+    const float mu = warp_sum(f2_lo(s) + f2_hi(s)) / C;
+    const F2 nmu = f2(-mu, -mu);
+    F2 q = f2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int p = lane + 32 * i;
+        if (p < npk) {
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const F2 d = f2_add(bf16x2_f2(w[k]), nmu);
+                q = f2_fma(d, d, q);
+            }
+        }
+    }
+    const float rs = rsqrtf(warp_sum(f2_lo(q) + f2_hi(q)) / C + 1e-5f);
+    const F2 rs2 = f2(rs, rs);
+    uint4 *yr = reinterpret_cast<uint4 *>(y + (int64_t)row * C);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int p = lane + 32 * i;
+        if (p < npk) {
+            const float4 g0 = *reinterpret_cast<const float4 *>(g + p * 8);
+            const float4 g1 = *reinterpret_cast<const float4 *>(g + p * 8 + 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(b + p * 8);
+            const float4 b1 = *reinterpret_cast<const float4 *>(b + p * 8 + 4);
+            const F2 gk[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
+            const F2 bk[4] = {f2(b0.x, b0.y), f2(b0.z, b0.w), f2(b1.x, b1.y), f2(b1.z, b1.w)};
+            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = f2_bf16x2(f2_fma(f2_mul(f2_add(bf16x2_f2(w[k]), nmu), rs2), gk[k], bk[k]));
+            yr[p] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    if (lane == 0) {
+        mean[row] = mu;
+        rstd[row] = rs;
+    }
+}
+
 template <typename T> static int ln_vpl(int C) {
     const int npk = C / Pack16<T>::N;
     const int per_lane = (npk + 31) / 32;
@@ -180,7 +250,11 @@ int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *m
                       cudaStream_t st) {
     if (C % Pack16<T>::N) return GPT2_ERR_BAD_SHAPE;
     const int warps = 8, grid = ceil_div(N, warps);
-    LN_VPL_SWITCH(ln_vpl<T>(C), ln_fwd_kernel<T, V_><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C))
+    if constexpr (sizeof(T) == 2) {
+        LN_VPL_SWITCH(ln_vpl<T>(C), ln_fwd_bf16_kernel<V_><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C))
+    } else {
+        LN_VPL_SWITCH(ln_vpl<T>(C), ln_fwd_kernel<T, V_><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C))
+    }
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
@@ -296,6 +370,108 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_kernel(const T *__restrict__ dy
     }
 }
 
+template <int VPL>
+__global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restrict__ dy, const bf16 *__restrict__ x,
+                                                             const float *__restrict__ mean,
+                                                             const float *__restrict__ rstd,
+                                                             const float *__restrict__ g, const bf16 *dres_in,
+                                                             bf16 *dres_out, float *__restrict__ dg,
+                                                             float *__restrict__ db, float *__restrict__ dsum, int N,
+                                                             int C) {
+    extern __shared__ float sh[];  // [warps][3C]: dg, db, column sums of dres_out
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, warps = blockDim.x >> 5;
+    const int npk = C / 8;
+    F2 adg[VPL][4], adb[VPL][4], ads[VPL][4];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) adg[i][k] = adb[i][k] = ads[i][k] = f2(0.f, 0.f);
+    for (int row = blockIdx.x * warps + wid; row < N; row += gridDim.x * warps) {
+        const int64_t off = (int64_t)row * C;
+        uint4 vdy[VPL], vx[VPL], vr[VPL];
+        const float mu = mean[row], rs = rstd[row];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
+                vdy[i] = __ldcs(reinterpret_cast<const uint4 *>(dy + off) + p);
+                vx[i] = __ldcs(reinterpret_cast<const uint4 *>(x + off) + p);
+                if (dres_in) vr[i] = __ldcs(reinterpret_cast<const uint4 *>(dres_in + off) + p);
+            }
+        }
+        const F2 rs2 = f2(rs, rs), nmr = f2(-mu * rs, -mu * rs);  // xhat = x rs - mu rs
+        F2 s1 = f2(0.f, 0.f), s2 = f2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
+                const float4 g0 = *reinterpret_cast<const float4 *>(g + p * 8);
+                const float4 g1 = *reinterpret_cast<const float4 *>(g + p * 8 + 4);
+                const F2 gk[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
+                const uint32_t wd[4] = {vdy[i].x, vdy[i].y, vdy[i].z, vdy[i].w};
+                const uint32_t wx[4] = {vx[i].x, vx[i].y, vx[i].z, vx[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const F2 d = bf16x2_f2(wd[k]);
+                    const F2 xh = f2_fma(bf16x2_f2(wx[k]), rs2, nmr);
+                    const F2 dxh = f2_mul(d, gk[k]);
+                    s1 = f2_add(s1, dxh);
+                    s2 = f2_fma(dxh, xh, s2);
+                    adg[i][k] = f2_fma(d, xh, adg[i][k]);
+                    adb[i][k] = f2_add(adb[i][k], d);
+                }
+            }
+        }
+        const float m1 = warp_sum(f2_lo(s1) + f2_hi(s1)) / C, m2 = warp_sum(f2_lo(s2) + f2_hi(s2)) / C;
+        const F2 nm1 = f2(-m1, -m1), nm2 = f2(-m2, -m2);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
+                const float4 g0 = *reinterpret_cast<const float4 *>(g + p * 8);
+                const float4 g1 = *reinterpret_cast<const float4 *>(g + p * 8 + 4);
+                const F2 gk[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
+                const uint32_t wd[4] = {vdy[i].x, vdy[i].y, vdy[i].z, vdy[i].w};
+                const uint32_t wx[4] = {vx[i].x, vx[i].y, vx[i].z, vx[i].w};
+                const uint32_t wr[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
+                uint32_t wo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const F2 xh = f2_fma(bf16x2_f2(wx[k]), rs2, nmr);
+                    // dx = rs (dy g - m1 - xhat m2)
+                    const F2 t = f2_fma(xh, nm2, f2_fma(bf16x2_f2(wd[k]), gk[k], nm1));
+                    F2 ov = f2_mul(t, rs2);
+                    if (dres_in) ov = f2_add(ov, bf16x2_f2(wr[k]));
+                    wo[k] = f2_bf16x2(ov);
+                    // column sums of the stored (rounded) output
+                    ads[i][k] = f2_add(ads[i][k], bf16x2_f2(wo[k]));
+                }
+                reinterpret_cast<uint4 *>(dres_out + off)[p] = make_uint4(wo[0], wo[1], wo[2], wo[3]);
+            }
+        }
+    }
+    float *my = sh + wid * 3 * C;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int p = lane + 32 * i;
+        if (p < npk)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int c = p * 8 + 2 * k;
+                *reinterpret_cast<float2 *>(my + c) = make_float2(f2_lo(adg[i][k]), f2_hi(adg[i][k]));
+                *reinterpret_cast<float2 *>(my + C + c) = make_float2(f2_lo(adb[i][k]), f2_hi(adb[i][k]));
+                *reinterpret_cast<float2 *>(my + 2 * C + c) = make_float2(f2_lo(ads[i][k]), f2_hi(ads[i][k]));
+            }
+    }
+    __syncthreads();
+    const int ncol = dsum ? 3 * C : 2 * C;
+    for (int c = threadIdx.x; c < ncol; c += blockDim.x) {
+        float sum = 0.f;
+        for (int w = 0; w < warps; ++w) sum += sh[w * 3 * C + c];
+        atomicAdd(c < C ? dg + c : c < 2 * C ? db + (c - C) : dsum + (c - 2 * C), sum);
+    }
+}
+
 template <typename T>
 int layernorm_backward(const T *dy, const T *x, const float *mean, const float *rstd, const float *g, const T *dres_in,
                        T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st, float *dsum) {
@@ -307,10 +483,21 @@ int layernorm_backward(const T *dy, const T *x, const float *mean, const float *
     GPT2_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     const int grid = std::max(1, std::min(ceil_div(N, warps), sms));
     const size_t smem = (size_t)warps * 3 * C * sizeof(float);
-    LN_VPL_SWITCH(ln_vpl<T>(C), {
-        GPT2_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_kernel<T, V_>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        ln_bwd_kernel<T, V_><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, dsum, N, C);
-    })
+    if constexpr (sizeof(T) == 2) {
+        LN_VPL_SWITCH(ln_vpl<T>(C), {
+            GPT2_CUDA_TRY(
+                cudaFuncSetAttribute(ln_bwd_bf16_kernel<V_>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+            ln_bwd_bf16_kernel<V_><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, dsum,
+                                                                   N, C);
+        })
+    } else {
+        LN_VPL_SWITCH(ln_vpl<T>(C), {
+            GPT2_CUDA_TRY(
+                cudaFuncSetAttribute(ln_bwd_kernel<T, V_>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+            ln_bwd_kernel<T, V_><<<grid, 32 * warps, smem, st>>>(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, dsum, N,
+                                                                 C);
+        })
+    }
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
