@@ -370,6 +370,12 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_kernel(const T *__restrict__ dy
     }
 }
 
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+
 template <int VPL>
 __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restrict__ dy, const bf16 *__restrict__ x,
                                                              const float *__restrict__ mean,
@@ -378,27 +384,55 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restr
                                                              bf16 *dres_out, float *__restrict__ dg,
                                                              float *__restrict__ db, float *__restrict__ dsum, int N,
                                                              int C) {
-    extern __shared__ float sh[];  // [warps][3C]: dg, db, column sums of dres_out
+    // Per warp, 3C floats of shared memory: while rows are processed they hold
+    // two row buffers (dy, x, dres_in: 3 x C bf16 each), the next row being
+    // fetched (cp.async) while the current one is computed; at the end they hold
+    // the warp's dg, db and column-sum partials.  A lane only ever touches its
+    // own packets of a buffer, so no warp synchronisation is needed around them.
+    extern __shared__ float sh[];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, warps = blockDim.x >> 5;
     const int npk = C / 8;
+    uint8_t *wbuf = reinterpret_cast<uint8_t *>(sh + (size_t)wid * 3 * C);
+    auto slot = [&](int b, int a) { return reinterpret_cast<uint4 *>(wbuf + (size_t)(b * 3 + a) * C * 2); };
+    auto fetch = [&](int row, int b) {
+        const int64_t off = (int64_t)row * C;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
+                cp_async16(slot(b, 0) + p, reinterpret_cast<const uint4 *>(dy + off) + p);
+                cp_async16(slot(b, 1) + p, reinterpret_cast<const uint4 *>(x + off) + p);
+                if (dres_in) cp_async16(slot(b, 2) + p, reinterpret_cast<const uint4 *>(dres_in + off) + p);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
     F2 adg[VPL][4], adb[VPL][4], ads[VPL][4];
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
 #pragma unroll
         for (int k = 0; k < 4; ++k) adg[i][k] = adb[i][k] = ads[i][k] = f2(0.f, 0.f);
-    for (int row = blockIdx.x * warps + wid; row < N; row += gridDim.x * warps) {
+    const int row0 = blockIdx.x * warps + wid, rstep = gridDim.x * warps;
+    float nmu = 0.f, nrs = 0.f;
+    if (row0 < N) {
+        fetch(row0, 0);
+        nmu = mean[row0];
+        nrs = rstd[row0];
+    }
+    int b = 0;
+    for (int row = row0; row < N; row += rstep, b ^= 1) {
         const int64_t off = (int64_t)row * C;
-        uint4 vdy[VPL], vx[VPL], vr[VPL];
-        const float mu = mean[row], rs = rstd[row];
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int p = lane + 32 * i;
-            if (p < npk) {
-                vdy[i] = __ldcs(reinterpret_cast<const uint4 *>(dy + off) + p);
-                vx[i] = __ldcs(reinterpret_cast<const uint4 *>(x + off) + p);
-                if (dres_in) vr[i] = __ldcs(reinterpret_cast<const uint4 *>(dres_in + off) + p);
-            }
+        const float mu = nmu, rs = nrs;
+        if (row + rstep < N) {
+            fetch(row + rstep, b ^ 1);
+            nmu = mean[row + rstep];
+            nrs = rstd[row + rstep];
+        } else {
+            asm volatile("cp.async.commit_group;" ::: "memory");  // keeps the group count uniform
         }
+        asm volatile("cp.async.wait_group 1;" ::: "memory");  // this row's copies have landed
+        // the row stays in shared memory: each pass reads the packets it needs
+        const uint4 *vdy = slot(b, 0), *vx = slot(b, 1), *vr = slot(b, 2);
         const F2 rs2 = f2(rs, rs), nmr = f2(-mu * rs, -mu * rs);  // xhat = x rs - mu rs
         F2 s1 = f2(0.f, 0.f), s2 = f2(0.f, 0.f);
 #pragma unroll
@@ -408,8 +442,9 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restr
                 const float4 g0 = *reinterpret_cast<const float4 *>(g + p * 8);
                 const float4 g1 = *reinterpret_cast<const float4 *>(g + p * 8 + 4);
                 const F2 gk[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
-                const uint32_t wd[4] = {vdy[i].x, vdy[i].y, vdy[i].z, vdy[i].w};
-                const uint32_t wx[4] = {vx[i].x, vx[i].y, vx[i].z, vx[i].w};
+                const uint4 pd = vdy[p], px = vx[p];
+                const uint32_t wd[4] = {pd.x, pd.y, pd.z, pd.w};
+                const uint32_t wx[4] = {px.x, px.y, px.z, px.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const F2 d = bf16x2_f2(wd[k]);
@@ -431,9 +466,10 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restr
                 const float4 g0 = *reinterpret_cast<const float4 *>(g + p * 8);
                 const float4 g1 = *reinterpret_cast<const float4 *>(g + p * 8 + 4);
                 const F2 gk[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
-                const uint32_t wd[4] = {vdy[i].x, vdy[i].y, vdy[i].z, vdy[i].w};
-                const uint32_t wx[4] = {vx[i].x, vx[i].y, vx[i].z, vx[i].w};
-                const uint32_t wr[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
+                const uint4 pd = vdy[p], px = vx[p], pr = dres_in ? vr[p] : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t wd[4] = {pd.x, pd.y, pd.z, pd.w};
+                const uint32_t wx[4] = {px.x, px.y, px.z, px.w};
+                const uint32_t wr[4] = {pr.x, pr.y, pr.z, pr.w};
                 uint32_t wo[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -450,6 +486,8 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restr
             }
         }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();  // the row buffers become the partial rows
     float *my = sh + wid * 3 * C;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
