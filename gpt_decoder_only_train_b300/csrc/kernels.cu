@@ -874,14 +874,15 @@ __global__ void __launch_bounds__(1024) classifier_bf16_kernel(bf16 *logits, con
     }
 }
 
-// Shared-memory pipelined variant for large vocabularies: each row (Vp bf16)
-// arrives by one bulk asynchronous copy into one of two shared-memory
-// buffers, so the next row streams in while this one is reduced and written.
-// Per row: max (block reduction), e = 2^(x log2e - M log2e) summed in fp32 and
-// stored back as bf16 in place, then dz = e * dscale / S written with 16-byte
-// stores; the target logit is read before the overwrite and its dz recomputed
-// in fp32.
+// Pipelined variant for large vocabularies: each row (Vp bf16) arrives by one
+// bulk asynchronous copy into one of two shared-memory buffers; a row is moved
+// to registers as soon as it has landed and its buffer is refilled, so three
+// rows per SM are in flight (two copies and the one being computed).
+// Per row: max (block reduction), e = 2^(x log2e - M log2e) rounded to bf16 and
+// summed in fp32, then dz = e * dscale / S written with 16-byte stores; the
+// target logit is read from the buffer and its dz recomputed in fp32.
 constexpr int CLS_SMEM_THREADS = 1024;
+constexpr int CLS_PPT = 7;  // 16-byte packets of a row per thread: Vp <= 7 * 1024 * 8
 
 // 2^x with the hardware approximation (MUFU.EX2, flush-to-zero); the values
 // are stored as bf16 and summed in fp32, far above its error.
@@ -946,65 +947,74 @@ __global__ void __launch_bounds__(CLS_SMEM_THREADS, 1)
         int tg = targets[row];
         const bool bad = tg < 0 || tg >= V;
         if (bad) tg = 0;
+        // The row moves to registers (at most CLS_PPT packets per thread) and
+        // its buffer is refilled with the row two ahead at once, so that copy
+        // has the rest of this row and all of the next to land.
+        uint4 ev[CLS_PPT];
+#pragma unroll
+        for (int j = 0; j < CLS_PPT; ++j) {
+            const int p = threadIdx.x + j * CLS_SMEM_THREADS;
+            if (p < npk) ev[j] = zs[p];
+        }
+        const float zt = __bfloat162float(reinterpret_cast<const bf16 *>(zs)[tg]);
+        __syncthreads();  // every thread is done with this row's buffer
+        if (threadIdx.x == 0 && row + 2 * (int)gridDim.x < N) issue(row + 2 * gridDim.x, buf);
         // Pass 1: row max.  Packets below full_pk hold only real columns; the
         // max of bf16 values is exact in bf16, two per instruction.
         uint32_t m2 = 0xff80ff80u;  // (-inf, -inf)
         float m = -INFINITY;
-        for (int p = threadIdx.x; p < full_pk; p += blockDim.x) {
-            const uint4 v = zs[p];
-            asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v.x));
-            asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v.y));
-            asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v.z));
-            asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(v.w));
-        }
-        for (int p = full_pk + threadIdx.x; p < npk; p += blockDim.x) {  // the padded tail
-            const uint4 v = zs[p];
-            const uint32_t *u = &v.x;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (p * 8 + 2 * k < V) m = fmaxf(m, bf_lo(u[k]));
-                if (p * 8 + 2 * k + 1 < V) m = fmaxf(m, bf_hi(u[k]));
+        for (int j = 0; j < CLS_PPT; ++j) {
+            const int p = threadIdx.x + j * CLS_SMEM_THREADS;
+            if (p < full_pk) {
+                asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(ev[j].x));
+                asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(ev[j].y));
+                asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(ev[j].z));
+                asm("max.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(ev[j].w));
+            } else if (p < npk) {  // the padded tail
+                const uint32_t *u = &ev[j].x;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (p * 8 + 2 * k < V) m = fmaxf(m, bf_lo(u[k]));
+                    if (p * 8 + 2 * k + 1 < V) m = fmaxf(m, bf_hi(u[k]));
+                }
             }
         }
         m = fmaxf(m, fmaxf(bf_lo(m2), bf_hi(m2)));
-        const float zt = __bfloat162float(reinterpret_cast<const bf16 *>(zs)[tg]);
         m = warp_max(m);
         if (lane == 0) red_m[buf][wid] = m;
-        __syncthreads();  // (also: everyone has read zt before the in-place overwrite)
+        __syncthreads();
         float M = red_m[buf][0];
         for (int w = 1; w < nw; ++w) M = fmaxf(M, red_m[buf][w]);
-        // Pass 2: e = 2^(x log2e - M log2e), summed in fp32 and stored back as
-        // bf16 in place; the arithmetic runs on column pairs (.f32x2).
+        // Pass 2: e = 2^(x log2e - M log2e), rounded to bf16 in place, summed
+        // in fp32; the arithmetic runs on column pairs (.f32x2).
         const F2 l2e2 = f2(L2E, L2E), nmc2 = f2(-M * L2E, -M * L2E);
-        F2 sacc2 = f2(0.f, 0.f);
-        for (int p = threadIdx.x; p < full_pk; p += blockDim.x) {
-            uint4 v = zs[p];
-            uint32_t *u = &v.x;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const F2 t = f2_fma(f2(bf_lo(u[k]), bf_hi(u[k])), l2e2, nmc2);
-                const float a = ex2_hw(f2_lo(t)), b2 = ex2_hw(f2_hi(t));
-                sacc2 = f2_add(sacc2, f2(a, b2));
-                u[k] = bf_pack(a, b2);
-            }
-            zs[p] = v;
-        }
-        float sacc = f2_lo(sacc2) + f2_hi(sacc2);
         const float Mc = M * L2E;
-        for (int p = full_pk + threadIdx.x; p < npk; p += blockDim.x) {  // the padded tail: 0 past V
-            uint4 v = zs[p];
-            uint32_t *u = &v.x;
+        F2 sacc2 = f2(0.f, 0.f);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int c = p * 8 + 2 * k;
-                const float a = c < V ? ex2_hw(fmaf(bf_lo(u[k]), L2E, -Mc)) : 0.f;
-                const float b2 = c + 1 < V ? ex2_hw(fmaf(bf_hi(u[k]), L2E, -Mc)) : 0.f;
-                sacc += a + b2;
-                u[k] = bf_pack(a, b2);
+        for (int j = 0; j < CLS_PPT; ++j) {
+            const int p = threadIdx.x + j * CLS_SMEM_THREADS;
+            uint32_t *u = &ev[j].x;
+            if (p < full_pk) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const F2 t = f2_fma(f2(bf_lo(u[k]), bf_hi(u[k])), l2e2, nmc2);
+                    const float a = ex2_hw(f2_lo(t)), b2 = ex2_hw(f2_hi(t));
+                    sacc2 = f2_add(sacc2, f2(a, b2));
+                    u[k] = bf_pack(a, b2);
+                }
+            } else if (p < npk) {  // the padded tail: 0 past V
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int c = p * 8 + 2 * k;
+                    const float a = c < V ? ex2_hw(fmaf(bf_lo(u[k]), L2E, -Mc)) : 0.f;
+                    const float b2 = c + 1 < V ? ex2_hw(fmaf(bf_hi(u[k]), L2E, -Mc)) : 0.f;
+                    sacc2 = f2_add(sacc2, f2(a, b2));
+                    u[k] = bf_pack(a, b2);
+                }
             }
-            zs[p] = v;
         }
-        sacc = warp_sum(sacc);
+        const float sacc = warp_sum(f2_lo(sacc2) + f2_hi(sacc2));
         if (lane == 0) red_s[buf][wid] = sacc;
         __syncthreads();
         float S = 0.f;
@@ -1012,28 +1022,30 @@ __global__ void __launch_bounds__(CLS_SMEM_THREADS, 1)
         const float lse = M + logf(S);
         const float scale = dscale / S;
         const F2 scale2 = f2(scale, scale);
-        // Pass 3: dz = e dscale / S, 16-byte stores
+        // Pass 3: dz = e dscale / S from the registers, 16-byte stores
         uint4 *zg = reinterpret_cast<uint4 *>(logits + (int64_t)row * Vp);
-        for (int p = threadIdx.x; p < npk; p += blockDim.x) {
-            uint4 v = zs[p];
-            uint32_t *u = &v.x;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const F2 y = f2_mul(f2(bf_lo(u[k]), bf_hi(u[k])), scale2);
-                u[k] = bf_pack(f2_lo(y), f2_hi(y));
+        for (int j = 0; j < CLS_PPT; ++j) {
+            const int p = threadIdx.x + j * CLS_SMEM_THREADS;
+            if (p < npk) {
+                uint4 v = ev[j];
+                uint32_t *u = &v.x;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const F2 y = f2_mul(f2(bf_lo(u[k]), bf_hi(u[k])), scale2);
+                    u[k] = bf_pack(f2_lo(y), f2_hi(y));
+                }
+                if (p == (tg >> 3)) {  // the target's dz from the logit itself, in fp32
+                    bf16 *e8 = reinterpret_cast<bf16 *>(&v);
+                    e8[tg & 7] = __float2bfloat16_rn((__expf(zt - lse) - 1.0f) * dscale);
+                }
+                zg[p] = v;
             }
-            if (p == (tg >> 3)) {  // the target's dz from the logit itself, in fp32
-                bf16 *e8 = reinterpret_cast<bf16 *>(&v);
-                e8[tg & 7] = __float2bfloat16_rn((__expf(zt - lse) - 1.0f) * dscale);
-            }
-            zg[p] = v;
         }
         if (threadIdx.x == 0) {
             loss_rows[row] = lse - zt;
             if (bad) raise_device_error(err, DEVERR_BAD_TOKEN);
         }
-        __syncthreads();  // the buffer is free again
-        if (threadIdx.x == 0 && row + 2 * (int)gridDim.x < N) issue(row + 2 * gridDim.x, buf);
     }
 }
 
@@ -1051,7 +1063,7 @@ int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, in
         // large rows: shared-memory pipeline (two rows of Vp bf16 in flight per SM)
         const int row_pad = (Vp * 2 + 127) / 128 * 128;
         const size_t cls_smem_bytes = 2 * (size_t)row_pad + 64;
-        if (Vp >= 8192 && cls_smem_bytes <= 200 * 1024) {
+        if (Vp >= 8192 && cls_smem_bytes <= 200 * 1024 && npk <= CLS_PPT * CLS_SMEM_THREADS) {
             static bool attr = false;
             if (!attr) {
                 GPT2_CUDA_TRY(cudaFuncSetAttribute(classifier_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
