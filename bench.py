@@ -110,8 +110,8 @@ class ClockSampler:
 GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
-    "sha256": "64b1ab090b0cb3b5bc990960cd11829e71a749b86ae2cc179f15001604a4cbdd",
-    "bytes_per_launch": 27.5776e9 / 147,
+    "sha256": "8617e6a8cb8608fb613538387fb1109018070f4f302f4a2cf0252289901347e2",
+    "bytes_per_launch": 21.6443e9 / 147,
 }
 
 
