@@ -43,6 +43,20 @@ def flops_per_token(w):
     return 3.0 * fwd
 
 
+def flops_per_token_6n(w):
+    """The 6N + 12 L C T convention (N = parameters without the position table, full T x T attention),
+    reported beside the algorithmic count for comparison with published MFU figures."""
+    L, C, V, T = w["L"], w["C"], w["V"], w["T"]
+    n = V * C + L * (12 * C * C + 13 * C) + 2 * C
+    return 6.0 * n + 12.0 * L * C * T
+
+
+def workload_label(name, w, accum):
+    return "%s: L=%d C=%d H=%d V=%d (Vp=%d) B=%d T=%d%s, %d micro-step(s) (fwd+bwd) + clip + AdamW per step" % (
+        name, w["L"], w["C"], w["H"], w["V"], w["Vp"], w["B"], w["T"],
+        ", GELU recompute" if w.get("recompute_gelu") else "", accum)
+
+
 def read_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -110,6 +124,7 @@ class ClockSampler:
 GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
+    "workload": "gpt2_124m",
     "sha256": "8617e6a8cb8608fb613538387fb1109018070f4f302f4a2cf0252289901347e2",
     "bytes_per_launch": 21.6443e9 / 147,
 }
@@ -164,9 +179,10 @@ def run_reference(args, w, rank, world):
     fpt = flops_per_token(w)
     line = {
         "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w["B"] * w["T"] / base["value"],
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * w["B"] * w["T"] * int(w.get("grad_accum", 1)) / base["value"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "gpt2_124m step, sample of B=1 x T=256 tokens", "seed": w["seed"]},
+        "config": {"workload": "%s step, sample of B=1 x T=256 tokens" % args.workload, "seed": w["seed"]},
         "cpu_baseline": base,
         "e2e": {"value": base["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "mfu_note": "%.3e FLOP/token" % fpt,
@@ -207,16 +223,18 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     build.build()
     B, T = w["B"], w["T"]
-    BT = B * T
+    accum = int(w.get("grad_accum", 1))  # micro-steps (consecutive stream windows) per optimizer step
+    BT = B * T * accum  # tokens per step
     nsteps = args.warmup + args.steps
     # independent batches per rank: the replica r reads stream windows offset by r
     xs, ys = [], []
     for i in range(nsteps):
-        x, y = synthetic.zipf_window(w["seed"], B, T, w["V"], micro_step=rank * nsteps + i)
-        xs.append(x)
-        ys.append(y)
-    X = torch.from_numpy(np.stack(xs)).cuda()
-    Y = torch.from_numpy(np.stack(ys)).cuda()
+        for j in range(accum):
+            x, y = synthetic.zipf_window(w["seed"], B, T, w["V"], micro_step=(rank * nsteps + i) * accum + j)
+            xs.append(x)
+            ys.append(y)
+    X = torch.from_numpy(np.stack(xs).reshape(nsteps, accum, B, T)).cuda()
+    Y = torch.from_numpy(np.stack(ys).reshape(nsteps, accum, B, T)).cuda()
     stream = torch.cuda.current_stream()
     model = g.GPT2(w, seed=w["seed"], stream=stream)
 
@@ -229,9 +247,12 @@ def main():
         return 6e-5 + 0.5 * (1 + cos(pi * r)) * (6e-4 - 6e-5)
 
     def step(i, x, y):
+        """One optimizer step over x, y [accum, B, T]: the loss is the mean over its micro-steps."""
         model.zero_grad()
-        loss = model.forward(x, y)
-        model.backward(1.0)
+        loss = 0.0
+        for j in range(accum):
+            loss += model.forward(x[j], y[j]) / accum
+            model.backward(1.0 / accum)
         norm = model.clip_and_adamw(lr_at(i), 0.9, 0.95, 1e-8, 0.1, 1.0)
         return loss, norm
 
@@ -270,9 +291,9 @@ def main():
     model.profile(False)
 
     # ---- end to end through the public API: host buffers, copies inside the timed region
-    Xh = torch.from_numpy(np.stack(xs)).pin_memory()
-    Yh = torch.from_numpy(np.stack(ys)).pin_memory()
-    xd = torch.empty(B, T, dtype=torch.int32, device="cuda")
+    Xh = torch.from_numpy(np.stack(xs).reshape(nsteps, accum, B, T)).pin_memory()
+    Yh = torch.from_numpy(np.stack(ys).reshape(nsteps, accum, B, T)).pin_memory()
+    xd = torch.empty(accum, B, T, dtype=torch.int32, device="cuda")
     yd = torch.empty_like(xd)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -316,15 +337,19 @@ def main():
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic Zipf(1.1) tokens over V=50257, random-init weights (seeded)",
-            "config": {"workload": "gpt2_124m: L=12 C=768 H=12 V=50257 (Vp=50304) B=16 T=1024, one micro-step "
-                                   "(fwd+bwd+clip+AdamW) per step", "global_batch": B * world, "seq_len": T,
+            "config": {"workload": workload_label(args.workload, w, accum), "global_batch": B * accum * world,
+                       "seq_len": T,
                        "parallelism": "replicas x%d (no gradient exchange)" % world,
                        "l2": "inputs larger than L2 (9 GB arena per step)"},
             "mfu": {"flops_per_token": fpt, "vs_nominal_dense_bf16_2250": per_gpu * fpt / (NOMINAL_BF16_TFLOPS * 1e12),
-                    "vs_measured_bf16_burst": per_gpu * fpt / (peaks["bf16_tflops"] * 1e12)},
+                    "vs_measured_bf16_burst": per_gpu * fpt / (peaks["bf16_tflops"] * 1e12),
+                    "flops_per_token_6n_12lct": flops_per_token_6n(w),
+                    "vs_nominal_dense_bf16_2250_6n_12lct":
+                        per_gpu * flops_per_token_6n(w) / (NOMINAL_BF16_TFLOPS * 1e12)},
             "roofline": {"kernel": "tcgen05 bf16 GEMM (all matmuls of the step)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": (achieved / peak) if achieved else None, "traffic": gemm_traffic(),
+                         "frac": (achieved / peak) if achieved else None,
+                         "traffic": gemm_traffic() if args.workload == GEMM_TRAFFIC["workload"] else None,
                          "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
                          "peak_source": "%s bf16_tflops_sustained" % peak_src,
                          "launches_per_step": mm_n / args.steps,

@@ -1,0 +1,63 @@
+"""Host-side checks of the benchmark's accounting (no GPU).
+
+The FLOP counts that MFU divides by are pinned against an independent count:
+the sum of 2*M*N*K over the matmuls the step performs (listed here shape by
+shape, forward and both backward products) plus the causal attention pairs,
+and the 6N + 12 L C T convention against the parameter count of the oracle's
+own parameter list.
+"""
+import bench
+import synthetic
+from oracle import gpt2 as og
+
+
+def _matmul_flops_per_token(w):
+    """Sum of 2*M*N*K over the step's matmuls, per token (M = tokens)."""
+    L, C, V = w["L"], w["C"], w["V"]
+    fwd_shapes = []
+    for _ in range(L):
+        fwd_shapes += [(C, 3 * C), (C, C), (C, 4 * C), (4 * C, C)]  # (in, out) of qkv, proj, fc, fcproj
+    fwd_shapes.append((C, V))  # tied LM head over the real vocabulary
+    fwd = sum(2 * k * n for k, n in fwd_shapes)
+    return 3 * fwd  # forward, dX and dW products have the same size
+
+
+def _attention_flops_per_token(w):
+    """QK^T and PV over the causal pairs (j <= i): 2 * 2 * hd per pair and head, 3x for training."""
+    L, C, T = w["L"], w["C"], w["T"]
+    pairs_per_token = (T + 1) / 2.0  # T(T+1)/2 pairs over T tokens
+    return 3 * L * 4 * C * pairs_per_token
+
+
+def test_flops_per_token_matches_the_shape_sum():
+    for name in ("gpt2_124m", "gpt2_350m_recompute"):
+        w = synthetic.WORKLOADS[name]
+        expect = _matmul_flops_per_token(w) + _attention_flops_per_token(w)
+        assert abs(bench.flops_per_token(w) - expect) <= 1e-9 * expect, name
+    # the figures the step is quoted with: 0.798 and 2.272 GFLOP per token
+    assert round(bench.flops_per_token(synthetic.WORKLOADS["gpt2_124m"]) / 1e9, 3) == 0.798
+    assert round(bench.flops_per_token(synthetic.WORKLOADS["gpt2_350m_recompute"]) / 1e9, 3) == 2.272
+
+
+def test_6n_convention_counts_the_oracle_parameters():
+    w = synthetic.WORKLOADS["gpt2_124m"]
+    cfg = og.Config.from_dict(w)
+    n = 0
+    for name, shape, _kind, _std, _decay in og.param_specs(cfg):
+        numel = 1
+        for s in shape:
+            numel *= s
+        if name == "wpe":
+            continue  # the convention leaves the position table out
+        if name == "wte":
+            numel = cfg.V * cfg.C  # padded rows are not parameters of the model
+        n += numel
+    expect = 6 * n + 12 * w["L"] * w["C"] * w["T"]
+    assert bench.flops_per_token_6n(w) == expect
+
+
+def test_workload_label_names_the_shape():
+    w = synthetic.WORKLOADS["gpt2_124m_accum32"]
+    label = bench.workload_label("gpt2_124m_accum32", w, 32)
+    for part in ("L=12", "C=768", "B=16", "T=1024", "32 micro-step"):
+        assert part in label
