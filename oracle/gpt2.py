@@ -48,7 +48,11 @@ Pins (tests that tie each function to something other than itself)
 * step: initial loss ~= ln V + 0.02^2 C / 2, one fixed batch overfits to loss
   < 0.1, AdamW step 1 closed form, clipped norm equals ``clip``, LR schedule
   values, causality of the logits, embedding backward vs a counting brute force;
-* init: SplitMix64 published outputs, Box-Muller moments (KS test).
+* init: SplitMix64 published outputs, Box-Muller moments (KS test);
+* sampling: the set of u in [0, 1) that draws token i has measure
+  softmax(z/temperature)_i over the candidates (exact interval lengths);
+  top_k = 1 is the argmax with the lower index on ties; a small temperature
+  tends to the argmax; generation agrees with teacher forcing.
 """
 from __future__ import annotations
 
@@ -358,6 +362,52 @@ def lr_schedule(it: int, max_lr=6e-4, min_lr=6e-5, warmup=700, max_steps=19073) 
     ratio = (it - warmup) / (max_steps - warmup)
     coeff = 0.5 * (1.0 + math.cos(math.pi * ratio))
     return min_lr + coeff * (max_lr - min_lr)
+
+
+# --------------------------------------------------------------------------- #
+# sampling ("llm.c kullanarak GPT-2 modelini düşük maliyetle yeniden
+# uygulamak", §Sampling and §SSS: a trained model can be sampled, with or
+# without a prompt; "Let's reproduce GPT-2 (124M)", §Bölümler 3: the sampling
+# loop).  The pages give no sampling rule; the reading used on both sides:
+# temperature-scaled softmax restricted to the top_k logits, the token drawn
+# by inverse CDF with a caller-supplied uniform.
+# --------------------------------------------------------------------------- #
+
+def sample_next(z, temperature: float, top_k: int, u: float) -> int:
+    """One draw from logits ``z`` [V] (any real dtype; compared as given).
+
+    Candidates: the top_k entries in the order (larger value first, equal
+    values lower index first).  Weights ``exp((z_i - z_max) / temperature)``;
+    the token is the first candidate whose cumulative weight exceeds
+    ``u * sum(weights)``; if rounding leaves none, the last candidate.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    order = [int(i) for i in np.lexsort((np.arange(z.shape[0]), -z))[:top_k]]  # by -z, then by index
+    w = [math.exp((z[i] - z[order[0]]) / temperature) for i in order]
+    target = u * sum(w)
+    cum = 0.0
+    for i, wi in zip(order, w):
+        cum += wi
+        if cum > target:
+            return int(i)
+    return int(order[-1])
+
+
+def generate(cfg: Config, P, prompt, n_new: int, temperature: float, top_k: int, uniforms):
+    """Autoregressive sampling by recomputing the whole forward for every new
+    token (no cache): prompt int [B, T0] -> [B, T0 + n_new]; uniforms [n_new, B].
+    Returns the sequences and the logits each token was drawn from
+    ([n_new, B, V], float64)."""
+    seq = torch.as_tensor(prompt).long().clone()
+    B = seq.shape[0]
+    drawn = []
+    for s in range(n_new):
+        _, z, _ = model_forward(cfg, P, seq, None)
+        last = z.reshape(B, seq.shape[1], -1)[:, -1, :]
+        drawn.append(last)
+        nxt = [sample_next(last[b].numpy(), temperature, top_k, float(uniforms[s][b])) for b in range(B)]
+        seq = torch.cat([seq, torch.tensor(nxt, dtype=torch.long).reshape(B, 1)], dim=1)
+    return seq, torch.stack(drawn)
 
 
 class OracleGPT2:
