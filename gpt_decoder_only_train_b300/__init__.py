@@ -77,6 +77,8 @@ _SIGS = {
                                                 _P]),
     "gpt2_op_matmul": (_I, [_P, _I64, _I, _P, _I64, _I, _P, _P, _P, _I64, _P, _I, _I, _I, _I, _P]),
     "gpt2_op_classifier": (_I, [_P, _P, _P, _I, _I, _I, _F, _P]),
+    "gpt2_op_sample": (_I, [_P, _I64, _I, _I, _P, _F, _I, _P, _P]),
+    "gpt2_generate": (_I, [_P, _P, _I, _I, _I, _P, _F, _I]),
     "gpt2_op_layernorm_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "gpt2_op_layernorm_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
 }
@@ -176,6 +178,14 @@ class GPT2:
 
     def backward(self, grad_scale=1.0):
         check("gpt2_backward", lib().gpt2_backward(self.handle, grad_scale))
+
+    def generate(self, seq, T0, uniforms, temperature=1.0, top_k=1):
+        """KV-cached sampling in place: seq device int32 [B, T_total] holds the prompt in
+        columns [0, T0) and receives the sampled tokens; uniforms device float32
+        [T_total - T0, B] in [0, 1) (see gpt2_generate)."""
+        B, T_total = seq.shape
+        check("gpt2_generate", lib().gpt2_generate(self.handle, _ptr(seq), B, T_total, T0, _ptr(uniforms),
+                                                   temperature, top_k))
 
     def zero_grad(self):
         check("gpt2_zero_grad", lib().gpt2_zero_grad(self.handle))
@@ -298,6 +308,12 @@ def layernorm_backward(dy, x, mean, rstd, g, dres_in, dres_out, dg, db, N, C, st
     check("gpt2_op_layernorm_backward", lib().gpt2_op_layernorm_backward(
         _ptr(dy), _ptr(x), _ptr(mean), _ptr(rstd), _ptr(g), _ptr(dres_in), _ptr(dres_out), _ptr(dg), _ptr(db),
         N, C, _stream(stream)))
+
+
+def sample(logits, ldl, B, V, uniforms, temperature, top_k, out, stream=None):
+    """out[b] = the token drawn from bf16 logits row b with uniforms[b] (the rule of gpt2_generate)."""
+    check("gpt2_op_sample", lib().gpt2_op_sample(
+        _ptr(logits), ldl, B, V, _ptr(uniforms), temperature, top_k, _ptr(out), _stream(stream)))
 
 
 def classifier(logits, targets, loss_rows, N, V, Vp, dscale, stream=None):

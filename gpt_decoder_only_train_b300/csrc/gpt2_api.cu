@@ -96,6 +96,7 @@ struct gpt2_model {
     double *norm_partials;
     unsigned *barrier;
     int *err_dev;
+    int *gen_pos;  // device position counter of gpt2_generate
     int max_adam_blocks;
     int fwd_B, fwd_T;
     bool have_dlogits;
@@ -242,6 +243,7 @@ void plan(gpt2_model &m, uint8_t *base) {
     m.norm_partials = b.take<double>((size_t)m.max_adam_blocks * 8);
     m.barrier = b.take<unsigned>(64);
     m.err_dev = b.take<int>(64);
+    m.gen_pos = b.take<int>(64);
     m.arena_bytes = b.off + 256;
 }
 
@@ -508,6 +510,93 @@ int backward_impl(gpt2_model *m, float grad_scale) {
     return GPT2_OK;
 }
 
+// ---- generation ----------------------------------------------------------------------
+// Position t of all B rows at a time.  The key/value cache is the step's qkv
+// buffer of each block with a row stride of cfg.T positions per sequence.
+// Scratch for the B rows of one position: dres (residual stream), dqkv
+// (mid-block residual), dsmall (LayerNorm outputs), datt (attention output),
+// dqkv + B*C (the position's QKV row), dbig (MLP pre-activation and GELU
+// output), layer 0's LayerNorm statistics.  The position lives in device
+// memory (gen_pos), so the launches of one position do not depend on t: the
+// first position of each kind (filling the cache from the prompt, or also
+// drawing a token) runs directly, the rest replay a CUDA graph of it.
+template <typename T>
+int decode_position(gpt2_model *m, int *d_seq, int B, int T_total, int T0, const float *d_u, float temperature,
+                    int top_k, bool draw) {
+    const gpt2_config &c = m->cfg;
+    const int C = c.C, hd = C / c.H, Tc = c.T;
+    cudaStream_t st = m->stream;
+    const int nt = (int)m->tensors.size();
+    T *x = (T *)m->dres, *xm = (T *)m->dqkv, *qkv = xm + (size_t)B * C, *y = (T *)m->dsmall, *att = (T *)m->datt;
+    T *hbuf = (T *)m->dbig, *gbuf = hbuf + (size_t)B * 4 * C;
+    float *mean = m->layers[0].ln1_mean, *rstd = m->layers[0].ln1_rstd;
+    TRY(k::embed_decode<T>(d_seq, T_total, m->gen_pos, Pf(m, 0), Pf(m, 1), x, B, C, c.V, m->err_dev, st));
+    for (int l = 0; l < c.L; ++l) {
+        const LayerParams &p = m->lp[l];
+        TRY(k::layernorm_forward<T>(x, Pf(m, p.ln1g), Pf(m, p.ln1b), y, mean, rstd, B, C, st));
+        TRY(mm<T>(m, y, C, true, W<T>(m, p.qkvw), C, true, qkv, nullptr, nullptr, 3 * C, Pf(m, p.qkvb), B, 3 * C, C,
+                  GPT2_EPI_STORE));
+        TRY(k::attention_decode<T>((T *)m->layers[l].qkv, qkv, Tc, m->gen_pos, T_total - 2, B, c.H, hd, att, st));
+        TRY(mm<T>(m, att, C, true, W<T>(m, p.projw), C, true, xm, nullptr, x, C, Pf(m, p.projb), B, C, C,
+                  GPT2_EPI_RESIDUAL));
+        TRY(k::layernorm_forward<T>(xm, Pf(m, p.ln2g), Pf(m, p.ln2b), y, mean, rstd, B, C, st));
+        TRY(mm<T>(m, y, C, true, W<T>(m, p.fcw), C, true, hbuf, gbuf, nullptr, 4 * C, Pf(m, p.fcb), B, 4 * C, C,
+                  GPT2_EPI_GELU));
+        TRY(mm<T>(m, gbuf, 4 * C, true, W<T>(m, p.fcprojw), 4 * C, true, x, nullptr, xm, C, Pf(m, p.fcprojb), B, C,
+                  4 * C, GPT2_EPI_RESIDUAL));
+    }
+    if (draw) {
+        TRY(k::layernorm_forward<T>(x, Pf(m, nt - 2), Pf(m, nt - 1), y, mean, rstd, B, C, st));
+        TRY(mm<T>(m, y, C, true, W<T>(m, 0), C, true, m->logits, nullptr, nullptr, c.Vp, nullptr, B, c.Vp, C,
+                  GPT2_EPI_STORE));
+        TRY(k::sample_topk<T>((const T *)m->logits, c.Vp, B, c.V, d_u, temperature, top_k, d_seq, T_total, 0,
+                              m->gen_pos, T0, st));
+    }
+    return k::advance_position(m->gen_pos, st);
+}
+
+template <typename T>
+int generate_impl(gpt2_model *m, int *d_seq, int B, int T_total, int T0, const float *d_u, float temperature,
+                  int top_k) {
+    GPT2_CUDA_TRY(cudaMemsetAsync(m->gen_pos, 0, sizeof(int), m->stream));
+    const int n_pos = T_total - 1;  // positions 0 .. T_total - 2; position t draws column t + 1 when t + 1 >= T0
+    int t = 0;
+    while (t < n_pos) {
+        const bool draw = t + 1 >= T0;
+        const int run = draw ? n_pos - t : T0 - 1 - t;  // positions of this kind from t on
+        TRY(decode_position<T>(m, d_seq, B, T_total, T0, d_u, temperature, top_k, draw));
+        if (run > 1) {
+            cudaStream_t cs;
+            GPT2_CUDA_TRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+            cudaStream_t saved = m->stream;
+            m->stream = cs;
+            cudaGraph_t graph = nullptr;
+            int rc = GPT2_OK;
+            const long long counted0 = g_launches.load(std::memory_order_relaxed);
+            if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+                rc = GPT2_ERR_CUDA;
+            } else {
+                rc = decode_position<T>(m, d_seq, B, T_total, T0, d_u, temperature, top_k, draw);
+                if (cudaStreamEndCapture(cs, &graph) != cudaSuccess && !rc) rc = GPT2_ERR_CUDA;
+            }
+            m->stream = saved;
+            // the launchers counted one position while capturing; each replay runs that many kernels
+            const long long per_position = g_launches.load(std::memory_order_relaxed) - counted0;
+            cudaGraphExec_t exec = nullptr;
+            if (!rc && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) rc = GPT2_ERR_CUDA;
+            for (int i = 1; !rc && i < run; ++i)
+                if (cudaGraphLaunch(exec, m->stream) != cudaSuccess) rc = GPT2_ERR_CUDA;
+            if (exec) cudaGraphExecDestroy(exec);
+            if (graph) cudaGraphDestroy(graph);
+            cudaStreamDestroy(cs);
+            if (rc) return rc;
+            gpt2_note_launches((int)((run - 2) * per_position));
+        }
+        t += run;
+    }
+    return GPT2_OK;
+}
+
 int read_error_word(gpt2_model *m, int &word) {
     GPT2_CUDA_TRY(cudaMemcpyAsync(&word, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
     GPT2_CUDA_TRY(cudaStreamSynchronize(m->stream));
@@ -601,6 +690,24 @@ extern "C" int gpt2_backward(gpt2_model *m, float grad_scale) {
     if (!m->have_dlogits) return GPT2_ERR_STATE;
     m->have_dlogits = false;  // dlogits are consumed
     return m->cfg.dtype == GPT2_DTYPE_BF16 ? backward_impl<bf16>(m, grad_scale) : backward_impl<float>(m, grad_scale);
+}
+
+extern "C" int gpt2_generate(gpt2_model *m, int32_t *d_seq, int B, int T_total, int T0, const float *d_uniforms,
+                             float temperature, int top_k) {
+    if (!m || !d_seq || !d_uniforms) return GPT2_ERR_BAD_ARG;
+    if (B <= 0 || B > m->cfg.B || T0 < 1 || T_total <= T0 || T_total > m->cfg.T) return GPT2_ERR_BAD_SHAPE;
+    if (top_k < 1 || top_k > GPT2_MAX_TOP_K || !(temperature > 0.f)) return GPT2_ERR_BAD_ARG;
+    m->have_dlogits = false;  // the activation buffers are reused
+    const bool prof = m->prof_on;  // no per-launch events inside captured graphs
+    m->prof_on = false;
+    const int rc = m->cfg.dtype == GPT2_DTYPE_BF16
+                       ? generate_impl<bf16>(m, d_seq, B, T_total, T0, d_uniforms, temperature, top_k)
+                       : generate_impl<float>(m, d_seq, B, T_total, T0, d_uniforms, temperature, top_k);
+    m->prof_on = prof;
+    if (rc) return rc;
+    int word = 0;
+    TRY(read_error_word(m, word));
+    return error_from_word(word);
 }
 
 extern "C" int gpt2_zero_grad(gpt2_model *m) {
@@ -823,6 +930,14 @@ extern "C" int gpt2_op_layernorm_backward(const void *dy, const void *x, const f
     if (N <= 0 || C <= 0 || C % 8 || C > 2048) return GPT2_ERR_BAD_SHAPE;
     return k::layernorm_backward<bf16>((const bf16 *)dy, (const bf16 *)x, mean, rstd, g, (const bf16 *)dres_in,
                                        (bf16 *)dres_out, dg, db, N, C, (cudaStream_t)stream);
+}
+
+extern "C" int gpt2_op_sample(const void *logits, int64_t ldl, int B, int V, const float *uniforms, float temperature,
+                              int top_k, int32_t *out, void *stream) {
+    if (!logits || !uniforms || !out) return GPT2_ERR_BAD_ARG;
+    if (B <= 0 || V <= 0 || ldl < V) return GPT2_ERR_BAD_SHAPE;
+    return k::sample_topk<bf16>((const bf16 *)logits, ldl, B, V, uniforms, temperature, top_k, out, 1, 0, nullptr, 0,
+                                (cudaStream_t)stream);
 }
 
 extern "C" int gpt2_op_classifier(void *logits, const int32_t *targets, float *loss_rows, int N, int V, int Vp,

@@ -64,6 +64,26 @@ int attention_backward_simt(const T *q, const T *kk, const T *v, int64_t rs, con
                             const float *lse, T *dq, T *dk, T *dv, float *dscratch, int B, int Tn, int H, int hd,
                             cudaStream_t st);
 
+// ---- forward-only decoding (generate.cu) ----------------------------------------
+// The position pos is read from device memory (*d_pos) by the kernels.
+// x[b, :] = wte[seq[b * ld + pos]] + wpe[pos]
+template <typename T>
+int embed_decode(const int *seq, int64_t ld, const int *d_pos, const float *wte, const float *wpe, T *x, int B, int C,
+                 int V, int *err, cudaStream_t st);
+// appends K, V of qkv_new [B, 3C] ([Q | K | V]) as cache row (b, pos), then
+// out[b, h*hd:(h+1)*hd] = softmax_j<=pos(q . k_j / sqrt(hd)) v_j over the cache
+// rows cache[(b * cache_T + j) * 3C]; pos <= max_pos < cache_T
+template <typename T>
+int attention_decode(T *cache, const T *qkv_new, int cache_T, const int *d_pos, int max_pos, int B, int H, int hd,
+                     T *out, cudaStream_t st);
+// the top-k sampled token of logits row b (see gpt2_generate) -> out[b * ld_out + col];
+// col = col_out and u[b], or with d_pos col = *d_pos + 1 and u[(col - T0) * B + b]
+template <typename T>
+int sample_topk(const T *logits, int64_t ldl, int B, int V, const float *u, float temperature, int top_k, int *out,
+                int64_t ld_out, int col_out, const int *d_pos, int T0, cudaStream_t st);
+// *d_pos += 1
+int advance_position(int *d_pos, cudaStream_t st);
+
 struct AdamArgs {
     float lr, beta1, beta2, eps, wd, clip;
     float bc1, bc2;  // 1 - beta^t

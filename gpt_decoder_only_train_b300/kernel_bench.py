@@ -6,6 +6,7 @@
     python -m gpt_decoder_only_train_b300.kernel_bench classifier --N 16384 --V 50257 --Vp 50304
     python -m gpt_decoder_only_train_b300.kernel_bench layernorm --N 16384 --C 768
     python -m gpt_decoder_only_train_b300.kernel_bench attention-sweep
+    python -m gpt_decoder_only_train_b300.kernel_bench generate --B 16 --prompt 32 --new 64 --top-k 50
 
 Inputs are seeded random bf16 on the device; each line reports the mean time
 per launch (CUDA events, after warm-up) and the algorithmic FLOP/s or bytes/s.
@@ -97,6 +98,26 @@ def bench_classifier(a):
     return {"op": "classifier", "N": a.N, "Vp": a.Vp, "ms": ms, "GB/s": nbytes / ms / 1e6}
 
 
+def bench_generate(a):
+    """KV-cached sampling with the 124M model: B rows, a T0-token prompt, n_new new tokens."""
+    import numpy as np
+
+    import synthetic
+
+    w = dict(synthetic.WORKLOADS["gpt2_124m"])
+    m = g.GPT2(w, seed=w["seed"])
+    B, T0, n_new = a.B, a.prompt, a.new
+    x, _ = synthetic.zipf_window(w["seed"], B, T0, w["V"])
+    seq0 = torch.zeros(B, T0 + n_new, dtype=torch.int32)
+    seq0[:, :T0] = torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32))
+    seq = seq0.cuda()
+    u = torch.rand(n_new, B, device="cuda")
+    ms = _time(lambda i: m.generate(seq, T0, u, 1.0, a.top_k), a.iters, a.warmup)
+    m.close()
+    return {"op": "generate", "model": "gpt2_124m", "B": B, "prompt": T0, "new": n_new, "top_k": a.top_k, "ms": ms,
+            "tokens/s": B * n_new / ms * 1e3, "ms_per_position": ms / (T0 + n_new - 1)}
+
+
 def bench_layernorm(a):
     gen = torch.Generator(device="cuda").manual_seed(0)
     N, C = a.N, a.C
@@ -121,7 +142,7 @@ def bench_layernorm(a):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["matmul", "attention", "classifier", "layernorm", "attention-sweep"])
+    ap.add_argument("op", choices=["matmul", "attention", "classifier", "layernorm", "attention-sweep", "generate"])
     ap.add_argument("--C", type=int, default=768)
     ap.add_argument("--M", type=int, default=16384)
     ap.add_argument("--N", type=int, default=2304)
@@ -135,6 +156,9 @@ def main(argv=None):
     ap.add_argument("--bwd", action="store_true")
     ap.add_argument("--V", type=int, default=50257)
     ap.add_argument("--Vp", type=int, default=50304)
+    ap.add_argument("--prompt", type=int, default=32)
+    ap.add_argument("--new", type=int, default=64)
+    ap.add_argument("--top-k", type=int, default=50)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     a = ap.parse_args(argv)
@@ -149,6 +173,8 @@ def main(argv=None):
         out = [bench_classifier(a)]
     elif a.op == "layernorm":
         out = bench_layernorm(a)
+    elif a.op == "generate":
+        out = [bench_generate(a)]
     else:
         out = []
         for T, B in ((256, 256), (1024, 64), (2048, 32), (4096, 16)):

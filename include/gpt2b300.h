@@ -120,6 +120,36 @@ int gpt2_backward(gpt2_model *m, float grad_scale);
 /* grads = 0 (enqueued). */
 int gpt2_zero_grad(gpt2_model *m);
 
+/* Largest top_k of gpt2_generate and gpt2_op_sample. */
+#define GPT2_MAX_TOP_K 128
+
+/*
+ * Autoregressive sampling with a key/value cache ("llm.c kullanarak GPT-2
+ * modelini düşük maliyetle yeniden uygulamak", §Sampling and §SSS: sampling
+ * works, conditionally or not; "Let's reproduce GPT-2 (124M)", §Bölümler 3).
+ * d_seq: device int32 [B, T_total], row-major.  Columns [0, T0) hold the
+ * prompt; columns [T0, T_total) receive the sampled tokens.
+ * 1 <= T0 < T_total <= cfg.T, 1 <= B <= cfg.B.
+ * d_uniforms: device float [T_total - T0, B] in [0, 1); the draw that picks
+ * column t of row b is d_uniforms[(t - T0) * B + b] (the caller owns the
+ * random numbers).
+ * The rule for column t: z = the logits of position t - 1 over v < V (rounded
+ * to bf16 in bf16 mode); candidates = the top_k largest, equal values lower
+ * index first; w_i = exp((z_i - z_max) / temperature); the token is the first
+ * candidate, in that order, whose cumulative weight exceeds u * sum(w).
+ * top_k = 1 is greedy decoding.  1 <= top_k <= GPT2_MAX_TOP_K, temperature > 0.
+ * The cache and the per-position work use the training step's activation
+ * buffers: afterwards the first B rows of the logits buffer hold the logits
+ * the last token was drawn from, and a backward needs a new forward with
+ * targets (GPT2_ERR_STATE otherwise).  Out-of-range prompt tokens give
+ * GPT2_ERR_BAD_TOKEN.  The position counter lives in device memory: the first
+ * prompt position and the first drawing position run as plain launches, the
+ * others replay a CUDA graph captured from them (on a stream the call creates
+ * and destroys).  Synchronises the stream once, at the end.
+ */
+int gpt2_generate(gpt2_model *m, int32_t *d_seq, int B, int T_total, int T0, const float *d_uniforms,
+                  float temperature, int top_k);
+
 /*
  * One fused pass over all parameters ([L] §Eğitim süreci, [R] §Video özeti):
  *   n = sqrt(sum of all grads^2) (every tensor, fp32 data, fp64 reduction);
@@ -291,6 +321,14 @@ int gpt2_op_layernorm_backward(const void *dy, const void *x, const float *mean,
 int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const void *B, int64_t ldb, int b_kmajor, void *D,
                    void *D2, const void *R, int64_t ldd, const float *bias, int M, int N, int K, int epilogue,
                    void *stream);
+
+/*
+ * The sampling rule of gpt2_generate on bf16 logits rows [B, ldl] (columns
+ * [0, V) are the candidates): out[b] = the token drawn with uniforms[b].
+ * Device pointers; ldl >= V.
+ */
+int gpt2_op_sample(const void *logits, int64_t ldl, int B, int V, const float *uniforms, float temperature, int top_k,
+                   int32_t *out, void *stream);
 
 /*
  * Fused classifier over rows of bf16 logits [N, Vp] (in place):
