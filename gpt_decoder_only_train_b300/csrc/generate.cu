@@ -18,6 +18,7 @@
 // the positions that produce a token.  The kernels read the position from
 // device memory, so the host captures one position's launches as a CUDA graph
 // and replays it (about 90 launches a position for the 124M model).
+#include <algorithm>
 #include <climits>
 
 #include "kernels.cuh"
@@ -249,6 +250,103 @@ int sample_topk(const T *logits, int64_t ldl, int B, int V, const float *u, floa
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
+}
+
+// ---- skinny matmul for the decode rows ------------------------------------------------------
+// D[b, n] = epilogue(sum_k X[b, k] W[n, k]) for Bm <= SK_MAX_ROWS rows: the
+// decode products are a few rows against a whole weight matrix, so the work
+// is the weight stream.  Each warp takes one output column n at a time and
+// reads W's row n (K-major, 16 bytes a lane) once for all rows; X sits in
+// shared memory.  The sums are warp reductions; lane b finishes row b.
+constexpr int SK_WARPS = 8;
+
+template <int EPI>
+__global__ void __launch_bounds__(SK_WARPS * 32)
+    skinny_gemm_kernel(const bf16 *__restrict__ X, int64_t ldx, const bf16 *__restrict__ W, int K, int N, int Bm,
+                       const float *__restrict__ bias, const bf16 *__restrict__ R, bf16 *__restrict__ D,
+                       bf16 *__restrict__ D2, int64_t ldd) {
+    extern __shared__ uint4 xs[];  // [Bm][K / 8] packets of X
+    const int kp = K >> 3;
+    for (int i = threadIdx.x; i < Bm * kp; i += blockDim.x) {
+        const int b = i / kp, p = i - (i / kp) * kp;
+        xs[i] = *reinterpret_cast<const uint4 *>(X + (int64_t)b * ldx + (int64_t)p * 8);
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int n = blockIdx.x * SK_WARPS + warp; n < N; n += gridDim.x * SK_WARPS) {
+        float acc[SK_MAX_ROWS];
+#pragma unroll
+        for (int b = 0; b < SK_MAX_ROWS; ++b) acc[b] = 0.f;
+        const uint4 *wr = reinterpret_cast<const uint4 *>(W + (int64_t)n * K);
+        for (int p = lane; p < kp; p += 32) {
+            const uint4 w = __ldg(wr + p);
+            const float w0 = bf16_lo(w.x), w1 = bf16_hi(w.x), w2 = bf16_lo(w.y), w3 = bf16_hi(w.y);
+            const float w4 = bf16_lo(w.z), w5 = bf16_hi(w.z), w6 = bf16_lo(w.w), w7 = bf16_hi(w.w);
+#pragma unroll
+            for (int b = 0; b < SK_MAX_ROWS; ++b) {
+                if (b < Bm) {
+                    const uint4 x = xs[b * kp + p];
+                    float a = acc[b];
+                    a = fmaf(w0, bf16_lo(x.x), a);
+                    a = fmaf(w1, bf16_hi(x.x), a);
+                    a = fmaf(w2, bf16_lo(x.y), a);
+                    a = fmaf(w3, bf16_hi(x.y), a);
+                    a = fmaf(w4, bf16_lo(x.z), a);
+                    a = fmaf(w5, bf16_hi(x.z), a);
+                    a = fmaf(w6, bf16_lo(x.w), a);
+                    a = fmaf(w7, bf16_hi(x.w), a);
+                    acc[b] = a;
+                }
+            }
+        }
+        float mine = 0.f;
+#pragma unroll
+        for (int b = 0; b < SK_MAX_ROWS; ++b) {
+            if (b < Bm) {
+                const float sum = warp_sum(acc[b]);
+                if (lane == b) mine = sum;
+            }
+        }
+        if (lane < Bm) {
+            float v = mine + (bias ? bias[n] : 0.f);
+            const int64_t o = (int64_t)lane * ldd + n;
+            if (EPI == GPT2_EPI_RESIDUAL) v += __bfloat162float(R[o]);
+            const bf16 h = __float2bfloat16_rn(v);
+            D[o] = h;
+            if (EPI == GPT2_EPI_GELU) D2[o] = __float2bfloat16_rn(gelu_tanh(__bfloat162float(h)));
+        }
+    }
+}
+
+// GPT2_ERR_UNSUPPORTED when X does not fit in shared memory (the caller then
+// takes the general matmul).  The first call of each epilogue sets the kernel's
+// shared-memory limit, so that call must not be inside a stream capture.
+int skinny_gemm(const bf16 *X, int64_t ldx, const bf16 *W, int K, int N, int Bm, const float *bias, const bf16 *R,
+                bf16 *D, bf16 *D2, int64_t ldd, int epi, int num_sms, cudaStream_t st) {
+    if (Bm < 1 || Bm > SK_MAX_ROWS || K % 8 || ldx % 8 || N < 1) return GPT2_ERR_BAD_SHAPE;
+    const size_t smem = (size_t)Bm * K * 2;
+    const int grid = std::min(ceil_div(N, SK_WARPS), 4 * num_sms);
+    auto go = [&](auto kern, int &limit) -> int {
+        if (limit < 0) {
+            int dev = 0, optin = 0;
+            GPT2_CUDA_TRY(cudaGetDevice(&dev));
+            GPT2_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+            GPT2_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin));
+            limit = optin;
+        }
+        if (smem > (size_t)limit) return GPT2_ERR_UNSUPPORTED;
+        kern<<<grid, SK_WARPS * 32, smem, st>>>(X, ldx, W, K, N, Bm, bias, R, D, D2, ldd);
+        GPT2_CUDA_TRY(cudaGetLastError());
+        gpt2_note_launches(1);
+        return GPT2_OK;
+    };
+    static int lim_store = -1, lim_res = -1, lim_gelu = -1;
+    switch (epi) {
+        case GPT2_EPI_STORE: return go(skinny_gemm_kernel<GPT2_EPI_STORE>, lim_store);
+        case GPT2_EPI_RESIDUAL: return R ? go(skinny_gemm_kernel<GPT2_EPI_RESIDUAL>, lim_res) : GPT2_ERR_BAD_ARG;
+        case GPT2_EPI_GELU: return D2 ? go(skinny_gemm_kernel<GPT2_EPI_GELU>, lim_gelu) : GPT2_ERR_BAD_ARG;
+        default: return GPT2_ERR_BAD_ARG;
+    }
 }
 
 __global__ void advance_position_kernel(int *d_pos) { *d_pos += 1; }

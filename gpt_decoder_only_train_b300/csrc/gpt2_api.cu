@@ -520,6 +520,21 @@ int backward_impl(gpt2_model *m, float grad_scale) {
 // memory (gen_pos), so the launches of one position do not depend on t: the
 // first position of each kind (filling the cache from the prompt, or also
 // drawing a token) runs directly, the rest replay a CUDA graph of it.
+// the decode products: a few rows against a K-major weight; bf16 rows take the
+// skinny weight-streaming kernel, the rest the general matmul
+template <typename T>
+int dmm(gpt2_model *m, const void *X, int ldx, const void *Wt, void *D, void *D2, const void *R, int64_t ldd,
+        const float *bias, int Bm, int N, int K, int epi) {
+    if constexpr (sizeof(T) == 2) {
+        if (Bm <= k::SK_MAX_ROWS) {
+            const int rc = k::skinny_gemm((const bf16 *)X, ldx, (const bf16 *)Wt, K, N, Bm, bias, (const bf16 *)R,
+                                          (bf16 *)D, (bf16 *)D2, ldd, epi, m->num_sms, m->stream);
+            if (rc != GPT2_ERR_UNSUPPORTED) return rc;
+        }
+    }
+    return mm<T>(m, X, ldx, true, Wt, K, true, D, D2, R, ldd, bias, Bm, N, K, epi);
+}
+
 template <typename T>
 int decode_position(gpt2_model *m, int *d_seq, int B, int T_total, int T0, const float *d_u, float temperature,
                     int top_k, bool draw) {
@@ -534,21 +549,18 @@ int decode_position(gpt2_model *m, int *d_seq, int B, int T_total, int T0, const
     for (int l = 0; l < c.L; ++l) {
         const LayerParams &p = m->lp[l];
         TRY(k::layernorm_forward<T>(x, Pf(m, p.ln1g), Pf(m, p.ln1b), y, mean, rstd, B, C, st));
-        TRY(mm<T>(m, y, C, true, W<T>(m, p.qkvw), C, true, qkv, nullptr, nullptr, 3 * C, Pf(m, p.qkvb), B, 3 * C, C,
-                  GPT2_EPI_STORE));
+        TRY(dmm<T>(m, y, C, W<T>(m, p.qkvw), qkv, nullptr, nullptr, 3 * C, Pf(m, p.qkvb), B, 3 * C, C,
+                   GPT2_EPI_STORE));
         TRY(k::attention_decode<T>((T *)m->layers[l].qkv, qkv, Tc, m->gen_pos, T_total - 2, B, c.H, hd, att, st));
-        TRY(mm<T>(m, att, C, true, W<T>(m, p.projw), C, true, xm, nullptr, x, C, Pf(m, p.projb), B, C, C,
-                  GPT2_EPI_RESIDUAL));
+        TRY(dmm<T>(m, att, C, W<T>(m, p.projw), xm, nullptr, x, C, Pf(m, p.projb), B, C, C, GPT2_EPI_RESIDUAL));
         TRY(k::layernorm_forward<T>(xm, Pf(m, p.ln2g), Pf(m, p.ln2b), y, mean, rstd, B, C, st));
-        TRY(mm<T>(m, y, C, true, W<T>(m, p.fcw), C, true, hbuf, gbuf, nullptr, 4 * C, Pf(m, p.fcb), B, 4 * C, C,
-                  GPT2_EPI_GELU));
-        TRY(mm<T>(m, gbuf, 4 * C, true, W<T>(m, p.fcprojw), 4 * C, true, x, nullptr, xm, C, Pf(m, p.fcprojb), B, C,
-                  4 * C, GPT2_EPI_RESIDUAL));
+        TRY(dmm<T>(m, y, C, W<T>(m, p.fcw), hbuf, gbuf, nullptr, 4 * C, Pf(m, p.fcb), B, 4 * C, C, GPT2_EPI_GELU));
+        TRY(dmm<T>(m, gbuf, 4 * C, W<T>(m, p.fcprojw), x, nullptr, xm, C, Pf(m, p.fcprojb), B, C, 4 * C,
+                   GPT2_EPI_RESIDUAL));
     }
     if (draw) {
         TRY(k::layernorm_forward<T>(x, Pf(m, nt - 2), Pf(m, nt - 1), y, mean, rstd, B, C, st));
-        TRY(mm<T>(m, y, C, true, W<T>(m, 0), C, true, m->logits, nullptr, nullptr, c.Vp, nullptr, B, c.Vp, C,
-                  GPT2_EPI_STORE));
+        TRY(dmm<T>(m, y, C, W<T>(m, 0), m->logits, nullptr, nullptr, c.Vp, nullptr, B, c.Vp, C, GPT2_EPI_STORE));
         TRY(k::sample_topk<T>((const T *)m->logits, c.Vp, B, c.V, d_u, temperature, top_k, d_seq, T_total, 0,
                               m->gen_pos, T0, st));
     }

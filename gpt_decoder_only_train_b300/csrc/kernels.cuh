@@ -83,6 +83,12 @@ int sample_topk(const T *logits, int64_t ldl, int B, int V, const float *u, floa
                 int64_t ld_out, int col_out, const int *d_pos, int T0, cudaStream_t st);
 // *d_pos += 1
 int advance_position(int *d_pos, cudaStream_t st);
+// D[b, n] = epi(sum_k X[b, k] W[n, k] (+ bias[n])) for b < Bm <= SK_MAX_ROWS, W K-major [N, K]
+// (ld K); epi: GPT2_EPI_STORE, GPT2_EPI_RESIDUAL (+ R[b, n]) or GPT2_EPI_GELU (D = h, D2 = gelu(h));
+// R, D and D2 use the leading dimension ldd
+constexpr int SK_MAX_ROWS = 16;
+int skinny_gemm(const bf16 *X, int64_t ldx, const bf16 *W, int K, int N, int Bm, const float *bias, const bf16 *R,
+                bf16 *D, bf16 *D2, int64_t ldd, int epi, int num_sms, cudaStream_t st);
 
 struct AdamArgs {
     float lr, beta1, beta2, eps, wd, clip;
