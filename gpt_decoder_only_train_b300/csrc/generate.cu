@@ -245,8 +245,10 @@ template <typename T>
 int sample_topk(const T *logits, int64_t ldl, int B, int V, const float *u, float temperature, int top_k, int *out,
                 int64_t ld_out, int col_out, const int *d_pos, int T0, cudaStream_t st) {
     if (B <= 0 || V <= 0 || top_k < 1 || top_k > GPT2_MAX_TOP_K || !(temperature > 0.f)) return GPT2_ERR_BAD_ARG;
-    sample_topk_kernel<T><<<B, SAMPLE_THREADS, 0, st>>>(logits, ldl, V, u, 1.0f / temperature, top_k, out, ld_out,
-                                                        col_out, d_pos, T0);
+    // a finite scale: (z_i - z_max) * scale must stay 0 for ties with the maximum
+    const float inv = 1.0f / temperature, inv_temp = isfinite(inv) ? inv : 3.0e38f;
+    sample_topk_kernel<T><<<B, SAMPLE_THREADS, 0, st>>>(logits, ldl, V, u, inv_temp, top_k, out, ld_out, col_out,
+                                                        d_pos, T0);
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
     return GPT2_OK;
