@@ -81,6 +81,8 @@ _SIGS = {
     "gpt2_generate": (_I, [_P, _P, _I, _I, _I, _P, _F, _I]),
     "gpt2_op_layernorm_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "gpt2_op_layernorm_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
+    "gpt2_op_embedding_backward": (_I, [_P, _I, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "gpt2_debug_set_barrier_wait": (_I, [ctypes.c_ulonglong, _I]),
 }
 
 
@@ -319,3 +321,18 @@ def sample(logits, ldl, B, V, uniforms, temperature, top_k, out, stream=None):
 def classifier(logits, targets, loss_rows, N, V, Vp, dscale, stream=None):
     check("gpt2_op_classifier", lib().gpt2_op_classifier(
         _ptr(logits), _ptr(targets), _ptr(loss_rows), N, V, Vp, dscale, _stream(stream)))
+
+
+def embedding_backward(dx, tokens, dwte, dwpe, B, T, C, V, stream=None):
+    """dwte[tokens] += dx rows; dwpe[t] += sum over the batch (device tensors)."""
+    import torch
+
+    dtype = GPT2_DTYPE_FP32 if dx.dtype == torch.float32 else GPT2_DTYPE_BF16
+    check("gpt2_op_embedding_backward",
+          lib().gpt2_op_embedding_backward(_ptr(dx), dtype, _ptr(tokens), B, T, C, V, _ptr(dwte), _ptr(dwpe),
+                                           _stream(stream)))
+
+
+def set_barrier_wait(wait_ns: int = 0, never_arrive: bool = False):
+    """Test hook: time limit of the clip + AdamW grid barrier (0: default) and an unreachable barrier."""
+    check("gpt2_debug_set_barrier_wait", lib().gpt2_debug_set_barrier_wait(int(wait_ns), int(bool(never_arrive))))

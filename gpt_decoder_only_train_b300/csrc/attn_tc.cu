@@ -1105,11 +1105,14 @@ int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs
     if (int rc = encode_qkv_map(&mq, q, rs, T, B, H)) return rc;
     if (int rc = encode_qkv_map(&mk, k, rs, T, B, H)) return rc;
     if (int rc = encode_qkv_map(&mv, v, rs, T, B, H)) return rc;
-    static bool init = false;
-    if (!init) {
-        GPT2_CUDA_TRY(cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::SMEM));
-        init = true;
-    }
+    static PerDevice init_pd;
+    int unused = 0;
+    if (int rc = per_device(init_pd, unused, [](int &v) -> int {
+            GPT2_CUDA_TRY(cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::SMEM));
+            v = 1;
+            return GPT2_OK;
+        }))
+        return rc;
     const float sl2 = LOG2E / sqrtf((float)HD);
     int dev = 0, sms = 0;
     GPT2_CUDA_TRY(cudaGetDevice(&dev));
@@ -1140,12 +1143,16 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
     if (int rc = encode_qkv_map(&k128, k, rs, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&v128, v, rs, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&do64, dout, ors, T, B, H, 64)) return rc;
-    static bool init = false;
-    if (!init) {
-        GPT2_CUDA_TRY(cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::SMEM));
-        GPT2_CUDA_TRY(cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::SMEM));
-        init = true;
-    }
+    static PerDevice init_pd;
+    int unused = 0;
+    if (int rc = per_device(init_pd, unused, [](int &v) -> int {
+            GPT2_CUDA_TRY(cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::SMEM));
+            GPT2_CUDA_TRY(
+                cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::SMEM));
+            v = 1;
+            return GPT2_OK;
+        }))
+        return rc;
     const float scale = 1.0f / sqrtf((float)HD), sl2 = LOG2E * scale;
     int dev = 0, sms = 0;
     GPT2_CUDA_TRY(cudaGetDevice(&dev));

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/gpt2b300.h"
 
 typedef __nv_bfloat16 bf16;
@@ -163,9 +165,29 @@ __device__ __forceinline__ F2 gelu_tanh_grad2(F2 h) {
     return f2_fma(f2_mul(na, t), t, base);
 }
 
-// GPT-2's tanh GELU and its derivative (the tanh form of "Let's reproduce
-// GPT-2 (124M)", §Bölümler 2; the constant is sqrt(2/pi)).
+// Precision by element type.  bf16 data (relative rounding 2^-9) takes the
+// hardware approximations above and __expf / rsqrtf; fp32 data takes CUDA's
+// accurate tanhf / expf and a correctly rounded 1 / sqrt, so that the fp32
+// mode computes in true fp32 throughout.
+template <typename T> __device__ __forceinline__ float tanh_t(float x) { return tanh_hw(x); }
+template <> __device__ __forceinline__ float tanh_t<float>(float x) { return tanhf(x); }
+template <typename T> __device__ __forceinline__ float exp_t(float x) { return __expf(x); }
+template <> __device__ __forceinline__ float exp_t<float>(float x) { return expf(x); }
+template <typename T> __device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }
+template <> __device__ __forceinline__ float rsqrt_t<float>(float x) { return 1.0f / sqrtf(x); }
 
+// GELU and its derivative at the precision of element type T: the same
+// operations as gelu_tanh / gelu_tanh_grad, with tanh_t<T>.
+template <typename T> __device__ __forceinline__ float gelu_tanh_t(float h) {
+    const float h2 = h * h, u = fmaf(h2, GELU_KC, GELU_K), t = tanh_t<T>(h * u), hh = 0.5f * h;
+    return fmaf(hh, t, hh);
+}
+template <typename T> __device__ __forceinline__ float gelu_tanh_grad_t(float h) {
+    const float h2 = h * h, u = fmaf(h2, GELU_KC, GELU_K), t = tanh_t<T>(h * u);
+    const float na = h * fmaf(h2, GELU_NA1, GELU_NA0);
+    const float base = fmaf(t, 0.5f, 0.5f) - na;
+    return fmaf(na * t, t, base);
+}
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
@@ -174,3 +196,27 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 static inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Per-device one-time set-up.  A kernel's opt-in shared-memory limit and an
+// occupancy result belong to one device, so they are set up and cached per
+// device ordinal (up to 64), by `make(int &value)` on the first call made with
+// that device current.  Thread-safe; `make` runs under the lock.
+struct PerDevice {
+    std::mutex mu;
+    int val[64] = {};
+    bool have[64] = {};
+};
+template <typename F> int per_device(PerDevice &pd, int &out, F &&make) {
+    int dev = 0;
+    GPT2_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return GPT2_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(pd.mu);
+    if (!pd.have[dev]) {
+        int v = 0;
+        if (int rc = make(v)) return rc;
+        pd.val[dev] = v;
+        pd.have[dev] = true;
+    }
+    out = pd.val[dev];
+    return GPT2_OK;
+}

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(DEC_THREADS) attn_decode_kernel(T *__restrict_
     __syncthreads();
     float sum = 0.f;
     for (int j = tid; j < n; j += DEC_THREADS) {
-        const float e = __expf(sc[j] - mx);
+        const float e = exp_t<T>(sc[j] - mx);
         sc[j] = e;
         sum += e;
     }
@@ -224,13 +224,18 @@ __global__ void __launch_bounds__(SAMPLE_THREADS) sample_topk_kernel(const T *__
     if (tid == 0) {
         int pick = 0;
         if (k > 1) {
+            // w_r = exp((z_r - z_max) / temperature); when z_max is not finite
+            // (+inf, or every candidate -inf) the weights are the limit of that
+            // rule: 1 for the candidates equal to z_max, 0 for the rest
+            const float top = cv[0];
+            const bool fin = isfinite(top);
             float s = 0.f;
-            for (int r = 0; r < k; ++r) s += __expf((cv[r] - cv[0]) * inv_temp);
+            for (int r = 0; r < k; ++r) s += fin ? exp_t<T>((cv[r] - top) * inv_temp) : (cv[r] == top ? 1.f : 0.f);
             const float target = ub * s;
             float cum = 0.f;
             pick = k - 1;
             for (int r = 0; r < k; ++r) {
-                cum += __expf((cv[r] - cv[0]) * inv_temp);
+                cum += fin ? exp_t<T>((cv[r] - top) * inv_temp) : (cv[r] == top ? 1.f : 0.f);
                 if (cum > target) {
                     pick = r;
                     break;
@@ -321,28 +326,32 @@ __global__ void __launch_bounds__(SK_WARPS * 32)
 }
 
 // GPT2_ERR_UNSUPPORTED when X does not fit in shared memory (the caller then
-// takes the general matmul).  The first call of each epilogue sets the kernel's
-// shared-memory limit, so that call must not be inside a stream capture.
+// takes the general matmul).  The first call of each epilogue on a device sets
+// the kernel's shared-memory limit there, so that call must not be inside a
+// stream capture.
 int skinny_gemm(const bf16 *X, int64_t ldx, const bf16 *W, int K, int N, int Bm, const float *bias, const bf16 *R,
                 bf16 *D, bf16 *D2, int64_t ldd, int epi, int num_sms, cudaStream_t st) {
     if (Bm < 1 || Bm > SK_MAX_ROWS || K % 8 || ldx % 8 || N < 1) return GPT2_ERR_BAD_SHAPE;
     const size_t smem = (size_t)Bm * K * 2;
     const int grid = std::min(ceil_div(N, SK_WARPS), 4 * num_sms);
-    auto go = [&](auto kern, int &limit) -> int {
-        if (limit < 0) {
-            int dev = 0, optin = 0;
-            GPT2_CUDA_TRY(cudaGetDevice(&dev));
-            GPT2_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-            GPT2_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin));
-            limit = optin;
-        }
+    auto go = [&](auto kern, PerDevice &lim_pd) -> int {
+        int limit = 0;
+        if (int rc = per_device(lim_pd, limit, [&](int &v) -> int {
+                int dev = 0, optin = 0;
+                GPT2_CUDA_TRY(cudaGetDevice(&dev));
+                GPT2_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+                GPT2_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin));
+                v = optin;
+                return GPT2_OK;
+            }))
+            return rc;
         if (smem > (size_t)limit) return GPT2_ERR_UNSUPPORTED;
         kern<<<grid, SK_WARPS * 32, smem, st>>>(X, ldx, W, K, N, Bm, bias, R, D, D2, ldd);
         GPT2_CUDA_TRY(cudaGetLastError());
         gpt2_note_launches(1);
         return GPT2_OK;
     };
-    static int lim_store = -1, lim_res = -1, lim_gelu = -1;
+    static PerDevice lim_store, lim_res, lim_gelu;
     switch (epi) {
         case GPT2_EPI_STORE: return go(skinny_gemm_kernel<GPT2_EPI_STORE>, lim_store);
         case GPT2_EPI_RESIDUAL: return R ? go(skinny_gemm_kernel<GPT2_EPI_RESIDUAL>, lim_res) : GPT2_ERR_BAD_ARG;

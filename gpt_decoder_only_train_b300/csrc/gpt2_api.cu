@@ -33,6 +33,11 @@ void gpt2_set_last_cuda_error(cudaError_t e, const char *what, int line) {
 extern "C" const char *gpt2_last_error_detail(void) { return g_last_error; }
 
 static std::atomic<long long> g_launches{0};
+
+// time limit of the clip + AdamW grid barrier, and the test hook that makes it unreachable
+constexpr unsigned long long kDefaultBarrierWaitNs = 2000000000ull;
+static std::atomic<unsigned long long> g_barrier_wait_ns{kDefaultBarrierWaitNs};
+static std::atomic<unsigned> g_barrier_extra{0};
 void gpt2_note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 extern "C" long long gpt2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -741,6 +746,8 @@ extern "C" int gpt2_clip_and_adamw(gpt2_model *m, float lr, float beta1, float b
     a.clip = clip;
     a.bc1 = (float)(1.0 - pow((double)beta1, t));
     a.bc2 = (float)(1.0 - pow((double)beta2, t));
+    a.wait_ns = g_barrier_wait_ns.load(std::memory_order_relaxed);
+    a.extra_arrivals = g_barrier_extra.load(std::memory_order_relaxed);
     const double adam_bytes = (double)m->n_params * (m->wbf ? 34.0 : 32.0);
     TIMED(GPT2_PROF_ADAMW, adam_bytes,
           k::clip_adamw(m->params, m->grads, m->adam_m, m->adam_v, m->wbf, m->n_params, m->n_decay, a,
@@ -752,6 +759,13 @@ extern "C" int gpt2_clip_and_adamw(gpt2_model *m, float lr, float beta1, float b
     TRY(error_from_word(word));
     if (!std::isfinite(*grad_norm_out)) return GPT2_ERR_NONFINITE;
     m->adam_t = t;
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_debug_set_barrier_wait(unsigned long long wait_ns, int never_arrive) {
+    if (never_arrive != 0 && never_arrive != 1) return GPT2_ERR_BAD_ARG;
+    g_barrier_wait_ns.store(wait_ns ? wait_ns : kDefaultBarrierWaitNs, std::memory_order_relaxed);
+    g_barrier_extra.store((unsigned)never_arrive, std::memory_order_relaxed);
     return GPT2_OK;
 }
 
@@ -950,6 +964,17 @@ extern "C" int gpt2_op_sample(const void *logits, int64_t ldl, int B, int V, con
     if (B <= 0 || V <= 0 || ldl < V) return GPT2_ERR_BAD_SHAPE;
     return k::sample_topk<bf16>((const bf16 *)logits, ldl, B, V, uniforms, temperature, top_k, out, 1, 0, nullptr, 0,
                                 (cudaStream_t)stream);
+}
+
+extern "C" int gpt2_op_embedding_backward(const void *dx, int dtype, const int32_t *tokens, int B, int T, int C,
+                                          int V, float *dwte, float *dwpe, void *stream) {
+    if (!dx || !tokens || !dwte || !dwpe) return GPT2_ERR_BAD_ARG;
+    if (B <= 0 || T <= 0 || C <= 0 || V <= 0 || C % 4) return GPT2_ERR_BAD_SHAPE;
+    if (dtype == GPT2_DTYPE_FP32)
+        return k::embed_backward<float>(tokens, (const float *)dx, dwte, dwpe, B, T, C, V, (cudaStream_t)stream);
+    if (dtype == GPT2_DTYPE_BF16)
+        return k::embed_backward<bf16>(tokens, (const bf16 *)dx, dwte, dwpe, B, T, C, V, (cudaStream_t)stream);
+    return GPT2_ERR_BAD_ARG;
 }
 
 extern "C" int gpt2_op_classifier(void *logits, const int32_t *targets, float *loss_rows, int N, int V, int Vp,

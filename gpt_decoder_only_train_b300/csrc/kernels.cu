@@ -135,7 +135,7 @@ __global__ void ln_fwd_kernel(const T *__restrict__ x, const float *__restrict__
             }
         }
     }
-    const float rs = rsqrtf(warp_sum(q) / C + 1e-5f);
+    const float rs = rsqrt_t<T>(warp_sum(q) / C + 1e-5f);
     T *yr = y + (int64_t)row * C;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
@@ -598,6 +598,7 @@ int column_sum(const T *dy, int M, int N, float *db, cudaStream_t st) {
 }
 
 // ============================================================== classifier
+template <typename T>
 __device__ __forceinline__ void lse_merge(float &m, float &s, float om, float os) {
     if (om == -INFINITY) return;
     if (m == -INFINITY) {
@@ -606,7 +607,7 @@ __device__ __forceinline__ void lse_merge(float &m, float &s, float om, float os
         return;
     }
     const float mn = fmaxf(m, om);
-    s = s * __expf(m - mn) + os * __expf(om - mn);
+    s = s * exp_t<T>(m - mn) + os * exp_t<T>(om - mn);
     m = mn;
 }
 
@@ -633,10 +634,10 @@ __global__ void __launch_bounds__(1024) classifier_kernel(T *logits, const int *
                 if (p * E + e < V) {
                     const float x = v.get(e);
                     if (x > m) {
-                        s = s * __expf(m - x) + 1.f;
+                        s = s * exp_t<T>(m - x) + 1.f;
                         m = x;
                     } else {
-                        s += __expf(x - m);
+                        s += exp_t<T>(x - m);
                     }
                 }
             }
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(1024) classifier_kernel(T *logits, const int *
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float om = __shfl_xor_sync(0xffffffffu, m, o), os = __shfl_xor_sync(0xffffffffu, s, o);
-            lse_merge(m, s, om, os);
+            lse_merge<T>(m, s, om, os);
         }
         if (lane == 0) {
             sm_m[wid] = m;
@@ -653,7 +654,7 @@ __global__ void __launch_bounds__(1024) classifier_kernel(T *logits, const int *
         __syncthreads();
         if (threadIdx.x == 0) {
             float M = sm_m[0], S = sm_s[0];
-            for (int w = 1; w < nw; ++w) lse_merge(M, S, sm_m[w], sm_s[w]);
+            for (int w = 1; w < nw; ++w) lse_merge<T>(M, S, sm_m[w], sm_s[w]);
             const float lse = M + logf(S);
             int tg = targets[row];
             if (tg < 0 || tg >= V) {
@@ -675,7 +676,7 @@ __global__ void __launch_bounds__(1024) classifier_kernel(T *logits, const int *
                 const int c = p * E + e;
                 float d = 0.f;
                 if (c < V) {
-                    d = __expf(v.get(e) - lse);
+                    d = exp_t<T>(v.get(e) - lse);
                     if (c == tg) d -= 1.f;
                     d *= dscale;
                 }
@@ -728,7 +729,7 @@ __global__ void __launch_bounds__(1024) classifier_reg_kernel(T *logits, const i
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const int c = p * E + e;
-                    if (c < V) s += __expf(v[i].get(e) - M);
+                    if (c < V) s += exp_t<T>(v[i].get(e) - M);
                     if (c == tg) zt = v[i].get(e);
                 }
             }
@@ -752,7 +753,7 @@ __global__ void __launch_bounds__(1024) classifier_reg_kernel(T *logits, const i
                     const int c = p * E + e;
                     float d = 0.f;
                     if (c < V) {
-                        d = __expf(v[i].get(e) - lse);
+                        d = exp_t<T>(v[i].get(e) - lse);
                         if (c == tg) d -= 1.f;
                         d *= dscale;
                     }
@@ -1064,12 +1065,15 @@ int classifier(T *logits, const int *targets, float *loss_rows, int N, int V, in
         const int row_pad = (Vp * 2 + 127) / 128 * 128;
         const size_t cls_smem_bytes = 2 * (size_t)row_pad + 64;
         if (Vp >= 8192 && cls_smem_bytes <= 200 * 1024 && npk <= CLS_PPT * CLS_SMEM_THREADS) {
-            static bool attr = false;
-            if (!attr) {
-                GPT2_CUDA_TRY(cudaFuncSetAttribute(classifier_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   200 * 1024 + 64));
-                attr = true;
-            }
+            static PerDevice attr_pd;
+            int unused = 0;
+            if (int rc = per_device(attr_pd, unused, [](int &v) -> int {
+                    GPT2_CUDA_TRY(cudaFuncSetAttribute(classifier_smem_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024 + 64));
+                    v = 1;
+                    return GPT2_OK;
+                }))
+                return rc;
             int dev = 0, sms = 148;
             cudaGetDevice(&dev);
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1135,7 +1139,7 @@ __global__ void gelu_fwd_kernel(const T *__restrict__ h, T *__restrict__ y, int6
     Pack16<T> v;
     v.load(h + i * E);
 #pragma unroll
-    for (int e = 0; e < E; ++e) v.set(e, gelu_tanh(v.get(e)));
+    for (int e = 0; e < E; ++e) v.set(e, gelu_tanh_t<T>(v.get(e)));
     v.store(y + i * E);
 }
 
@@ -1173,10 +1177,10 @@ __device__ __forceinline__ void simt_epilogue(int epi, float acc, int m, int n, 
         case GPT2_EPI_GELU: {
             const T h = from_f32<T>(acc + bv);
             reinterpret_cast<T *>(D)[o] = h;
-            D2[o] = from_f32<T>(gelu_tanh(to_f32(h)));
+            D2[o] = from_f32<T>(gelu_tanh_t<T>(to_f32(h)));
             break;
         }
-        case GPT2_EPI_GELU_BWD: reinterpret_cast<T *>(D)[o] = from_f32<T>(acc * gelu_tanh_grad(to_f32(R[o]))); break;
+        case GPT2_EPI_GELU_BWD: reinterpret_cast<T *>(D)[o] = from_f32<T>(acc * gelu_tanh_grad_t<T>(to_f32(R[o]))); break;
         case GPT2_EPI_ACCUM_F32: reinterpret_cast<float *>(D)[o] += acc; break;
     }
 }
@@ -1475,8 +1479,10 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 }
 
 // Phase 1: sum of squares of every gradient (fp32 per thread, fp64 per block);
-// grid barrier (cooperative launch, bounded spin); every block then reduces the
-// block partials in the same fixed order, so all blocks see one norm.
+// grid barrier (cooperative launch, spin bounded by a.wait_ns: a block whose
+// wait runs out sets DEVERR_TIMEOUT and returns without updating); every block
+// then reduces the block partials in the same fixed order, so all blocks see
+// one norm.
 // Phase 2: clip coefficient and the AdamW update, bf16 copy of the new weights.
 __global__ void __launch_bounds__(ADAM_THREADS) clip_adamw_kernel(float *__restrict__ p, const float *__restrict__ g,
                                                                   float *__restrict__ m, float *__restrict__ v,
@@ -1500,8 +1506,9 @@ __global__ void __launch_bounds__(ADAM_THREADS) clip_adamw_kernel(float *__restr
         atomicAdd(counter, 1u);
         ok = 1;
         const uint64_t t0 = global_timer_ns();
-        while (ld_acquire(counter) < gridDim.x) {
-            if (global_timer_ns() - t0 > 2000000000ull) {
+        const unsigned target = gridDim.x + a.extra_arrivals;
+        while (ld_acquire(counter) < target) {
+            if (global_timer_ns() - t0 > a.wait_ns) {
                 ok = 0;
                 raise_device_error(err, DEVERR_TIMEOUT);
                 break;

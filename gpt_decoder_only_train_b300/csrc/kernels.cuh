@@ -92,7 +92,9 @@ int skinny_gemm(const bf16 *X, int64_t ldx, const bf16 *W, int K, int N, int Bm,
 
 struct AdamArgs {
     float lr, beta1, beta2, eps, wd, clip;
-    float bc1, bc2;  // 1 - beta^t
+    float bc1, bc2;                // 1 - beta^t
+    unsigned long long wait_ns;    // time limit of the grid barrier's spin
+    unsigned extra_arrivals;       // blocks the barrier waits for beyond the grid (0; tests only)
 };
 
 // Fused global-norm + clip + AdamW over one flat parameter arena (see

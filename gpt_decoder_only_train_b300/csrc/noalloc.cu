@@ -11,35 +11,25 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it (4 MiB) until the process exits.  Host code cannot use the
-// array's name as a device address, so the device address is looked up once
-// per device with cudaGetSymbolAddress, on the first call made with that
-// device current.
-#include <mutex>
-
+// array's name as a device address, so every call looks the device address up
+// with cudaGetSymbolAddress, with the calling device current.  Looking it up
+// on each call (not once per device) keeps the address right after a device
+// reset, which reloads the module at a new address.  The first call on a
+// device loads the library's module there, so it must come before any stream
+// capture.
 #include "flash_attn.cuh"
 
 namespace {
 
 constexpr int64_t kMaxRows = GPT2_NOALLOC_ATTN_MAX_ROWS;  // B * H * T
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_attn_scratch[kMaxRows];
 
-std::mutex g_mutex;
-float *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_attn_scratch on the current device (looked up once).
+// Device address of g_attn_scratch on the current device.
 int scratch_for_current_device(float **out) {
-    int dev = 0;
-    GPT2_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= kMaxDevices) return GPT2_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        GPT2_CUDA_TRY(cudaGetSymbolAddress(&p, g_attn_scratch));
-        g_scratch_ptr[dev] = static_cast<float *>(p);
-    }
-    *out = g_scratch_ptr[dev];
+    void *p = nullptr;
+    GPT2_CUDA_TRY(cudaGetSymbolAddress(&p, g_attn_scratch));
+    *out = static_cast<float *>(p);
     return GPT2_OK;
 }
 

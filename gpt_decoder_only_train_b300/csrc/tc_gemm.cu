@@ -40,12 +40,14 @@ static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params
                       cudaStream_t st) {
     using Lay = SmemLayout<BN, STAGES, PAIR>;
     auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, PAIR>;
-    static bool attr_set = false;
-    static int max_pairs = 0;
-    if (!attr_set) {
-        GPT2_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL));
-        attr_set = true;
-    }
+    static PerDevice attr_pd, pairs_pd;
+    int unused = 0;
+    if (int rc = per_device(attr_pd, unused, [&](int &v) -> int {
+            GPT2_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL));
+            v = 1;
+            return GPT2_OK;
+        }))
+        return rc;
     if constexpr (PAIR) {
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -58,12 +60,15 @@ static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (!max_pairs) {  // how many CTA pairs can be resident at once (about half the SMs)
-            cfg.gridDim = dim3(2 * (num_sms / 2));
-            int n = 0;
-            GPT2_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
-            max_pairs = n > 0 ? n : 1;
-        }
+        int max_pairs = 1;  // how many CTA pairs can be resident at once (about half the SMs)
+        if (int rc = per_device(pairs_pd, max_pairs, [&](int &v) -> int {
+                cfg.gridDim = dim3(2 * (num_sms / 2));
+                int n = 0;
+                GPT2_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+                v = n > 0 ? n : 1;
+                return GPT2_OK;
+            }))
+            return rc;
         cfg.gridDim = dim3(2 * std::min(units, max_pairs));
         GPT2_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, P));
     } else {

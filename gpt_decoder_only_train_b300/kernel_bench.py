@@ -7,6 +7,8 @@
     python -m gpt_decoder_only_train_b300.kernel_bench layernorm --N 16384 --C 768
     python -m gpt_decoder_only_train_b300.kernel_bench attention-sweep
     python -m gpt_decoder_only_train_b300.kernel_bench generate --B 16 --prompt 32 --new 64 --top-k 50
+    python -m gpt_decoder_only_train_b300.kernel_bench attention-fb --B 64 --T 1024 --H 12
+    python -m gpt_decoder_only_train_b300.kernel_bench adamw
 
 Inputs are seeded random bf16 on the device; each line reports the mean time
 per launch (CUDA events, after warm-up) and the algorithmic FLOP/s or bytes/s.
@@ -87,6 +89,44 @@ def bench_attention(B, T, H, bwd, iters, warmup):
             "TFLOP/s": fl / ms / 1e9}
 
 
+def bench_attention_fb(B, T, H, iters, warmup):
+    """Forward then backward per iteration (one launch of each attention kernel)."""
+    hd = 64
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    mk = lambda: torch.randn(B, T, H, hd, device="cuda", generator=gen).to(torch.bfloat16)
+    q, k, v, do = mk(), mk(), mk(), mk()
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, T, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    sc = torch.empty(B * H * T, device="cuda")
+
+    def run(i):
+        g.attention_forward(q, k, v, o, lse, B, T, H)
+        g.attention_backward(q, k, v, o, do, lse, dq, dk, dv, sc, B, T, H)
+
+    ms = _time(run, iters, warmup)
+    return {"op": "attention_fwd_bwd", "B": B, "T": T, "H": H, "ms": ms, "TFLOP/s": 3.0 * attn_flops(B, T, H) / ms / 1e9}
+
+
+def bench_adamw(a):
+    """The fused clip + AdamW over the 124M parameters (a model with a one-row batch, so the
+    arena is the parameter state plus little else)."""
+    import synthetic
+
+    w = dict(synthetic.WORKLOADS["gpt2_124m"], B=1, T=64)
+    m = g.GPT2(w, seed=1)
+    rng = torch.Generator().manual_seed(0)
+    for i in range(len(m.names)):
+        gr = torch.randn(m.shapes[i], generator=rng) * 1e-3
+        m.set_grads(i, gr.numpy())
+    n_params = sum(int(torch.tensor(s).prod()) for s in m.shapes)
+    ms = _time(lambda i: m.clip_and_adamw(6e-4), a.iters, a.warmup)
+    m.close()
+    # norm pass reads g (4 B); the update reads p, g, m, v (16 B), writes p, m, v (12 B) and the bf16 copy (2 B)
+    return {"op": "clip_adamw", "params": n_params, "ms": ms, "GB/s": 34.0 * n_params / ms / 1e6,
+            "note": "ms includes the host read-back of the norm"}
+
+
 def bench_classifier(a):
     gen = torch.Generator(device="cuda").manual_seed(0)
     z0 = torch.randn(a.N, a.Vp, device="cuda", generator=gen).to(torch.bfloat16)
@@ -142,7 +182,8 @@ def bench_layernorm(a):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["matmul", "attention", "classifier", "layernorm", "attention-sweep", "generate"])
+    ap.add_argument("op", choices=["matmul", "attention", "classifier", "layernorm", "attention-sweep", "generate",
+                                   "attention-fb", "adamw"])
     ap.add_argument("--C", type=int, default=768)
     ap.add_argument("--M", type=int, default=16384)
     ap.add_argument("--N", type=int, default=2304)
@@ -175,6 +216,10 @@ def main(argv=None):
         out = bench_layernorm(a)
     elif a.op == "generate":
         out = [bench_generate(a)]
+    elif a.op == "attention-fb":
+        out = [bench_attention_fb(a.B, a.T, a.H, a.iters, a.warmup)]
+    elif a.op == "adamw":
+        out = [bench_adamw(a)]
     else:
         out = []
         for T, B in ((256, 256), (1024, 64), (2048, 32), (4096, 16)):

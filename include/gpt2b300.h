@@ -135,8 +135,10 @@ int gpt2_zero_grad(gpt2_model *m);
  * random numbers).
  * The rule for column t: z = the logits of position t - 1 over v < V (rounded
  * to bf16 in bf16 mode); candidates = the top_k largest, equal values lower
- * index first; w_i = exp((z_i - z_max) / temperature); the token is the first
- * candidate, in that order, whose cumulative weight exceeds u * sum(w).
+ * index first; w_i = exp((z_i - z_max) / temperature) (when z_max is not
+ * finite, the limit of that rule: w_i = 1 where z_i == z_max, else 0); the
+ * token is the first candidate, in that order, whose cumulative weight
+ * exceeds u * sum(w).
  * top_k = 1 is greedy decoding.  1 <= top_k <= GPT2_MAX_TOP_K, temperature > 0.
  * The cache and the per-position work use the training step's activation
  * buffers: afterwards the first B rows of the logits buffer hold the logits
@@ -163,6 +165,18 @@ int gpt2_generate(gpt2_model *m, int32_t *d_seq, int B, int T_total, int T0, con
  */
 int gpt2_clip_and_adamw(gpt2_model *m, float lr, float beta1, float beta2, float eps, float wd, float clip,
                         float *grad_norm_out);
+
+/*
+ * Test hook for the bounded device waits (not a step of the training path).
+ * Sets, for this process, the time limit of the spin at the grid barrier of
+ * gpt2_clip_and_adamw (wait_ns = 0 restores the default of 2 s).  With
+ * never_arrive = 1 that barrier waits for one block more than its grid has,
+ * so every block's wait runs out: gpt2_clip_and_adamw then returns
+ * GPT2_ERR_TIMEOUT, updates nothing and leaves the step counter as it was,
+ * and the model stays usable once the hook is reset (never_arrive = 0).
+ * Returns GPT2_ERR_BAD_ARG for never_arrive other than 0 or 1.
+ */
+int gpt2_debug_set_barrier_wait(unsigned long long wait_ns, int never_arrive);
 
 /* Number of parameter tensors: 2 + 12 L + 2. */
 int gpt2_num_tensors(const gpt2_model *m);
@@ -269,9 +283,10 @@ int gpt2_op_attention_backward(const void *q, const void *k, const void *v, int6
  * GPT2_NOALLOC_ATTN_MAX_ROWS floats (4 MiB) that every GPU loading the
  * library holds until the process exits.  B*H*T above that limit returns
  * GPT2_ERR_BAD_SHAPE.  The call makes no cudaMalloc / cudaFree and uses no
- * allocating library routine.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  All calls on a device
+ * allocating library routine.  Each call looks up the array's device
+ * address (cudaGetSymbolAddress) with the calling device current; the first
+ * call on a device also loads the library there, so make that first call
+ * before any stream capture.  All calls on a device
  * share the one array, which keeps the previous call's contents (the kernels
  * overwrite the part they read before reading it): calls that can overlap on
  * the GPU (different streams, or different host threads) race on it and must
@@ -329,6 +344,20 @@ int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const void *B, int6
  */
 int gpt2_op_sample(const void *logits, int64_t ldl, int B, int V, const float *uniforms, float temperature, int top_k,
                    int32_t *out, void *stream);
+
+/*
+ * Embedding backward ("Let's build GPT: from scratch", 01:00:18: token and
+ * position embeddings are added, so each receives the residual gradient):
+ *   dwte[tokens[b, t], :] += dx[b, t, :];   dwpe[t, :] += sum_b dx[b, t, :].
+ * dx: device [B, T, C] of dtype GPT2_DTYPE_FP32 (float) or GPT2_DTYPE_BF16;
+ * tokens: device int32 [B, T]; dwte: device fp32 [>= V, C]; dwpe: device fp32
+ * [>= T, C]; both accumulated into (zero them for a plain result).  Tokens
+ * outside [0, V) are added to row 0 (the forward reports them).  The token
+ * rows are summed with fp32 atomics, so the order of additions into a row
+ * that several positions share is not fixed.  C a multiple of 4.
+ */
+int gpt2_op_embedding_backward(const void *dx, int dtype, const int32_t *tokens, int B, int T, int C, int V,
+                               float *dwte, float *dwpe, void *stream);
 
 /*
  * Fused classifier over rows of bf16 logits [N, Vp] (in place):

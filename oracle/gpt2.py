@@ -378,12 +378,18 @@ def sample_next(z, temperature: float, top_k: int, u: float) -> int:
 
     Candidates: the top_k entries in the order (larger value first, equal
     values lower index first).  Weights ``exp((z_i - z_max) / temperature)``;
-    the token is the first candidate whose cumulative weight exceeds
-    ``u * sum(weights)``; if rounding leaves none, the last candidate.
+    when ``z_max`` is not finite (+inf, or every candidate -inf) the weights
+    are the limit of that rule: 1 for the candidates equal to ``z_max``, 0 for
+    the others.  The token is the first candidate whose cumulative weight
+    exceeds ``u * sum(weights)``; if rounding leaves none, the last candidate.
     """
     z = np.asarray(z, dtype=np.float64)
     order = [int(i) for i in np.lexsort((np.arange(z.shape[0]), -z))[:top_k]]  # by -z, then by index
-    w = [math.exp((z[i] - z[order[0]]) / temperature) for i in order]
+    zmax = z[order[0]]
+    if math.isfinite(zmax):
+        w = [math.exp((z[i] - zmax) / temperature) for i in order]
+    else:
+        w = [1.0 if z[i] == zmax else 0.0 for i in order]
     target = u * sum(w)
     cum = 0.0
     for i, wi in zip(order, w):

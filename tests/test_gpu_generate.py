@@ -72,6 +72,33 @@ def test_sampler_matches_the_oracle_rule(g, V, ldl):
                 assert abs(order.index(int(got[b])) - order.index(ref)) <= 1
 
 
+def test_sampler_nonfinite_maximum_matches_the_oracle(g):
+    """+inf logits, and rows whose candidates are all -inf, follow the oracle's limit rule."""
+    V, ldl, B = 300, 304, 6
+    rng = np.random.default_rng(11)
+    z = torch.from_numpy(rng.normal(size=(B, ldl)).astype(np.float32)).to(torch.bfloat16)
+    inf = float("inf")
+    z[0, 17] = inf                      # one +inf
+    z[1, 5] = inf
+    z[1, 250] = inf                     # two +inf
+    z[2, :V] = -inf                     # every logit -inf
+    z[3, :V] = -inf
+    z[3, 40] = 2.0                      # one finite logit among -inf
+    z[4, 3] = -inf                      # finite maximum, a -inf candidate excluded by its weight
+    z[5, 299] = inf                     # +inf in the last real column
+    zd = z.cuda()
+    out = torch.empty(B, dtype=torch.int32, device="cuda")
+    for top_k in (1, 2, 7):
+        for u0 in (0.05, 0.45, 0.55, 0.95):
+            u = np.full(B, u0, dtype=np.float32)
+            g.sample(zd, ldl, B, V, torch.from_numpy(u).cuda(), 0.8, top_k, out)
+            torch.cuda.synchronize()
+            got = out.cpu().numpy()
+            for b in range(B):
+                ref = og.sample_next(z[b, :V].double().numpy(), 0.8, top_k, float(u[b]))
+                assert got[b] == ref, (b, top_k, u0, int(got[b]), ref)
+
+
 def _peaked(g, cfg, seed, scale):
     """GPU model and oracle parameters with the 2-D weights scaled (spread-out logits)."""
     m = g.GPT2(cfg, seed=seed)

@@ -9,7 +9,10 @@ exp((z_i - z_max) / temperature) exceeds u * sum.  What pins it:
 * top_k = 1 is the argmax with the lower index winning ties, for every u;
 * a vanishing temperature turns any top_k into the argmax;
 * generation equals teacher forcing: every drawn token is the draw from the
-  forward pass over the sequence before it.
+  forward pass over the sequence before it;
+* non-finite maxima (+inf, or every candidate -inf) draw exactly as the limit
+  of large finite logits: as if the infinite entries were equal finite values
+  far from the rest.
 """
 import math
 
@@ -90,3 +93,23 @@ def test_generation_equals_teacher_forcing():
                 assert int(seq[b, t]) == og.sample_next(last[b].numpy(), temperature, top_k, float(uniforms[s][b]))
                 if top_k == 1:
                     assert int(seq[b, t]) == int(torch.argmax(last[b]))
+
+
+def test_nonfinite_maximum_draws_as_the_finite_limit():
+    n = 20001
+    inf = float("inf")
+    cases = [
+        # one +inf: always that entry
+        (np.array([0.3, -1.2, inf, 0.3, 0.0]), np.array([0.3, -1.2, 1e300, 0.3, 0.0])),
+        # two +inf: the two, half each, lower index first
+        (np.array([inf, -1.2, inf, 0.3]), np.array([1e300, -1.2, 1e300, 0.3])),
+        # every candidate -inf: uniform over the top_k lowest indices
+        (np.array([-inf, -inf, -inf, -inf]), np.array([-1e300, -1e300, -1e300, -1e300])),
+    ]
+    for z_inf, z_big in cases:
+        for top_k in (1, 3, 4):
+            a = _draws(z_inf, 0.7, top_k, n)
+            b = _draws(z_big, 0.7, top_k, n)
+            assert np.array_equal(a, b), (z_inf, top_k)
+    d = _draws(cases[1][0], 1.0, 4, n)
+    assert set(np.unique(d)) == {0, 2} and abs((d == 0).mean() - 0.5) <= 2.0 / n
