@@ -51,6 +51,21 @@ def flops_per_token_6n(w):
     return 6.0 * n + 12.0 * L * C * T
 
 
+# AdamW learning rate of optimizer step `it` (0-based): linear warmup over 700
+# steps to 6e-4, then cosine decay to 6e-5 at step 19073 (10B tokens / 524,288
+# tokens a step), "Let's reproduce GPT-2 (124M)", §Video özeti.
+LR_MAX, LR_MIN, LR_WARMUP, LR_HORIZON = 6e-4, 6e-5, 700, 19073
+
+
+def lr_at(it):
+    if it < LR_WARMUP:
+        return LR_MAX * (it + 1) / LR_WARMUP
+    if it > LR_HORIZON:
+        return LR_MIN
+    r = (it - LR_WARMUP) / (LR_HORIZON - LR_WARMUP)
+    return LR_MIN + 0.5 * (1.0 + math.cos(math.pi * r)) * (LR_MAX - LR_MIN)
+
+
 def workload_label(name, w, accum):
     return "%s: L=%d C=%d H=%d V=%d (Vp=%d) B=%d T=%d%s, %d micro-step(s) (fwd+bwd) + clip + AdamW per step" % (
         name, w["L"], w["C"], w["H"], w["V"], w["Vp"], w["B"], w["T"],
@@ -117,10 +132,11 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# DRAM traffic of the GEMM launches of one step, from one ncu capture of the
-# 147 GEMM launches of a bench step (dram__bytes_read.sum + dram__bytes_write.sum,
-# a single-pass metric set; profiles/gemm_tcgen05_gpt2_124m_shapes.md).  It is
-# reported only while the GEMM sources are the ones that were measured.
+# DRAM traffic per GEMM launch of the step (dram__bytes_read.sum +
+# dram__bytes_write.sum from ncu, one launch of each of the step's GEMM shapes,
+# weighted by how often the step launches that shape).  It is a stored
+# capture, not a measurement of this run, and is reported only while the GEMM
+# sources hash to the ones that were captured.
 GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
@@ -143,51 +159,158 @@ def gemm_traffic():
     return GEMM_TRAFFIC["bytes_per_launch"] if h.hexdigest() == GEMM_TRAFFIC["sha256"] else None
 
 
-def cpu_baseline(w, min_s=12.0, budget_s=30.0):
-    """The oracle, as it stands, on a bounded sample: the 124M step on B=1 x T=256 tokens, repeated
-    until at least min_s seconds of CPU work (and at most budget_s) have elapsed."""
+def _oracle_sample_steps(w, max_steps, min_s, budget_s, warmup=0):
+    """Run the oracle step (fwd + bwd + clip + AdamW) on one full-length sequence of the
+    workload (B=1, the workload's T, so attention keeps its share of the work) until
+    max_steps steps or min_s seconds have passed, never starting a step that would end past
+    budget_s.  Returns (timed steps, seconds, tokens per step, threads)."""
     import torch
 
     from oracle import gpt2 as og
 
     torch.set_num_threads(os.cpu_count() or 1)
-    cfg = og.Config.from_dict(w)
-    B, T = 1, 256
-    x, y = synthetic.zipf_window(w["seed"], B, T, w["V"])
+    cfg = og.Config.from_dict(dict(w, B=1))
+    T = w["T"]
+    x, y = synthetic.zipf_window(w["seed"], 1, T, w["V"])
     m = og.OracleGPT2(cfg, w["seed"])
-    t0 = time.perf_counter()
-    steps = 0
-    while True:
+
+    def one(i):
         m.zero_grad()
         m.forward(x, y)
         m.backward(1.0)
-        m.clip_and_adamw(6e-4)
+        m.clip_and_adamw(lr_at(i))
+
+    for i in range(warmup):
+        one(i)
+    t0 = time.perf_counter()
+    steps = 0
+    while steps < max_steps:
+        one(warmup + steps)
         steps += 1
         el = time.perf_counter() - t0
         if el >= min_s or el + el / steps > budget_s:
             break
-    return {"value": steps * B * T / el, "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
-            "sample": "GPT-2 124M fp64 oracle step (fwd+bwd+clip+AdamW) on %d x %d Zipf tokens, %d step(s), %.1f s"
-                      % (B, T, steps, el)}
+    return steps, time.perf_counter() - t0, T, torch.get_num_threads()
+
+
+def cpu_baseline(w, min_s=12.0, budget_s=30.0):
+    """The oracle, as it stands, on a bounded sample of the workload (see _oracle_sample_steps)."""
+    steps, el, tok, cores = _oracle_sample_steps(w, 10 ** 9, min_s, budget_s)
+    return {"value": steps * tok / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "GPT-2 fp64 oracle step (fwd+bwd+clip+AdamW) on 1 x %d Zipf tokens of the workload, "
+                      "%d step(s) in %.1f s" % (tok, steps, el)}
 
 
 def run_reference(args, w, rank, world):
-    """The CPU oracle timed as the reference arm (rank 0 only)."""
+    """The CPU oracle timed as the reference arm (rank 0 only): W untimed and up to K timed
+    steps, each one full-length sequence of the workload, within a few minutes in all."""
     if rank != 0:
         return
-    base = cpu_baseline(w)
-    fpt = flops_per_token(w)
+    accum = int(w.get("grad_accum", 1))
+    steps, el, tok, cores = _oracle_sample_steps(w, args.steps, float("inf"), 240.0, warmup=min(args.warmup, 1))
+    value = steps * tok / el
     line = {
-        "impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * w["B"] * w["T"] * int(w.get("grad_accum", 1)) / base["value"],
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": min(args.warmup, 1),
+        "ms_per_step": 1e3 * el / steps,
+        "ms_per_step_note": "one sample step: the oracle step on 1 x %d tokens; the workload's own step "
+                            "(%d tokens) would take about %.0f ms at this rate (extrapolated, not run)"
+                            % (tok, w["B"] * w["T"] * accum, 1e3 * w["B"] * w["T"] * accum / value),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s step, sample of B=1 x T=256 tokens" % args.workload, "seed": w["seed"]},
-        "cpu_baseline": base,
-        "e2e": {"value": base["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "mfu_note": "%.3e FLOP/token" % fpt,
+        "config": {"workload": workload_label(args.workload, w, accum), "global_batch": w["B"] * accum,
+                   "seq_len": w["T"], "parallelism": "host cores, rank 0 only"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d step(s) of 1 x %d tokens of the workload in %.1f s" % (steps, tok, el)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def attention_sweep(args):
+    """The isolated causal attention workload: H=12, hd=64, B*T = 65,536 at T in {256, 1024, 2048,
+    4096}; Q, K, V, dO ~ N(0,1) rounded to bf16 (seed 4).  Forward and backward are timed apart with
+    CUDA events after warm-up (every operand is 100 MB, together above L2); FLOPs count the causal
+    pairs: 4 hd T(T+1)/2 per head forward, twice that backward.  The oracle's naive attention
+    (full T x T scores, float64) is timed at T=256 on the host cores as the CPU baseline."""
+    import torch
+
+    import gpt_decoder_only_train_b300 as g
+    from gpt_decoder_only_train_b300 import build
+
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps are required")
+    build.build()
+    H, hd = 12, 64
+    stream = torch.cuda.current_stream()
+    rows = []
+    launches0 = g.launch_count()
+    for cfg in synthetic.ATTN_SWEEP:
+        T, B = cfg["T"], cfg["B"]
+        dev = [torch.from_numpy(a).to(torch.bfloat16).cuda() for a in synthetic.attention_operands(4, B, H, T, hd)]
+        q, k, v, do = dev
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, T, dtype=torch.float32, device="cuda")
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        scratch = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
+        fwd = lambda: g.attention_forward(q, k, v, o, lse, B, T, H)
+        bwd = lambda: g.attention_backward(q, k, v, o, do, lse, dq, dk, dv, scratch, B, T, H)
+        out = {"T": T, "B": B}
+        for name, fn, mult in (("fwd", fwd, 1.0), ("bwd", bwd, 2.0)):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with ClockSampler(0) as clk:
+                e0.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            flops = mult * 4.0 * hd * (T * (T + 1) / 2.0) * B * H
+            out[name] = {"ms": ms, "tflops": flops / ms / 1e9, "clocks": clk.summary()}
+        rows.append(out)
+        del dev, q, k, v, do, o, lse, dq, dk, dv, scratch
+        torch.cuda.empty_cache()
+    launches = g.launch_count() - launches0
+    line = {
+        "metric": "causal attention fwd+bwd TFLOP/s (H=12, hd=64, B*T=65536, bf16, fp32 softmax statistics)",
+        "unit": "TFLOP/s", "higher_is_better": True, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "dtype": "bf16", "data": "synthetic N(0,1) Q, K, V, dO (seed 4)",
+        "value": min(r["fwd"]["tflops"] for r in rows), "value_note": "slowest forward of the sweep",
+        "sweep": rows, "gpu_launches": launches,
+        "config": {"workload": "isolated causal attention sweep, T in {256, 1024, 2048, 4096}, B*T = 65536",
+                   "l2": "every operand is 100 MB (inputs larger than L2)"},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = attention_cpu_baseline()
+    print(json.dumps(line), flush=True)
+
+
+def attention_cpu_baseline(min_s=5.0, budget_s=30.0):
+    """The oracle's naive causal attention (forward + backward, float64, full T x T scores) at T=256
+    on the host cores, on a sample of heads of the sweep's T=256 inputs."""
+    import torch
+
+    from oracle import gpt2 as og
+
+    torch.set_num_threads(os.cpu_count() or 1)
+    B, H, T, hd = 4, 12, 256, 64
+    q, k, v, do = (torch.from_numpy(a).double().permute(0, 2, 1, 3).contiguous()
+                   for a in synthetic.attention_operands(4, B, H, T, hd))
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        b = n % B
+        og.causal_attention_forward(q[b], k[b], v[b])
+        og.causal_attention_backward(q[b], k[b], v[b], do[b])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_s or el + el / n > budget_s:
+            break
+    flops = 3.0 * 4.0 * hd * (T * (T + 1) / 2.0) * H * n
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": "naive fp64 causal attention fwd+bwd, T=256, %d sequence(s) x 12 heads in %.1f s" % (n, el)}
 
 
 def main():
@@ -198,7 +321,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gpt2_124m", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attention-sweep", action="store_true",
+                    help="time the isolated causal attention workload instead of the training step")
     args = ap.parse_args()
+    if args.attention_sweep:
+        attention_sweep(args)
+        return
     w = dict(synthetic.WORKLOADS[args.workload])
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -237,14 +365,6 @@ def main():
     Y = torch.from_numpy(np.stack(ys).reshape(nsteps, accum, B, T)).cuda()
     stream = torch.cuda.current_stream()
     model = g.GPT2(w, seed=w["seed"], stream=stream)
-
-    def lr_at(it):
-        from math import cos, pi
-
-        if it < 700:
-            return 6e-4 * (it + 1) / 700
-        r = (it - 700) / (19073 - 700)
-        return 6e-5 + 0.5 * (1 + cos(pi * r)) * (6e-4 - 6e-5)
 
     def step(i, x, y):
         """One optimizer step over x, y [accum, B, T]: the loss is the mean over its micro-steps."""
@@ -317,7 +437,15 @@ def main():
         per_gpu = value / world
         mm_ms, mm_flops, mm_n = prof["matmul"]
         achieved = mm_flops / (mm_ms / 1e3) / 1e12 if mm_ms > 0 else None
-        peak = peaks["bf16_tflops_sustained"]
+        # The burst peak was measured over a short run at high clocks, the sustained one over
+        # seconds under the power cap: a short timed region near the maximum SM clock is held
+        # to the burst figure, a long or power-capped one to the sustained figure.
+        clocks = clk.summary()
+        near_max = (clocks["sm_mhz"] is not None and clocks["sm_max_mhz"]
+                    and clocks["sm_mhz"] >= 0.9 * clocks["sm_max_mhz"])
+        burst = ms / 1e3 < 2.0 and (near_max or clocks["sm_mhz"] is None)
+        peak_key = "bf16_tflops" if burst else "bf16_tflops_sustained"
+        peak = peaks[peak_key]
         kernels = {}
         for cat, (cms, work, n) in prof.items():
             unit = "TFLOP/s" if cat in ("matmul", "attention") else "GB/s"
@@ -349,16 +477,20 @@ def main():
             "roofline": {"kernel": "tcgen05 bf16 GEMM (all matmuls of the step)", "bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": (achieved / peak) if achieved else None,
+                         "frac_vs_burst": (achieved / peaks["bf16_tflops"]) if achieved else None,
+                         "frac_vs_sustained": (achieved / peaks["bf16_tflops_sustained"]) if achieved else None,
                          "traffic": gemm_traffic() if args.workload == GEMM_TRAFFIC["workload"] else None,
                          "traffic_unit": "bytes per launch (DRAM read + write, ncu)",
-                         "peak_source": "%s bf16_tflops_sustained" % peak_src,
+                         "traffic_source": "stored ncu capture of the same GEMM sources (not measured in this run)",
+                         "peak_source": "%s %s (timed region %.2f s, median SM clock %s MHz)"
+                                        % (peak_src, peak_key, ms / 1e3, clocks["sm_mhz"]),
                          "launches_per_step": mm_n / args.steps,
                          "timing": "CUDA events around each launch, second pass over the same steps"},
             "kernels": kernels,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * BT * 4,
                     "d2h_bytes_per_step": 8},
             "gpu_launches": launches,
-            "clocks": clk.summary(),
+            "clocks": clocks,
             "loss_first_last": [losses[0], losses[-1]],
         }
         if not args.no_cpu_baseline:

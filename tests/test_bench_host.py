@@ -61,3 +61,9 @@ def test_workload_label_names_the_shape():
     label = bench.workload_label("gpt2_124m_accum32", w, 32)
     for part in ("L=12", "C=768", "B=16", "T=1024", "32 micro-step"):
         assert part in label
+
+
+def test_bench_learning_rate_is_the_oracle_schedule():
+    """bench.py restates the warmup + cosine schedule; it must give the oracle's values."""
+    for it in (0, 1, 19, 20, 698, 699, 700, 701, 5000, 9886, 19072, 19073, 19074, 25000):
+        assert bench.lr_at(it) == og.lr_schedule(it), it
