@@ -29,6 +29,13 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&f)[32]) {
     for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
 }
 
+// max of three fp32 values in one instruction (sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // 2^x with the hardware approximation (MUFU.EX2, flush-to-zero): the results
 // feed bf16 operands and fp32 sums whose error budget is far above its ~2 ulp.
 __device__ __forceinline__ float ex2(float x) {
@@ -335,19 +342,27 @@ __global__ void __launch_bounds__(fwd::NTH, 1)
                 // blocks below the diagonal and inside T need no mask (same for the whole CTA)
                 const bool block_full = jj < qb && (jj + 1) * BKV <= T;
                 const int lim = min(T - 1 - kbase, jj == qb ? r - half * 64 : 63);  // last visible column
-                // pass 1: row max of the masked scores
+                // the thread's 64 scores, read from TMEM once (both loads in flight, one wait)
+                uint32_t sr[2][32];
+                tmem_ld32(ts, sr[0]);
+                tmem_ld32(ts + 32, sr[1]);
+                tmem_ld_wait();
+                // pass 1: row max of the masked scores (three-input max)
                 float mx = -INFINITY;
                 if (ok) {
 #pragma unroll
-                    for (int c0 = 0; c0 < 64; c0 += 32) {
-                        float f[32];
-                        tmem_ld32f(ts + c0, f);
+                    for (int h2 = 0; h2 < 2; ++h2) {
                         if (block_full) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, f[i]);
+                            for (int i = 0; i < 32; i += 2)
+                                mx = fmax3(mx, __uint_as_float(sr[h2][i]), __uint_as_float(sr[h2][i + 1]));
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, c0 + i <= lim ? f[i] : -INFINITY);
+                            for (int i = 0; i < 32; i += 2) {
+                                const int c = 32 * h2 + i;
+                                mx = fmax3(mx, c <= lim ? __uint_as_float(sr[h2][i]) : -INFINITY,
+                                           c + 1 <= lim ? __uint_as_float(sr[h2][i + 1]) : -INFINITY);
+                            }
                         }
                     }
                 }
@@ -362,12 +377,11 @@ __global__ void __launch_bounds__(fwd::NTH, 1)
                 F2 ls2 = f2(0.f, 0.f);
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
-                    float f[32];
-                    tmem_ld32f(ts + c0, f);
+                    const uint32_t *f = sr[c0 >> 5];
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        const F2 t = f2_fma(f2(f[i], f[i + 1]), sl2x2, nmu);
+                        const F2 t = f2_fma(f2(__uint_as_float(f[i]), __uint_as_float(f[i + 1])), sl2x2, nmu);
                         float p0 = ex2(f2_lo(t)), p1 = ex2(f2_hi(t));
                         if (!block_full) {
                             p0 = c0 + i <= lim ? p0 : 0.f;

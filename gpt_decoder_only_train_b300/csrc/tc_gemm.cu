@@ -36,8 +36,8 @@ int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer
 // units: work units (tiles x splits); the grid is one CTA per SM (or one pair
 // of CTAs per two SMs) up to that count.
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR>
-static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params &P, int units, int num_sms,
-                      cudaStream_t st) {
+static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td, const CUtensorMap &td2,
+                      const Params &P, int units, int num_sms, cudaStream_t st) {
     using Lay = SmemLayout<BN, STAGES, PAIR>;
     auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, PAIR>;
     static PerDevice attr_pd, pairs_pd;
@@ -70,9 +70,9 @@ static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params
             }))
             return rc;
         cfg.gridDim = dim3(2 * std::min(units, max_pairs));
-        GPT2_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, P));
+        GPT2_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, td, td2, P));
     } else {
-        kern<<<std::min(units, num_sms), NUM_THREADS, Lay::TOTAL, st>>>(ta, tb, P);
+        kern<<<std::min(units, num_sms), NUM_THREADS, Lay::TOTAL, st>>>(ta, tb, td, td2, P);
     }
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
@@ -80,12 +80,12 @@ static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const Params
 }
 
 template <int BN, int STAGES, bool PAIR>
-static int dispatch_major(bool a_mn, bool b_mn, const CUtensorMap &ta, const CUtensorMap &tb, const Params &P,
-                          int units, int num_sms, cudaStream_t st) {
-    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false, PAIR>(ta, tb, P, units, num_sms, st);
-    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true, PAIR>(ta, tb, P, units, num_sms, st);
-    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true, PAIR>(ta, tb, P, units, num_sms, st);
-    return launch_one<BN, STAGES, true, false, PAIR>(ta, tb, P, units, num_sms, st);
+static int dispatch_major(bool a_mn, bool b_mn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td,
+                          const CUtensorMap &td2, const Params &P, int units, int num_sms, cudaStream_t st) {
+    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false, PAIR>(ta, tb, td, td2, P, units, num_sms, st);
+    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true, PAIR>(ta, tb, td, td2, P, units, num_sms, st);
+    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true, PAIR>(ta, tb, td, td2, P, units, num_sms, st);
+    return launch_one<BN, STAGES, true, false, PAIR>(ta, tb, td, td2, P, units, num_sms, st);
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -169,22 +169,31 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
                     : encode_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64);
     if (rc) return rc;
 
+    // bf16 outputs leave through TMA stores from the epilogue's staging blocks (box 64 x 32)
+    CUtensorMap td = ta, td2 = ta;  // unused copies when there is no bf16 output
+    if (g.epi != GPT2_EPI_ACCUM_F32 && (rc = encode_tmap(&td, g.D, g.N, g.M, g.ldd, 64, 32))) return rc;
+    if (g.epi == GPT2_EPI_GELU && (rc = encode_tmap(&td2, g.D2, g.N, g.M, g.ldd, 64, 32))) return rc;
+
     const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;
     const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
     const bool reads_r = g.epi == GPT2_EPI_RESIDUAL || g.epi == GPT2_EPI_GELU_BWD;
+    // epilogues with a second staging block per warp (the prefetched operand, or the GELU
+    // output) trade a ring stage for it; the model uses them with K-major A only
+    const bool two_bufs = (reads_r || g.epi == GPT2_EPI_GELU) && !a_mn;
     if (BN == 256 && pair) {
-        // operand-reading epilogues (only K-major A, as the model uses them) trade a ring stage for prefetch
-        if (reads_r && !a_mn) return b_mn ? launch_one<256, 5, false, true, true>(ta, tb, P, num_work, num_sms, stream)
-                                          : launch_one<256, 5, false, false, true>(ta, tb, P, num_work, num_sms, stream);
-        return dispatch_major<256, 6, true>(a_mn, b_mn, ta, tb, P, num_work, num_sms, stream);
+        if (two_bufs)
+            return b_mn ? launch_one<256, 5, false, true, true>(ta, tb, td, td2, P, num_work, num_sms, stream)
+                        : launch_one<256, 5, false, false, true>(ta, tb, td, td2, P, num_work, num_sms, stream);
+        return dispatch_major<256, 6, true>(a_mn, b_mn, ta, tb, td, td2, P, num_work, num_sms, stream);
     }
     if (BN == 256) {
-        if (reads_r && !a_mn) return b_mn ? launch_one<256, 3, false, true, false>(ta, tb, P, num_work, num_sms, stream)
-                                          : launch_one<256, 3, false, false, false>(ta, tb, P, num_work, num_sms, stream);
-        return dispatch_major<256, 4, false>(a_mn, b_mn, ta, tb, P, num_work, num_sms, stream);
+        if (two_bufs)
+            return b_mn ? launch_one<256, 3, false, true, false>(ta, tb, td, td2, P, num_work, num_sms, stream)
+                        : launch_one<256, 3, false, false, false>(ta, tb, td, td2, P, num_work, num_sms, stream);
+        return dispatch_major<256, 4, false>(a_mn, b_mn, ta, tb, td, td2, P, num_work, num_sms, stream);
     }
-    if (BN == 128) return dispatch_major<128, 6, false>(a_mn, b_mn, ta, tb, P, num_work, num_sms, stream);
-    return dispatch_major<64, 8, false>(a_mn, b_mn, ta, tb, P, num_work, num_sms, stream);
+    if (BN == 128) return dispatch_major<128, 6, false>(a_mn, b_mn, ta, tb, td, td2, P, num_work, num_sms, stream);
+    return dispatch_major<64, 8, false>(a_mn, b_mn, ta, tb, td, td2, P, num_work, num_sms, stream);
 }
 
 }  // namespace tcg

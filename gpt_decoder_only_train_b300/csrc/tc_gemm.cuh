@@ -142,6 +142,22 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, ui
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
+// TMA store of a shared-memory box to global memory (bulk async-group of the issuing thread)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's bulk groups still read shared memory
+template <int N> __device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until all of this thread's bulk groups have completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// make this thread's shared-memory writes visible to the async proxy (TMA, tensor cores)
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // ---- tcgen05 ------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
@@ -264,10 +280,10 @@ __device__ __forceinline__ void release_accumulator(uint64_t *bar, uint32_t rank
 
 constexpr int EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16
 
-// Epilogues that read a second operand (residual, GELU input) run with a
-// 3-deep ring so that each epilogue warp gets a second staging block: the next
-// 32 x 64 block of that operand is fetched (cp.async) while the current one is
-// being computed and stored.
+// Epilogues with a second staging block per warp (3-deep ring single, 5-deep
+// pair): operand-reading epilogues (residual, GELU input) fetch the next 32 x 64
+// block of that operand (cp.async) into it while the current one is computed
+// and stored; the GELU epilogue stores its two outputs from the two blocks.
 // PAIR: a CTA pair shares one 256 x BN tile (cta_group::2), each CTA holding
 // 128 rows of A and BN / 2 rows of B per stage; the R-reading variant of the
 // pair kernel has 5 stages.
@@ -394,16 +410,6 @@ __device__ __forceinline__ void stage_load(uint8_t *stage, const bf16 *g, int64_
     }
 }
 
-__device__ __forceinline__ void stage_store(uint8_t *stage, bf16 *g, int64_t ld, int row0, int col0, int M, int N,
-                                            int lane) {
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int rr = it * 4 + (lane >> 3), ch = lane & 7;
-        const int row = row0 + rr, col = col0 + ch * 8;
-        if (row < M && col < N) *reinterpret_cast<uint4 *>(g + (int64_t)row * ld + col) = *stage_at(stage, rr, ch);
-    }
-}
-
 // Asynchronous version of stage_load (cp.async, 16 bytes per lane per step,
 // zero fill outside [M, N)); complete it with cp_async_wait_all + __syncwarp.
 __device__ __forceinline__ void stage_prefetch(uint8_t *stage, const bf16 *g, int64_t ld, int row0, int col0, int M,
@@ -427,7 +433,13 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // first column.
 // rstage: if non-null, the block of R for this group is already being fetched
 // there (stage_prefetch); otherwise R is loaded through `stage`.
-__device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage, uint8_t *rstage, int row0, int col0,
+// The bf16 outputs leave through TMA stores of the warp's staging block (the
+// staging layout is the 128-byte swizzle of the store maps, box 64 x 32): lane 0
+// issues them and, before a staging block is written again, waits until the
+// store that last used it has read it.  `stage2` is a second staging block for
+// the GELU output (or null: the first one is reused).
+__device__ __forceinline__ void epilogue_group64(const Params &P, const CUtensorMap *tmD, const CUtensorMap *tmD2,
+                                                 uint8_t *stage, uint8_t *stage2, uint8_t *rstage, int row0, int col0,
                                                  int lane, const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
     // x[i] holds columns 2i, 2i+1; the arithmetic runs on pairs (.f32x2)
     F2 x[32];
@@ -450,6 +462,14 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage
             x[i / 2 + 1] = f2_add(x[i / 2 + 1], f2(b.z, b.w));
         }
     }
+    // the output staging block is free once the TMA store that last used it has read it
+    if (lane == 0) {
+        if (stage2)
+            bulk_wait_read<1>();  // the GELU output's store (other block) may still be reading
+        else
+            bulk_wait_read<0>();
+    }
+    __syncwarp();
     if (P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD) {
         uint8_t *rs = rstage;
         if (rs) {
@@ -476,9 +496,12 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage
     for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(f2_lo(x[i]), f2_hi(x[i]));
 #pragma unroll
     for (int c = 0; c < 8; ++c) *stage_at(stage, lane, c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    fence_async_smem();
     __syncwarp();
-    stage_store(stage, reinterpret_cast<bf16 *>(P.D), P.ldd, row0, col0, P.M, P.N, lane);
-    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmD, stage, col0, row0);
+        bulk_commit();
+    }
     if (P.epi == GPT2_EPI_GELU) {
         // GELU of the bf16-rounded pre-activation (a recompute from stored h matches bit for bit)
 #pragma unroll
@@ -486,12 +509,23 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage
             const F2 y = gelu_tanh2(f2(bf16_lo(w[i]), bf16_hi(w[i])));
             w[i] = pack_bf16x2(f2_lo(y), f2_hi(y));
         }
+        uint8_t *g2 = stage2 ? stage2 : stage;
+        if (lane == 0) {
+            if (stage2)
+                bulk_wait_read<1>();  // the previous GELU store from stage2 has read it
+            else
+                bulk_wait_read<0>();  // the store just issued from `stage` has read it
+        }
+        __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-            *stage_at(stage, lane, c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            *stage_at(g2, lane, c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        fence_async_smem();
         __syncwarp();
-        stage_store(stage, P.D2, P.ldd, row0, col0, P.M, P.N, lane);
-        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmD2, g2, col0, row0);
+            bulk_commit();
+        }
     }
 }
 
@@ -503,7 +537,7 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, uint8_t *stage
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const Params P) {
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2, const Params P) {
     using Lay = SmemLayout<BN, STAGES, PAIR>;
     constexpr uint32_t IDESC = PAIR ? instr_desc_pair(BN, A_MN, B_MN) : instr_desc(BN, A_MN, B_MN);
     constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -538,6 +572,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (P.epi != GPT2_EPI_ACCUM_F32) tma_prefetch_desc(&tmD);
+        if (P.epi == GPT2_EPI_GELU) tma_prefetch_desc(&tmD2);
     }
     if (warp == 1) {
         if constexpr (PAIR) {  // one warp of each CTA of the pair allocates collectively
@@ -712,6 +748,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (HALF >= 64) {
                 const bool need_r = P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD;
                 uint8_t *rstage = (Lay::EPI_BUFS > 1 && need_r) ? stage + EPI_STAGE_BYTES : nullptr;
+                uint8_t *gstage = (Lay::EPI_BUFS > 1 && P.epi == GPT2_EPI_GELU) ? stage + EPI_STAGE_BYTES : nullptr;
                 const int row0 = m0 + quad * 32;
 #pragma unroll 1
                 for (int c0 = 0; c0 < HALF; c0 += 64) {
@@ -734,7 +771,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (col < P.N) epilogue_chunk(P, row, col, r0);
                         if (col + 32 < P.N) epilogue_chunk(P, row, col + 32, r1);
                     } else if (col < P.N) {
-                        epilogue_group64(P, stage, rstage, row0, col, lane, r0, r1);
+                        epilogue_group64(P, &tmD, &tmD2, stage, gstage, rstage, row0, col, lane, r0, r1);
                     }
                     // fetch the operand block of the next group (this tile or the next one)
                     if (rstage) {
@@ -770,6 +807,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     }
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // the epilogue's TMA stores have completed
     tc_fence_before();
     __syncthreads();
     if constexpr (PAIR) cluster_sync();  // the pair's MMAs and both epilogues are done with TMEM
