@@ -141,8 +141,8 @@ GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
     "workload": "gpt2_124m",
-    "sha256": "8617e6a8cb8608fb613538387fb1109018070f4f302f4a2cf0252289901347e2",
-    "bytes_per_launch": 21.6443e9 / 147,
+    "sha256": "cd54b224514ac7445c9c7975b6cd0f04a1ea6590b484733c2b48dbbf7963a90b",
+    "bytes_per_launch": 23.29e9 / 147,
 }
 
 

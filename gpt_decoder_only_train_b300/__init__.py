@@ -81,8 +81,10 @@ _SIGS = {
     "gpt2_generate": (_I, [_P, _P, _I, _I, _I, _P, _F, _I]),
     "gpt2_op_layernorm_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "gpt2_op_layernorm_backward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P]),
-    "gpt2_op_embedding_backward": (_I, [_P, _I, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "gpt2_op_embedding_backward": (_I, [_P, _I, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "gpt2_embedding_backward_workspace": (ctypes.c_size_t, [_I, _I, _I]),
     "gpt2_debug_set_barrier_wait": (_I, [ctypes.c_ulonglong, _I]),
+    "gpt2_set_graphs": (_I, [_P, _I]),
 }
 
 
@@ -191,6 +193,10 @@ class GPT2:
 
     def zero_grad(self):
         check("gpt2_zero_grad", lib().gpt2_zero_grad(self.handle))
+
+    def set_graphs(self, enable: bool):
+        """CUDA-graph replay of forward / backward (on by default; see gpt2_set_graphs)."""
+        check("gpt2_set_graphs", lib().gpt2_set_graphs(self.handle, int(bool(enable))))
 
     def clip_and_adamw(self, lr, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, clip=1.0):
         norm = ctypes.c_float(0.0)
@@ -323,14 +329,20 @@ def classifier(logits, targets, loss_rows, N, V, Vp, dscale, stream=None):
         _ptr(logits), _ptr(targets), _ptr(loss_rows), N, V, Vp, dscale, _stream(stream)))
 
 
-def embedding_backward(dx, tokens, dwte, dwpe, B, T, C, V, stream=None):
-    """dwte[tokens] += dx rows; dwpe[t] += sum over the batch (device tensors)."""
+def embedding_backward_workspace(B, T, C) -> int:
+    return int(lib().gpt2_embedding_backward_workspace(B, T, C))
+
+
+def embedding_backward(dx, tokens, dwte, dwpe, B, T, C, V, workspace=None, stream=None):
+    """dwte[tokens] += dx rows; dwpe[t] += sum over the batch (device tensors).  With a
+    workspace (uint8 device tensor of embedding_backward_workspace bytes) the rows are summed
+    in a fixed order; without, with atomics."""
     import torch
 
     dtype = GPT2_DTYPE_FP32 if dx.dtype == torch.float32 else GPT2_DTYPE_BF16
     check("gpt2_op_embedding_backward",
           lib().gpt2_op_embedding_backward(_ptr(dx), dtype, _ptr(tokens), B, T, C, V, _ptr(dwte), _ptr(dwpe),
-                                           _stream(stream)))
+                                           _ptr(workspace), _stream(stream)))
 
 
 def set_barrier_wait(wait_ns: int = 0, never_arrive: bool = False):

@@ -95,9 +95,10 @@ struct gpt2_model {
     float *lnf_mean, *lnf_rstd;
     void *logits;
     float *loss_rows, *loss_dev, *norm_dev;
-    int *tokens;
+    int *tokens, *targets;
     void *dres, *dbig, *dqkv, *datt, *dsmall, *gelu_buf;
     float *attn_D;
+    void *emb_ws;  // embedding backward: sorted keys and partial sums
     double *norm_partials;
     unsigned *barrier;
     int *err_dev;
@@ -115,6 +116,17 @@ struct gpt2_model {
     std::vector<Rec> prof;
     size_t prof_used = 0;
     bool prof_on = false;
+    // CUDA graphs of the forward and backward launch sequences, keyed by shape
+    // (and, for the backward, the loss weight): replayed on the model's stream
+    struct Graph {
+        int kind, B, T;
+        uint32_t key;
+        cudaGraphExec_t exec;
+        long long kernels;
+        int uses;  // calls seen for this key; the first runs direct, the second captures
+    };
+    std::vector<Graph> graphs;
+    bool graphs_on = true;
     double prof_ms[GPT2_PROF_NCAT] = {}, prof_work[GPT2_PROF_NCAT] = {};
     long long prof_n[GPT2_PROF_NCAT] = {};
 };
@@ -238,6 +250,7 @@ void plan(gpt2_model &m, uint8_t *base) {
     m.loss_dev = b.take<float>(64);
     m.norm_dev = b.take<float>(64);
     m.tokens = b.take<int>(BT * 4);
+    m.targets = b.take<int>(BT * 4);
     m.dres = b.take<void>(BT * C * es);
     m.dbig = b.take<void>(BT * 4 * C * es);
     m.dqkv = b.take<void>(BT * 3 * C * es);
@@ -245,6 +258,7 @@ void plan(gpt2_model &m, uint8_t *base) {
     m.dsmall = b.take<void>(BT * C * es);
     m.gelu_buf = take_opt<void>(b, c.recompute_gelu != 0, BT * 4 * C * es);
     m.attn_D = b.take<float>((int64_t)c.B * c.H * c.T * 4);
+    m.emb_ws = b.take<void>(k::embed_backward_workspace((int)BT, c.C));
     m.norm_partials = b.take<double>((size_t)m.max_adam_blocks * 8);
     m.barrier = b.take<unsigned>(64);
     m.err_dev = b.take<int>(64);
@@ -408,7 +422,7 @@ int attn_bwd(gpt2_model *m, const T *qkv, const T *o, const T *dout, const float
 
 // ---- forward ----------------------------------------------------------------------
 template <typename T>
-int forward_impl(gpt2_model *m, const int32_t *d_targets, int B, int Tn) {
+int forward_impl(gpt2_model *m, bool with_targets, int B, int Tn) {
     const gpt2_config &c = m->cfg;
     const int BT = B * Tn, C = c.C;
     cudaStream_t st = m->stream;
@@ -442,9 +456,9 @@ int forward_impl(gpt2_model *m, const int32_t *d_targets, int B, int Tn) {
                                   m->lnf_rstd, BT, C, st));
     TRY(mm<T>(m, m->lnf, C, true, W<T>(m, 0), C, true, m->logits, nullptr, nullptr, c.Vp, nullptr, BT, c.Vp, C,
               GPT2_EPI_STORE));
-    if (d_targets) {
+    if (with_targets) {
         TIMED(GPT2_PROF_CLASSIFIER, 2.0 * BT * c.Vp * es + 8.0 * BT,
-              k::classifier<T>((T *)m->logits, d_targets, m->loss_rows, BT, c.V, c.Vp, 1.0f / BT, m->err_dev, st));
+              k::classifier<T>((T *)m->logits, m->targets, m->loss_rows, BT, c.V, c.Vp, 1.0f / BT, m->err_dev, st));
         TIMED(GPT2_PROF_OTHER, 4.0 * BT, k::mean_rows(m->loss_rows, BT, m->loss_dev, st));
     }
     return GPT2_OK;
@@ -511,7 +525,7 @@ int backward_impl(gpt2_model *m, float grad_scale) {
                                        l > 0 ? Gf(m, m->lp[l - 1].fcprojb) : nullptr));
     }
     TIMED(GPT2_PROF_OTHER, act + 8.0 * BT * C + 4.0 * BT,
-          k::embed_backward<T>(m->tokens, dres, Gf(m, 0), Gf(m, 1), B, Tn, C, c.V, st));
+          k::embed_backward<T>(m->tokens, dres, Gf(m, 0), Gf(m, 1), B, Tn, C, c.V, st, m->emb_ws));
     return GPT2_OK;
 }
 
@@ -614,6 +628,66 @@ int generate_impl(gpt2_model *m, int *d_seq, int B, int T_total, int T0, const f
     return GPT2_OK;
 }
 
+// Run `launch` (which enqueues work on m->stream) through a CUDA graph cached
+// under (kind, B, T, key): the first call with a key launches directly (which
+// also performs the per-device set-up of the kernels it uses), the second
+// captures the launch sequence on a private stream and replays it, later
+// calls replay.  The graph bakes in every kernel argument, so the key must
+// cover what varies; buffers live in the arena at fixed addresses.  With
+// profiling on, or if capturing fails, the launches run directly.
+template <typename F> int run_graphed(gpt2_model *m, int kind, int B, int T, uint32_t key, F &&launch) {
+    if (m->prof_on || !m->graphs_on) return launch();
+    gpt2_model::Graph *gr = nullptr;
+    for (auto &e : m->graphs)
+        if (e.kind == kind && e.B == B && e.T == T && e.key == key) gr = &e;
+    if (!gr) {
+        m->graphs.push_back(gpt2_model::Graph{kind, B, T, key, nullptr, 0, 0});
+        gr = &m->graphs.back();
+    }
+    if (gr->exec) {
+        GPT2_CUDA_TRY(cudaGraphLaunch(gr->exec, m->stream));
+        gpt2_note_launches((int)gr->kernels);
+        return GPT2_OK;
+    }
+    if (gr->uses++ != 1) return launch();  // first call (or capture failed before): direct
+    cudaStream_t cs;
+    GPT2_CUDA_TRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    cudaStream_t saved = m->stream;
+    m->stream = cs;
+    cudaGraph_t graph = nullptr;
+    int rc = GPT2_OK;
+    const long long n0 = g_launches.load(std::memory_order_relaxed);
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        rc = GPT2_ERR_CUDA;
+    } else {
+        rc = launch();
+        if (cudaStreamEndCapture(cs, &graph) != cudaSuccess && !rc) rc = GPT2_ERR_CUDA;
+    }
+    m->stream = saved;
+    const long long kernels = g_launches.load(std::memory_order_relaxed) - n0;
+    g_launches.fetch_sub(kernels, std::memory_order_relaxed);  // captured, not launched
+    cudaGraphExec_t exec = nullptr;
+    if (!rc && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) rc = GPT2_ERR_CUDA;
+    if (graph) cudaGraphDestroy(graph);
+    cudaStreamDestroy(cs);
+    cudaGetLastError();  // a failed capture leaves no sticky error
+    if (rc) {  // run this call directly; later calls with this key stay direct
+        if (exec) cudaGraphExecDestroy(exec);
+        return launch();
+    }
+    gr->exec = exec;
+    gr->kernels = kernels;
+    GPT2_CUDA_TRY(cudaGraphLaunch(exec, m->stream));
+    gpt2_note_launches((int)kernels);
+    return GPT2_OK;
+}
+
+void drop_graphs(gpt2_model *m) {
+    for (auto &e : m->graphs)
+        if (e.exec) cudaGraphExecDestroy(e.exec);
+    m->graphs.clear();
+}
+
 int read_error_word(gpt2_model *m, int &word) {
     GPT2_CUDA_TRY(cudaMemcpyAsync(&word, m->err_dev, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
     GPT2_CUDA_TRY(cudaStreamSynchronize(m->stream));
@@ -688,8 +762,13 @@ extern "C" int gpt2_forward(gpt2_model *m, const int32_t *d_tokens, const int32_
     if (d_targets && !loss_out) return GPT2_ERR_BAD_ARG;
     m->have_dlogits = false;
     GPT2_CUDA_TRY(cudaMemcpyAsync(m->tokens, d_tokens, (size_t)B * T * 4, cudaMemcpyDeviceToDevice, m->stream));
-    const int rc = m->cfg.dtype == GPT2_DTYPE_BF16 ? forward_impl<bf16>(m, d_targets, B, T)
-                                                   : forward_impl<float>(m, d_targets, B, T);
+    if (d_targets)
+        GPT2_CUDA_TRY(
+            cudaMemcpyAsync(m->targets, d_targets, (size_t)B * T * 4, cudaMemcpyDeviceToDevice, m->stream));
+    const bool tg = d_targets != nullptr;
+    const int rc = run_graphed(m, tg ? 1 : 0, B, T, 0u, [&]() -> int {
+        return m->cfg.dtype == GPT2_DTYPE_BF16 ? forward_impl<bf16>(m, tg, B, T) : forward_impl<float>(m, tg, B, T);
+    });
     if (rc) return rc;
     m->fwd_B = B;
     m->fwd_T = T;
@@ -706,7 +785,12 @@ extern "C" int gpt2_backward(gpt2_model *m, float grad_scale) {
     if (!m) return GPT2_ERR_BAD_ARG;
     if (!m->have_dlogits) return GPT2_ERR_STATE;
     m->have_dlogits = false;  // dlogits are consumed
-    return m->cfg.dtype == GPT2_DTYPE_BF16 ? backward_impl<bf16>(m, grad_scale) : backward_impl<float>(m, grad_scale);
+    uint32_t key;
+    memcpy(&key, &grad_scale, 4);  // the loss weight is a kernel argument of the graph
+    return run_graphed(m, 2, m->fwd_B, m->fwd_T, key, [&]() -> int {
+        return m->cfg.dtype == GPT2_DTYPE_BF16 ? backward_impl<bf16>(m, grad_scale)
+                                               : backward_impl<float>(m, grad_scale);
+    });
 }
 
 extern "C" int gpt2_generate(gpt2_model *m, int32_t *d_seq, int B, int T_total, int T0, const float *d_uniforms,
@@ -766,6 +850,13 @@ extern "C" int gpt2_debug_set_barrier_wait(unsigned long long wait_ns, int never
     if (never_arrive != 0 && never_arrive != 1) return GPT2_ERR_BAD_ARG;
     g_barrier_wait_ns.store(wait_ns ? wait_ns : kDefaultBarrierWaitNs, std::memory_order_relaxed);
     g_barrier_extra.store((unsigned)never_arrive, std::memory_order_relaxed);
+    return GPT2_OK;
+}
+
+extern "C" int gpt2_set_graphs(gpt2_model *m, int enable) {
+    if (!m || (enable != 0 && enable != 1)) return GPT2_ERR_BAD_ARG;
+    m->graphs_on = enable != 0;
+    if (!enable) drop_graphs(m);
     return GPT2_OK;
 }
 
@@ -879,6 +970,7 @@ extern "C" int gpt2_profile_read(gpt2_model *m, int category, double *total_ms, 
 
 extern "C" void gpt2_free(gpt2_model *m) {
     if (!m) return;
+    drop_graphs(m);
     for (auto &r : m->prof) {
         cudaEventDestroy(r.a);
         cudaEventDestroy(r.b);
@@ -966,14 +1058,22 @@ extern "C" int gpt2_op_sample(const void *logits, int64_t ldl, int B, int V, con
                                 (cudaStream_t)stream);
 }
 
+extern "C" size_t gpt2_embedding_backward_workspace(int B, int T, int C) {
+    if (B <= 0 || T <= 0 || C <= 0) return 0;
+    return k::embed_backward_workspace(B * T, C);
+}
+
 extern "C" int gpt2_op_embedding_backward(const void *dx, int dtype, const int32_t *tokens, int B, int T, int C,
-                                          int V, float *dwte, float *dwpe, void *stream) {
+                                          int V, float *dwte, float *dwpe, void *d_workspace, void *stream) {
     if (!dx || !tokens || !dwte || !dwpe) return GPT2_ERR_BAD_ARG;
     if (B <= 0 || T <= 0 || C <= 0 || V <= 0 || C % 4) return GPT2_ERR_BAD_SHAPE;
+    if (reinterpret_cast<uintptr_t>(d_workspace) & 255) return GPT2_ERR_BAD_ARG;
     if (dtype == GPT2_DTYPE_FP32)
-        return k::embed_backward<float>(tokens, (const float *)dx, dwte, dwpe, B, T, C, V, (cudaStream_t)stream);
+        return k::embed_backward<float>(tokens, (const float *)dx, dwte, dwpe, B, T, C, V, (cudaStream_t)stream,
+                                        d_workspace);
     if (dtype == GPT2_DTYPE_BF16)
-        return k::embed_backward<bf16>(tokens, (const bf16 *)dx, dwte, dwpe, B, T, C, V, (cudaStream_t)stream);
+        return k::embed_backward<bf16>(tokens, (const bf16 *)dx, dwte, dwpe, B, T, C, V, (cudaStream_t)stream,
+                                       d_workspace);
     return GPT2_ERR_BAD_ARG;
 }
 

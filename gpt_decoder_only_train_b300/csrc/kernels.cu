@@ -77,14 +77,245 @@ __global__ void embed_bwd_wpe_kernel(const T *__restrict__ dx, float *__restrict
     dwpe[idx] += s;
 }
 
+// ---- token rows in a fixed order ----------------------------------------------
+// The positions of a chunk (at most EMB_CHUNK of them) are sorted by token with
+// a stable radix sort (so each token's positions stay in position order); the
+// sorted list is cut into pieces of 32.  A warp sums the rows of each run of
+// equal tokens in its piece in list order; a run that is a whole token
+// segment is added to dwte[token] by that warp (its only writer), a run of a
+// segment that crosses a piece boundary goes to a partial slot, and one block
+// per crossing segment adds the slots in list order.  Every row of dwte is so
+// summed in one fixed order: the result does not depend on scheduling.
+constexpr int EMB_CHUNK = 16384;     // positions sorted by one CTA (keys in shared memory)
+constexpr int EMB_SORT_THREADS = 1024;
+
+// key = token << 16 | position in the chunk; stable LSD radix sort on the
+// token's two bytes (shared-memory counts per warp and digit, digit-major
+// exclusive scan, ranks within a warp from __match_any_sync).
+__global__ void __launch_bounds__(EMB_SORT_THREADS) embed_sort_kernel(const int *__restrict__ tok, int n, int V,
+                                                                     uint32_t *__restrict__ keys_out) {
+    extern __shared__ uint32_t esm[];
+    uint32_t *buf0 = esm, *buf1 = esm + EMB_CHUNK;
+    int *cnt = reinterpret_cast<int *>(esm + 2 * EMB_CHUNK);  // [32 warps][256 digits]
+    __shared__ int wsum[32];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    for (int i = tid; i < n; i += EMB_SORT_THREADS) {
+        int t = tok[i];
+        if (t < 0 || t >= V) t = 0;  // the forward reported it; its row is treated as token 0
+        buf0[i] = ((uint32_t)t << 16) | (uint32_t)i;
+    }
+    const int per_warp = (n + 31) / 32;  // each warp owns a contiguous range of the input order
+    const int w0 = min(n, w * per_warp), w1 = min(n, w0 + per_warp);
+    uint32_t *in = buf0, *out = buf1;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = 16 + 8 * pass;
+        for (int i = tid; i < 32 * 256; i += EMB_SORT_THREADS) cnt[i] = 0;
+        __syncthreads();
+        for (int b = w0; b < w1; b += 32) {
+            const int i = b + lane;
+            const bool v = i < w1;
+            const uint32_t d = v ? (in[i] >> shift) & 255u : 256u + lane;  // lanes past the end: unique digits
+            const uint32_t peers = __match_any_sync(0xffffffffu, d);
+            if (v && lane == __ffs(peers) - 1) cnt[w * 256 + d] += __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        // exclusive scan in digit-major order: entry (digit, warp) at index digit * 32 + warp
+        int loc[8], run = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = tid * 8 + j, d = e >> 5, ww = e & 31;
+            loc[j] = run;
+            run += cnt[ww * 256 + d];
+        }
+        int x = run;  // inclusive scan of the per-thread totals
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int z = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, z, o);
+                if (lane >= o) z += y;
+            }
+            wsum[lane] = z - wsum[lane];  // exclusive
+        }
+        __syncthreads();
+        const int base = wsum[w] + x - run;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = tid * 8 + j, d = e >> 5, ww = e & 31;
+            cnt[ww * 256 + d] = base + loc[j];
+        }
+        __syncthreads();
+        for (int b = w0; b < w1; b += 32) {
+            const int i = b + lane;
+            const bool v = i < w1;
+            const uint32_t k = v ? in[i] : 0u;
+            const uint32_t d = v ? (k >> shift) & 255u : 256u + lane;
+            const uint32_t peers = __match_any_sync(0xffffffffu, d);
+            int dst = 0;
+            if (v) dst = cnt[w * 256 + d] + __popc(peers & ((1u << lane) - 1u));
+            __syncwarp();
+            if (v) {
+                out[dst] = k;
+                if (lane == __ffs(peers) - 1) cnt[w * 256 + d] += __popc(peers);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        uint32_t *t = in;
+        in = out;
+        out = t;
+    }
+    for (int i = tid; i < n; i += EMB_SORT_THREADS) keys_out[i] = in[i];
+}
+
+// 8 consecutive elements of row `row` from column `col` as fp32
+__device__ __forceinline__ void load8(const bf16 *p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = bf16_lo(w[k]);
+        v[2 * k + 1] = bf16_hi(w[k]);
+    }
+}
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+}
+
+// One warp per (piece of 32 sorted entries, slab of 256 columns; 8 per lane).
+template <typename T>
+__global__ void embed_runs_kernel(const uint32_t *__restrict__ keys, const T *__restrict__ dx, float *__restrict__ dwte,
+                                  float *__restrict__ part, int n, int C) {
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int nslab = (C + 255) / 256, npieces = (n + 31) / 32;
+    const int piece = gw / nslab, slab = gw - piece * nslab;
+    if (piece >= npieces) return;
+    const int i0 = piece * 32, cnt = min(32, n - i0);
+    const uint32_t myk = lane < cnt ? keys[i0 + lane] : 0u;
+    const int tok_before = i0 > 0 ? (int)(keys[i0 - 1] >> 16) : -1;
+    const int tok_after = i0 + cnt < n ? (int)(keys[i0 + cnt] >> 16) : -1;
+    const int col = slab * 256 + lane * 8;
+    const bool active = col < C;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    int run_start = 0, cur = (int)(__shfl_sync(0xffffffffu, myk, 0) >> 16);
+    auto flush = [&](int rs, int re) {
+        const bool crosses = (rs == 0 && tok_before == cur) || (re == cnt && tok_after == cur);
+        if (!active) return;
+        float *dst;
+        if (crosses) {
+            dst = part + (int64_t)(rs == 0 ? piece : npieces + piece) * C + col;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = acc[e];
+        } else {
+            dst = dwte + (int64_t)cur * C + col;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] += acc[e];
+        }
+    };
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+        // the rows of up to 8 entries are requested together, then added in order
+        float v[8][8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t k = __shfl_sync(0xffffffffu, myk, (j0 + u) & 31);
+            if (active && j0 + u < cnt) load8(dx + (int64_t)(k & 0xFFFFu) * C + col, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u;
+            if (j >= cnt) break;
+            const int tk = (int)(__shfl_sync(0xffffffffu, myk, j & 31) >> 16);
+            if (tk != cur) {
+                flush(run_start, j);
+                run_start = j;
+                cur = tk;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            }
+            if (active)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] += v[u][e];
+        }
+    }
+    flush(run_start, cnt);
+}
+
+// One block per piece boundary b = 32 k: if a token segment crosses it and
+// starts in piece k - 1, add its partial slots in list order to dwte[token].
+__global__ void embed_cross_kernel(const uint32_t *__restrict__ keys, const float *__restrict__ part,
+                                   float *__restrict__ dwte, int n, int C) {
+    const int npieces = (n + 31) / 32, k = blockIdx.x + 1, b = 32 * k;
+    if (b >= n) return;
+    const uint32_t tk = keys[b] >> 16;
+    if ((keys[b - 1] >> 16) != tk) return;                    // no segment crosses this boundary
+    if (k >= 2 && (keys[32 * (k - 1) - 1] >> 16) == tk) return;  // it started before piece k - 1
+    const bool starts_at_piece = (keys[32 * (k - 1)] >> 16) == tk;
+    const int first = starts_at_piece ? k - 1 : npieces + k - 1;
+    int last = k;  // pieces k .. last - 1 begin with this token
+    while (last < npieces && (keys[32 * last] >> 16) == tk) ++last;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+        float s = part[(int64_t)first * C + c];
+        for (int q = k; q < last; ++q) s += part[(int64_t)q * C + c];
+        dwte[(int64_t)tk * C + c] += s;
+    }
+}
+
+size_t embed_backward_workspace(int n, int C) {
+    const int chunk = std::min(n, EMB_CHUNK), npieces = (chunk + 31) / 32;
+    return (size_t)chunk * 4 + (size_t)2 * npieces * C * 4 + 256;
+}
+
 template <typename T>
 int embed_backward(const int *tok, const T *dx, float *dwte, float *dwpe, int B, int Tn, int C, int V,
-                   cudaStream_t st) {
-    const int64_t n = (int64_t)B * Tn * C;
-    embed_bwd_wte_kernel<T><<<ceil_div(n, 256), 256, 0, st>>>(tok, dx, dwte, B * Tn, C, V);
+                   cudaStream_t st, void *ws) {
+    const int n = B * Tn;
+    if (!ws || C % 8 || V > 65536) {  // fp32 atomics: the order of additions into a shared row is not fixed
+        const int64_t ne = (int64_t)n * C;
+        embed_bwd_wte_kernel<T><<<ceil_div(ne, 256), 256, 0, st>>>(tok, dx, dwte, n, C, V);
+        GPT2_CUDA_TRY(cudaGetLastError());
+        gpt2_note_launches(1);
+    } else {
+        static PerDevice attr_pd;
+        const int sort_smem = (2 * EMB_CHUNK + 32 * 256) * 4;
+        int unused = 0;
+        if (int rc = per_device(attr_pd, unused, [&](int &v) -> int {
+                GPT2_CUDA_TRY(
+                    cudaFuncSetAttribute(embed_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sort_smem));
+                v = 1;
+                return GPT2_OK;
+            }))
+            return rc;
+        uint32_t *keys = reinterpret_cast<uint32_t *>(ws);
+        const int npieces_max = (std::min(n, EMB_CHUNK) + 31) / 32;
+        float *part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) +
+                                                (((size_t)std::min(n, EMB_CHUNK) * 4 + 255) & ~(size_t)255));
+        (void)npieces_max;
+        // chunks of positions in order; within a chunk, rows in sorted order
+        for (int c0 = 0; c0 < n; c0 += EMB_CHUNK) {
+            const int m = std::min(EMB_CHUNK, n - c0), npieces = (m + 31) / 32, nslab = (C + 255) / 256;
+            embed_sort_kernel<<<1, EMB_SORT_THREADS, sort_smem, st>>>(tok + c0, m, V, keys);
+            embed_runs_kernel<T><<<ceil_div(npieces * nslab, 8), 256, 0, st>>>(keys, dx + (int64_t)c0 * C, dwte, part,
+                                                                                m, C);
+            if (npieces > 1) embed_cross_kernel<<<npieces - 1, 256, 0, st>>>(keys, part, dwte, m, C);
+            GPT2_CUDA_TRY(cudaGetLastError());
+            gpt2_note_launches(npieces > 1 ? 3 : 2);
+        }
+    }
     embed_bwd_wpe_kernel<T><<<ceil_div((int64_t)Tn * C, 256), 256, 0, st>>>(dx, dwpe, B, Tn, C);
     GPT2_CUDA_TRY(cudaGetLastError());
-    gpt2_note_launches(2);
+    gpt2_note_launches(1);
     return GPT2_OK;
 }
 
@@ -1580,7 +1811,8 @@ int clip_adamw(float *p, const float *g, float *m, float *v, bf16 *shadow, int64
 #define INST(T)                                                                                                  \
     template int embed_forward<T>(const int *, const float *, const float *, T *, int, int, int, int, int *,       \
                                   cudaStream_t);                                                                 \
-    template int embed_backward<T>(const int *, const T *, float *, float *, int, int, int, int, cudaStream_t);    \
+    template int embed_backward<T>(const int *, const T *, float *, float *, int, int, int, int, cudaStream_t,     \
+                                   void *);                                                                      \
     template int layernorm_forward<T>(const T *, const float *, const float *, T *, float *, float *, int, int,    \
                                       cudaStream_t);                                                             \
     template int layernorm_backward<T>(const T *, const T *, const float *, const float *, const float *,          \

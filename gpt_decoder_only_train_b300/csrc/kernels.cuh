@@ -12,10 +12,14 @@ template <typename T>
 int embed_forward(const int *tok, const float *wte, const float *wpe, T *x, int B, int Tn, int C, int V, int *err,
                   cudaStream_t st);
 
-// dwte[tok[b,t]] += dx[b,t];  dwpe[t] += sum_b dx[b,t]
+// dwte[tok[b,t]] += dx[b,t];  dwpe[t] += sum_b dx[b,t].  With a workspace of
+// embed_backward_workspace(B*T, C) bytes (and C % 8 == 0, V <= 65536) every row
+// is summed in a fixed order (positions sorted by token); without one, with
+// fp32 atomics.
 template <typename T>
 int embed_backward(const int *tok, const T *dx, float *dwte, float *dwpe, int B, int Tn, int C, int V,
-                   cudaStream_t st);
+                   cudaStream_t st, void *ws);
+size_t embed_backward_workspace(int n, int C);
 
 // y = (x - mean) * rstd * g + b per row of C; mean/rstd fp32 [N]
 template <typename T>

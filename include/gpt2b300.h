@@ -120,6 +120,21 @@ int gpt2_backward(gpt2_model *m, float grad_scale);
 /* grads = 0 (enqueued). */
 int gpt2_zero_grad(gpt2_model *m);
 
+/*
+ * CUDA-graph replay of the forward and backward launch sequences (on by
+ * default).  The first gpt2_forward / gpt2_backward of a shape (B, T, with or
+ * without targets; for the backward also grad_scale) launches its kernels
+ * directly, the second captures them into a graph on a stream the library
+ * creates and destroys, later calls replay that graph on the model's stream:
+ * the same kernels with the same arguments, without the per-launch gaps.
+ * Tokens and targets are copied into the model's own buffers before the
+ * graph runs, so callers may pass different buffers on every call.  While
+ * per-launch profiling is on (gpt2_profile) the kernels run directly.
+ * enable = 0 drops the cached graphs and launches directly from then on.
+ * GPT2_ERR_BAD_ARG for a NULL model or enable other than 0 or 1.
+ */
+int gpt2_set_graphs(gpt2_model *m, int enable);
+
 /* Largest top_k of gpt2_generate and gpt2_op_sample. */
 #define GPT2_MAX_TOP_K 128
 
@@ -352,12 +367,18 @@ int gpt2_op_sample(const void *logits, int64_t ldl, int B, int V, const float *u
  * dx: device [B, T, C] of dtype GPT2_DTYPE_FP32 (float) or GPT2_DTYPE_BF16;
  * tokens: device int32 [B, T]; dwte: device fp32 [>= V, C]; dwpe: device fp32
  * [>= T, C]; both accumulated into (zero them for a plain result).  Tokens
- * outside [0, V) are added to row 0 (the forward reports them).  The token
- * rows are summed with fp32 atomics, so the order of additions into a row
- * that several positions share is not fixed.  C a multiple of 4.
+ * outside [0, V) are added to row 0 (the forward reports them).
+ * With d_workspace (device, 256-byte aligned, at least
+ * gpt2_embedding_backward_workspace(B, T, C) bytes, owned by the caller) and
+ * C a multiple of 8, V <= 65536: the positions are sorted by token (stable, in
+ * chunks of 16384 positions) and every row of dwte is summed in one fixed
+ * order, so the result is the same bits on every run.  With d_workspace NULL
+ * the token rows are summed with fp32 atomics (order not fixed).  dwpe[t] is
+ * always the batch rows added in order b = 0 .. B-1.  C a multiple of 4.
  */
+size_t gpt2_embedding_backward_workspace(int B, int T, int C);
 int gpt2_op_embedding_backward(const void *dx, int dtype, const int32_t *tokens, int B, int T, int C, int V,
-                               float *dwte, float *dwpe, void *stream);
+                               float *dwte, float *dwpe, void *d_workspace, void *stream);
 
 /*
  * Fused classifier over rows of bf16 logits [N, Vp] (in place):

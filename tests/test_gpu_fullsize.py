@@ -112,6 +112,24 @@ def test_350m_recompute_sampled_rows_and_property(g):
     m2.close()
 
 
+def test_124m_embedding_gradients_bitwise_reproducible(g):
+    """At 124M, B=16, T=1024: two backward passes of the same batch give bit-identical wte
+    and wpe gradients."""
+    w = synthetic.WORKLOADS["gpt2_124m"]
+    x, y = synthetic.step_batch(w)
+    m = g.GPT2(w, seed=w["seed"])
+    res = []
+    for _ in range(2):
+        m.zero_grad()
+        m.forward(_dev(x), _dev(y))
+        m.backward(1.0)
+        res.append((m.grads(0), m.grads(1)))
+    m.close()
+    assert res[0][0].tobytes() == res[1][0].tobytes()
+    assert res[0][1].tobytes() == res[1][1].tobytes()
+    assert np.abs(res[0][0]).max() > 0
+
+
 def test_350m_recompute_one_sequence_gradient_parity(g):
     """The 350M step with GELU recompute on one full-length sequence: loss, every gradient
     tensor and the global norm against the fp64 oracle."""

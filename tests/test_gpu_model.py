@@ -325,11 +325,13 @@ def test_fp32_target_handling_is_exact(g):
     m.close()
 
 
+@pytest.mark.parametrize("fixed_order", [True, False], ids=["sorted", "atomics"])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-def test_embedding_backward_rows_are_exact(g, dtype):
+def test_embedding_backward_rows_are_exact(g, dtype, fixed_order):
     """dwte receives gradient in exactly the rows of the tokens present, dwpe in exactly the
     first T rows; a row hit once equals that dx row bit for bit, a row hit several times is the
-    fp32 sum of its rows (oracle: the float64 scatter-add)."""
+    fp32 sum of its rows (oracle: the float64 scatter-add).  With a workspace the rows are summed
+    in a fixed order: a second call gives the same bits."""
     B, T, C, V, Tmax = 3, 40, 64, 256, 48
     x, _ = synthetic.uniform_batch(13, B, T, 50)  # tokens in [0, 50): many repeats, rows >= 50 untouched
     x[1, 7] = 200                                  # one token present exactly once
@@ -338,11 +340,21 @@ def test_embedding_backward_rows_are_exact(g, dtype):
     tdt = torch.float32 if dtype == "fp32" else torch.bfloat16
     dx_t = torch.from_numpy(dx32).to(tdt)
     dx_used = dx_t.float().numpy().astype(np.float64)  # the values the kernel reads
+    ws = None
+    if fixed_order:
+        ws = torch.empty(g.embedding_backward_workspace(B, T, C), dtype=torch.uint8, device="cuda")
     dwte = torch.zeros(V, C, dtype=torch.float32, device="cuda")
     dwpe = torch.zeros(Tmax, C, dtype=torch.float32, device="cuda")
-    g.embedding_backward(dx_t.cuda().contiguous(), _dev(x), dwte, dwpe, B, T, C, V)
+    dx_d = dx_t.cuda().contiguous()
+    g.embedding_backward(dx_d, _dev(x), dwte, dwpe, B, T, C, V, workspace=ws)
     torch.cuda.synchronize()
     gw, gp = dwte.cpu().numpy(), dwpe.cpu().numpy()
+    if fixed_order:
+        dwte2 = torch.zeros_like(dwte)
+        dwpe2 = torch.zeros_like(dwpe)
+        g.embedding_backward(dx_d, _dev(x), dwte2, dwpe2, B, T, C, V, workspace=ws)
+        torch.cuda.synchronize()
+        assert dwte2.cpu().numpy().tobytes() == gw.tobytes() and dwpe2.cpu().numpy().tobytes() == gp.tobytes()
     ref_w, ref_p = og.embedding_backward(torch.from_numpy(dx_used), torch.from_numpy(x), V, Tmax)
     ref_w, ref_p = ref_w.numpy(), ref_p.numpy()
     present = np.unique(x)
@@ -429,3 +441,80 @@ def test_adamw_barrier_timeout_is_reported_and_recoverable(g):
     assert math.isfinite(norm) and m.adam_step() == 1
     assert math.isfinite(m.forward(_dev(x), _dev(y)))
     m.close()
+
+
+def test_graph_replay_matches_direct_launches(g):
+    """Forward and backward replayed from CUDA graphs (the default from the second call of a
+    shape on) give the results of direct launches: losses bit for bit, gradients to the fp32
+    summation noise of the split-K accumulation; changing the shape, the token buffers or the
+    loss weight between calls is handled."""
+    cfg = SMALL_BF16
+    batches = [synthetic.zipf_window(31 + i, cfg["B"], cfg["T"], cfg["V"]) for i in range(2)]
+    short = synthetic.zipf_window(40, 2, cfg["T"] // 2, cfg["V"])
+    plan = [(0, 1.0), (1, 1.0), (0, 1.0), (1, 0.5), (1, 0.5), (1, 0.5), (0, 1.0)]
+    runs = {}
+    for graphs in (False, True):
+        m = g.GPT2(cfg, seed=31)
+        m.set_graphs(graphs)
+        out = []
+        for bi, scale in plan:
+            x, y = batches[bi]
+            m.zero_grad()
+            loss = m.forward(_dev(x), _dev(y))
+            m.backward(scale)
+            out.append((loss, [m.grads(i) for i in range(len(m.names))]))
+            # interleave a shorter batch and a logits-only forward (other graph keys)
+            xs, ys = short
+            out.append((m.forward(_dev(xs), _dev(ys)), None))
+            m.forward(_dev(x), None)
+        runs[graphs] = out
+        m.close()
+    for (la, ga), (lb, gb) in zip(runs[False], runs[True]):
+        assert la == lb
+        if ga is not None:
+            for a, b in zip(ga, gb):
+                assert np.abs(a - b).max() <= 1e-5 * max(np.abs(a).max(), 1e-30)
+
+
+@pytest.mark.parametrize("n,C,V", [(16384, 768, 50257), (20000, 128, 300), (70, 256, 5)],
+                         ids=["124m_rows", "two_chunks", "few_tokens"])
+def test_embedding_backward_fixed_order_at_scale(g, n, C, V):
+    """The sorted (fixed-order) embedding backward on Zipf tokens: the hot tokens' segments span
+    many pieces of the sorted list (and, past 16384 positions, two sort chunks); every row is the
+    oracle's scatter-add within the fp32 summation bound, untouched rows stay zero, and repeated
+    calls give the same bits."""
+    x = synthetic.zipf_tokens(17, n, V).reshape(1, n)
+    rng = np.random.default_rng(n)
+    dx = torch.from_numpy(rng.standard_normal((1, n, C)).astype(np.float32)).to(torch.bfloat16)
+    dx_used = dx.float().numpy().astype(np.float64)
+    ws = torch.empty(g.embedding_backward_workspace(1, n, C), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        dwte = torch.zeros(V, C, dtype=torch.float32, device="cuda")
+        dwpe = torch.zeros(n, C, dtype=torch.float32, device="cuda")
+        g.embedding_backward(dx.cuda().contiguous(), _dev(x), dwte, dwpe, 1, n, C, V, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append(dwte.cpu().numpy())
+    assert outs[0].tobytes() == outs[1].tobytes()
+    ref, _ = og.embedding_backward(torch.from_numpy(dx_used), torch.from_numpy(x), V, n)
+    absr, _ = og.embedding_backward(torch.from_numpy(np.abs(dx_used)), torch.from_numpy(x), V, n)
+    counts = np.bincount(x.reshape(-1), minlength=V)
+    bound = (counts[:, None] * 2.0 ** -24) * absr.numpy() + 1e-30
+    assert (np.abs(outs[0] - ref.numpy()) <= bound).all()
+    assert (outs[0][counts == 0] == 0).all()
+
+
+def test_embedding_gradients_bitwise_reproducible(g):
+    """Two identical steps give bit-identical wte and wpe gradients (the embedding rows are
+    summed in a fixed order; the tied LM-head weight gradient has no split-K)."""
+    cfg = SMALL_BF16
+    x, y = synthetic.zipf_window(44, cfg["B"], cfg["T"], cfg["V"])
+    res = []
+    for _ in range(2):
+        m = g.GPT2(cfg, seed=44)
+        m.forward(_dev(x), _dev(y))
+        m.backward(1.0)
+        res.append((m.grads(0), m.grads(1)))
+        m.close()
+    assert res[0][0].tobytes() == res[1][0].tobytes()
+    assert res[0][1].tobytes() == res[1][1].tobytes()
