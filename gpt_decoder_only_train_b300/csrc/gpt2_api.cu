@@ -362,7 +362,8 @@ inline float *Gf(gpt2_model *m, int id) { return m->grads + m->tensors[id].offse
 // acc[m,n] = sum_k A(m,k) B(n,k) with the majorness conventions of gpt2_op_matmul.
 template <typename T>
 int mm(gpt2_model *m, const void *A, int64_t lda, bool a_km, const void *B, int64_t ldb, bool b_km, void *D, void *D2,
-       const void *R, int64_t ldd, const float *bias, int M, int N, int K, int epi, float alpha = 1.0f) {
+       const void *R, int64_t ldd, const float *bias, int M, int N, int K, int epi, float alpha = 1.0f,
+       float *dbias = nullptr) {
     if constexpr (sizeof(T) == 2) {
         tcg::GemmDesc g;
         g.A = (const bf16 *)A;
@@ -382,6 +383,7 @@ int mm(gpt2_model *m, const void *A, int64_t lda, bool a_km, const void *B, int6
         g.epi = epi;
         g.alpha = alpha;
         g.err = m->err_dev;
+        g.dbias = dbias;
         return timed(m, GPT2_PROF_MATMUL, 2.0 * M * N * K, [&] { return tcg::launch_gemm_tc(g, m->num_sms, m->stream); });
     } else {
         return timed(m, GPT2_PROF_MATMUL, 2.0 * M * N * K, [&] {
@@ -496,12 +498,14 @@ int backward_impl(gpt2_model *m, float grad_scale) {
         // FC projection: x' = x1 + g Wfcproj^T + b
         TRY(mm<T>(m, dres, C, false, g_in, 4 * C, false, Gf(m, p.fcprojw), nullptr, nullptr, 4 * C, nullptr, C, 4 * C,
                   BT, GPT2_EPI_ACCUM_F32));
+        // bf16: the GELU-backward product also sums its output's columns into the FC bias gradient
+        constexpr bool fold_fcb = sizeof(T) == 2;
         TRY(mm<T>(m, dres, C, true, W<T>(m, p.fcprojw), 4 * C, false, dbig, nullptr, y.fch, 4 * C, nullptr, BT, 4 * C,
-                  C, GPT2_EPI_GELU_BWD));
+                  C, GPT2_EPI_GELU_BWD, 1.0f, fold_fcb ? Gf(m, p.fcb) : nullptr));
         // FC: h = y2 Wfc^T + b
         TRY(mm<T>(m, dbig, 4 * C, false, y.ln2, C, false, Gf(m, p.fcw), nullptr, nullptr, C, nullptr, 4 * C, C, BT,
                   GPT2_EPI_ACCUM_F32));
-        TIMED(GPT2_PROF_OTHER, 4 * act, k::column_sum<T>(dbig, BT, 4 * C, Gf(m, p.fcb), st));
+        if (!fold_fcb) TIMED(GPT2_PROF_OTHER, 4 * act, k::column_sum<T>(dbig, BT, 4 * C, Gf(m, p.fcb), st));
         TRY(mm<T>(m, dbig, 4 * C, true, W<T>(m, p.fcw), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, 4 * C,
                   GPT2_EPI_STORE));
         TIMED(GPT2_PROF_LAYERNORM, 4 * act + stats,

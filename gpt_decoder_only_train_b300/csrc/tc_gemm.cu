@@ -100,8 +100,10 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
         return GPT2_ERR_BAD_ARG;
     if (g.epi == GPT2_EPI_GELU && (!g.D2 || !aligned16(g.D2))) return GPT2_ERR_BAD_ARG;
     if (g.bias && (reinterpret_cast<uintptr_t>(g.bias) & 15)) return GPT2_ERR_BAD_ARG;
+    if (g.dbias && (reinterpret_cast<uintptr_t>(g.dbias) & 7)) return GPT2_ERR_BAD_ARG;
 
     const int BN = g.N >= 256 ? 256 : (g.N > 64 ? 128 : 64);
+    if (g.dbias && g.epi != GPT2_EPI_ACCUM_F32 && BN < 128) return GPT2_ERR_UNSUPPORTED;  // staged epilogue only
     // CTA pairs on 256 x 256 tiles (cta_group::2): each SM reads half of the B
     // tile per stage, which keeps shared-memory traffic per MMA within what the
     // SM delivers, at the cost of pair synchronisation per tile.  Measured on
@@ -156,6 +158,7 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     P.epi = g.epi;
     P.alpha = g.alpha;
     P.bias = g.bias;
+    P.dbias = g.epi == GPT2_EPI_ACCUM_F32 ? nullptr : g.dbias;
     P.R = g.R;
     P.D = g.D;
     P.D2 = g.D2;

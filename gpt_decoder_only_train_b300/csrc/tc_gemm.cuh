@@ -49,6 +49,7 @@ struct Params {
     float alpha;
     const float *bias;
     const bf16 *R;
+    float *dbias;  // optional: += column sums of the stored bf16 output (bias gradient of the product)
     void *D;
     bf16 *D2;
     int64_t ldd;
@@ -502,6 +503,22 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, const CUtensor
         tma_store_2d(tmD, stage, col0, row0);
         bulk_commit();
     }
+    if (P.dbias) {
+        // column sums of the stored (rounded) block: lane l reads columns 2l, 2l + 1 of each
+        // of the warp's rows (rows at or past M excluded) and adds them to the bias gradient
+        F2 cs = f2(0.f, 0.f);
+        const int nrows = min(32, P.M - row0);
+#pragma unroll 4
+        for (int r = 0; r < nrows; ++r) {
+            const uint32_t wv = *reinterpret_cast<const uint32_t *>(
+                stage + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) | ((lane & 3) << 2)));
+            cs = f2_add(cs, f2(bf16_lo(wv), bf16_hi(wv)));
+        }
+        const int c = col0 + 2 * lane;
+        if (c < P.N)
+            asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(P.dbias + c), "f"(f2_lo(cs)), "f"(f2_hi(cs))
+                         : "memory");
+    }
     if (P.epi == GPT2_EPI_GELU) {
         // GELU of the bf16-rounded pre-activation (a recompute from stored h matches bit for bit)
 #pragma unroll
@@ -841,6 +858,7 @@ struct GemmDesc {
     int epi;
     float alpha;  // acc is scaled by alpha before the epilogue
     int *err;
+    float *dbias = nullptr;  // bf16 epilogues: += column sums of the stored output (8-aligned fp32)
 };
 
 int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream);
