@@ -85,6 +85,9 @@ _SIGS = {
     "gpt2_embedding_backward_workspace": (ctypes.c_size_t, [_I, _I, _I]),
     "gpt2_debug_set_barrier_wait": (_I, [ctypes.c_ulonglong, _I]),
     "gpt2_set_graphs": (_I, [_P, _I]),
+    "gpt2_op_quantize_e4m3_rows": (_I, [_P, _I64, _I, _I, _P, _I64, _P, _P]),
+    "gpt2_op_quantize_e4m3_tensor": (_I, [_P, _I64, _P, _P, _P, _P]),
+    "gpt2_op_matmul_e4m3": (_I, [_P, _I64, _P, _P, _I64, _P, _P, _P, _P, _I64, _P, _I, _I, _I, _I, _P]),
 }
 
 
@@ -348,3 +351,22 @@ def embedding_backward(dx, tokens, dwte, dwpe, B, T, C, V, workspace=None, strea
 def set_barrier_wait(wait_ns: int = 0, never_arrive: bool = False):
     """Test hook: time limit of the clip + AdamW grid barrier (0: default) and an unreachable barrier."""
     check("gpt2_debug_set_barrier_wait", lib().gpt2_debug_set_barrier_wait(int(wait_ns), int(bool(never_arrive))))
+
+
+def quantize_e4m3_rows(x, q, row_inv, M, K, stream=None):
+    """Per-row E4M3 codes of bf16 x [M, K] into uint8 q [M, K] and fp32 row_inv [M]."""
+    check("gpt2_op_quantize_e4m3_rows", lib().gpt2_op_quantize_e4m3_rows(
+        _ptr(x), x.stride(0), M, K, _ptr(q), q.stride(0), _ptr(row_inv), _stream(stream)))
+
+
+def quantize_e4m3_tensor(x, q, inv, work, stream=None):
+    """Per-tensor E4M3 codes of bf16 x into uint8 q and fp32 inv [1]; work: one int32 of scratch."""
+    check("gpt2_op_quantize_e4m3_tensor", lib().gpt2_op_quantize_e4m3_tensor(
+        _ptr(x), x.numel(), _ptr(q), _ptr(inv), _ptr(work), _stream(stream)))
+
+
+def matmul_e4m3(A, a_inv, B, b_inv, D, M, N, K, epilogue=EPI_STORE, D2=None, R=None, bias=None, stream=None):
+    """D = a_inv[m] b_inv sum_k A(m,k) B(n,k) (E4M3 codes, K-major) with a bf16 epilogue."""
+    check("gpt2_op_matmul_e4m3", lib().gpt2_op_matmul_e4m3(
+        _ptr(A), A.stride(0), _ptr(a_inv), _ptr(B), B.stride(0), _ptr(b_inv), _ptr(D), _ptr(D2), _ptr(R),
+        D.stride(0), _ptr(bias), M, N, K, epilogue, _stream(stream)))

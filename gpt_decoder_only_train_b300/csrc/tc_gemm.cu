@@ -18,28 +18,31 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map with 128-byte swizzle; OOB elements read as zero.
-int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld_elems, uint32_t box_inner,
-                uint32_t box_outer) {
+// 2-D tensor map with 128-byte swizzle (bf16, or bytes for E4M3); OOB elements read as zero.
+static int encode_tmap_t(CUtensorMap *tm, CUtensorMapDataType dt, uint32_t esize, const void *ptr, uint64_t inner,
+                         uint64_t outer, uint64_t ld_elems, uint32_t box_inner, uint32_t box_outer) {
     auto fn = encode_fn();
     if (!fn) return GPT2_ERR_CUDA;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {ld_elems * 2};
+    cuuint64_t strides[1] = {ld_elems * esize};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(tm, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GPT2_OK : GPT2_ERR_CUDA;
+}
+int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld_elems, uint32_t box_inner,
+                uint32_t box_outer) {
+    return encode_tmap_t(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, inner, outer, ld_elems, box_inner, box_outer);
 }
 
 // units: work units (tiles x splits); the grid is one CTA per SM (or one pair
 // of CTAs per two SMs) up to that count.
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR>
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR, bool F8 = false>
 static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td, const CUtensorMap &td2,
                       const Params &P, int units, int num_sms, cudaStream_t st) {
     using Lay = SmemLayout<BN, STAGES, PAIR>;
-    auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, PAIR>;
+    auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, PAIR, F8>;
     static PerDevice attr_pd, pairs_pd;
     int unused = 0;
     if (int rc = per_device(attr_pd, unused, [&](int &v) -> int {
@@ -94,6 +97,12 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPT2_ERR_BAD_SHAPE;
     if (!g.A || !g.B || !g.D) return GPT2_ERR_BAD_ARG;
     if ((g.lda % 8) || (g.ldb % 8) || (g.ldd % 8) || (g.N % 8)) return GPT2_ERR_BAD_SHAPE;
+    if (g.fp8 && (!g.a_kmajor || !g.b_kmajor || g.lda % 16 || g.ldb % 16 || g.N < 128 ||
+                  g.epi == GPT2_EPI_ACCUM_F32 || g.epi == GPT2_EPI_GELU_BWD))
+        return GPT2_ERR_UNSUPPORTED;  // E4M3: K-major operands, 16-byte rows, bf16 forward epilogues
+    if ((g.a_scale && (reinterpret_cast<uintptr_t>(g.a_scale) & 3)) ||
+        (g.b_scale && (reinterpret_cast<uintptr_t>(g.b_scale) & 3)))
+        return GPT2_ERR_BAD_ARG;
     if (!aligned16(g.A) || !aligned16(g.B) || !aligned16(g.D)) return GPT2_ERR_BAD_ARG;
     if (g.epi < GPT2_EPI_STORE || g.epi > GPT2_EPI_ACCUM_F32) return GPT2_ERR_BAD_ARG;
     if ((g.epi == GPT2_EPI_RESIDUAL || g.epi == GPT2_EPI_GELU_BWD) && (!g.R || !aligned16(g.R)))
@@ -123,7 +132,7 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     P.K = g.K;
     P.num_m_blocks = ceil_div(g.M, pair ? 2 * BM : BM);
     P.num_n_blocks = ceil_div(g.N, BN);
-    P.num_k_blocks = ceil_div(g.K, BK);
+    P.num_k_blocks = ceil_div(g.K, g.fp8 ? 2 * BK : BK);
     P.splits = 1;
     if (g.epi == GPT2_EPI_ACCUM_F32) {
         // Split K (partial products are added into D) so that the work units
@@ -159,6 +168,8 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     P.alpha = g.alpha;
     P.bias = g.bias;
     P.dbias = g.epi == GPT2_EPI_ACCUM_F32 ? nullptr : g.dbias;
+    P.a_scale = g.a_scale;
+    P.b_scale = g.b_scale;
     P.R = g.R;
     P.D = g.D;
     P.D2 = g.D2;
@@ -166,11 +177,19 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     P.err = g.err;
 
     CUtensorMap ta, tb;
-    int rc = g.a_kmajor ? encode_tmap(&ta, g.A, g.K, g.M, g.lda, 64, BM) : encode_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64);
-    if (rc) return rc;
-    rc = g.b_kmajor ? encode_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, pair ? BN / 2 : BN)
-                    : encode_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64);
-    if (rc) return rc;
+    int rc;
+    if (g.fp8) {  // bytes: 128 E4M3 values per 128-byte k-block row
+        rc = encode_tmap_t(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.A, g.K, g.M, g.lda, 128, BM);
+        if (rc) return rc;
+        rc = encode_tmap_t(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B, g.K, g.N, g.ldb, 128, pair ? BN / 2 : BN);
+        if (rc) return rc;
+    } else {
+        rc = g.a_kmajor ? encode_tmap(&ta, g.A, g.K, g.M, g.lda, 64, BM) : encode_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64);
+        if (rc) return rc;
+        rc = g.b_kmajor ? encode_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, pair ? BN / 2 : BN)
+                        : encode_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64);
+        if (rc) return rc;
+    }
 
     // bf16 outputs leave through TMA stores from the epilogue's staging blocks (box 64 x 32)
     CUtensorMap td = ta, td2 = ta;  // unused copies when there is no bf16 output
@@ -183,6 +202,15 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     // epilogues with a second staging block per warp (the prefetched operand, or the GELU
     // output) trade a ring stage for it; the model uses them with K-major A only
     const bool two_bufs = (reads_r || g.epi == GPT2_EPI_GELU) && !a_mn;
+    if (g.fp8) {  // E4M3 operands: K-major, BN 256 (pairs or single CTAs) or 128
+        if (BN == 256 && pair)
+            return two_bufs ? launch_one<256, 5, false, false, true, true>(ta, tb, td, td2, P, num_work, num_sms, stream)
+                            : launch_one<256, 6, false, false, true, true>(ta, tb, td, td2, P, num_work, num_sms, stream);
+        if (BN == 256)
+            return two_bufs ? launch_one<256, 3, false, false, false, true>(ta, tb, td, td2, P, num_work, num_sms, stream)
+                            : launch_one<256, 4, false, false, false, true>(ta, tb, td, td2, P, num_work, num_sms, stream);
+        return launch_one<128, 6, false, false, false, true>(ta, tb, td, td2, P, num_work, num_sms, stream);
+    }
     if (BN == 256 && pair) {
         if (two_bufs)
             return b_mn ? launch_one<256, 5, false, true, true>(ta, tb, td, td2, P, num_work, num_sms, stream)

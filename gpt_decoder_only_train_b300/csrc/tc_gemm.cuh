@@ -50,6 +50,8 @@ struct Params {
     const float *bias;
     const bf16 *R;
     float *dbias;  // optional: += column sums of the stored bf16 output (bias gradient of the product)
+    const float *a_scale;  // optional: per-row factor of acc (E4M3 operands: row dequantisation of A)
+    const float *b_scale;  // optional: one factor of acc (E4M3 operands: dequantisation of B)
     void *D;
     bf16 *D2;
     int64_t ldd;
@@ -213,17 +215,30 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
-// Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B,
-// operand majorness, N >> 3 and M >> 4.
-__host__ __device__ constexpr uint32_t instr_desc(int bn, bool a_mn, bool b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor: fp32 accumulator (bit 4), A and B formats (bits 7-9,
+// 10-12: 1 = bf16 for kind::f16, 0 = E4M3 for kind::f8f6f4), operand
+// majorness, N >> 3 and M >> 4.
+__host__ __device__ constexpr uint32_t instr_desc(int bn, bool a_mn, bool b_mn, bool f8 = false) {
+    return (1u << 4) | ((f8 ? 0u : 1u) << 7) | ((f8 ? 0u : 1u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
 // Instruction descriptor for a CTA-pair MMA (cta_group::2): M = 256.
-__host__ __device__ constexpr uint32_t instr_desc_pair(int bn, bool a_mn, bool b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-           ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+__host__ __device__ constexpr uint32_t instr_desc_pair(int bn, bool a_mn, bool b_mn, bool f8 = false) {
+    return (1u << 4) | ((f8 ? 0u : 1u) << 7) | ((f8 ? 0u : 1u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+// E4M3 x E4M3 -> fp32 MMAs (kind::f8f6f4, K = 32 per instruction: the same
+// 32 bytes of each operand row as a bf16 MMA with K = 16)
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // ---- CTA pairs (cluster of two, cta_group::2) ------------------------------------
@@ -247,6 +262,15 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *t
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -318,9 +342,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // 32 accumulator columns of one row -> global memory.
 __device__ __forceinline__ void epilogue_chunk(const Params &P, int row, int col0, const uint32_t (&r)[32]) {
     if (row >= P.M) return;
+    float fac = P.alpha;
+    if (P.a_scale) fac *= P.a_scale[row];
+    if (P.b_scale) fac *= *P.b_scale;
     float acc[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(r[i]) * P.alpha;
+    for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(r[i]) * fac;
     if (P.epi == GPT2_EPI_ACCUM_F32) {
         float *D = reinterpret_cast<float *>(P.D) + (int64_t)row * P.ldd;
 #pragma unroll
@@ -449,8 +476,11 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, const CUtensor
         x[i] = f2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
         x[16 + i] = f2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
     }
-    if (P.alpha != 1.0f) {
-        const F2 al = f2(P.alpha, P.alpha);
+    if (P.alpha != 1.0f || P.a_scale || P.b_scale) {
+        float fac = P.alpha;
+        if (P.a_scale) fac *= P.a_scale[min(row0 + lane, P.M - 1)];
+        if (P.b_scale) fac *= *P.b_scale;
+        const F2 al = f2(fac, fac);
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = f2_mul(x[i], al);
     }
@@ -551,12 +581,16 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, const CUtensor
 // issues the cta_group::2 MMAs for both, each CTA loads its own 128 rows of A
 // and BN / 2 rows of B (completions counted on the even CTA's barriers) and
 // runs the epilogue of its own 128 rows.
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR = false>
+// F8: E4M3 operands (K-major only); a k-block is then 128 elements (the same
+// 128-byte rows), and the MMAs are kind::f8f6f4.
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR = false, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2, const Params P) {
     using Lay = SmemLayout<BN, STAGES, PAIR>;
-    constexpr uint32_t IDESC = PAIR ? instr_desc_pair(BN, A_MN, B_MN) : instr_desc(BN, A_MN, B_MN);
+    static_assert(!F8 || (!A_MN && !B_MN), "E4M3 operands are K-major");
+    constexpr uint32_t IDESC = PAIR ? instr_desc_pair(BN, A_MN, B_MN, F8) : instr_desc(BN, A_MN, B_MN, F8);
+    constexpr int BK_E = F8 ? 2 * BK : BK;  // elements of K per 128-byte k-block row
     constexpr uint32_t TMEM_COLS = 2 * BN;
     constexpr int TM = PAIR ? 2 * BM : BM;        // rows of a tile
     constexpr int BN_CTA = PAIR ? BN / 2 : BN;    // rows of B this CTA loads per stage
@@ -630,7 +664,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     uint8_t *a_dst = smem + stage * Lay::STAGE_BYTES;
                     uint8_t *b_dst = a_dst + A_STAGE_BYTES;
-                    const int k0 = kb * BK;
+                    const int k0 = kb * BK_E;
                     if constexpr (PAIR) {
                         // both CTAs' bytes are counted on the even CTA's barrier, which it arms
                         if (rank == 0) mbar_expect_tx(&full[stage], 2 * Lay::STAGE_BYTES);
@@ -710,10 +744,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                  : smem_desc(a_addr + j * 32, 16, 1024);
                         const uint64_t bd = B_MN ? smem_desc(b_addr + j * 2048, MN_BLOCK_BYTES, 1024)
                                                  : smem_desc(b_addr + j * 32, 16, 1024);
-                        if constexpr (PAIR)
-                            tc_mma_pair(d_tmem, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+                        const uint32_t accum = (kb > kb0 || j > 0) ? 1u : 0u;
+                        if constexpr (PAIR && F8)
+                            tc_mma_pair_f8(d_tmem, ad, bd, IDESC, accum);
+                        else if constexpr (PAIR)
+                            tc_mma_pair(d_tmem, ad, bd, IDESC, accum);
+                        else if constexpr (F8)
+                            tc_mma_f8(d_tmem, ad, bd, IDESC, accum);
                         else
-                            tc_mma(d_tmem, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+                            tc_mma(d_tmem, ad, bd, IDESC, accum);
                     }
                     if constexpr (PAIR)
                         tc_commit_pair(&empty[stage], 3);
@@ -859,6 +898,11 @@ struct GemmDesc {
     float alpha;  // acc is scaled by alpha before the epilogue
     int *err;
     float *dbias = nullptr;  // bf16 epilogues: += column sums of the stored output (8-aligned fp32)
+    // E4M3 operands (A and B K-major, bytes; lda / ldb multiples of 16): acc is
+    // scaled by alpha * a_scale[row] (if given) * b_scale[0] (if given)
+    bool fp8 = false;
+    const float *a_scale = nullptr;
+    const float *b_scale = nullptr;
 };
 
 int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream);

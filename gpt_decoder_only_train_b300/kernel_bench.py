@@ -9,6 +9,7 @@
     python -m gpt_decoder_only_train_b300.kernel_bench generate --B 16 --prompt 32 --new 64 --top-k 50
     python -m gpt_decoder_only_train_b300.kernel_bench attention-fb --B 64 --T 1024 --H 12
     python -m gpt_decoder_only_train_b300.kernel_bench adamw
+    python -m gpt_decoder_only_train_b300.kernel_bench matmul --M 16384 --N 3072 --K 768 --epi gelu --fp8
 
 Inputs are seeded random bf16 on the device; each line reports the mean time
 per launch (CUDA events, after warm-up) and the algorithmic FLOP/s or bytes/s.
@@ -42,7 +43,35 @@ def _time(fn, iters, warmup):
     return e0.elapsed_time(e1) / iters
 
 
+def bench_matmul_fp8(a):
+    """E4M3 operands (row-scaled A, tensor-scaled B, both K-major), bf16 epilogue."""
+    M, N, K = a.M, a.N, a.K
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    A = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda", generator=gen).to(torch.bfloat16)
+    qa = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    qb = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+    ainv = torch.empty(M, device="cuda")
+    binv = torch.empty(1, device="cuda")
+    work = torch.empty(1, dtype=torch.int32, device="cuda")
+    g.quantize_e4m3_rows(A, qa, ainv, M, K)
+    g.quantize_e4m3_tensor(B, qb, binv, work)
+    epi = EPIS[a.epi]
+    D = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    D2 = torch.empty_like(D) if epi == g.EPI_GELU else None
+    R = torch.randn(M, N, device="cuda", generator=gen).to(torch.bfloat16) if epi == g.EPI_RESIDUAL else None
+    bias = torch.randn(N, device="cuda", generator=gen)
+    ms = _time(lambda i: g.matmul_e4m3(qa, ainv, qb, binv, D, M, N, K, epilogue=epi, D2=D2, R=R, bias=bias),
+               a.iters, a.warmup)
+    qms = _time(lambda i: g.quantize_e4m3_rows(A, qa, ainv, M, K), a.iters, a.warmup)
+    return {"op": "matmul_e4m3", "M": M, "N": N, "K": K, "epi": a.epi, "ms": ms,
+            "TFLOP/s": 2.0 * M * N * K / ms / 1e9, "quantize_rows_ms": qms,
+            "quantize_rows_GB/s": (3.0 * M * K + 4 * M) / qms / 1e6}
+
+
 def bench_matmul(a):
+    if getattr(a, "fp8", False):
+        return bench_matmul_fp8(a)
     M, N, K = a.M, a.N, a.K
     gen = torch.Generator(device="cuda").manual_seed(0)
     A = torch.randn(K if a.a_mn else M, M if a.a_mn else K, device="cuda", generator=gen).to(torch.bfloat16)
@@ -191,6 +220,7 @@ def main(argv=None):
     ap.add_argument("--a-mn", action="store_true")
     ap.add_argument("--b-mn", action="store_true")
     ap.add_argument("--epi", default="store", choices=sorted(EPIS))
+    ap.add_argument("--fp8", action="store_true", help="matmul: E4M3 operands (K-major) instead of bf16")
     ap.add_argument("--B", type=int, default=16)
     ap.add_argument("--T", type=int, default=1024)
     ap.add_argument("--H", type=int, default=12)

@@ -352,6 +352,39 @@ int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const void *B, int6
                    void *D2, const void *R, int64_t ldd, const float *bias, int M, int N, int K, int epilogue,
                    void *stream);
 
+/* ---- E4M3 (FP8) matmul -------------------------------------------------------
+ * The pages name FP8 as the next precision step of this training code ("llm.c
+ * kullanarak GPT-2 modelini düşük maliyetle yeniden uygulamak", §SSS; the
+ * "PyTorch Howsam" post on llm.c) and fix no format.  Format: E4M3 of the OCP
+ * 8-bit floating point specification (largest finite 448), converted with
+ * round to nearest even and saturation.  Codes are uint8 device arrays.
+ *
+ * gpt2_op_quantize_e4m3_rows: x bf16 [M, K] (row stride ldx) -> q [M, K]
+ * (row stride ldq) and row_inv fp32 [M]: row m is multiplied by
+ * s = 448 / amax_m (fp32) and rounded; it represents q * row_inv[m] with
+ * row_inv[m] = amax_m / 448 (1 and codes 0 for a row of zeros).  K, ldx, ldq
+ * multiples of 8; x and q 16-byte aligned.
+ *
+ * gpt2_op_quantize_e4m3_tensor: the same with one amax over x bf16 [n]
+ * (n a multiple of 8): q [n], inv fp32 [1].  d_amax_work: one device uint of
+ * caller-owned scratch (overwritten).
+ *
+ * gpt2_op_matmul_e4m3: D = a_row_inv[m] * b_inv[0] * sum_k A(m, k) B(n, k)
+ * with the epilogues GPT2_EPI_STORE (+ bias), GPT2_EPI_RESIDUAL (+ bias + R)
+ * or GPT2_EPI_GELU (D = h, D2 = gelu(h)), bf16 outputs; A [M, K] and B [N, K]
+ * E4M3 codes K-major (lda, ldb in bytes, multiples of 16), fp32
+ * accumulation in TMEM (tcgen05.mma kind::f8f6f4).  N >= 128 and a multiple
+ * of 8; other requirements as gpt2_op_matmul.  GPT2_ERR_UNSUPPORTED or
+ * GPT2_ERR_BAD_SHAPE otherwise.
+ */
+int gpt2_op_quantize_e4m3_rows(const void *x, int64_t ldx, int M, int K, uint8_t *q, int64_t ldq, float *row_inv,
+                               void *stream);
+int gpt2_op_quantize_e4m3_tensor(const void *x, int64_t n, uint8_t *q, float *inv, unsigned *d_amax_work,
+                                 void *stream);
+int gpt2_op_matmul_e4m3(const uint8_t *A, int64_t lda, const float *a_row_inv, const uint8_t *B, int64_t ldb,
+                        const float *b_inv, void *D, void *D2, const void *R, int64_t ldd, const float *bias, int M,
+                        int N, int K, int epilogue, void *stream);
+
 /*
  * The sampling rule of gpt2_generate on bf16 logits rows [B, ldl] (columns
  * [0, V) are the candidates): out[b] = the token drawn with uniforms[b].
