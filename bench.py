@@ -321,6 +321,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gpt2_124m", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="E4M3 block projections in the forward (fp8_forward); a separate line, not the headline")
     ap.add_argument("--attention-sweep", action="store_true",
                     help="time the isolated causal attention workload instead of the training step")
     args = ap.parse_args()
@@ -328,6 +330,8 @@ def main():
         attention_sweep(args)
         return
     w = dict(synthetic.WORKLOADS[args.workload])
+    if args.fp8:
+        w["fp8_forward"] = 1
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -448,7 +452,9 @@ def main():
         peak = peaks[peak_key]
         kernels = {}
         for cat, (cms, work, n) in prof.items():
-            unit = "TFLOP/s" if cat in ("matmul", "attention") else "GB/s"
+            if n == 0:
+                continue
+            unit = "TFLOP/s" if cat in ("matmul", "attention", "matmul_e4m3") else "GB/s"
             rate = (work / (cms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)) if cms > 0 else None
             kernels[cat] = {"ms_per_step": cms / args.steps, "launches_per_step": n / args.steps,
                             "achieved": rate, "unit": unit}
@@ -463,7 +469,7 @@ def main():
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": "bf16+e4m3" if args.fp8 else "bf16",
             "data": "synthetic Zipf(1.1) tokens over V=50257, random-init weights (seeded)",
             "config": {"workload": workload_label(args.workload, w, accum), "global_batch": B * accum * world,
                        "seq_len": T,
@@ -493,7 +499,21 @@ def main():
             "clocks": clocks,
             "loss_first_last": [losses[0], losses[-1]],
         }
-        if not args.no_cpu_baseline:
+        if args.fp8:
+            # E4M3 operands run at twice the bf16 tensor rate (nominal 4.5 vs 2.25 PFLOP/s dense)
+            f8_ms, f8_flops, f8_n = prof["matmul_e4m3"]
+            f8_ach = f8_flops / (f8_ms / 1e3) / 1e12 if f8_ms > 0 else None
+            f8_peak = 2.0 * peak
+            line["config"]["precision"] = ("E4M3 QKV / attention-output / FC / FC-output products in the forward "
+                                           "(activations per row, weights per tensor); LM head, backward and "
+                                           "optimizer bf16/fp32")
+            line["roofline_e4m3"] = {
+                "kernel": "tcgen05 kind::f8f6f4 GEMM (the forward's block projections)", "bound": "tensor",
+                "achieved": f8_ach, "peak": f8_peak, "unit": "TFLOP/s",
+                "frac": (f8_ach / f8_peak) if f8_ach else None,
+                "peak_source": "%s %s x 2 (nominal E4M3 / bf16 dense ratio)" % (peak_src, peak_key),
+                "launches_per_step": f8_n / args.steps}
+        if not (args.no_cpu_baseline or args.fp8):  # the oracle's step is the bf16 headline's baseline
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
     if dist is not None:

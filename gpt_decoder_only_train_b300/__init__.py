@@ -40,7 +40,8 @@ class Gpt2Error(RuntimeError):
 
 
 class gpt2_config(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int) for n in ("L", "C", "H", "V", "Vp", "T", "B", "dtype", "recompute_gelu")]
+    _fields_ = [(n, ctypes.c_int)
+                for n in ("L", "C", "H", "V", "Vp", "T", "B", "dtype", "recompute_gelu", "fp8_forward")]
 
 
 _lib = None
@@ -126,7 +127,8 @@ def _stream(stream=None):
 def make_config(d: dict) -> gpt2_config:
     dt = d.get("dtype", "bf16")
     dtype = GPT2_DTYPE_BF16 if dt in ("bf16", GPT2_DTYPE_BF16) else GPT2_DTYPE_FP32
-    return gpt2_config(d["L"], d["C"], d["H"], d["V"], d["Vp"], d["T"], d["B"], dtype, int(d.get("recompute_gelu", 0)))
+    return gpt2_config(d["L"], d["C"], d["H"], d["V"], d["Vp"], d["T"], d["B"], dtype, int(d.get("recompute_gelu", 0)),
+                       int(d.get("fp8_forward", 0)))
 
 
 def launch_count() -> int:
@@ -238,7 +240,7 @@ class GPT2:
         check("gpt2_adam_step", lib().gpt2_adam_step(self.handle, ctypes.byref(t)))
         return t.value
 
-    PROF_CATEGORIES = ("matmul", "attention", "classifier", "adamw", "layernorm", "other")
+    PROF_CATEGORIES = ("matmul", "attention", "classifier", "adamw", "layernorm", "other", "matmul_e4m3")
 
     def profile(self, enable: bool):
         """Start (clearing totals) or stop per-launch CUDA-event timing of model calls."""

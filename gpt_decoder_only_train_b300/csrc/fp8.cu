@@ -8,17 +8,14 @@
 // saturation.  Scaling: per row for activations and per tensor for weights,
 // by s = 448 / amax computed in fp32, the element scaled by one fp32
 // multiply; the dequantisation factor amax / 448 is kept beside the codes.
-#include <cuda_fp8.h>
-
+#include "kernels.cuh"
 #include "tc_gemm.cuh"
 
 namespace {
 
 constexpr float E4M3_MAX = 448.0f;
 
-__device__ __forceinline__ uint8_t to_e4m3(float x) {
-    return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-}
+__device__ __forceinline__ uint32_t to_e4m3(float x) { return k::e4m3_of(x); }
 
 // One warp per row: amax of the row, then the codes of x * (448 / amax).
 __global__ void quantize_rows_kernel(const bf16 *__restrict__ x, int64_t ldx, int M, int K, uint8_t *__restrict__ q,
@@ -90,6 +87,50 @@ __global__ void quantize_tensor_kernel(const bf16 *__restrict__ x, int64_t n, co
     if (blockIdx.x == 0 && threadIdx.x == 0) *inv = amax > 0.f ? amax / E4M3_MAX : 1.0f;
 }
 
+// Several tensors of one flat bf16 array, one amax each: block (x, t) covers a
+// chunk of tensor t.
+__global__ void amax_multi_kernel(const bf16 *__restrict__ w, const int64_t *__restrict__ off,
+                                  const int64_t *__restrict__ n, unsigned *__restrict__ amax_bits) {
+    const int t = blockIdx.y;
+    const int64_t n8 = n[t] / 8;
+    const uint4 *src = reinterpret_cast<const uint4 *>(w + off[t]);
+    float m = 0.f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 u = src[i];
+        const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m = fmaxf(m, fmaxf(fabsf(bf16_lo(ww[k])), fabsf(bf16_hi(ww[k]))));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0) atomicMax(amax_bits + t, __float_as_uint(m));
+}
+
+__global__ void quantize_multi_kernel(const bf16 *__restrict__ w, const int64_t *__restrict__ off,
+                                      const int64_t *__restrict__ n, const unsigned *__restrict__ amax_bits,
+                                      uint8_t *__restrict__ q, float *__restrict__ inv) {
+    const int t = blockIdx.y;
+    const int64_t n8 = n[t] / 8;
+    const uint4 *src = reinterpret_cast<const uint4 *>(w + off[t]);
+    uint2 *dst = reinterpret_cast<uint2 *>(q + off[t]);
+    const float amax = __uint_as_float(amax_bits[t]);
+    const float s = amax > 0.f ? E4M3_MAX / amax : 1.0f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 u = src[i];
+        const uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t pair = to_e4m3(bf16_lo(ww[k]) * s) | (to_e4m3(bf16_hi(ww[k]) * s) << 8);
+            if (k < 2)
+                lo |= pair << (16 * k);
+            else
+                hi |= pair << (16 * (k - 2));
+        }
+        dst[i] = make_uint2(lo, hi);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) inv[t] = amax > 0.f ? amax / E4M3_MAX : 1.0f;
+}
+
 int sms_of_current_device() {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -155,3 +196,28 @@ extern "C" int gpt2_op_matmul_e4m3(const uint8_t *A, int64_t lda, const float *a
     g.b_scale = b_inv;
     return tcg::launch_gemm_tc(g, sms_of_current_device(), (cudaStream_t)stream);
 }
+
+namespace k {
+
+int quantize_rows_e4m3(const bf16 *x, int64_t ldx, int M, int K, uint8_t *q, int64_t ldq, float *inv,
+                       cudaStream_t st) {
+    if (M <= 0 || K <= 0 || K % 8 || ldx % 8 || ldq % 8) return GPT2_ERR_BAD_SHAPE;
+    quantize_rows_kernel<<<ceil_div(M, 8), 256, 0, st>>>(x, ldx, M, K, q, ldq, inv);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
+int quantize_tensors_e4m3(const bf16 *w, const int64_t *d_off, const int64_t *d_n, int ntens, int64_t max_n,
+                          uint8_t *q, float *inv, unsigned *amax_bits, cudaStream_t st) {
+    if (ntens <= 0) return GPT2_OK;
+    GPT2_CUDA_TRY(cudaMemsetAsync(amax_bits, 0, sizeof(unsigned) * ntens, st));
+    const dim3 grid((unsigned)std::max<int64_t>(1, std::min<int64_t>(64, (max_n / 8 + 255) / 256)), (unsigned)ntens);
+    amax_multi_kernel<<<grid, 256, 0, st>>>(w, d_off, d_n, amax_bits);
+    quantize_multi_kernel<<<grid, 256, 0, st>>>(w, d_off, d_n, amax_bits, q, inv);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(2);
+    return GPT2_OK;
+}
+
+}  // namespace k

@@ -90,6 +90,15 @@ struct gpt2_model {
     int64_t n_params, n_decay;
     float *params, *grads, *adam_m, *adam_v;
     bf16 *wbf;  // bf16 copy of the weights (bf16 mode)
+    // E4M3 forward (fp8_forward): codes of the four projection weights of every
+    // block (same offsets as the parameters), one dequantisation factor per
+    // tensor, and one activation code buffer [B*T, 4C] with its row factors
+    uint8_t *w8, *a8;
+    float *w8_inv, *a8_inv;
+    unsigned *w8_amax;
+    int64_t *w8_off, *w8_n;  // device tables over the quantised tensors
+    std::vector<int> w8_ids;  // tensor ids of the quantised tensors, in table order
+    int64_t w8_maxn;
     std::vector<LayerBuf> layers;
     void *resid_final, *lnf;
     float *lnf_mean, *lnf_rstd;
@@ -149,6 +158,8 @@ bool valid_config(const gpt2_config &c) {
     if (c.L <= 0 || c.C <= 0 || c.H <= 0 || c.V <= 0 || c.Vp < c.V || c.T <= 0 || c.B <= 0) return false;
     if (c.C % c.H) return false;
     if (c.dtype != GPT2_DTYPE_FP32 && c.dtype != GPT2_DTYPE_BF16) return false;
+    if (c.fp8_forward != 0 && c.fp8_forward != 1) return false;
+    if (c.fp8_forward && (c.dtype != GPT2_DTYPE_BF16 || c.C < 128)) return false;
     const int hd = c.C / c.H;
     if (c.dtype == GPT2_DTYPE_FP32) {
         if (c.C % 4 || c.Vp % 4 || (hd != 8 && hd != 16 && hd != 32 && hd != 64)) return false;
@@ -224,6 +235,15 @@ void plan(gpt2_model &m, uint8_t *base) {
     m.adam_m = b.take<float>(m.n_params * 4);
     m.adam_v = b.take<float>(m.n_params * 4);
     m.wbf = take_opt<bf16>(b, bf, m.n_params * 2);
+    const bool f8 = c.fp8_forward != 0;
+    const size_t nq = f8 ? (size_t)4 * c.L : 0;
+    m.w8 = take_opt<uint8_t>(b, f8, m.n_params);
+    m.a8 = take_opt<uint8_t>(b, f8, BT * 4 * C);
+    m.a8_inv = take_opt<float>(b, f8, BT * 4);
+    m.w8_inv = take_opt<float>(b, f8, nq * 4);
+    m.w8_amax = take_opt<unsigned>(b, f8, nq * 4);
+    m.w8_off = take_opt<int64_t>(b, f8, nq * 8);
+    m.w8_n = take_opt<int64_t>(b, f8, nq * 8);
     m.layers.assign(c.L, LayerBuf{});
     for (int l = 0; l < c.L; ++l) {
         LayerBuf &y = m.layers[l];
@@ -394,6 +414,45 @@ int mm(gpt2_model *m, const void *A, int64_t lda, bool a_km, const void *B, int6
     }
 }
 
+// E4M3 product for the forward projections: D = a8_inv[m] w8_inv[slot] (A8 B8^T) + bias, with
+// the bf16 epilogue `epi` (both operands K-major byte rows).
+int mm8(gpt2_model *m, const uint8_t *A8, int64_t lda, const float *a_inv, int w_id, int slot, void *D, void *D2,
+        const void *R, int64_t ldd, const float *bias, int M, int N, int K, int epi) {
+    tcg::GemmDesc g;
+    g.A = (const bf16 *)A8;
+    g.lda = lda;
+    g.a_kmajor = true;
+    g.B = (const bf16 *)(m->w8 + m->tensors[w_id].offset);
+    g.ldb = K;
+    g.b_kmajor = true;
+    g.D = D;
+    g.D2 = (bf16 *)D2;
+    g.R = (const bf16 *)R;
+    g.ldd = ldd;
+    g.bias = bias;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.epi = epi;
+    g.alpha = 1.0f;
+    g.err = m->err_dev;
+    g.fp8 = true;
+    g.a_scale = a_inv;
+    g.b_scale = m->w8_inv + slot;
+    return timed(m, GPT2_PROF_MATMUL_E4M3, 2.0 * M * N * K, [&] { return tcg::launch_gemm_tc(g, m->num_sms, m->stream); });
+}
+
+// Refresh the E4M3 weight codes from the bf16 weight copy (one amax per tensor).
+int quantize_weights(gpt2_model *m) {
+    if (!m->w8) return GPT2_OK;
+    double n = 0;
+    for (int id : m->w8_ids) n += (double)m->tensors[id].numel;
+    return timed(m, GPT2_PROF_OTHER, 5.0 * n, [&] {  // bf16 read twice (amax, codes), one code byte written
+        return k::quantize_tensors_e4m3(m->wbf, m->w8_off, m->w8_n, (int)m->w8_ids.size(), m->w8_maxn, m->w8,
+                                        m->w8_inv, m->w8_amax, m->stream);
+    });
+}
+
 // algorithmic FLOP of causal attention forward: 4 hd per causal (i, j) pair
 inline double attn_flops(int B, int Tn, int H, int hd) { return 4.0 * hd * (0.5 * Tn * (Tn + 1.0)) * B * H; }
 
@@ -423,6 +482,38 @@ int attn_bwd(gpt2_model *m, const T *qkv, const T *o, const T *dout, const float
 }
 
 // ---- forward ----------------------------------------------------------------------
+// One transformer block with E4M3 projections.  The LayerNorms write the E4M3
+// codes of their bf16 output rows next to it; the attention output and GELU
+// output are quantised per row by a separate pass.  Every bf16 activation the
+// backward reads is still stored.
+int forward_block_e4m3(gpt2_model *m, int l, int BT, int B, int Tn, bf16 *next, bf16 *gbuf) {
+    const gpt2_config &c = m->cfg;
+    const int C = c.C;
+    cudaStream_t st = m->stream;
+    LayerBuf &y = m->layers[l];
+    const LayerParams &p = m->lp[l];
+    const double act = 2.0 * BT * C, stats = 8.0 * BT, codes = (double)BT * C + 4.0 * BT;
+    TIMED(GPT2_PROF_LAYERNORM, 2 * act + stats + codes,
+          k::layernorm_forward<bf16>((bf16 *)y.resid, Pf(m, p.ln1g), Pf(m, p.ln1b), (bf16 *)y.ln1, y.ln1_mean,
+                                     y.ln1_rstd, BT, C, st, m->a8, m->a8_inv));
+    TRY(mm8(m, m->a8, C, m->a8_inv, p.qkvw, 4 * l, y.qkv, nullptr, nullptr, 3 * C, Pf(m, p.qkvb), BT, 3 * C, C,
+            GPT2_EPI_STORE));
+    TRY(attn_fwd<bf16>(m, (bf16 *)y.qkv, (bf16 *)y.att, y.lse, B, Tn));
+    TIMED(GPT2_PROF_OTHER, act + codes, k::quantize_rows_e4m3((bf16 *)y.att, C, BT, C, m->a8, C, m->a8_inv, st));
+    TRY(mm8(m, m->a8, C, m->a8_inv, p.projw, 4 * l + 1, y.resid_mid, nullptr, y.resid, C, Pf(m, p.projb), BT, C, C,
+            GPT2_EPI_RESIDUAL));
+    TIMED(GPT2_PROF_LAYERNORM, 2 * act + stats + codes,
+          k::layernorm_forward<bf16>((bf16 *)y.resid_mid, Pf(m, p.ln2g), Pf(m, p.ln2b), (bf16 *)y.ln2, y.ln2_mean,
+                                     y.ln2_rstd, BT, C, st, m->a8, m->a8_inv));
+    TRY(mm8(m, m->a8, C, m->a8_inv, p.fcw, 4 * l + 2, y.fch, gbuf, nullptr, 4 * C, Pf(m, p.fcb), BT, 4 * C, C,
+            GPT2_EPI_GELU));
+    TIMED(GPT2_PROF_OTHER, 4 * (act + codes),
+          k::quantize_rows_e4m3(gbuf, 4 * C, BT, 4 * C, m->a8, 4 * C, m->a8_inv, st));
+    TRY(mm8(m, m->a8, 4 * C, m->a8_inv, p.fcprojw, 4 * l + 3, next, nullptr, y.resid_mid, C, Pf(m, p.fcprojb), BT,
+            C, 4 * C, GPT2_EPI_RESIDUAL));
+    return GPT2_OK;
+}
+
 template <typename T>
 int forward_impl(gpt2_model *m, bool with_targets, int B, int Tn) {
     const gpt2_config &c = m->cfg;
@@ -436,6 +527,12 @@ int forward_impl(gpt2_model *m, bool with_targets, int B, int Tn) {
         const LayerParams &p = m->lp[l];
         T *next = (T *)(l + 1 < c.L ? m->layers[l + 1].resid : m->resid_final);
         T *gbuf = (T *)(c.recompute_gelu ? m->gelu_buf : y.fcg);
+        if constexpr (sizeof(T) == 2) {
+            if (c.fp8_forward) {
+                TRY(forward_block_e4m3(m, l, BT, B, Tn, next, gbuf));
+                continue;
+            }
+        }
         TIMED(GPT2_PROF_LAYERNORM, 2 * act + stats,
               k::layernorm_forward<T>((T *)y.resid, Pf(m, p.ln1g), Pf(m, p.ln1b), (T *)y.ln1, y.ln1_mean, y.ln1_rstd,
                                       BT, C, st));
@@ -753,6 +850,23 @@ extern "C" int gpt2_build(const gpt2_config *cfg, uint64_t seed, void *dev_arena
         return fail(GPT2_ERR_CUDA);
     if (cudaMemsetAsync(m->grads, 0, m->n_params * 4 * 3, m->stream) != cudaSuccess) return fail(GPT2_ERR_CUDA);
     if (m->wbf && (rc = k::cast_f32_bf16(m->params, m->wbf, m->n_params, m->stream))) return fail(rc);
+    std::vector<int64_t> w8_tab;  // offsets then sizes of the E4M3 weight tensors (copied below)
+    if (m->w8) {
+        m->w8_maxn = 0;
+        for (const LayerParams &p : m->lp)
+            for (int id : {p.qkvw, p.projw, p.fcw, p.fcprojw}) {
+                m->w8_ids.push_back(id);
+                m->w8_maxn = std::max(m->w8_maxn, m->tensors[id].numel);
+            }
+        for (int id : m->w8_ids) w8_tab.push_back(m->tensors[id].offset);
+        for (int id : m->w8_ids) w8_tab.push_back(m->tensors[id].numel);
+        const size_t nb = m->w8_ids.size() * 8;
+        if (cudaMemcpyAsync(m->w8_off, w8_tab.data(), nb, cudaMemcpyHostToDevice, m->stream) != cudaSuccess ||
+            cudaMemcpyAsync(m->w8_n, w8_tab.data() + m->w8_ids.size(), nb, cudaMemcpyHostToDevice, m->stream) !=
+                cudaSuccess)
+            return fail(GPT2_ERR_CUDA);
+        if ((rc = quantize_weights(m))) return fail(rc);
+    }
     if (cudaMemsetAsync(m->err_dev, 0, 256, m->stream) != cudaSuccess) return fail(GPT2_ERR_CUDA);
     if (cudaStreamSynchronize(m->stream) != cudaSuccess) return fail(GPT2_ERR_CUDA);
     *out = m;
@@ -841,6 +955,7 @@ extern "C" int gpt2_clip_and_adamw(gpt2_model *m, float lr, float beta1, float b
           k::clip_adamw(m->params, m->grads, m->adam_m, m->adam_v, m->wbf, m->n_params, m->n_decay, a,
                         m->norm_partials, m->barrier, m->max_adam_blocks, m->norm_dev, m->err_dev, m->num_sms,
                         m->stream));
+    TRY(quantize_weights(m));
     GPT2_CUDA_TRY(cudaMemcpyAsync(grad_norm_out, m->norm_dev, 4, cudaMemcpyDeviceToHost, m->stream));
     int word = 0;
     TRY(read_error_word(m, word));
@@ -904,6 +1019,7 @@ extern "C" int gpt2_set_params(gpt2_model *m, int id, const float *host_in, size
     if (n < (size_t)t.numel) return GPT2_ERR_BAD_ARG;
     GPT2_CUDA_TRY(cudaMemcpyAsync(m->params + t.offset, host_in, t.numel * 4, cudaMemcpyHostToDevice, m->stream));
     if (m->wbf) TRY(k::cast_f32_bf16(m->params + t.offset, m->wbf + t.offset, t.numel, m->stream));
+    TRY(quantize_weights(m));
     GPT2_CUDA_TRY(cudaStreamSynchronize(m->stream));
     return GPT2_OK;
 }
@@ -936,10 +1052,20 @@ extern "C" int gpt2_debug_buffer(gpt2_model *m, const char *name, void **dev_ptr
     else if ((l = layer_of("qkv.", c.L)) >= 0) { *dev_ptr = m->layers[l].qkv; *bytes = BT * 3 * c.C * es; }
     else if ((l = layer_of("att.", c.L)) >= 0) { *dev_ptr = m->layers[l].att; *bytes = BT * c.C * es; }
     else if ((l = layer_of("lse.", c.L)) >= 0) { *dev_ptr = m->layers[l].lse; *bytes = (size_t)c.B * c.H * c.T * 4; }
+    else if ((l = layer_of("ln1.", c.L)) >= 0) { *dev_ptr = m->layers[l].ln1; *bytes = BT * c.C * es; }
+    else if ((l = layer_of("ln2.", c.L)) >= 0) { *dev_ptr = m->layers[l].ln2; *bytes = BT * c.C * es; }
+    else if ((l = layer_of("resid_mid.", c.L)) >= 0) { *dev_ptr = m->layers[l].resid_mid; *bytes = BT * c.C * es; }
+    else if ((l = layer_of("fch.", c.L)) >= 0) { *dev_ptr = m->layers[l].fch; *bytes = BT * 4 * c.C * es; }
     else if ((l = layer_of("resid.", c.L + 1)) >= 0) {
         *dev_ptr = l < c.L ? m->layers[l].resid : m->resid_final;
         *bytes = BT * c.C * es;
-    } else return GPT2_ERR_BAD_ARG;
+    } else if (m->w8 && (l = layer_of("w8.", (int)m->tensors.size())) >= 0) {
+        *dev_ptr = m->w8 + m->tensors[l].offset;
+        *bytes = (size_t)m->tensors[l].numel;
+    } else if (m->w8 && s == "w8_inv") { *dev_ptr = m->w8_inv; *bytes = m->w8_ids.size() * 4; }
+    else if (m->w8 && s == "a8") { *dev_ptr = m->a8; *bytes = BT * 4 * c.C; }
+    else if (m->w8 && s == "a8_inv") { *dev_ptr = m->a8_inv; *bytes = BT * 4; }
+    else return GPT2_ERR_BAD_ARG;
     return GPT2_OK;
 }
 

@@ -399,7 +399,8 @@ __device__ __forceinline__ uint32_t f2_bf16x2(F2 v) {
 template <int VPL>
 __global__ void ln_fwd_bf16_kernel(const bf16 *__restrict__ x, const float *__restrict__ g,
                                    const float *__restrict__ b, bf16 *__restrict__ y, float *__restrict__ mean,
-                                   float *__restrict__ rstd, int N, int C) {
+                                   float *__restrict__ rstd, int N, int C, uint8_t *__restrict__ q,
+                                   float *__restrict__ qinv) {
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= N) return;
@@ -418,7 +419,7 @@ __global__ void ln_fwd_bf16_kernel(const bf16 *__restrict__ x, const float *__re
     }
     const float mu = warp_sum(f2_lo(s) + f2_hi(s)) / C;
     const F2 nmu = f2(-mu, -mu);
-    F2 q = f2(0.f, 0.f);
+    F2 ss = f2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int p = lane + 32 * i;
@@ -427,11 +428,11 @@ __global__ void ln_fwd_bf16_kernel(const bf16 *__restrict__ x, const float *__re
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const F2 d = f2_add(bf16x2_f2(w[k]), nmu);
-                q = f2_fma(d, d, q);
+                ss = f2_fma(d, d, ss);
             }
         }
     }
-    const float rs = rsqrtf(warp_sum(f2_lo(q) + f2_hi(q)) / C + 1e-5f);
+    const float rs = rsqrtf(warp_sum(f2_lo(ss) + f2_hi(ss)) / C + 1e-5f);
     const F2 rs2 = f2(rs, rs);
     uint4 *yr = reinterpret_cast<uint4 *>(y + (int64_t)row * C);
 #pragma unroll
@@ -449,11 +450,47 @@ __global__ void ln_fwd_bf16_kernel(const bf16 *__restrict__ x, const float *__re
 #pragma unroll
             for (int k = 0; k < 4; ++k) o[k] = f2_bf16x2(f2_fma(f2_mul(f2_add(bf16x2_f2(w[k]), nmu), rs2), gk[k], bk[k]));
             yr[p] = make_uint4(o[0], o[1], o[2], o[3]);
+            v[i] = make_uint4(o[0], o[1], o[2], o[3]);  // the stored row, for the E4M3 copy
         }
     }
     if (lane == 0) {
         mean[row] = mu;
         rstd[row] = rs;
+    }
+    if (q) {
+        // E4M3 copy of the stored (bf16) row: s = 448 / amax in fp32, one multiply, saturating
+        // round to nearest even; qinv = amax / 448 (a row of zeros: codes 0, factor 1)
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+            }
+        }
+        amax = warp_max(amax);
+        const float s = amax > 0.f ? 448.0f / amax : 1.0f;
+        uint8_t *qr = q + (int64_t)row * C;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int p = lane + 32 * i;
+            if (p < npk) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t pair = e4m3_of(bf16_lo(w[k]) * s) | (e4m3_of(bf16_hi(w[k]) * s) << 8);
+                    if (k < 2)
+                        lo |= pair << (16 * k);
+                    else
+                        hi |= pair << (16 * (k - 2));
+                }
+                *reinterpret_cast<uint2 *>(qr + p * 8) = make_uint2(lo, hi);
+            }
+        }
+        if (lane == 0) qinv[row] = amax > 0.f ? amax / 448.0f : 1.0f;
     }
 }
 
@@ -478,12 +515,14 @@ template <typename T> static int ln_vpl(int C) {
 
 template <typename T>
 int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *mean, float *rstd, int N, int C,
-                      cudaStream_t st) {
+                      cudaStream_t st, uint8_t *q, float *qinv) {
     if (C % Pack16<T>::N) return GPT2_ERR_BAD_SHAPE;
     const int warps = 8, grid = ceil_div(N, warps);
     if constexpr (sizeof(T) == 2) {
-        LN_VPL_SWITCH(ln_vpl<T>(C), ln_fwd_bf16_kernel<V_><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C))
+        LN_VPL_SWITCH(ln_vpl<T>(C),
+                      ln_fwd_bf16_kernel<V_><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C, q, qinv))
     } else {
+        if (q) return GPT2_ERR_UNSUPPORTED;  // the E4M3 copy is made from bf16 rows only
         LN_VPL_SWITCH(ln_vpl<T>(C), ln_fwd_kernel<T, V_><<<grid, 32 * warps, 0, st>>>(x, g, b, y, mean, rstd, N, C))
     }
     GPT2_CUDA_TRY(cudaGetLastError());
@@ -1814,7 +1853,7 @@ int clip_adamw(float *p, const float *g, float *m, float *v, bf16 *shadow, int64
     template int embed_backward<T>(const int *, const T *, float *, float *, int, int, int, int, cudaStream_t,     \
                                    void *);                                                                      \
     template int layernorm_forward<T>(const T *, const float *, const float *, T *, float *, float *, int, int,    \
-                                      cudaStream_t);                                                             \
+                                      cudaStream_t, uint8_t *, float *);                                         \
     template int layernorm_backward<T>(const T *, const T *, const float *, const float *, const float *,          \
                                        const T *, T *, float *, float *, int, int, cudaStream_t, float *);         \
     template int column_sum<T>(const T *, int, int, float *, cudaStream_t);                                        \

@@ -3,6 +3,8 @@
 // (fp32 mode) or bf16.  Every launcher only enqueues work on `st`.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 
 namespace k {
@@ -21,10 +23,26 @@ int embed_backward(const int *tok, const T *dx, float *dwte, float *dwpe, int B,
                    cudaStream_t st, void *ws);
 size_t embed_backward_workspace(int n, int C);
 
-// y = (x - mean) * rstd * g + b per row of C; mean/rstd fp32 [N]
+// y = (x - mean) * rstd * g + b per row of C; mean/rstd fp32 [N].  bf16 only:
+// with q (uint8 [N, C]) and qinv (fp32 [N]) also the E4M3 copy of each stored
+// row, scaled by 448 / amax of the row (qinv = amax / 448).
 template <typename T>
 int layernorm_forward(const T *x, const float *g, const float *b, T *y, float *mean, float *rstd, int N, int C,
-                      cudaStream_t st);
+                      cudaStream_t st, uint8_t *q = nullptr, float *qinv = nullptr);
+
+// E4M3 with saturation, round to nearest even (CUDA's conversion)
+__device__ __forceinline__ uint32_t e4m3_of(float x) {
+    return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+// E4M3 per-row copy of bf16 x [M, K] (rows scaled by 448 / amax; inv = amax / 448)
+int quantize_rows_e4m3(const bf16 *x, int64_t ldx, int M, int K, uint8_t *q, int64_t ldq, float *inv,
+                       cudaStream_t st);
+// E4M3 copies of several bf16 tensors of one flat array, one scale each:
+// tensor t is w[off[t] .. off[t] + n[t]) -> q (same offsets), inv[t];
+// amax_bits: [ntens] uint scratch (zeroed here).  off[t], n[t] multiples of 8.
+int quantize_tensors_e4m3(const bf16 *w, const int64_t *d_off, const int64_t *d_n, int ntens, int64_t max_n,
+                          uint8_t *q, float *inv, unsigned *amax_bits, cudaStream_t st);
 
 // dres_out = dres_in (may be NULL) + LN'(dy); dg += sum dy*xhat; db += sum dy;
 // dsum (may be NULL) += column sums of dres_out as stored, i.e. the bias

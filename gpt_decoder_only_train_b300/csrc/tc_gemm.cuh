@@ -882,21 +882,21 @@ int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer
                 uint32_t box_outer);
 
 struct GemmDesc {
-    const bf16 *A;
-    int64_t lda;
-    bool a_kmajor;
-    const bf16 *B;
-    int64_t ldb;
-    bool b_kmajor;
-    void *D;
-    bf16 *D2;
-    const bf16 *R;
-    int64_t ldd;
-    const float *bias;
-    int M, N, K;
-    int epi;
-    float alpha;  // acc is scaled by alpha before the epilogue
-    int *err;
+    const bf16 *A = nullptr;
+    int64_t lda = 0;
+    bool a_kmajor = true;
+    const bf16 *B = nullptr;
+    int64_t ldb = 0;
+    bool b_kmajor = true;
+    void *D = nullptr;
+    bf16 *D2 = nullptr;
+    const bf16 *R = nullptr;
+    int64_t ldd = 0;
+    const float *bias = nullptr;
+    int M = 0, N = 0, K = 0;
+    int epi = GPT2_EPI_STORE;
+    float alpha = 1.0f;  // acc is scaled by alpha before the epilogue
+    int *err = nullptr;
     float *dbias = nullptr;  // bf16 epilogues: += column sums of the stored output (8-aligned fp32)
     // E4M3 operands (A and B K-major, bytes; lda / ldb multiples of 16): acc is
     // scaled by alpha * a_scale[row] (if given) * b_scale[0] (if given)

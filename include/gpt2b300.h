@@ -68,6 +68,10 @@ typedef struct {
     int B;              /* maximum micro-batch */
     int dtype;          /* GPT2_DTYPE_* */
     int recompute_gelu; /* 1: do not store GELU(h); recompute it in backward ([L] -r) */
+    int fp8_forward;    /* 1 (bf16 only, C >= 128): the four per-block projections of the
+                           forward (QKV, attention output, FC, FC output) multiply E4M3
+                           codes -- activations scaled per row, weights per tensor -- and
+                           the backward stays bf16 (straight-through); 0: bf16 throughout */
 } gpt2_config;
 
 typedef struct gpt2_model gpt2_model; /* opaque host handle */
@@ -221,7 +225,14 @@ int gpt2_set_grads(gpt2_model *m, int id, const float *host_in, size_t n);
  * "logits" ([B*T, Vp], dtype of the model; after a forward with targets it
  * holds dlogits), "loss_rows" (fp32 [B*T]), "lnf" (final LN output), "qkv.<l>",
  * "att.<l>", "lse.<l>", "resid.<l>" (input of layer l; resid.L is the final
- * residual stream).  GPT2_ERR_BAD_ARG for an unknown name.
+ * residual stream), "ln1.<l>", "ln2.<l>", "resid_mid.<l>" (after attention),
+ * "fch.<l>" (FC pre-activation [B*T, 4C]); with fp8_forward also "w8.<id>"
+ * (E4M3 codes of tensor id, uint8 in its shape; filled for the four block
+ * projection weights of every layer), "w8_inv" (fp32 [4L]: their
+ * dequantisation factors, QKV / attention output / FC / FC output of layer 0,
+ * then layer 1 ...), "a8" (uint8 [B*T, 4C]: the activation codes of the last
+ * quantised product) and "a8_inv" (fp32 [B*T]).  GPT2_ERR_BAD_ARG for an
+ * unknown name.
  */
 int gpt2_debug_buffer(gpt2_model *m, const char *name, void **dev_ptr, size_t *bytes);
 
@@ -249,8 +260,9 @@ long long gpt2_launch_count(void);
 #define GPT2_PROF_CLASSIFIER 2  /* fused classifier: work = bytes read + written */
 #define GPT2_PROF_ADAMW      3  /* clip + AdamW: bytes */
 #define GPT2_PROF_LAYERNORM  4  /* LayerNorm forward/backward: bytes */
-#define GPT2_PROF_OTHER      5  /* embedding, bias sums, GELU recompute, loss mean: bytes */
-#define GPT2_PROF_NCAT       6
+#define GPT2_PROF_OTHER      5  /* embedding, bias sums, GELU recompute, loss mean, E4M3 quantisers: bytes */
+#define GPT2_PROF_MATMUL_E4M3 6 /* E4M3 matmuls of the fp8_forward mode: work = 2 M N K FLOP */
+#define GPT2_PROF_NCAT       7
 int gpt2_profile(gpt2_model *m, int enable);
 int gpt2_profile_read(gpt2_model *m, int category, double *total_ms, double *total_work, long long *launches);
 

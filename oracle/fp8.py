@@ -23,17 +23,35 @@ What it follows
   point, so both sides take that decision in the same precision.
 * The matmul: ``D[m, n] = a_f[m] b_f sum_k qa[m, k] qb[n, k] (+ bias[n])``
   with the codes' exact values; everything after decoding is float64.
+* The E4M3 forward of the model (:func:`model_forward_e4m3`): the four
+  projections of every block (QKV, attention output, FC, FC output) multiply
+  E4M3 codes -- the activation operand quantised per row, the weight operand
+  per tensor from the bf16 weight copy the bf16 forward multiplies -- and
+  everything else (embeddings, LayerNorm, attention, GELU, residual adds,
+  the tied LM head, the loss) is the float64 forward of :mod:`oracle.gpt2`.
+  The backward is that module's ``model_backward`` applied to this forward's
+  cache with the unquantised weights (straight-through: the quantiser counts
+  as the identity in the backward).  Readings: which products are quantised,
+  the scaling granularity and the straight-through backward are not on the
+  pages; they are the usual choices of FP8 training recipes and are listed
+  in the design notes.
 
 Pins (``tests/test_oracle_fp8.py``): every one of the 254 finite codes
 decodes to the value the format defines and re-encodes to itself; the
 printed limits (448, 2^-6, 2^-9); ties go to the even mantissa; values past
 448 saturate; rounding error at most half a quantum; a brute-force nearest
 search over all finite codes agrees with the rounding everywhere; row
-quantisation reproduces the row to within its quantisation bound.
+quantisation reproduces the row to within its quantisation bound; the E4M3
+forward with its quantiser switched off is bit-identical to the float64
+forward (same block structure), and with it on stays within the loss change
+that 3-bit mantissas allow.
 """
 from __future__ import annotations
 
 import numpy as np
+import torch
+
+from . import gpt2 as og
 
 E4M3_MAX = 448.0
 
@@ -106,3 +124,60 @@ def matmul_e4m3(qa, a_inv, qb, b_inv, bias=None):
     if bias is not None:
         d = d + np.asarray(bias, dtype=np.float64)[None, :]
     return d
+
+
+def _product(x, w, quantise: bool):
+    """``x @ w^T`` over the last axis; with ``quantise`` both operands go through E4M3 first."""
+    if not quantise:
+        return x @ w.T
+    lead = x.shape[:-1]
+    qa, ai = quantize_rows(x.reshape(-1, x.shape[-1]).numpy())
+    wb = w.to(torch.bfloat16).to(og.F64).numpy()  # the bf16 weight copy of the forward
+    qb, bi = quantize_tensor(wb)
+    return torch.from_numpy(matmul_e4m3(qa, ai, qb, bi)).reshape(*lead, w.shape[0])
+
+
+def model_forward_e4m3(cfg, P, tokens, targets=None, quantise: bool = True):
+    """The model's forward with E4M3 block projections; returns what ``og.model_forward`` returns.
+
+    The cache feeds ``og.model_backward`` unchanged (straight-through backward).
+    With ``quantise=False`` the result is bit-identical to ``og.model_forward``.
+    """
+    tokens = torch.as_tensor(tokens).long()
+    B, T = tokens.shape
+    C, H, V = cfg.C, cfg.H, cfg.V
+    hd = C // H
+    x = P["wte"][tokens] + P["wpe"][:T]
+    layers = []
+    for l in range(cfg.L):
+        p = "h%d." % l
+        c = {"x": x}
+        y, c["m1"], c["r1"] = og.layernorm_forward(x, P[p + "ln1.g"], P[p + "ln1.b"])
+        c["y"] = y
+        qkv = _product(y, P[p + "qkv.w"], quantise) + P[p + "qkv.b"]
+        q = og._split_heads(qkv[..., 0:C], B, T, H, hd)
+        k = og._split_heads(qkv[..., C:2 * C], B, T, H, hd)
+        v = og._split_heads(qkv[..., 2 * C:3 * C], B, T, H, hd)
+        o, lse = og._attention_per_sequence(og.causal_attention_forward, q, k, v)
+        c["q"], c["k"], c["v"], c["lse"] = q, k, v, lse
+        of = og._merge_heads(o, B, T, C)
+        c["o"] = of
+        x1 = x + _product(of, P[p + "proj.w"], quantise) + P[p + "proj.b"]
+        c["x1"] = x1
+        y2, c["m2"], c["r2"] = og.layernorm_forward(x1, P[p + "ln2.g"], P[p + "ln2.b"])
+        c["y2"] = y2
+        h = _product(y2, P[p + "fc.w"], quantise) + P[p + "fc.b"]
+        c["h"] = h
+        g = og.gelu_forward(h)
+        x = x1 + _product(g, P[p + "fcproj.w"], quantise) + P[p + "fcproj.b"]
+        layers.append(c)
+    yf, mf, rf = og.layernorm_forward(x, P["lnf.g"], P["lnf.b"])
+    z = yf.reshape(B * T, C) @ P["wte"][:V].T
+    cache = {"tokens": tokens, "targets": targets, "layers": layers, "xL": x, "yf": yf, "mf": mf, "rf": rf,
+             "z": z, "B": B, "T": T}
+    loss = None
+    if targets is not None:
+        tg = torch.as_tensor(targets).long().reshape(-1)
+        loss, lse, rows = og.cross_entropy_forward(z, tg)
+        cache["lse"], cache["tg"], cache["rows"] = lse, tg, rows
+    return loss, z, cache

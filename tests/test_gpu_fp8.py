@@ -9,11 +9,19 @@
   two E4M3 values are exact in fp32, so the GPU's error is the fp32
   accumulation and one bf16 rounding: |D - ref| <= 2^-8 |ref| + 1e-3 max|ref|.
   Shapes are ragged in M and N and cover single-CTA and CTA-pair tiles.
+* The model with E4M3 block projections (fp8_forward) against the oracle's
+  E4M3 forward (model_forward_e4m3) and its straight-through backward: the
+  GPU quantises the bf16 activations it stores, the oracle its float64 ones,
+  so a few codes per row sit one quantum apart and the comparison carries
+  the bf16 step's tolerances, |loss - ref| <= 2e-2 and per-tensor gradient
+  cosine >= 0.99, also over optimizer steps at a learning rate that moves
+  the weights by several E4M3 quanta per step (stale weight codes would show).
 """
 import numpy as np
 import pytest
 import torch
 
+import synthetic
 from oracle import fp8 as of
 from oracle import gpt2 as og
 
@@ -141,3 +149,119 @@ def test_e4m3_matmul_full_size_sampled_rows(g):
     rqb, rbinv = of.quantize_tensor(bf)
     ref = of.matmul_e4m3(rqa, rainv, rqb, rbinv)
     _check(D.float().cpu().numpy()[rows], ref, "full size")
+
+
+# ---- the model's E4M3 forward -------------------------------------------------------
+
+SMALL_F8 = dict(L=2, C=128, H=2, V=500, Vp=512, T=192, B=3, dtype="bf16", recompute_gelu=0, fp8_forward=1)
+RAGGED_F8 = dict(L=1, C=192, H=3, V=1000, Vp=1024, T=77, B=2, dtype="bf16", recompute_gelu=0, fp8_forward=1)
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def _cos(a, b):
+    a = np.asarray(a, dtype=np.float64).reshape(-1)
+    b = np.asarray(b, dtype=np.float64).reshape(-1)
+    na, nb = np.linalg.norm(a), np.linalg.norm(b)
+    if na == 0 and nb == 0:
+        return 1.0
+    return float(a @ b / (na * nb))
+
+
+def _oracle_e4m3_micro_step(ref, x, y, grad_scale=1.0):
+    loss, _, cache = of.model_forward_e4m3(ref.cfg, ref.params, x, y)
+    ref._cache = cache
+    ref.backward(grad_scale)
+    return float(loss)
+
+
+@pytest.mark.parametrize("cfg", [SMALL_F8, RAGGED_F8], ids=["small", "ragged"])
+def test_e4m3_forward_step_parity(g, cfg):
+    seed = 21
+    m = g.GPT2(cfg, seed=seed)
+    ref = og.OracleGPT2(og.Config.from_dict(cfg), seed)
+    x, y = synthetic.zipf_window(seed, cfg["B"], cfg["T"], cfg["V"])
+    loss = m.forward(_dev(x), _dev(y))
+    m.backward(1.0)
+    ref_loss = _oracle_e4m3_micro_step(ref, x, y)
+    assert abs(loss - ref_loss) <= 2e-2, (loss, ref_loss)
+    for i, name in enumerate(m.names):
+        c = _cos(m.grads(i), ref.grads[name].numpy())
+        assert c >= 0.99, (name, c)
+    norm = m.clip_and_adamw(6e-4)
+    ref_norm = ref.clip_and_adamw(6e-4)
+    assert abs(norm - ref_norm) <= 0.02 * ref_norm
+    # the quantiser is active: the bf16 forward of the same weights gives another loss
+    m16 = g.GPT2(dict(cfg, fp8_forward=0), seed=seed)
+    assert m16.forward(_dev(x), _dev(y)) != loss
+    m16.close()
+    m.close()
+
+
+def test_e4m3_forward_follows_the_oracle_over_optimizer_steps(g):
+    cfg = dict(SMALL_F8, B=2, T=128)
+    seed, lr = 5, 3e-3
+    m = g.GPT2(cfg, seed=seed)
+    ref = og.OracleGPT2(og.Config.from_dict(cfg), seed)
+    for step in range(3):
+        x, y = synthetic.zipf_window(seed, cfg["B"], cfg["T"], cfg["V"], micro_step=step)
+        m.zero_grad()
+        ref.zero_grad()
+        loss = m.forward(_dev(x), _dev(y))
+        m.backward(1.0)
+        ref_loss = _oracle_e4m3_micro_step(ref, x, y)
+        assert abs(loss - ref_loss) <= 2e-2, (step, loss, ref_loss)
+        norm = m.clip_and_adamw(lr)
+        ref_norm = ref.clip_and_adamw(lr)
+        assert abs(norm - ref_norm) <= 0.02 * ref_norm, (step, norm, ref_norm)
+    m.close()
+
+
+def test_e4m3_weight_codes_follow_set_params(g):
+    """Weights written through the ABI are re-quantised before the next forward."""
+    cfg = SMALL_F8
+    m = g.GPT2(cfg, seed=3)
+    ref = og.OracleGPT2(og.Config.from_dict(cfg), 3)
+    rng = np.random.default_rng(0)
+    for i, name in enumerate(m.names):
+        if len(m.shapes[i]) == 2 and name != "wte" and name != "wpe":
+            w = (rng.normal(size=m.shapes[i]) * 0.08).astype(np.float32)
+            m.set_params(i, w)
+            ref.params[name] = torch.from_numpy(w.astype(np.float64))
+    x, y = synthetic.zipf_window(3, cfg["B"], cfg["T"], cfg["V"])
+    loss = m.forward(_dev(x), _dev(y))
+    ref_loss, _, _ = of.model_forward_e4m3(ref.cfg, ref.params, x, y)
+    assert abs(loss - float(ref_loss)) <= 2e-2, (loss, float(ref_loss))
+    m.close()
+
+
+def test_e4m3_model_codes_and_first_product(g):
+    """The model's weight codes and factors equal the oracle's quantisation of its bf16
+    weights bit for bit; layer 0's QKV product, from the model's own LayerNorm output (the
+    same bf16 input on both sides, hence the same activation codes), matches the oracle's
+    E4M3 product within the matmul tolerance."""
+    cfg = SMALL_F8
+    m = g.GPT2(cfg, seed=21)
+    L, C, BT = cfg["L"], cfg["C"], cfg["B"] * cfg["T"]
+    inv = m.debug_tensor("w8_inv", torch.float32, (4 * L,)).cpu().numpy()
+    for l in range(L):
+        for j, nm in enumerate(("qkv.w", "proj.w", "fc.w", "fcproj.w")):
+            i = m.names.index("h%d.%s" % (l, nm))
+            codes = m.debug_tensor("w8.%d" % i, torch.uint8, tuple(m.shapes[i])).cpu().numpy()
+            wb = torch.from_numpy(m.params(i)).to(torch.bfloat16).double().numpy()
+            rq, rinv = of.quantize_tensor(wb)
+            assert np.array_equal(codes, rq), (l, nm)
+            assert inv[4 * l + j] == np.float32(rinv), (l, nm)
+    x, _ = synthetic.zipf_window(21, cfg["B"], cfg["T"], cfg["V"])
+    m.forward(_dev(x), None)
+    torch.cuda.synchronize()
+    y = m.debug_tensor("ln1.0", torch.bfloat16, (BT, C)).float().cpu().numpy().astype(np.float64)
+    qkv = m.debug_tensor("qkv.0", torch.bfloat16, (BT, 3 * C)).float().cpu().numpy()
+    i = m.names.index("h0.qkv.w")
+    qa, ai = of.quantize_rows(y)
+    qb, bi = of.quantize_tensor(torch.from_numpy(m.params(i)).to(torch.bfloat16).double().numpy())
+    ref = of.matmul_e4m3(qa, ai, qb, bi, bias=m.params(m.names.index("h0.qkv.b")).astype(np.float64))
+    _check(qkv, ref, "qkv.0")
+    m.close()

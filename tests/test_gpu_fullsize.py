@@ -28,6 +28,7 @@ import pytest
 import torch
 
 import synthetic
+from oracle import fp8 as of
 from oracle import gpt2 as og
 
 pytestmark = pytest.mark.gpu
@@ -78,6 +79,33 @@ def test_124m_full_step_parity(g):
     ref_norm = og.global_norm(ref.grads)
     assert abs(norm - ref_norm) <= 0.02 * ref_norm, (norm, ref_norm)
     assert (gpu_grads[0][w["V"]:] == 0).all()
+
+
+def test_124m_e4m3_forward_sampled_sequence_and_gradients(g):
+    """E4M3 block projections at 124M: the full batch in the bench's launch configuration,
+    one sampled sequence's per-position losses against the oracle's E4M3 forward, and the
+    gradients of that sequence (a B=1 call) against its straight-through backward."""
+    w = dict(synthetic.WORKLOADS["gpt2_124m"], fp8_forward=1)
+    x, y = synthetic.step_batch(w)
+    m = g.GPT2(w, seed=w["seed"])
+    loss = m.forward(_dev(x), _dev(y))
+    assert math.isfinite(loss)
+    rows = m.debug_tensor("loss_rows", torch.float32, (w["B"] * w["T"],)).cpu().numpy().reshape(w["B"], w["T"])
+    b = 5
+    ref = og.OracleGPT2(og.Config.from_dict(dict(w, B=1)), w["seed"])
+    ref_loss, _, cache = of.model_forward_e4m3(ref.cfg, ref.params, x[b:b + 1], y[b:b + 1])
+    ref_rows = cache["rows"].numpy().reshape(-1)
+    assert abs(rows[b].mean() - float(ref_loss)) <= 2e-2
+    assert np.corrcoef(rows[b], ref_rows)[0, 1] >= 0.99
+    m.zero_grad()
+    m.forward(_dev(x[b:b + 1]), _dev(y[b:b + 1]))
+    m.backward(1.0)
+    G = og.model_backward(ref.cfg, ref.params, cache)
+    worst = (1.0, None)
+    for i, name in enumerate(m.names):
+        worst = min(worst, (_cos(m.grads(i), G[name].numpy()), name))
+    assert worst[0] >= 0.99, worst
+    m.close()
 
 
 def test_350m_recompute_sampled_rows_and_property(g):

@@ -114,3 +114,97 @@ def test_matmul_is_the_decoded_product():
     assert np.allclose(d, ref, rtol=1e-12, atol=1e-12)
     # and close to the unquantised product (E4M3 keeps 3 mantissa bits)
     assert np.abs(d - (a @ b.T + np.arange(5.0))).max() <= 0.2 * np.abs(a @ b.T).max()
+
+
+# ---- the E4M3 forward of the model ------------------------------------------------
+
+TINY = dict(L=2, C=32, H=2, V=61, Vp=64, T=8, B=2)
+
+
+def _tiny_model(seed=7):
+    from oracle import gpt2 as og
+
+    cfg = og.Config.from_dict(TINY)
+    P = og.init_params(cfg, seed)
+    # larger weights than the initial 0.02 so that the blocks move the logits
+    rng = np.random.default_rng(seed)
+    for k, v in P.items():
+        if v.dim() == 2:
+            P[k] = v * 10.0
+        elif not k.endswith(".g"):
+            P[k] = torch.from_numpy(rng.normal(scale=0.1, size=v.shape))
+    tok = torch.from_numpy(rng.integers(0, TINY["V"], size=(TINY["B"], TINY["T"])))
+    tg = torch.from_numpy(rng.integers(0, TINY["V"], size=(TINY["B"], TINY["T"])))
+    return og, cfg, P, tok, tg
+
+
+import torch  # noqa: E402
+
+
+def test_e4m3_forward_without_quantiser_is_the_float64_forward():
+    og, cfg, P, tok, tg = _tiny_model()
+    l0, z0, _ = og.model_forward(cfg, P, tok, tg)
+    l1, z1, _ = fp8.model_forward_e4m3(cfg, P, tok, tg, quantise=False)
+    assert float(l0) == float(l1)
+    assert torch.equal(z0, z1)
+
+
+def _brute_dequantised(x2d, per_row: bool):
+    """E4M3 quantise-dequantise by nearest-value search over the finite codes (ties to the
+    even code): scale 448 / amax and factor amax / 448 in fp32, per row or per tensor."""
+    codes, vals = _finite_table()
+    x32 = np.asarray(x2d, dtype=np.float32)
+    amax = np.abs(x32).max(axis=1, keepdims=True) if per_row else np.abs(x32).max(keepdims=True)
+    safe = np.where(amax > 0, amax, np.float32(1))
+    s = np.where(amax > 0, np.float32(448) / safe, np.float32(1)).astype(np.float32)
+    inv = np.where(amax > 0, safe / np.float32(448), np.float32(1)).astype(np.float32)
+    scaled = (x32 * s).astype(np.float64)
+    d = np.abs(scaled[..., None] - vals)
+    best = d == d.min(-1, keepdims=True)
+    pick = np.where(best & (codes % 2 == 0), 0, 1) + np.where(best, 0, 2)  # even ties first, then any
+    v = vals[np.argmin(pick, axis=-1)]
+    return v * inv.astype(np.float64)
+
+
+def test_e4m3_forward_products_are_the_quantised_products():
+    og, cfg, P, tok, tg = _tiny_model()
+    _, _, cache = fp8.model_forward_e4m3(cfg, P, tok, tg)
+    C = cfg.C
+    for l, c in enumerate(cache["layers"]):
+        p = "h%d." % l
+        # the cache keeps every projection's input and output
+        checks = [
+            (c["y"], P[p + "qkv.w"], P[p + "qkv.b"],
+             torch.cat([og._merge_heads(t, cfg.B, cfg.T, C) for t in (c["q"], c["k"], c["v"])], -1)),
+            (c["o"], P[p + "proj.w"], P[p + "proj.b"], c["x1"] - c["x"]),
+            (c["y2"], P[p + "fc.w"], P[p + "fc.b"], c["h"]),
+        ]
+        nxt = cache["layers"][l + 1]["x"] if l + 1 < cfg.L else cache["xL"]
+        checks.append((og.gelu_forward(c["h"]), P[p + "fcproj.w"], P[p + "fcproj.b"], nxt - c["x1"]))
+        for x, w, b, got in checks:
+            xq = _brute_dequantised(x.reshape(-1, x.shape[-1]).numpy(), per_row=True)
+            wq = _brute_dequantised(w.to(torch.bfloat16).double().numpy(), per_row=False)
+            want = torch.from_numpy(xq @ wq.T).reshape(got.shape) + b
+            scale = (x.abs() @ w.abs().T).reshape(got.shape) + b.abs() + 1
+            assert ((got - want).abs() <= 1e-12 * scale).all(), l
+            # and it is not the unquantised product
+            assert not torch.allclose(got, x @ w.T + b, rtol=1e-6, atol=0)
+
+
+def test_e4m3_forward_backward_is_straight_through():
+    og, cfg, P, tok, tg = _tiny_model()
+    loss, _, cache = fp8.model_forward_e4m3(cfg, P, tok, tg)
+    l0, _, cache0 = og.model_forward(cfg, P, tok, tg)
+    # the loss differs from the float64 forward's by quantisation noise only
+    assert float(loss) != float(l0)
+    assert abs(float(loss) - float(l0)) < 0.05 * float(l0)
+    # the backward of the quantised forward's cache is the float64 backward evaluated at
+    # that forward's activations: close to the unquantised gradients, tensor by tensor
+    G = og.model_backward(cfg, P, cache)
+    G0 = og.model_backward(cfg, P, cache0)
+    for k in G:
+        a, b = G[k].flatten(), G0[k].flatten()
+        if float(b.norm()) == 0.0:
+            continue
+        cos = float(a @ b / (a.norm() * b.norm()))
+        assert cos > 0.98, (k, cos)
