@@ -29,6 +29,24 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&f)[32]) {
     for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(r[i]);
 }
 
+// Column sums over a warp's 32 rows (one row per lane, 16 values each) added to g[0, 16)
+// (shared memory).
+// A butterfly that keeps half of the columns at each step (16 shuffles in all) leaves
+// lanes 2c and 2c + 1 with the sum of column c; the even lane adds it.
+__device__ __forceinline__ void warp_colsum16_add(const float (&v)[16], float *g, int lane) {
+    float a[8], b[4], c[2];
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (b4 ? v[8 + i] : v[i]) + __shfl_xor_sync(~0u, b4 ? v[i] : v[8 + i], 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = (b3 ? a[4 + i] : a[i]) + __shfl_xor_sync(~0u, b3 ? a[i] : a[4 + i], 8);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) c[i] = (b2 ? b[2 + i] : b[i]) + __shfl_xor_sync(~0u, b2 ? b[i] : b[2 + i], 4);
+    float d = (b1 ? c[1] : c[0]) + __shfl_xor_sync(~0u, b1 ? c[0] : c[1], 2);
+    d += __shfl_xor_sync(~0u, d, 1);
+    if (!(lane & 1)) atomicAdd(g + (lane >> 1), d);
+}
+
 // max of three fp32 values in one instruction (sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
@@ -471,7 +489,9 @@ constexpr int TQ = BQ * HD * 2;   // 16 KB: a Q, dO or O tile
 constexpr int TK = BK * HD * 2;   // 8 KB: a K or V tile
 constexpr int OFF_ITEM = NST * 2 * TK;      // [2 item slots][Q | dO | O]
 constexpr int OFF_LSE = OFF_ITEM + 6 * TQ;  // [2][128] floats
-constexpr int OFF_BAR = OFF_LSE + 2 * BQ * 4;
+constexpr int MAXC = 2048;                   // query- and value-bias partial sums of the CTA, [2][H * 64] floats
+constexpr int OFF_BSUM = OFF_LSE + 2 * BQ * 4;
+constexpr int OFF_BAR = OFF_BSUM + 2 * MAXC * 4;
 constexpr int SMEM = 1024 + OFF_BAR + 512;
 constexpr uint32_t TCOLS = 512;
 constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 256, C_QD = 320;
@@ -488,7 +508,7 @@ __global__ void __launch_bounds__(dq::NTH, 1)
                      const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const float *__restrict__ lse,
                      bf16 *__restrict__ dqo, int64_t rs, float *__restrict__ Dscr, int T, int H, int nitems,
-                     float sl2, float scale) {
+                     float sl2, float scale, float *__restrict__ dbq, float *__restrict__ dbv) {
     constexpr int BQ = dq::BQ, BK = dq::BK, NST = dq::NST, SWARPS = dq::SWARPS;
     constexpr int TQ = dq::TQ, TK = dq::TK, OFF_ITEM = dq::OFF_ITEM, OFF_LSE = dq::OFF_LSE, OFF_BAR = dq::OFF_BAR;
     constexpr uint32_t TCOLS = dq::TCOLS, C_S = dq::C_S, C_DP = dq::C_DP, C_DQ = dq::C_DQ, C_QD = dq::C_QD;
@@ -498,6 +518,9 @@ __global__ void __launch_bounds__(dq::NTH, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + sizeof(dq::Bars));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *lsebuf = reinterpret_cast<float *>(sm + OFF_LSE);
+    float *bsum = reinterpret_cast<float *>(sm + dq::OFF_BSUM), *bsum_v = bsum + dq::MAXC;
+    if (dbq)
+        for (int c = threadIdx.x; c < H * HD; c += blockDim.x) bsum[c] = bsum_v[c] = 0.f;
     const int nqb = (T + BQ - 1) / BQ, nkb = (T + BK - 1) / BK, BH = nitems / nqb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // item p: query block nqb - 1 - p / BH (heaviest first), b*h = p % BH
@@ -671,6 +694,15 @@ __global__ void __launch_bounds__(dq::NTH, 1)
             Dr = acc;
             l2 = lsebuf[s * BQ + r] * LOG2E;
             const int q = item_qb(p) * BQ + r;
+            if (dbq) {  // value-bias gradient: column sums of dO (every row of P sums to one)
+                float cv[16];
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    cv[2 * w] = q < T ? bf16_lo(wd[w]) : 0.f;
+                    cv[2 * w + 1] = q < T ? bf16_hi(wd[w]) : 0.f;
+                }
+                warp_colsum16_add(cv, bsum_v + ((p % BH) % H) * HD + sub * 16, lane);
+            }
             if (sub == 0 && q < T) Dscr[(int64_t)(p % BH) * T + q] = acc;
             tmem_st_wait();
             tc_fence_before();
@@ -737,6 +769,12 @@ __global__ void __launch_bounds__(dq::NTH, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar->dq_free);
+            if (dbq) {  // query-bias gradient: column sums of dQ (one warp = 32 rows) into the CTA's partials
+                float cv[16];
+#pragma unroll
+                for (int d = 0; d < 16; ++d) cv[d] = q < T ? __uint_as_float(ra[d]) * scale : 0.f;
+                warp_colsum16_add(cv, bsum + h * HD + sub * 16, lane);
+            }
             if (q < T) {
                 bf16 *row = dqo + ((int64_t)b * T + q) * rs + h * HD + sub * 16;
 #pragma unroll
@@ -757,6 +795,11 @@ __global__ void __launch_bounds__(dq::NTH, 1)
         tc_fence_after();
         tmem_dealloc(tmem, TCOLS);
     }
+    if (dbq)  // one atomic per head column and CTA
+        for (int c = threadIdx.x; c < H * HD; c += blockDim.x) {
+            if (bsum[c] != 0.f) atomicAdd(dbq + c, bsum[c]);
+            if (bsum_v[c] != 0.f) atomicAdd(dbv + c, bsum_v[c]);
+        }
 }
 
 // ---------------------------------------------------------------- dK/dV kernel
@@ -1141,13 +1184,14 @@ int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs
 
 int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
                           int64_t ors, const float *lse, bf16 *dq_out, bf16 *dk_out, bf16 *dv_out, float *Dscr, int B,
-                          int T, int H, cudaStream_t st) {
+                          int T, int H, cudaStream_t st, float *dbias) {
     using namespace fatc;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
          reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq_out) |
          reinterpret_cast<uintptr_t>(dk_out) | reinterpret_cast<uintptr_t>(dv_out)) & 15)
         return GPT2_ERR_BAD_ARG;
     CUtensorMap q128, do128, o128, k64, v64, q64, do64, k128, v128;
+    if (dbias && H * HD > dq::MAXC) return GPT2_ERR_UNSUPPORTED;
     if (int rc = encode_qkv_map(&q128, q, rs, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&do128, dout, ors, T, B, H, 128)) return rc;
     if (int rc = encode_qkv_map(&o128, o, ors, T, B, H, 128)) return rc;
@@ -1174,7 +1218,8 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
     // persistent dQ grid: one CTA per SM over (query block, b*h) items, heaviest first
     const int nq_items = ((T + dq::BQ - 1) / dq::BQ) * B * H;
     bwd_dq_tc_kernel<<<std::min(nq_items, sms), dq::NTH, dq::SMEM, st>>>(q128, do128, o128, k64, v64, lse, dq_out, rs,
-                                                                         Dscr, T, H, nq_items, sl2, scale);
+                                                                         Dscr, T, H, nq_items, sl2, scale, dbias,
+                                                                         dbias ? dbias + 2 * H * HD : nullptr);
     GPT2_CUDA_TRY(cudaGetLastError());
     // persistent dK/dV grid: one CTA per SM over (key block, b*h) items, heaviest first
     const int nitems = ((T + dkv::BKY - 1) / dkv::BKY) * B * H;

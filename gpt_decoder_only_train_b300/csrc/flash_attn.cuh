@@ -21,12 +21,18 @@ int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs
 // tcgen05 implementation of attention_backward (attn_tc.cu).
 int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
                           int64_t ors, const float *lse, bf16 *dq, bf16 *dk, bf16 *dv, float *Dscr, int B, int T,
-                          int H, cudaStream_t st);
+                          int H, cudaStream_t st, float *dbias = nullptr);
 
 // dq/dk/dv (row stride rs) from O, dO (row stride ors) and lse; Dscr holds
-// D = rowsum(dO * O) as fp32 [B, H, T].
+// D = rowsum(dO * O) as fp32 [B, H, T].  With dbias (fp32 [3 H 64], columns
+// [q | k | v] as in the fused projection, H 64 <= 2048) the gradient of a bias
+// added to q, k and v is added to it: the column sums of dq over all B*T rows
+// for the query part; the column sums of dout for the value part (every row of
+// P sums to one, so the rows of dv sum to the rows of dout); nothing for the
+// key part, which is zero (a key bias moves all scores of a query by the same
+// amount).
 int attention_backward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
                        int64_t ors, const float *lse, bf16 *dq, bf16 *dk, bf16 *dv, float *Dscr, int B, int T, int H,
-                       int hd, cudaStream_t st);
+                       int hd, cudaStream_t st, float *dbias = nullptr);
 
 }  // namespace fa

@@ -469,12 +469,13 @@ int attn_fwd(gpt2_model *m, const T *qkv, T *o, float *lse, int B, int Tn) {
 }
 
 template <typename T>
-int attn_bwd(gpt2_model *m, const T *qkv, const T *o, const T *dout, const float *lse, T *dqkv, int B, int Tn) {
+int attn_bwd(gpt2_model *m, const T *qkv, const T *o, const T *dout, const float *lse, T *dqkv, int B, int Tn,
+             float *dbias) {
     const int C = m->cfg.C, H = m->cfg.H, hd = C / H;
     return timed(m, GPT2_PROF_ATTENTION, 2.0 * attn_flops(B, Tn, H, hd), [&] {
         if constexpr (sizeof(T) == 2)
             return fa::attention_backward(qkv, qkv + C, qkv + 2 * C, 3 * C, o, dout, C, lse, dqkv, dqkv + C,
-                                          dqkv + 2 * C, m->attn_D, B, Tn, H, hd, m->stream);
+                                          dqkv + 2 * C, m->attn_D, B, Tn, H, hd, m->stream, dbias);
         else
             return k::attention_backward_simt<T>(qkv, qkv + C, qkv + 2 * C, 3 * C, o, dout, C, lse, dqkv, dqkv + C,
                                                  dqkv + 2 * C, m->attn_D, B, Tn, H, hd, m->stream);
@@ -595,14 +596,17 @@ int backward_impl(gpt2_model *m, float grad_scale) {
         // FC projection: x' = x1 + g Wfcproj^T + b
         TRY(mm<T>(m, dres, C, false, g_in, 4 * C, false, Gf(m, p.fcprojw), nullptr, nullptr, 4 * C, nullptr, C, 4 * C,
                   BT, GPT2_EPI_ACCUM_F32));
-        // bf16: the GELU-backward product also sums its output's columns into the FC bias gradient
-        constexpr bool fold_fcb = sizeof(T) == 2;
+        // bf16: bias gradients from the kernels that read the gradients they sum: the GELU-backward
+        // product sums its output's columns into the FC bias gradient; the attention backward adds
+        // the QKV bias gradient (query part: column sums of dq; value part: column sums of dO, since
+        // every row of P sums to one; key part: zero, a key bias moves all scores of a query alike)
+        constexpr bool fold_bias = sizeof(T) == 2;
         TRY(mm<T>(m, dres, C, true, W<T>(m, p.fcprojw), 4 * C, false, dbig, nullptr, y.fch, 4 * C, nullptr, BT, 4 * C,
-                  C, GPT2_EPI_GELU_BWD, 1.0f, fold_fcb ? Gf(m, p.fcb) : nullptr));
+                  C, GPT2_EPI_GELU_BWD, 1.0f, fold_bias ? Gf(m, p.fcb) : nullptr));
         // FC: h = y2 Wfc^T + b
         TRY(mm<T>(m, dbig, 4 * C, false, y.ln2, C, false, Gf(m, p.fcw), nullptr, nullptr, C, nullptr, 4 * C, C, BT,
                   GPT2_EPI_ACCUM_F32));
-        if (!fold_fcb) TIMED(GPT2_PROF_OTHER, 4 * act, k::column_sum<T>(dbig, BT, 4 * C, Gf(m, p.fcb), st));
+        if (!fold_bias) TIMED(GPT2_PROF_OTHER, 4 * act, k::column_sum<T>(dbig, BT, 4 * C, Gf(m, p.fcb), st));
         TRY(mm<T>(m, dbig, 4 * C, true, W<T>(m, p.fcw), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, 4 * C,
                   GPT2_EPI_STORE));
         TIMED(GPT2_PROF_LAYERNORM, 4 * act + stats,
@@ -613,11 +617,11 @@ int backward_impl(gpt2_model *m, float grad_scale) {
                   GPT2_EPI_ACCUM_F32));
         TRY(mm<T>(m, dres, C, true, W<T>(m, p.projw), C, false, datt, nullptr, nullptr, C, nullptr, BT, C, C,
                   GPT2_EPI_STORE));
-        TRY(attn_bwd<T>(m, (T *)y.qkv, (T *)y.att, datt, y.lse, dqkv, B, Tn));
+        TRY(attn_bwd<T>(m, (T *)y.qkv, (T *)y.att, datt, y.lse, dqkv, B, Tn, fold_bias ? Gf(m, p.qkvb) : nullptr));
         // QKV: qkv = y Wqkv^T + b
         TRY(mm<T>(m, dqkv, 3 * C, false, y.ln1, C, false, Gf(m, p.qkvw), nullptr, nullptr, C, nullptr, 3 * C, C, BT,
                   GPT2_EPI_ACCUM_F32));
-        TIMED(GPT2_PROF_OTHER, 3 * act, k::column_sum<T>(dqkv, BT, 3 * C, Gf(m, p.qkvb), st));
+        if (!fold_bias) TIMED(GPT2_PROF_OTHER, 3 * act, k::column_sum<T>(dqkv, BT, 3 * C, Gf(m, p.qkvb), st));
         TRY(mm<T>(m, dqkv, 3 * C, true, W<T>(m, p.qkvw), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, 3 * C,
                   GPT2_EPI_STORE));
         TIMED(GPT2_PROF_LAYERNORM, 4 * act + stats,

@@ -90,6 +90,29 @@ def test_attention_backward_finite_differences():
 
 # ---------------------------------------------------------------- layernorm
 
+def test_attention_bias_gradient_identities():
+    """Two identities of the attention backward that the CUDA path uses for the bias of the
+    fused Q|K|V projection: a bias added to every key moves all scores of a query by the same
+    amount, so the keys' gradients sum to zero over the sequence; a bias added to every value
+    adds itself to every output row (each softmax row sums to one), so the values' gradients
+    sum to the output gradients' sum.  Checked on the oracle's hand-derived backward, and on
+    the gradient of the forward by finite differences in the bias direction."""
+    g = torch.Generator().manual_seed(11)
+    T, hd = 9, 8
+    q, k, v, do = (torch.randn(T, hd, generator=g, dtype=torch.float64) for _ in range(4))
+    dq, dk, dv = og.causal_attention_backward(q, k, v, do)
+    assert torch.allclose(dk.sum(0), torch.zeros(hd, dtype=torch.float64), atol=1e-12)
+    assert torch.allclose(dv.sum(0), do.sum(0), rtol=1e-12, atol=1e-12)
+    assert float(dq.sum(0).abs().max()) > 1e-3  # the query part is not degenerate
+    bk = torch.randn(hd, generator=g, dtype=torch.float64)
+    bv = torch.randn(hd, generator=g, dtype=torch.float64)
+    f = lambda kk, vv: float((og.causal_attention_forward(q, kk, vv)[0] * do).sum())
+    h = 1e-6
+    assert abs((f(k + h * bk, v) - f(k - h * bk, v)) / (2 * h)) < 1e-8
+    fd_v = (f(k, v + h * bv) - f(k, v - h * bv)) / (2 * h)
+    assert abs(fd_v - float(do.sum(0) @ bv)) < 1e-7
+
+
 def test_layernorm_invariants():
     x = _rand(5, 64, seed=12) * 3 + 1.5
     g, b = torch.ones(64, dtype=F64), torch.zeros(64, dtype=F64)
