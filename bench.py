@@ -141,8 +141,8 @@ GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
     "workload": "gpt2_124m",
-    "sha256": "cd54b224514ac7445c9c7975b6cd0f04a1ea6590b484733c2b48dbbf7963a90b",
-    "bytes_per_launch": 23.29e9 / 147,
+    "sha256": "49240494b0761574f0c1a0e13bdc385f516bc72de05462f788215b14cc8ae8a8",
+    "bytes_per_launch": 22.99e9 / 147,
 }
 
 
@@ -260,15 +260,22 @@ def attention_sweep(args):
                 fn()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            # at least --steps calls and at least 0.6 s, so that the clock sampler (every 200 ms)
+            # records the timed region
+            calls = max(args.steps, int(600.0 / max(e0.elapsed_time(e1), 1e-3)) + 1)
             with ClockSampler(0) as clk:
                 e0.record(stream)
-                for _ in range(args.steps):
+                for _ in range(calls):
                     fn()
                 e1.record(stream)
                 torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / args.steps
+            ms = e0.elapsed_time(e1) / calls
             flops = mult * 4.0 * hd * (T * (T + 1) / 2.0) * B * H
-            out[name] = {"ms": ms, "tflops": flops / ms / 1e9, "clocks": clk.summary()}
+            out[name] = {"ms": ms, "tflops": flops / ms / 1e9, "calls": calls, "clocks": clk.summary()}
         rows.append(out)
         del dev, q, k, v, do, o, lse, dq, dk, dv, scratch
         torch.cuda.empty_cache()

@@ -91,7 +91,20 @@ constexpr int EMB_SORT_THREADS = 1024;
 
 // key = token << 16 | position in the chunk; stable LSD radix sort on the
 // token's two bytes (shared-memory counts per warp and digit, digit-major
-// exclusive scan, ranks within a warp from __match_any_sync).
+// exclusive scan, ranks within a warp from ballots of the digit bits).
+// Lanes of the warp whose 8-bit digit equals this lane's, among the lanes with v set (one
+// ballot per digit bit and one for v); 0 for a lane without v.
+__device__ __forceinline__ uint32_t digit_peers(uint32_t d, bool v) {
+    uint32_t peers = __ballot_sync(0xffffffffu, v);
+#pragma unroll
+    for (int bit = 0; bit < 8; ++bit) {
+        const bool on = (d >> bit) & 1u;
+        const uint32_t m = __ballot_sync(0xffffffffu, on);
+        peers &= on ? m : ~m;
+    }
+    return v ? peers : 0u;
+}
+
 __global__ void __launch_bounds__(EMB_SORT_THREADS) embed_sort_kernel(const int *__restrict__ tok, int n, int V,
                                                                      uint32_t *__restrict__ keys_out) {
     extern __shared__ uint32_t esm[];
@@ -111,14 +124,8 @@ __global__ void __launch_bounds__(EMB_SORT_THREADS) embed_sort_kernel(const int 
         const int shift = 16 + 8 * pass;
         for (int i = tid; i < 32 * 256; i += EMB_SORT_THREADS) cnt[i] = 0;
         __syncthreads();
-        for (int b = w0; b < w1; b += 32) {
-            const int i = b + lane;
-            const bool v = i < w1;
-            const uint32_t d = v ? (in[i] >> shift) & 255u : 256u + lane;  // lanes past the end: unique digits
-            const uint32_t peers = __match_any_sync(0xffffffffu, d);
-            if (v && lane == __ffs(peers) - 1) cnt[w * 256 + d] += __popc(peers);
-            __syncwarp();
-        }
+        for (int i = w0 + lane; i < w1; i += 32)  // counts need no order: shared atomics on the warp's row
+            atomicAdd(&cnt[w * 256 + ((in[i] >> shift) & 255u)], 1);
         __syncthreads();
         // exclusive scan in digit-major order: entry (digit, warp) at index digit * 32 + warp
         int loc[8], run = 0;
@@ -157,8 +164,8 @@ __global__ void __launch_bounds__(EMB_SORT_THREADS) embed_sort_kernel(const int 
             const int i = b + lane;
             const bool v = i < w1;
             const uint32_t k = v ? in[i] : 0u;
-            const uint32_t d = v ? (k >> shift) & 255u : 256u + lane;
-            const uint32_t peers = __match_any_sync(0xffffffffu, d);
+            const uint32_t d = v ? (k >> shift) & 255u : 0u;
+            const uint32_t peers = digit_peers(d, v);
             int dst = 0;
             if (v) dst = cnt[w * 256 + d] + __popc(peers & ((1u << lane) - 1u));
             __syncwarp();
@@ -213,15 +220,19 @@ __global__ void embed_runs_kernel(const uint32_t *__restrict__ keys, const T *__
     auto flush = [&](int rs, int re) {
         const bool crosses = (rs == 0 && tok_before == cur) || (re == cnt && tok_after == cur);
         if (!active) return;
-        float *dst;
         if (crosses) {
-            dst = part + (int64_t)(rs == 0 ? piece : npieces + piece) * C + col;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dst[e] = acc[e];
+            float4 *dst = reinterpret_cast<float4 *>(part + (int64_t)(rs == 0 ? piece : npieces + piece) * C + col);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         } else {
-            dst = dwte + (int64_t)cur * C + col;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dst[e] += acc[e];
+            // the segment's only addition into these elements: a reduction without a wait
+            float *dst = dwte + (int64_t)cur * C + col;
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc[0]), "f"(acc[1]),
+                         "f"(acc[2]), "f"(acc[3])
+                         : "memory");
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4), "f"(acc[4]), "f"(acc[5]),
+                         "f"(acc[6]), "f"(acc[7])
+                         : "memory");
         }
     };
     for (int j0 = 0; j0 < cnt; j0 += 8) {
@@ -263,12 +274,23 @@ __global__ void embed_cross_kernel(const uint32_t *__restrict__ keys, const floa
     if (k >= 2 && (keys[32 * (k - 1) - 1] >> 16) == tk) return;  // it started before piece k - 1
     const bool starts_at_piece = (keys[32 * (k - 1)] >> 16) == tk;
     const int first = starts_at_piece ? k - 1 : npieces + k - 1;
-    int last = k;  // pieces k .. last - 1 begin with this token
-    while (last < npieces && (keys[32 * last] >> 16) == tk) ++last;
+    // pieces k .. last - 1 begin with this token: the first piece after k that begins with
+    // another token, all boundaries tested at once (block-wide minimum)
+    __shared__ int s_last;
+    if (threadIdx.x == 0) s_last = npieces;
+    __syncthreads();
+    for (int q = k + 1 + threadIdx.x; q < npieces; q += blockDim.x)
+        if ((keys[32 * q] >> 16) != tk) {
+            atomicMin(&s_last, q);
+            break;
+        }
+    __syncthreads();
+    const int last = s_last;
     for (int c = threadIdx.x; c < C; c += blockDim.x) {
         float s = part[(int64_t)first * C + c];
+#pragma unroll 8
         for (int q = k; q < last; ++q) s += part[(int64_t)q * C + c];
-        dwte[(int64_t)tk * C + c] += s;
+        atomicAdd(dwte + (int64_t)tk * C + c, s);  // the segment's only addition into this element
     }
 }
 
