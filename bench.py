@@ -330,6 +330,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
                     help="E4M3 block projections in the forward (fp8_forward); a separate line, not the headline")
+    ap.add_argument("--fused-lm-head", action="store_true",
+                    help="LM head fused with the cross-entropy, no logits buffer; a separate line, not the headline")
     ap.add_argument("--attention-sweep", action="store_true",
                     help="time the isolated causal attention workload instead of the training step")
     args = ap.parse_args()
@@ -339,6 +341,8 @@ def main():
     w = dict(synthetic.WORKLOADS[args.workload])
     if args.fp8:
         w["fp8_forward"] = 1
+    if args.fused_lm_head:
+        w["fused_lm_head"] = 1
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -520,7 +524,10 @@ def main():
                 "frac": (f8_ach / f8_peak) if f8_ach else None,
                 "peak_source": "%s %s x 2 (nominal E4M3 / bf16 dense ratio)" % (peak_src, peak_key),
                 "launches_per_step": f8_n / args.steps}
-        if not (args.no_cpu_baseline or args.fp8):  # the oracle's step is the bf16 headline's baseline
+        if args.fused_lm_head:
+            line["config"]["lm_head"] = ("fused with the cross-entropy: row partials in the forward, logits "
+                                         "recomputed in 8,192-position chunks in the backward (no full logits buffer)")
+        if not (args.no_cpu_baseline or args.fp8 or args.fused_lm_head):  # the bf16 headline's baseline
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
     if dist is not None:

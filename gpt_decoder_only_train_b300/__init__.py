@@ -41,7 +41,8 @@ class Gpt2Error(RuntimeError):
 
 class gpt2_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int)
-                for n in ("L", "C", "H", "V", "Vp", "T", "B", "dtype", "recompute_gelu", "fp8_forward")]
+                for n in ("L", "C", "H", "V", "Vp", "T", "B", "dtype", "recompute_gelu", "fp8_forward",
+                          "fused_lm_head")]
 
 
 _lib = None
@@ -128,7 +129,7 @@ def make_config(d: dict) -> gpt2_config:
     dt = d.get("dtype", "bf16")
     dtype = GPT2_DTYPE_BF16 if dt in ("bf16", GPT2_DTYPE_BF16) else GPT2_DTYPE_FP32
     return gpt2_config(d["L"], d["C"], d["H"], d["V"], d["Vp"], d["T"], d["B"], dtype, int(d.get("recompute_gelu", 0)),
-                       int(d.get("fp8_forward", 0)))
+                       int(d.get("fp8_forward", 0)), int(d.get("fused_lm_head", 0)))
 
 
 def launch_count() -> int:

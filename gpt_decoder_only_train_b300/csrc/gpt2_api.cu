@@ -99,6 +99,11 @@ struct gpt2_model {
     int64_t *w8_off, *w8_n;  // device tables over the quantised tensors
     std::vector<int> w8_ids;  // tensor ids of the quantised tensors, in table order
     int64_t w8_maxn;
+    // fused LM head (fused_lm_head): cross-entropy partials [B*T, ce_stride], target logits
+    // and lse [B*T]; the logits buffer holds lm_rows rows (a chunk of the backward)
+    float2 *ce_part;
+    float *ce_zt, *ce_lse;
+    int ce_stride, lm_rows;
     std::vector<LayerBuf> layers;
     void *resid_final, *lnf;
     float *lnf_mean, *lnf_rstd;
@@ -160,6 +165,8 @@ bool valid_config(const gpt2_config &c) {
     if (c.dtype != GPT2_DTYPE_FP32 && c.dtype != GPT2_DTYPE_BF16) return false;
     if (c.fp8_forward != 0 && c.fp8_forward != 1) return false;
     if (c.fp8_forward && (c.dtype != GPT2_DTYPE_BF16 || c.C < 128)) return false;
+    if (c.fused_lm_head != 0 && c.fused_lm_head != 1) return false;
+    if (c.fused_lm_head && (c.dtype != GPT2_DTYPE_BF16 || c.Vp < 128)) return false;
     const int hd = c.C / c.H;
     if (c.dtype == GPT2_DTYPE_FP32) {
         if (c.C % 4 || c.Vp % 4 || (hd != 8 && hd != 16 && hd != 32 && hd != 64)) return false;
@@ -224,6 +231,8 @@ void make_tensors(const gpt2_config &c, std::vector<TensorInfo> &ts, std::vector
 
 template <typename P> P *take_opt(Bump &b, bool on, size_t bytes) { return on ? b.take<P>(bytes) : nullptr; }
 
+constexpr int64_t kLmChunkRows = 8192;  // positions per chunk of the fused LM head's backward
+
 void plan(gpt2_model &m, uint8_t *base) {
     const gpt2_config &c = m.cfg;
     const bool bf = c.dtype == GPT2_DTYPE_BF16;
@@ -265,7 +274,13 @@ void plan(gpt2_model &m, uint8_t *base) {
     m.lnf = b.take<void>(BT * C * es);
     m.lnf_mean = b.take<float>(BT * 4);
     m.lnf_rstd = b.take<float>(BT * 4);
-    m.logits = b.take<void>(BT * (int64_t)c.Vp * es);
+    const bool fl = c.fused_lm_head != 0;
+    m.lm_rows = (int)(fl ? std::min<int64_t>(BT, kLmChunkRows) : BT);
+    m.logits = b.take<void>((int64_t)m.lm_rows * c.Vp * es);
+    m.ce_stride = fl ? 2 * ceil_div(c.Vp, c.Vp >= 256 ? 256 : 128) : 0;
+    m.ce_part = take_opt<float2>(b, fl, (size_t)BT * m.ce_stride * 8);
+    m.ce_zt = take_opt<float>(b, fl, BT * 4);
+    m.ce_lse = take_opt<float>(b, fl, BT * 4);
     m.loss_rows = b.take<float>(BT * 4);
     m.loss_dev = b.take<float>(64);
     m.norm_dev = b.take<float>(64);
@@ -442,6 +457,34 @@ int mm8(gpt2_model *m, const uint8_t *A8, int64_t lda, const float *a_inv, int w
     return timed(m, GPT2_PROF_MATMUL_E4M3, 2.0 * M * N * K, [&] { return tcg::launch_gemm_tc(g, m->num_sms, m->stream); });
 }
 
+// The fused LM head's product z = y_f wte^T over rows [r0, r0 + rows) with a cross-entropy
+// epilogue: EPI_LSE (forward: row partials and target logits) or EPI_DZ (backward:
+// dlogits for a unit loss weight into the logits buffer).
+int lm_head_ce(gpt2_model *m, int epi, int r0, int rows, int BT) {
+    const gpt2_config &c = m->cfg;
+    tcg::GemmDesc g;
+    g.A = (const bf16 *)m->lnf + (int64_t)r0 * c.C;
+    g.lda = c.C;
+    g.B = W<bf16>(m, 0);
+    g.ldb = c.C;
+    g.D = epi == tcg::EPI_DZ ? m->logits : nullptr;
+    g.ldd = c.Vp;
+    g.M = rows;
+    g.N = c.Vp;
+    g.K = c.C;
+    g.epi = epi;
+    g.err = m->err_dev;
+    g.vocab = c.V;
+    g.row_tgt = m->targets + r0;
+    g.row_lse = m->ce_lse + r0;
+    g.row_part = m->ce_part + (int64_t)r0 * m->ce_stride;
+    g.part_stride = m->ce_stride;
+    g.row_zt = m->ce_zt + r0;
+    g.dz_scale = 1.0f / BT;
+    return timed(m, GPT2_PROF_MATMUL, 2.0 * rows * c.Vp * c.C,
+                 [&] { return tcg::launch_gemm_tc(g, m->num_sms, m->stream); });
+}
+
 // Refresh the E4M3 weight codes from the bf16 weight copy (one amax per tensor).
 int quantize_weights(gpt2_model *m) {
     if (!m->w8) return GPT2_OK;
@@ -554,6 +597,17 @@ int forward_impl(gpt2_model *m, bool with_targets, int B, int Tn) {
     TIMED(GPT2_PROF_LAYERNORM, 2 * act + stats,
           k::layernorm_forward<T>((T *)m->resid_final, Pf(m, nt - 2), Pf(m, nt - 1), (T *)m->lnf, m->lnf_mean,
                                   m->lnf_rstd, BT, C, st));
+    if constexpr (sizeof(T) == 2) {
+        if (c.fused_lm_head && with_targets) {  // no logits: row partials, then lse and the loss
+            TRY(lm_head_ce(m, tcg::EPI_LSE, 0, BT, BT));
+            TIMED(GPT2_PROF_CLASSIFIER, 8.0 * BT * m->ce_stride + 16.0 * BT,
+                  k::ce_combine(m->ce_part, m->ce_stride, m->ce_stride, m->ce_zt, m->targets, BT, c.V, m->ce_lse,
+                                m->loss_rows, m->err_dev, st));
+            TIMED(GPT2_PROF_OTHER, 4.0 * BT, k::mean_rows(m->loss_rows, BT, m->loss_dev, st));
+            return GPT2_OK;
+        }
+    }
+    if (BT > m->lm_rows) return GPT2_ERR_UNSUPPORTED;  // fused LM head: logits of at most lm_rows positions
     TRY(mm<T>(m, m->lnf, C, true, W<T>(m, 0), C, true, m->logits, nullptr, nullptr, c.Vp, nullptr, BT, c.Vp, C,
               GPT2_EPI_STORE));
     if (with_targets) {
@@ -574,11 +628,19 @@ int backward_impl(gpt2_model *m, float grad_scale) {
     const double es = sizeof(T), act = (double)BT * C * es, stats = 8.0 * BT;
     T *dres = (T *)m->dres, *dbig = (T *)m->dbig, *dqkv = (T *)m->dqkv, *datt = (T *)m->datt,
       *dsmall = (T *)m->dsmall;
-    // LM head (tied): dy_f = alpha dz wte ; dwte += alpha dz^T y_f
-    TRY(mm<T>(m, m->logits, Vp, true, W<T>(m, 0), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, Vp,
-              GPT2_EPI_STORE, grad_scale));
-    TRY(mm<T>(m, m->logits, Vp, false, m->lnf, C, false, Gf(m, 0), nullptr, nullptr, C, nullptr, Vp, C, BT,
-              GPT2_EPI_ACCUM_F32, grad_scale));
+    // LM head (tied): dy_f = alpha dz wte ; dwte += alpha dz^T y_f.  With the fused LM head dz
+    // is recomputed chunk by chunk (logits, then dlogits in the product's epilogue).
+    const int lm_rows = c.fused_lm_head ? m->lm_rows : BT;
+    for (int r0 = 0; r0 < BT; r0 += lm_rows) {
+        const int rows = std::min(lm_rows, BT - r0);
+        if constexpr (sizeof(T) == 2) {
+            if (c.fused_lm_head) TRY(lm_head_ce(m, tcg::EPI_DZ, r0, rows, BT));
+        }
+        TRY(mm<T>(m, m->logits, Vp, true, W<T>(m, 0), C, false, dsmall + (int64_t)r0 * C, nullptr, nullptr, C, nullptr,
+                  rows, C, Vp, GPT2_EPI_STORE, grad_scale));
+        TRY(mm<T>(m, m->logits, Vp, false, (T *)m->lnf + (int64_t)r0 * C, C, false, Gf(m, 0), nullptr, nullptr, C,
+                  nullptr, Vp, C, rows, GPT2_EPI_ACCUM_F32, grad_scale));
+    }
     // The LayerNorm backward kernels also add the column sums of the residual
     // gradient they produce into the bias gradient of the projection that
     // consumes it (the last block's MLP output projection here).
@@ -1050,7 +1112,7 @@ extern "C" int gpt2_debug_buffer(gpt2_model *m, const char *name, void **dev_ptr
         return (l >= 0 && l < lim) ? l : -1;
     };
     int l;
-    if (s == "logits") { *dev_ptr = m->logits; *bytes = BT * c.Vp * es; }
+    if (s == "logits") { *dev_ptr = m->logits; *bytes = (size_t)m->lm_rows * c.Vp * es; }
     else if (s == "loss_rows") { *dev_ptr = m->loss_rows; *bytes = BT * 4; }
     else if (s == "lnf") { *dev_ptr = m->lnf; *bytes = BT * c.C * es; }
     else if ((l = layer_of("qkv.", c.L)) >= 0) { *dev_ptr = m->layers[l].qkv; *bytes = BT * 3 * c.C * es; }

@@ -1422,6 +1422,42 @@ int mean_rows(const float *rows, int N, float *out, cudaStream_t st) {
     return GPT2_OK;
 }
 
+// One warp per row: the row's lse from its half-tile partials, combined in a fixed
+// order (lane stride, then the warp tree), and its loss.
+__global__ void ce_combine_kernel(const float2 *__restrict__ part, int stride, int nparts, const float *__restrict__ zt,
+                                  const int *__restrict__ targets, int N, int V, float *__restrict__ lse,
+                                  float *__restrict__ loss_rows, int *err) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= N) return;
+    const float2 *p = part + (int64_t)row * stride;
+    float m = -INFINITY;
+    for (int j = lane; j < nparts; j += 32) m = fmaxf(m, p[j].x);
+    m = warp_max(m);
+    float s = 0.f;
+    for (int j = lane; j < nparts; j += 32) {
+        const float2 v = p[j];
+        if (v.y > 0.f) s += v.y * expf(v.x - m);
+    }
+    s = warp_sum(s);
+    if (lane == 0) {
+        const float l = m + logf(s);
+        lse[row] = l;
+        loss_rows[row] = l - zt[row];
+        const int t = targets[row];
+        if (t < 0 || t >= V) raise_device_error(err, DEVERR_BAD_TOKEN);
+    }
+}
+
+int ce_combine(const float2 *part, int stride, int nparts, const float *zt, const int *targets, int N, int V,
+               float *lse, float *loss_rows, int *err, cudaStream_t st) {
+    if (N <= 0 || nparts <= 0 || stride < nparts) return GPT2_ERR_BAD_SHAPE;
+    ce_combine_kernel<<<ceil_div(N, 8), 256, 0, st>>>(part, stride, nparts, zt, targets, N, V, lse, loss_rows, err);
+    GPT2_CUDA_TRY(cudaGetLastError());
+    gpt2_note_launches(1);
+    return GPT2_OK;
+}
+
 // ============================================================== GELU recompute, casts
 template <typename T>
 __global__ void gelu_fwd_kernel(const T *__restrict__ h, T *__restrict__ y, int64_t n) {

@@ -36,6 +36,14 @@ __device__ __forceinline__ uint32_t e4m3_of(float x) {
 }
 
 // E4M3 per-row copy of bf16 x [M, K] (rows scaled by 448 / amax; inv = amax / 448)
+// Cross-entropy from the LM head's partials (the fused LM head): part[row * stride + j],
+// j < nparts, holds (max, sum of exp(z - max)) over one half tile of the row's real
+// logits (max -inf and sum 0 for none); zt[row] is the target's logit.  Writes
+// lse[row] and loss_rows[row] = lse - zt; an invalid target raises the device
+// error word (its row was computed as token 0).
+int ce_combine(const float2 *part, int stride, int nparts, const float *zt, const int *targets, int N, int V,
+               float *lse, float *loss_rows, int *err, cudaStream_t st);
+
 int quantize_rows_e4m3(const bf16 *x, int64_t ldx, int M, int K, uint8_t *q, int64_t ldq, float *inv,
                        cudaStream_t st);
 // E4M3 copies of several bf16 tensors of one flat array, one scale each:

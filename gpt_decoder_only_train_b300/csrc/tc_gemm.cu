@@ -95,7 +95,17 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPT2_ERR_BAD_SHAPE;
-    if (!g.A || !g.B || !g.D) return GPT2_ERR_BAD_ARG;
+    const bool lse = g.epi == EPI_LSE, dz = g.epi == EPI_DZ;
+    if (!g.A || !g.B || (!g.D && !lse)) return GPT2_ERR_BAD_ARG;
+    if (lse || dz) {  // the cross-entropy epilogues: bf16 K-major operands, plain products
+        if (g.fp8 || !g.a_kmajor || !g.b_kmajor || g.alpha != 1.0f || g.bias || g.dbias || g.N < 128 ||
+            g.vocab <= 0 || g.vocab > g.N || !g.row_tgt)
+            return GPT2_ERR_UNSUPPORTED;
+        if (lse && (!g.row_part || !g.row_zt || g.part_stride < 2 * ceil_div(g.N, g.N >= 256 ? 256 : 128) ||
+                    (reinterpret_cast<uintptr_t>(g.row_part) & 7)))
+            return GPT2_ERR_BAD_ARG;
+        if (dz && !g.row_lse) return GPT2_ERR_BAD_ARG;
+    }
     if ((g.lda % 8) || (g.ldb % 8) || (g.ldd % 8) || (g.N % 8)) return GPT2_ERR_BAD_SHAPE;
     if (g.fp8 && (!g.a_kmajor || !g.b_kmajor || g.lda % 16 || g.ldb % 16 || g.N < 128 ||
                   g.epi == GPT2_EPI_ACCUM_F32 || g.epi == GPT2_EPI_GELU_BWD))
@@ -103,8 +113,8 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     if ((g.a_scale && (reinterpret_cast<uintptr_t>(g.a_scale) & 3)) ||
         (g.b_scale && (reinterpret_cast<uintptr_t>(g.b_scale) & 3)))
         return GPT2_ERR_BAD_ARG;
-    if (!aligned16(g.A) || !aligned16(g.B) || !aligned16(g.D)) return GPT2_ERR_BAD_ARG;
-    if (g.epi < GPT2_EPI_STORE || g.epi > GPT2_EPI_ACCUM_F32) return GPT2_ERR_BAD_ARG;
+    if (!aligned16(g.A) || !aligned16(g.B) || (!lse && !aligned16(g.D))) return GPT2_ERR_BAD_ARG;
+    if ((g.epi < GPT2_EPI_STORE || g.epi > GPT2_EPI_ACCUM_F32) && !lse && !dz) return GPT2_ERR_BAD_ARG;
     if ((g.epi == GPT2_EPI_RESIDUAL || g.epi == GPT2_EPI_GELU_BWD) && (!g.R || !aligned16(g.R)))
         return GPT2_ERR_BAD_ARG;
     if (g.epi == GPT2_EPI_GELU && (!g.D2 || !aligned16(g.D2))) return GPT2_ERR_BAD_ARG;
@@ -124,7 +134,7 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     const bool pair = BN == 256 && (g.epi == GPT2_EPI_ACCUM_F32
                                         ? pair_tiles >= 16
                                         : (g.K >= 1024 || g.epi == GPT2_EPI_GELU ||
-                                           (g.epi == GPT2_EPI_STORE && g.N >= 2048)));
+                                           ((g.epi == GPT2_EPI_STORE || lse || dz) && g.N >= 2048)));
     const int conc = pair ? num_sms / 2 : num_sms;  // work units that run at once
     Params P;
     P.M = g.M;
@@ -170,6 +180,13 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     P.dbias = g.epi == GPT2_EPI_ACCUM_F32 ? nullptr : g.dbias;
     P.a_scale = g.a_scale;
     P.b_scale = g.b_scale;
+    P.vocab = g.vocab;
+    P.part_stride = g.part_stride;
+    P.row_tgt = g.row_tgt;
+    P.row_lse = g.row_lse;
+    P.row_part = g.row_part;
+    P.row_zt = g.row_zt;
+    P.dz_scale = g.dz_scale;
     P.R = g.R;
     P.D = g.D;
     P.D2 = g.D2;
@@ -193,7 +210,7 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
 
     // bf16 outputs leave through TMA stores from the epilogue's staging blocks (box 64 x 32)
     CUtensorMap td = ta, td2 = ta;  // unused copies when there is no bf16 output
-    if (g.epi != GPT2_EPI_ACCUM_F32 && (rc = encode_tmap(&td, g.D, g.N, g.M, g.ldd, 64, 32))) return rc;
+    if (g.epi != GPT2_EPI_ACCUM_F32 && !lse && (rc = encode_tmap(&td, g.D, g.N, g.M, g.ldd, 64, 32))) return rc;
     if (g.epi == GPT2_EPI_GELU && (rc = encode_tmap(&td2, g.D2, g.N, g.M, g.ldd, 64, 32))) return rc;
 
     const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;

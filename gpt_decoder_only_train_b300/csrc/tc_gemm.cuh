@@ -40,6 +40,16 @@ constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quadrant, each owning h
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;  // 4 s: far above any legitimate wait
 
+// Epilogues of the LM head fused with the cross-entropy (not part of the C ABI's
+// GPT2_EPI_* set).  Columns at or past `vocab` are padding and take no part.
+//  EPI_LSE: no output; per row and per half tile (BN / 2 columns) the pair
+//           (max, sum of exp(z - max)) goes to row_part[row * part_stride +
+//           2 * n_tile + half], and z[row, tgt[row]] to row_zt[row].
+//  EPI_DZ:  bf16 output dz = (exp(z - lse[row]) - [col == tgt[row]]) * dz_scale
+//           for col < vocab, 0 past it.
+constexpr int EPI_LSE = 100;
+constexpr int EPI_DZ = 101;
+
 struct Params {
     int M, N, K;
     int num_m_blocks, num_n_blocks, num_k_blocks;
@@ -52,6 +62,13 @@ struct Params {
     float *dbias;  // optional: += column sums of the stored bf16 output (bias gradient of the product)
     const float *a_scale;  // optional: per-row factor of acc (E4M3 operands: row dequantisation of A)
     const float *b_scale;  // optional: one factor of acc (E4M3 operands: dequantisation of B)
+    // EPI_LSE / EPI_DZ (see above)
+    int vocab, part_stride;
+    const int *row_tgt;
+    const float *row_lse;
+    float2 *row_part;
+    float *row_zt;
+    float dz_scale;
     void *D;
     bf16 *D2;
     int64_t ldd;
@@ -339,6 +356,56 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// EPI_LSE: fold 64 columns of one row's logits (starting at col) into its
+// running (max m, sum s of 2^((z - m) log2 e)); record z at the row's target.
+__device__ __forceinline__ void lse_group(const Params &P, int row, int col, const uint32_t (&r0)[32],
+                                          const uint32_t (&r1)[32], float &m, float &s);
+
+// 2^x with the hardware approximation (MUFU.EX2, flush-to-zero): the
+// cross-entropy's exponentials are summed in fp32 or stored as bf16, far above
+// its error.
+__device__ __forceinline__ float ex2_hw(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float LOG2E_F = 1.4426950408889634f;
+
+__device__ __forceinline__ void lse_group(const Params &P, int row, int col, const uint32_t (&r0)[32],
+                                          const uint32_t (&r1)[32], float &m, float &s) {
+    const int nv = min(64, P.vocab - col);  // real columns of the group (may be <= 0)
+    if (nv <= 0) return;
+    float gm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        gm = fmaxf(gm, i < nv ? __uint_as_float(r0[i]) : -INFINITY);
+        gm = fmaxf(gm, 32 + i < nv ? __uint_as_float(r1[i]) : -INFINITY);
+    }
+    const float nm = fmaxf(m, gm), nb = -nm * LOG2E_F;
+    float acc = s * ex2_hw((m - nm) * LOG2E_F);  // m = -inf: the factor is 0 (s is 0 too)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        acc += i < nv ? ex2_hw(fmaf(__uint_as_float(r0[i]), LOG2E_F, nb)) : 0.f;
+        acc += 32 + i < nv ? ex2_hw(fmaf(__uint_as_float(r1[i]), LOG2E_F, nb)) : 0.f;
+    }
+    m = nm;
+    s = acc;
+    if (row < P.M) {
+        int tg = P.row_tgt[row];
+        if (tg < 0 || tg >= P.vocab) tg = 0;  // an invalid target counts as token 0 (reported elsewhere)
+        const int tc = tg - col;
+        if (tc >= 0 && tc < 64) {
+            float z = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                z = tc == i ? __uint_as_float(r0[i]) : z;
+                z = tc == 32 + i ? __uint_as_float(r1[i]) : z;
+            }
+            P.row_zt[row] = z;
+        }
+    }
+}
+
 // 32 accumulator columns of one row -> global memory.
 __device__ __forceinline__ void epilogue_chunk(const Params &P, int row, int col0, const uint32_t (&r)[32]) {
     if (row >= P.M) return;
@@ -491,6 +558,21 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, const CUtensor
             if (col0 + i < P.N) b = *reinterpret_cast<const float4 *>(P.bias + col0 + i);
             x[i / 2] = f2_add(x[i / 2], f2(b.x, b.y));
             x[i / 2 + 1] = f2_add(x[i / 2 + 1], f2(b.z, b.w));
+        }
+    }
+    if (P.epi == EPI_DZ) {  // dz of the cross-entropy from the recomputed logits
+        const int rr = min(row0 + lane, P.M - 1);
+        const float nl = -P.row_lse[rr] * LOG2E_F;
+        int tg = P.row_tgt[rr];
+        if (tg < 0 || tg >= P.vocab) tg = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int c = col0 + 2 * i;
+            float d0 = c < P.vocab ? ex2_hw(fmaf(f2_lo(x[i]), LOG2E_F, nl)) : 0.f;
+            float d1 = c + 1 < P.vocab ? ex2_hw(fmaf(f2_hi(x[i]), LOG2E_F, nl)) : 0.f;
+            if (c == tg) d0 -= 1.f;
+            if (c + 1 == tg) d1 -= 1.f;
+            x[i] = f2(d0 * P.dz_scale, d1 * P.dz_scale);
         }
     }
     // the output staging block is free once the TMA store that last used it has read it
@@ -802,6 +884,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int c_begin = col_half * HALF;
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + c_begin);
             if constexpr (HALF >= 64) {
+                if (P.epi == EPI_LSE) {  // cross-entropy partials of the row over this half tile; no output
+                    float lm = -INFINITY, ls = 0.f;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < HALF; c0 += 64) {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(tbase + c0, r0);
+                        tmem_ld32(tbase + c0 + 32, r1);
+                        tmem_ld_wait();
+                        if (c0 + 64 == HALF) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if constexpr (PAIR)
+                                    release_accumulator(&tempty[acc], rank);
+                                else
+                                    mbar_arrive(&tempty[acc]);
+                            }
+                        }
+                        lse_group(P, row, n0 + c_begin + c0, r0, r1, lm, ls);
+                    }
+                    if (row < P.M) P.row_part[(int64_t)row * P.part_stride + 2 * (n0 / BN) + col_half] = make_float2(lm, ls);
+                    continue;
+                }
                 const bool need_r = P.epi == GPT2_EPI_RESIDUAL || P.epi == GPT2_EPI_GELU_BWD;
                 uint8_t *rstage = (Lay::EPI_BUFS > 1 && need_r) ? stage + EPI_STAGE_BYTES : nullptr;
                 uint8_t *gstage = (Lay::EPI_BUFS > 1 && P.epi == GPT2_EPI_GELU) ? stage + EPI_STAGE_BYTES : nullptr;
@@ -903,6 +1008,14 @@ struct GemmDesc {
     bool fp8 = false;
     const float *a_scale = nullptr;
     const float *b_scale = nullptr;
+    // EPI_LSE / EPI_DZ: vocabulary size, targets, per-row lse (EPI_DZ), partials and
+    // target logits (EPI_LSE, part_stride >= 2 * ceil(N / 256) float2 per row), dz factor
+    int vocab = 0, part_stride = 0;
+    const int *row_tgt = nullptr;
+    const float *row_lse = nullptr;
+    float2 *row_part = nullptr;
+    float *row_zt = nullptr;
+    float dz_scale = 1.0f;
 };
 
 int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream);

@@ -72,6 +72,14 @@ typedef struct {
                            forward (QKV, attention output, FC, FC output) multiply E4M3
                            codes -- activations scaled per row, weights per tensor -- and
                            the backward stays bf16 (straight-through); 0: bf16 throughout */
+    int fused_lm_head;  /* 1 (bf16 only): the LM head and the cross-entropy without a [B*T, Vp]
+                           logits buffer.  The forward's LM-head product keeps per-row
+                           (max, sum exp) partials and the target logit in its epilogue; the
+                           backward recomputes the logits in row chunks of up to 8,192
+                           positions, turns them into dlogits in the epilogue and runs the
+                           two LM-head gradient products per chunk.  A forward without
+                           targets then serves at most that many positions (else
+                           GPT2_ERR_UNSUPPORTED).  0: logits stored, classifier pass */
 } gpt2_config;
 
 typedef struct gpt2_model gpt2_model; /* opaque host handle */
