@@ -418,8 +418,10 @@ __device__ __forceinline__ uint32_t f2_bf16x2(F2 v) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Rows of up to 1,024 bf16 (VPL <= 4 packets a lane): six blocks per SM (40 registers, no
+// spills) instead of the five the unconstrained build allows; wider rows unconstrained.
 template <int VPL>
-__global__ void ln_fwd_bf16_kernel(const bf16 *__restrict__ x, const float *__restrict__ g,
+__global__ void __launch_bounds__(256, (VPL <= 4 ? 6 : 1)) ln_fwd_bf16_kernel(const bf16 *__restrict__ x, const float *__restrict__ g,
                                    const float *__restrict__ b, bf16 *__restrict__ y, float *__restrict__ mean,
                                    float *__restrict__ rstd, int N, int C, uint8_t *__restrict__ q,
                                    float *__restrict__ qinv) {
