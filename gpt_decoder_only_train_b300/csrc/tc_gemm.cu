@@ -126,15 +126,12 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     // CTA pairs on 256 x 256 tiles (cta_group::2): each SM reads half of the B
     // tile per stage, which keeps shared-memory traffic per MMA within what the
     // SM delivers, at the cost of pair synchronisation per tile.  Measured on
-    // the model's shapes, pairs pay off for long K, for large plain outputs, for
-    // the GELU forward and for weight gradients with enough tiles; short-K
-    // products that read a second operand (residual, GELU backward) or have few
-    // tiles stay on single CTAs.
-    const int pair_tiles = ceil_div(g.M, 2 * BM) * ceil_div(g.N, 256);
-    const bool pair = BN == 256 && (g.epi == GPT2_EPI_ACCUM_F32
-                                        ? pair_tiles >= 16
-                                        : (g.K >= 1024 || g.epi == GPT2_EPI_GELU ||
-                                           ((g.epi == GPT2_EPI_STORE || lse || dz) && g.N >= 2048)));
+    // the model's shapes (one build, alternating), pairs pay off everywhere
+    // except for short-K products that add a residual (16384 x 768 x 768: equal
+    // times), which stay on single CTAs; the last to move were the plain and
+    // the weight-gradient 768-wide products (-9% and -7%) and the GELU backward
+    // (-3%).
+    const bool pair = BN == 256 && (g.epi != GPT2_EPI_RESIDUAL || g.K >= 1024);
     const int conc = pair ? num_sms / 2 : num_sms;  // work units that run at once
     Params P;
     P.M = g.M;
