@@ -141,8 +141,8 @@ GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
     "workload": "gpt2_124m",
-    "sha256": "49240494b0761574f0c1a0e13bdc385f516bc72de05462f788215b14cc8ae8a8",
-    "bytes_per_launch": 22.99e9 / 147,
+    "sha256": "3df45b041602d180f09f4f2ce2e7c689e19c30612c585784bbbea39b93a13a13",
+    "bytes_per_launch": 22.96e9 / 147,
 }
 
 
