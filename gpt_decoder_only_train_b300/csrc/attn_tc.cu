@@ -118,7 +118,7 @@ constexpr uint32_t C_S = 0, C_O = 256, C_Q = 384;  // S[b] [128b, +128), O[b] [2
 struct Bars {
     uint64_t drain;
     uint64_t q_sfull[2], q_sempty[2], q_tfull[2];
-    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];  // o_done: per block parity; o_free: per item parity
     uint64_t xmax[4][2], xsum[4];  // exchanges between the two softmax warps of a TMEM lane quadrant
     uint64_t full[SLOTS], empty[SLOTS];
 };
@@ -131,13 +131,16 @@ struct Bars {
 //              a ring of SLOTS shared-memory tiles (128-byte swizzle);
 //   warp 1     one thread issues tcgen05.mma: S_j = Q K_j^T (A = Q in TMEM)
 //              two key blocks ahead into a double-buffered S, and
-//              O_j = P_j V_j (A = P_j in TMEM) into a double-buffered O;
+//              O += P_j V_j (A = P_j in TMEM) into the item's O accumulator
+//              (two, alternating by item);
 //   warps 2-9  softmax: two threads per query row (= TMEM lane), each owning
 //              64 of a block's 128 keys and 32 of the 64 output columns.  They
-//              read S with tcgen05.ld, mask, exchange the row max, write
+//              read S with tcgen05.ld, mask, exchange the row max, and write
 //              P = 2^(s - m) as bf16 over the first 32 of their own 64 S
-//              columns, and fold O_{j-1} into a register accumulator with the
-//              running rescale.  O = acc / l and lse are written per item.
+//              columns.  The reference max m of a row moves only when a block
+//              exceeds it by more than 2^8; the O accumulated so far is then
+//              rescaled in TMEM before P_j is released.  O / l and lse are
+//              written per item.
 // The T x T matrix is never stored ("Let's reproduce GPT-2 (124M)", §Video
 // özeti: flash attention); the mask lets a query see itself and the past
 // ("Let's build GPT: from scratch", 00:57:00 erratum; scale 1/sqrt(head_size),
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(fwd::NTH, 1)
             mbar_init(&bar->q_tfull[i], SWARPS);
             mbar_init(&bar->s_full[i], 1);
             mbar_init(&bar->p_full[i], SWARPS);
-            mbar_init(&bar->o_full[i], 1);
+            mbar_init(&bar->o_done[i], 1);
             mbar_init(&bar->o_free[i], SWARPS);
         }
         for (int qd = 0; qd < 4; ++qd) {
@@ -259,21 +262,23 @@ __global__ void __launch_bounds__(fwd::NTH, 1)
                 if (++sit == sn) sit = 0, s_on = item_len(++sj, sn);
                 return true;
             };
-            auto issue_o = [&]() -> bool {  // O_go = P V into O[go & 1]
-                const int b2 = go & 1, tv_ = 2 * go + 1, s = tv_ % SLOTS;
+            auto issue_o = [&]() -> bool {  // O[item] (+)= P_go V: the item's O accumulates in TMEM
+                const int b2 = go & 1, tv_ = 2 * go + 1, s = tv_ % SLOTS, ob = gj & 1;
                 if (!mbar_wait(&bar->p_full[b2], (go >> 1) & 1, abort_flag, nullptr)) return false;
-                if (go >= 2 && !mbar_wait(&bar->o_free[b2], ((go - 2) >> 1) & 1, abort_flag, nullptr)) return false;
+                // the item two back used this O buffer: its read-out must be done
+                if (git == 0 && gj >= 2 && !mbar_wait(&bar->o_free[ob], ((gj - 2) >> 1) & 1, abort_flag, nullptr))
+                    return false;
                 if (!mbar_wait(&bar->full[s], (tv_ / SLOTS) & 1, abort_flag, nullptr)) return false;
                 tc_fence_after();
-                const uint32_t pa = tmem + C_S + 128 * b2, to = tmem + C_O + 64 * b2;
+                const uint32_t pa = tmem + C_S + 128 * b2, to = tmem + C_O + 64 * ob;
                 const uint64_t bv = ring_mn + (uint64_t)(s * (TILE >> 4));
                 // K-step kk (keys 16kk..16kk+15): P columns 64 (kk / 4) + 8 (kk % 4)
-                tc_mma_ts(to, pa, bv, ID_O, 0u);
+                tc_mma_ts(to, pa, bv, ID_O, git > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 1; kk < BKV / 16; ++kk)
                     tc_mma_ts(to, pa + 64 * (kk >> 2) + 8 * (kk & 3), bv + 128 * kk, ID_O, 1u);
                 tc_commit(&bar->empty[s]);
-                tc_commit(&bar->o_full[b2]);
+                tc_commit(&bar->o_done[b2]);
                 ++go;
                 if (++git == gn) git = 0, o_on = item_len(++gj, gn);
                 return true;
@@ -326,30 +331,17 @@ __global__ void __launch_bounds__(fwd::NTH, 1)
             if (p < 0) break;
             const int qb = item_qb(p), bh = p % BH, b = bh / H, h = bh % H, nkv = qb + 1;
             const int q = qb * BQ + r;
-            float acc[32];
-#pragma unroll
-            for (int d = 0; d < 32; ++d) acc[d] = 0.f;
-            float m = -INFINITY, l = 0.f, m_acc = -INFINITY, m_pend = -INFINITY;
-            // fold O_gp (block gp of this item) into acc with the running rescale
-            auto fold_o = [&](int gp) -> bool {
-                const int b2 = gp & 1;
-                if (!mbar_wait(&bar->o_full[b2], (gp >> 1) & 1, abort_flag, nullptr)) return false;
-                tc_fence_after();
-                const float c = ex2(m_acc - m_pend);
-                float f[32];
-                tmem_ld32f(tmem + lane_off + C_O + 64 * b2 + 32 * half, f);
-                const F2 c2 = f2(c, c);
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const F2 a = f2_fma(f2(acc[i], acc[i + 1]), c2, f2(f[i], f[i + 1]));
-                    acc[i] = f2_lo(a);
-                    acc[i + 1] = f2_hi(a);
-                }
-                m_acc = m_pend;
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar->o_free[b2]);
-                return true;
+            const int ob = j & 1;
+            const uint32_t to = tmem + lane_off + C_O + 64 * ob + 32 * half;  // this thread's 32 O columns
+            // m: the row's reference maximum (log2 units) of P and of the O accumulated so far.  It
+            // moves only when a block's maximum exceeds it by more than RESCALE (always in the first
+            // block): P then stays below 2^RESCALE and the accumulated O is rescaled once.
+            constexpr float RESCALE = 8.0f;
+            float m = -INFINITY, l = 0.f;
+            // block gp's O product has completed (waits are taken in block order: at most one
+            // completion of each barrier is pending, so its parity identifies it)
+            auto o_done_wait = [&](int gp) -> bool {
+                return mbar_wait(&bar->o_done[gp & 1], (gp >> 1) & 1, abort_flag, nullptr);
             };
             for (int jj = 0; jj < nkv; ++jj, ++g) {
                 const int bb = g & 1;
@@ -365,31 +357,59 @@ __global__ void __launch_bounds__(fwd::NTH, 1)
                 tmem_ld32(ts, sr[0]);
                 tmem_ld32(ts + 32, sr[1]);
                 tmem_ld_wait();
-                // pass 1: row max of the masked scores (three-input max)
+                // pass 1: row max of the masked scores (three-input max, four independent chains)
                 float mx = -INFINITY;
                 if (ok) {
+                    float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         if (block_full) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 2)
-                                mx = fmax3(mx, __uint_as_float(sr[h2][i]), __uint_as_float(sr[h2][i + 1]));
+                                mc[(i >> 1) & 3] = fmax3(mc[(i >> 1) & 3], __uint_as_float(sr[h2][i]),
+                                                         __uint_as_float(sr[h2][i + 1]));
                         } else {
 #pragma unroll
                             for (int i = 0; i < 32; i += 2) {
                                 const int c = 32 * h2 + i;
-                                mx = fmax3(mx, c <= lim ? __uint_as_float(sr[h2][i]) : -INFINITY,
-                                           c + 1 <= lim ? __uint_as_float(sr[h2][i + 1]) : -INFINITY);
+                                mc[(i >> 1) & 3] = fmax3(mc[(i >> 1) & 3], c <= lim ? __uint_as_float(sr[h2][i]) : -INFINITY,
+                                                         c + 1 <= lim ? __uint_as_float(sr[h2][i + 1]) : -INFINITY);
                             }
                         }
                     }
+                    mx = fmax3(fmax3(mc[0], mc[1], mc[2]), mc[3], -INFINITY);
                 }
                 mx *= sl2;
                 mx = fmaxf(mx, exchange(red + bb * 256, &bar->xmax[quad][bb], (g >> 1) & 1, mx, ok));
                 if (!ok) break;
-                const float m_new = fmaxf(m, mx);
-                const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-                const float corr = ex2(m - mu);
+                const bool move = mx > m + RESCALE;
+                const float m_new = move ? mx : m;
+                if (jj > 0 && __any_sync(0xffffffffu, move)) {
+                    // O holds blocks < jj: once the last of them has landed, scale this thread's columns
+                    if (!(ok = o_done_wait(g - 1))) break;
+                    tc_fence_after();
+                    const float c = move ? ex2(m - m_new) : 1.0f;
+                    const F2 c2 = f2(c, c);
+                    uint32_t ov[32];
+                    tmem_ld32(to, ov);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const F2 v = f2_mul(f2(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), c2);
+                        ov[i] = __float_as_uint(f2_lo(v));
+                        ov[i + 1] = __float_as_uint(f2_hi(v));
+                    }
+#pragma unroll
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        uint32_t w8[8];
+#pragma unroll
+                        for (int k2 = 0; k2 < 8; ++k2) w8[k2] = ov[c8 + k2];
+                        tmem_st8(to + c8, w8);
+                    }
+                    l *= c;
+                }
+                m = m_new;
+                const float mu = (m == -INFINITY) ? 0.f : m;
                 const F2 nmu = f2(-mu, -mu);
                 // pass 2: P = 2^(s sl2 - m) as bf16 over the first 32 of this thread's 64 S columns
                 F2 ls2 = f2(0.f, 0.f);
@@ -414,18 +434,23 @@ __global__ void __launch_bounds__(fwd::NTH, 1)
                     tmem_st8(ts + c0 / 2, w0);
                     tmem_st8(ts + c0 / 2 + 8, w1);
                 }
-                l = l * corr + (f2_lo(ls2) + f2_hi(ls2));
-                m = m_new;
+                l += f2_lo(ls2) + f2_hi(ls2);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar->p_full[bb]);
-                if (jj > 0 && !(ok = fold_o(g - 1))) break;
-                m_pend = m_new;
+                if (jj > 0 && !(ok = o_done_wait(g - 1))) break;  // retire block g - 1 (normally long done)
                 if (jj == 0 && item_of(j + 1, nitems) >= 0 && !(ok = stage_in(j + 1))) break;
             }
             if (!ok) break;
-            if (!(ok = fold_o(g - 1))) break;
+            // the item's O: once its last block has landed, read it and release the buffer
+            if (!(ok = o_done_wait(g - 1))) break;
+            tc_fence_after();
+            float acc[32];
+            tmem_ld32f(to, acc);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar->o_free[ob]);
             // the row sum is split over the two halves
             const float lt = l + exchange(red + 2 * 256, &bar->xsum[quad], j & 1, l, ok);
             if (!ok) break;
