@@ -61,6 +61,33 @@ def test_arena_bytes_and_config_validation(libh):
         assert L.gpt2_arena_bytes(ctypes.byref(c)) == 0, d
 
 
+def test_precision_and_lm_head_modes_are_validated_and_sized(libh):
+    """fp8_forward and fused_lm_head: bf16 only, 0 or 1; the E4M3 mode adds its code buffers
+    (one byte a parameter, the [B*T, 4C] activation codes and their factors), the fused LM head
+    replaces the [B*T, Vp] logits by one chunk of 8,192 rows plus its row partials."""
+    import gpt_decoder_only_train_b300 as g
+
+    L = g.lib()
+    base = dict(L=12, C=768, H=12, V=50257, Vp=50304, T=1024, B=16, dtype="bf16")
+    size = lambda **kw: L.gpt2_arena_bytes(ctypes.byref(g.make_config(dict(base, **kw))))
+    n0 = size()
+    n8 = size(fp8_forward=1)
+    nf = size(fused_lm_head=1)
+    assert n0 > 0 and n8 > 0 and nf > 0
+    BT, C, Vp = 16 * 1024, 768, 50304
+    # E4M3: at least one byte per parameter (124.5M) and the activation codes, at most a few MB more
+    extra8 = n8 - n0
+    assert 124.4e6 + BT * 4 * C <= extra8 <= 124.5e6 + BT * 4 * C + 8e6, extra8
+    # fused LM head: the logits shrink from B*T to 8,192 rows; partials (2 x 197 float2 a row) and
+    # two floats a row are added
+    saved = n0 - nf
+    want = (BT - 8192) * Vp * 2 - BT * 2 * 197 * 8 - 2 * BT * 4
+    assert abs(saved - want) <= 4096, (saved, want)
+    for bad in (dict(fp8_forward=1, dtype="fp32"), dict(fused_lm_head=1, dtype="fp32"), dict(fp8_forward=2),
+                dict(fused_lm_head=-1), dict(fp8_forward=1, C=64, H=1)):
+        assert size(**bad) == 0, bad
+
+
 def test_build_rejects_bad_arguments_without_touching_a_gpu(libh):
     import gpt_decoder_only_train_b300 as g
 
