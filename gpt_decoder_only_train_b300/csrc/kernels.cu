@@ -678,7 +678,8 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restr
                                                              bf16 *dres_out, float *__restrict__ dg,
                                                              float *__restrict__ db, float *__restrict__ dsum, int N,
                                                              int C) {
-    // Per warp, 3C floats of shared memory: while rows are processed they hold
+    // Per warp, 3C floats of shared memory (and C floats for the gain after all of them): while
+    // rows are processed they hold
     // two row buffers (dy, x, dres_in: 3 x C bf16 each), the next row being
     // fetched (cp.async) while the current one is computed; at the end they hold
     // the warp's dg, db and column-sum partials.  A lane only ever touches its
@@ -687,6 +688,12 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restr
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, warps = blockDim.x >> 5;
     const int npk = C / 8;
     uint8_t *wbuf = reinterpret_cast<uint8_t *>(sh + (size_t)wid * 3 * C);
+    // the gain, staged once per block in shared memory after the warps' rows: both passes of
+    // every row read it from there (global / L1 reads of it were measured 3% slower in the step)
+    float *sg = sh + (size_t)warps * 3 * C;
+    for (int c = threadIdx.x * 4; c < C; c += blockDim.x * 4)
+        *reinterpret_cast<float4 *>(sg + c) = *reinterpret_cast<const float4 *>(g + c);
+    __syncthreads();
     auto slot = [&](int b, int a) { return reinterpret_cast<uint4 *>(wbuf + (size_t)(b * 3 + a) * C * 2); };
     auto fetch = [&](int row, int b) {
         const int64_t off = (int64_t)row * C;
@@ -733,8 +740,8 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restr
         for (int i = 0; i < VPL; ++i) {
             const int p = lane + 32 * i;
             if (p < npk) {
-                const float4 g0 = *reinterpret_cast<const float4 *>(g + p * 8);
-                const float4 g1 = *reinterpret_cast<const float4 *>(g + p * 8 + 4);
+                const float4 g0 = *reinterpret_cast<const float4 *>(sg + p * 8);
+                const float4 g1 = *reinterpret_cast<const float4 *>(sg + p * 8 + 4);
                 const F2 gk[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
                 const uint4 pd = vdy[p], px = vx[p];
                 const uint32_t wd[4] = {pd.x, pd.y, pd.z, pd.w};
@@ -757,8 +764,8 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_bf16_kernel(const bf16 *__restr
         for (int i = 0; i < VPL; ++i) {
             const int p = lane + 32 * i;
             if (p < npk) {
-                const float4 g0 = *reinterpret_cast<const float4 *>(g + p * 8);
-                const float4 g1 = *reinterpret_cast<const float4 *>(g + p * 8 + 4);
+                const float4 g0 = *reinterpret_cast<const float4 *>(sg + p * 8);
+                const float4 g1 = *reinterpret_cast<const float4 *>(sg + p * 8 + 4);
                 const F2 gk[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
                 const uint4 pd = vdy[p], px = vx[p], pr = dres_in ? vr[p] : make_uint4(0u, 0u, 0u, 0u);
                 const uint32_t wd[4] = {pd.x, pd.y, pd.z, pd.w};
@@ -809,12 +816,12 @@ int layernorm_backward(const T *dy, const T *x, const float *mean, const float *
                        T *dres_out, float *dg, float *db, int N, int C, cudaStream_t st, float *dsum) {
     if (C % Pack16<T>::N) return GPT2_ERR_BAD_SHAPE;
     // 16 warps per block unless the per-warp partial rows (3C floats each) do not fit in shared memory
-    const int warps = std::max(1, std::min(16, (int)((227 * 1024) / (3 * C * sizeof(float)))));
+    const int warps = std::max(1, std::min(16, (int)((227 * 1024 - C * sizeof(float)) / (3 * C * sizeof(float)))));
     int dev = 0, sms = 0;
     GPT2_CUDA_TRY(cudaGetDevice(&dev));
     GPT2_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     const int grid = std::max(1, std::min(ceil_div(N, warps), sms));
-    const size_t smem = (size_t)warps * 3 * C * sizeof(float);
+    const size_t smem = (size_t)warps * 3 * C * sizeof(float) + (sizeof(T) == 2 ? C * sizeof(float) : 0);
     if constexpr (sizeof(T) == 2) {
         LN_VPL_SWITCH(ln_vpl<T>(C), {
             GPT2_CUDA_TRY(
