@@ -175,6 +175,8 @@ int gpt2_set_graphs(gpt2_model *m, int enable);
  * prompt position and the first drawing position run as plain launches, the
  * others replay a CUDA graph captured from them (on a stream the call creates
  * and destroys).  Synchronises the stream once, at the end.
+ * Decoding always uses the bf16 weights, whatever fp8_forward is; with
+ * fused_lm_head the B rows of logits fit in its one-chunk buffer.
  */
 int gpt2_generate(gpt2_model *m, int32_t *d_seq, int B, int T_total, int T0, const float *d_uniforms,
                   float temperature, int top_k);

@@ -177,7 +177,8 @@ def _oracle_e4m3_micro_step(ref, x, y, grad_scale=1.0):
     return float(loss)
 
 
-@pytest.mark.parametrize("cfg", [SMALL_F8, RAGGED_F8], ids=["small", "ragged"])
+@pytest.mark.parametrize("cfg", [SMALL_F8, RAGGED_F8, dict(SMALL_F8, recompute_gelu=1)],
+                         ids=["small", "ragged", "gelu_recompute"])
 def test_e4m3_forward_step_parity(g, cfg):
     seed = 21
     m = g.GPT2(cfg, seed=seed)

@@ -108,6 +108,34 @@ def test_124m_e4m3_forward_sampled_sequence_and_gradients(g):
     m.close()
 
 
+def test_124m_fused_lm_head_matches_stored_logits(g):
+    """The LM head fused with the cross-entropy at 124M (two backward chunks of 8,192 positions):
+    per-position losses within 2e-2 of the step with stored logits, every gradient's cosine
+    >= 0.999, the same norm within 0.5%, and the padded vocabulary rows untouched."""
+    w = synthetic.WORKLOADS["gpt2_124m"]
+    x, y = synthetic.step_batch(w)
+    BT = w["B"] * w["T"]
+    out = []
+    for fused in (1, 0):
+        m = g.GPT2(dict(w, fused_lm_head=fused), seed=w["seed"])
+        loss = m.forward(_dev(x), _dev(y))
+        rows = m.debug_tensor("loss_rows", torch.float32, (BT,)).cpu().numpy().copy()
+        m.backward(1.0)
+        grads = [m.grads(i) for i in range(len(m.names))]
+        norm = m.clip_and_adamw(6e-4)
+        out.append((loss, rows, grads, norm))
+        m.close()
+        del m
+        torch.cuda.empty_cache()
+    (l1, r1, g1, n1), (l0, r0, g0, n0) = out
+    assert abs(l1 - l0) <= 1e-2
+    assert np.abs(r1 - r0).max() <= 2e-2
+    for a, b in zip(g1, g0):
+        assert _cos(a, b) >= 0.999
+    assert abs(n1 - n0) <= 0.005 * n0
+    assert (g1[0][w["V"]:] == 0).all()
+
+
 def test_350m_recompute_sampled_rows_and_property(g):
     w = synthetic.WORKLOADS["gpt2_350m_recompute"]
     x, y = synthetic.step_batch(w)

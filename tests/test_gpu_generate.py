@@ -229,3 +229,23 @@ def test_generation_errors_leave_the_model_usable(g):
     m.backward(1.0)
     assert math.isfinite(loss)
     m.close()
+
+
+def test_generation_is_the_bf16_path_in_every_mode(g):
+    """Sampling decodes with the bf16 weights whatever the training forward's precision or LM-head
+    mode: an E4M3-forward model and a fused-LM-head model draw the same tokens as the plain one."""
+    cfg = SMALL_BF16
+    rng = np.random.default_rng(9)
+    B, T0, T_total = 3, 6, 30
+    prompt = rng.integers(0, cfg["V"], size=(B, T0))
+    uniforms = torch.from_numpy(rng.random((T_total - T0, B)).astype(np.float32)).cuda()
+    out = []
+    for mode in ({}, {"fp8_forward": 1}, {"fused_lm_head": 1}):
+        m, _ = _peaked(g, dict(cfg, **mode), 12, 6.0)
+        seq = np.zeros((B, T_total), dtype=np.int32)
+        seq[:, :T0] = prompt
+        sd = _dev(seq)
+        m.generate(sd, T0, uniforms, 0.9, 20)
+        out.append(sd.cpu().numpy())
+        m.close()
+    assert np.array_equal(out[0], out[1]) and np.array_equal(out[0], out[2])

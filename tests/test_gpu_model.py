@@ -154,6 +154,14 @@ def test_bf16_step_parity(g, cfg):
     for i, name in enumerate(m.names):
         c = _cos(m.grads(i), ref.grads[name].numpy())
         assert c >= 0.995, (name, c)
+    # the key part of the QKV bias gradient is zero (a key bias moves all scores of a query
+    # alike): the GPU adds nothing there, the oracle's sum cancels to rounding
+    C = cfg["C"]
+    for l in range(cfg["L"]):
+        i = m.names.index("h%d.qkv.b" % l)
+        gb, rb = m.grads(i), ref.grads["h%d.qkv.b" % l].numpy()
+        assert (gb[C:2 * C] == 0).all()
+        assert np.abs(rb[C:2 * C]).max() <= 1e-9 * np.abs(rb).max()
     norm = m.clip_and_adamw(6e-4)
     ref_norm = ref.clip_and_adamw(6e-4)
     assert abs(norm - ref_norm) <= 0.02 * ref_norm
