@@ -418,6 +418,28 @@ def main():
     ms_per_step = ms / args.steps
     value = world * args.steps * BT / (ms / 1e3)
 
+    # ---- per-step and per-phase pass (same steps, events at the step and phase boundaries on the
+    # model's stream): the median step and the forward / backward / optimizer split
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier()
+    for n, i in enumerate(range(args.warmup, nsteps)):
+        model.zero_grad()
+        ev[n][0].record(stream)
+        model.forward(X[i][0], Y[i][0])
+        ev[n][1].record(stream)
+        model.backward(1.0 / accum)
+        for j in range(1, accum):  # accumulation: the remaining pairs, timed as backward
+            model.forward(X[i][j], Y[i][j])
+            model.backward(1.0 / accum)
+        ev[n][2].record(stream)
+        model.clip_and_adamw(lr_at(i), 0.9, 0.95, 1e-8, 0.1, 1.0)
+        ev[n][3].record(stream)
+    barrier()
+    step_ms = sorted(e[0].elapsed_time(e[3]) for e in ev)
+    phases = {"forward": sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps,
+              "backward": sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps,
+              "clip_adamw": sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps}
+
     # ---- per-launch timing pass (same steps, events around every launch) for the roofline
     model.profile(True)
     for i in range(args.warmup, nsteps):
@@ -507,6 +529,11 @@ def main():
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 2 * BT * 4,
                     "d2h_bytes_per_step": 8},
             "gpu_launches": launches,
+            "step_ms": {"median": step_ms[len(step_ms) // 2], "min": step_ms[0], "max": step_ms[-1],
+                        "note": "a separate pass over the same steps, events at the step boundaries"},
+            "phases_ms_per_step": dict(phases, note=(
+                "forward = the first micro-step's forward (with the loss read back), backward = its backward "
+                "plus the remaining micro-steps, clip_adamw = norm, clip and AdamW; a separate pass")),
             "clocks": clocks,
             "loss_first_last": [losses[0], losses[-1]],
         }
