@@ -193,6 +193,28 @@ def _oracle_sample_steps(w, max_steps, min_s, budget_s, warmup=0):
     return steps, time.perf_counter() - t0, T, torch.get_num_threads()
 
 
+def rank_micro_steps(rank, nsteps, accum):
+    """Stream-window indices of every micro-step a replica runs: [step][micro-step].  Replica r
+    reads the windows after those of replicas 0..r-1, so no two replicas see the same tokens."""
+    return [[(rank * nsteps + i) * accum + j for j in range(accum)] for i in range(nsteps)]
+
+
+def max_over_ranks(ms, dist, device):
+    """The slowest replica's time (the job's time), or ms itself on one process."""
+    if dist is None:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, steps, tokens_per_step, ms):
+    """Whole-job tokens/s: the tokens of all replicas over the slowest replica's time."""
+    return world * steps * tokens_per_step / (ms / 1e3)
+
+
 def cpu_baseline(w, min_s=12.0, budget_s=30.0):
     """The oracle, as it stands, on a bounded sample of the workload (see _oracle_sample_steps)."""
     steps, el, tok, cores = _oracle_sample_steps(w, 10 ** 9, min_s, budget_s)
@@ -371,9 +393,9 @@ def main():
     nsteps = args.warmup + args.steps
     # independent batches per rank: the replica r reads stream windows offset by r
     xs, ys = [], []
-    for i in range(nsteps):
-        for j in range(accum):
-            x, y = synthetic.zipf_window(w["seed"], B, T, w["V"], micro_step=(rank * nsteps + i) * accum + j)
+    for row in rank_micro_steps(rank, nsteps, accum):
+        for ms_ in row:
+            x, y = synthetic.zipf_window(w["seed"], B, T, w["V"], micro_step=ms_)
             xs.append(x)
             ys.append(y)
     X = torch.from_numpy(np.stack(xs).reshape(nsteps, accum, B, T)).cuda()
@@ -410,13 +432,9 @@ def main():
         ev1.record(stream)
         barrier()
     launches = g.launch_count() - launches0
-    ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dist, "cuda")
     ms_per_step = ms / args.steps
-    value = world * args.steps * BT / (ms / 1e3)
+    value = job_throughput(world, args.steps, BT, ms)
 
     # ---- per-step and per-phase pass (same steps, events at the step and phase boundaries on the
     # model's stream): the median step and the forward / backward / optimizer split
@@ -461,12 +479,8 @@ def main():
         step(i, xd, yd)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * args.steps * BT / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
+    e2e_value = job_throughput(world, args.steps, BT, e2e_ms)
 
     if rank == 0:
         peaks, peak_src = read_peaks()
