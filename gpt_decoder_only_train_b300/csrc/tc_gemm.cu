@@ -206,8 +206,12 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     }
 
     // bf16 outputs leave through TMA stores from the epilogue's staging blocks (box 64 x 32)
-    CUtensorMap td = ta, td2 = ta;  // unused copies when there is no bf16 output
+    CUtensorMap td = ta, td2 = ta;  // unused copies when the output has no tensor map
     if (g.epi != GPT2_EPI_ACCUM_F32 && !lse && (rc = encode_tmap(&td, g.D, g.N, g.M, g.ldd, 64, 32))) return rc;
+    // fp32 outputs are added through TMA reduce-adds of 32 x 32 blocks (BN of 128 and up)
+    if (g.epi == GPT2_EPI_ACCUM_F32 && BN >= 128 &&
+        (rc = encode_tmap_t(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.D, g.N, g.M, g.ldd, 32, 32)))
+        return rc;
     if (g.epi == GPT2_EPI_GELU && (rc = encode_tmap(&td2, g.D2, g.N, g.M, g.ldd, 64, 32))) return rc;
 
     const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;

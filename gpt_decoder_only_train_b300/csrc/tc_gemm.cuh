@@ -169,6 +169,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *
                  "r"(smem_u32(src)), "r"(x), "r"(y)
                  : "memory");
 }
+// TMA reduction of a shared-memory box into global memory: D[box] += smem, element
+// type from the tensor map (fp32 here); same bulk async-group rules as the store.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *tm, const void *src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until at most N of this thread's bulk groups still read shared memory
 template <int N> __device__ __forceinline__ void bulk_wait_read() {
@@ -523,6 +531,33 @@ __device__ __forceinline__ void stage_prefetch(uint8_t *stage, const bf16 *g, in
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// 32 accumulator columns of the warp's 32 rows added into the fp32 output: the
+// scaled block passes through the warp's swizzled staging block (32 rows x 128
+// bytes) and leaves as one TMA reduce-add, so the L2 receives whole 128-byte row
+// segments instead of 16 bytes from each of 32 rows.  Rows at or past M and
+// columns at or past N fall outside the tensor map and are not written.  The
+// result is D + acc whether or not other work units add into the same block.
+__device__ __forceinline__ void reduce_block32(const Params &P, const CUtensorMap *tmD, uint8_t *stage, int row0,
+                                               int col, int lane, const uint32_t (&r)[32]) {
+    float fac = P.alpha;
+    if (P.a_scale) fac *= P.a_scale[min(row0 + lane, P.M - 1)];
+    if (P.b_scale) fac *= *P.b_scale;
+    if (lane == 0) bulk_wait_read<0>();  // the previous TMA store / reduce from this block has read it
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *stage_at(stage, lane, c) =
+            make_uint4(__float_as_uint(__uint_as_float(r[4 * c]) * fac), __float_as_uint(__uint_as_float(r[4 * c + 1]) * fac),
+                       __float_as_uint(__uint_as_float(r[4 * c + 2]) * fac),
+                       __float_as_uint(__uint_as_float(r[4 * c + 3]) * fac));
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_reduce_add_2d(tmD, stage, col, row0);
+        bulk_commit();
+    }
+}
+
 // 64 accumulator columns (two 32-column TMEM loads) of the warp's 32 rows -> bf16
 // outputs with the fused epilogue; row0 is the warp's first row, col0 the group's
 // first column.
@@ -705,7 +740,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (P.epi != GPT2_EPI_ACCUM_F32) tma_prefetch_desc(&tmD);
+        if (P.epi != EPI_LSE) tma_prefetch_desc(&tmD);
         if (P.epi == GPT2_EPI_GELU) tma_prefetch_desc(&tmD2);
     }
     if (warp == 1) {
@@ -929,8 +964,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                     if (P.epi == GPT2_EPI_ACCUM_F32) {
-                        if (col < P.N) epilogue_chunk(P, row, col, r0);
-                        if (col + 32 < P.N) epilogue_chunk(P, row, col + 32, r1);
+                        if (col < P.N) reduce_block32(P, &tmD, stage, row0, col, lane, r0);
+                        if (col + 32 < P.N) reduce_block32(P, &tmD, stage, row0, col + 32, lane, r1);
                     } else if (col < P.N) {
                         epilogue_group64(P, &tmD, &tmD2, stage, gstage, rstage, row0, col, lane, r0, r1);
                     }

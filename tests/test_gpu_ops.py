@@ -119,6 +119,25 @@ def test_matmul_accumulate_fp32_split_k(g, M, N, K):
     assert (out - ref).abs().max().item() < 1e-4 * ref.abs().max().item() + 1e-5
 
 
+@pytest.mark.parametrize("M,N,ldd,K", [(300, 136, 144, 128), (1024, 1024, 1032, 256), (130, 264, 272, 2048)])
+def test_matmul_accumulate_fp32_touches_only_its_block(g, M, N, ldd, K):
+    """fp32 accumulation with a row pitch wider than N, one split and several: the
+    product is added to every element of the [M, N] block and the pitch padding
+    keeps its value."""
+    A, As, lda = _operand(M, K, 0, 8)
+    B, Bs, ldb = _operand(N, K, 0, 9)
+    base = torch.randn(M, ldd, dtype=torch.float32)
+    base[:, N:] = 12345.0
+    D = base.clone().cuda()
+    g.matmul(As.cuda(), lda, 0, Bs.cuda(), ldb, 0, D, ldd, M, N, K, g.EPI_ACCUM_F32)
+    torch.cuda.synchronize()
+    out = D.double().cpu()
+    assert torch.equal(out[:, N:], base[:, N:].double())
+    ref = base[:, :N].double() + A.double() @ B.double().T
+    assert ((out[:, :N] - ref).norm() / ref.norm()).item() < 1e-5
+    assert (out[:, :N] - ref).abs().max().item() < 1e-4 * ref.abs().max().item() + 1e-5
+
+
 def test_matmul_rejects_bad_shapes(g):
     a = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
     d = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
