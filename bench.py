@@ -252,7 +252,9 @@ def attention_sweep(args):
     """The isolated causal attention workload: H=12, hd=64, B*T = 65,536 at T in {256, 1024, 2048,
     4096}; Q, K, V, dO ~ N(0,1) rounded to bf16 (seed 4).  Forward and backward are timed apart with
     CUDA events after warm-up (every operand is 100 MB, together above L2); FLOPs count the causal
-    pairs: 4 hd T(T+1)/2 per head forward, twice that backward.  The oracle's naive attention
+    pairs: 4 hd T(T+1)/2 per head forward, twice that backward.  "bwd" is the backward the model
+    runs (dS kept in a workspace, dQ formed from it); "bwd_recompute" the entry without that
+    workspace (a second kernel recomputes S and dP per query block).  The oracle's naive attention
     (full T x T scores, float64) is timed at T=256 on the host cores as the CPU baseline."""
     import torch
 
@@ -274,10 +276,12 @@ def attention_sweep(args):
         lse = torch.empty(B, H, T, dtype=torch.float32, device="cuda")
         dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
         scratch = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
+        ds = torch.empty(g.attention_backward_ds_bytes(B, T, H), dtype=torch.uint8, device="cuda")
         fwd = lambda: g.attention_forward(q, k, v, o, lse, B, T, H)
-        bwd = lambda: g.attention_backward(q, k, v, o, do, lse, dq, dk, dv, scratch, B, T, H)
+        bwd = lambda: g.attention_backward_ds(q, k, v, o, do, lse, dq, dk, dv, scratch, ds, B, T, H)
+        bwd_rc = lambda: g.attention_backward(q, k, v, o, do, lse, dq, dk, dv, scratch, B, T, H)
         out = {"T": T, "B": B}
-        for name, fn, mult in (("fwd", fwd, 1.0), ("bwd", bwd, 2.0)):
+        for name, fn, mult in (("fwd", fwd, 1.0), ("bwd", bwd, 2.0), ("bwd_recompute", bwd_rc, 2.0)):
             for _ in range(args.warmup):
                 fn()
             torch.cuda.synchronize()
@@ -299,7 +303,7 @@ def attention_sweep(args):
             flops = mult * 4.0 * hd * (T * (T + 1) / 2.0) * B * H
             out[name] = {"ms": ms, "tflops": flops / ms / 1e9, "calls": calls, "clocks": clk.summary()}
         rows.append(out)
-        del dev, q, k, v, do, o, lse, dq, dk, dv, scratch
+        del dev, q, k, v, do, o, lse, dq, dk, dv, scratch, ds
         torch.cuda.empty_cache()
     launches = g.launch_count() - launches0
     line = {

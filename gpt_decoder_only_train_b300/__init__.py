@@ -77,6 +77,9 @@ _SIGS = {
     "gpt2_op_attention_backward": (_I, [_P, _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "gpt2_op_attention_backward_noalloc": (_I, [_P, _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I,
                                                 _P]),
+    "gpt2_op_attention_backward_ds": (_I, [_P, _P, _P, _I64, _P, _P, _I64, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                           _I, _I, _I, _I, _P]),
+    "gpt2_attention_backward_ds_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "gpt2_op_matmul": (_I, [_P, _I64, _I, _P, _I64, _I, _P, _P, _P, _I64, _P, _I, _I, _I, _I, _P]),
     "gpt2_op_classifier": (_I, [_P, _P, _P, _I, _I, _I, _F, _P]),
     "gpt2_op_sample": (_I, [_P, _I64, _I, _I, _P, _F, _I, _P, _P]),
@@ -291,6 +294,22 @@ def attention_backward(q, k, v, o, do, lse, dq, dk, dv, scratch, B, T, H, hd=64,
     check("gpt2_op_attention_backward", lib().gpt2_op_attention_backward(
         _ptr(q), _ptr(k), _ptr(v), rs, _ptr(o), _ptr(do), ors, _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
         _ptr(scratch), B, T, H, hd, _stream(stream)))
+
+
+def attention_backward_ds_bytes(B, T, H) -> int:
+    return int(lib().gpt2_attention_backward_ds_bytes(B, T, H))
+
+
+def attention_backward_ds(q, k, v, o, do, lse, dq, dk, dv, scratch, ds, B, T, H, hd=64, qkv_row_stride=None,
+                          o_row_stride=None, stream=None):
+    """attention_backward that keeps dS^T in `ds` (a device tensor of at least
+    attention_backward_ds_bytes(B, T, H) bytes) and forms dQ from it."""
+    rs = qkv_row_stride if qkv_row_stride is not None else H * hd
+    ors = o_row_stride if o_row_stride is not None else H * hd
+    nbytes = ds.numel() * ds.element_size()
+    check("gpt2_op_attention_backward_ds", lib().gpt2_op_attention_backward_ds(
+        _ptr(q), _ptr(k), _ptr(v), rs, _ptr(o), _ptr(do), ors, _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(scratch), _ptr(ds), nbytes, B, T, H, hd, _stream(stream)))
 
 
 NOALLOC_ATTN_MAX_ROWS = 1 << 20

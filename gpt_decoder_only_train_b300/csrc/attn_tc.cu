@@ -97,6 +97,30 @@ __device__ __forceinline__ void tile_row16(const uint8_t *tile, int r, int sub, 
     const uint4 c = *reinterpret_cast<const uint4 *>(row + (((2 * sub + 1) ^ (r & 7)) << 4));
     w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w, w[4] = c.x, w[5] = c.y, w[6] = c.z, w[7] = c.w;
 }
+// L2 policy that evicts these lines first: for data written or read once (the stored dS)
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// Box of the blocked dS^T layout (see encode_ds_map) at query block qb, key block kb
+// (blocks of 64), head bh; the two inner coordinates are always 0.
+__device__ __forceinline__ void tma_load_ds_hint(void *dst, const CUtensorMap *tm, uint64_t *bar, int qb, int kb,
+                                                 int bh, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(qb), "r"(kb), "r"(bh), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_ds_hint(const CUtensorMap *tm, const void *src, int qb, int kb, int bh,
+                                                  uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %2, %3, %4, %5}], [%1], %6;" ::"l"(
+            reinterpret_cast<uint64_t>(tm)),
+        "r"(smem_u32(src)), "r"(0), "r"(qb), "r"(kb), "r"(bh), "l"(pol)
+        : "memory");
+}
 // Item j of this CTA in a persistent grid: every gridDim.x-th entry of a
 // heaviest-first list, in alternating direction, or -1 past the end.
 __device__ __forceinline__ int item_of(int j, int nitems) {
@@ -857,10 +881,13 @@ constexpr int TQ = BQ * HD * 2;    // 8 KB
 constexpr int TKV = BKY * HD * 2;  // 16 KB: a K or V tile
 constexpr int OFF_KV = SLOTS * TQ;  // [2 item slots][K | V]
 constexpr int OFF_LD = OFF_KV + 4 * TKV;  // [NLD][lse 64 | D 64] floats
-constexpr int OFF_BAR = OFF_LD + NLD * 2 * BQ * 4;
+constexpr int TDS = BKY * BQ * 2;         // 16 KB: dS^T of one block, staged for its TMA store
+constexpr int OFF_DS = OFF_LD + NLD * 2 * BQ * 4;  // [2 block parities]
+constexpr int OFF_BAR = OFF_DS + 2 * TDS;
 constexpr int SMEM = 1024 + OFF_BAR + 512;
 constexpr uint32_t TCOLS = 512;
 constexpr uint32_t C_ST = 0, C_DPT = 128, C_DV = 256, C_DK = 320, C_KV = 384;
+static_assert(OFF_DS % 1024 == 0, "swizzled staging blocks start on 1024-byte boundaries");
 struct Bars {
     uint64_t dkv_done, dkv_free, drain;
     uint64_t kv_sfull[2], kv_sempty[2], kv_tfull[2];
@@ -873,8 +900,9 @@ struct Bars {
 __global__ void __launch_bounds__(dkv::NTH, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                      const float *__restrict__ lse, const float *__restrict__ Dscr, bf16 *__restrict__ dko,
-                      bf16 *__restrict__ dvo, int64_t rs, int T, int H, int nitems, float sl2, float scale) {
+                      const __grid_constant__ CUtensorMap tds, const float *__restrict__ lse,
+                      const float *__restrict__ Dscr, bf16 *__restrict__ dko, bf16 *__restrict__ dvo, int64_t rs,
+                      int T, int H, int nitems, float sl2, float scale, int store_ds) {
     constexpr int BKY = dkv::BKY, BQ = dkv::BQ, SWARPS = dkv::SWARPS, NLD = dkv::NLD;
     constexpr int TQ = dkv::TQ, TKV = dkv::TKV, OFF_KV = dkv::OFF_KV, OFF_LD = dkv::OFF_LD, OFF_BAR = dkv::OFF_BAR;
     constexpr uint32_t TCOLS = dkv::TCOLS, C_ST = dkv::C_ST, C_DPT = dkv::C_DPT, C_DV = dkv::C_DV, C_DK = dkv::C_DK,
@@ -980,9 +1008,15 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
             const uint64_t ring_mn = smem_desc(smem_u32(sm), 8192, 1024);  // MN-major view of slot 0
             bool ok = true;
             // dV / dK products of query block gp, the it-th block of item j
+            const uint64_t pol = l2_evict_first_policy();
             auto grads = [&](int gp, int j, int it, bool last) -> bool {
                 const int pb = gp & 1, pe = gp % NLD;
                 if (!mbar_wait(&bar->pds_full[pb], (gp >> 1) & 1, abort_flag, nullptr)) return false;
+                if (store_ds) {  // dS^T of block gp, staged by the softmax warps: rows = its 128 keys
+                    const int p = item_of(j, nitems), kb = p / BH, bh = p % BH;
+                    tma_store_ds_hint(&tds, sm + dkv::OFF_DS + pb * dkv::TDS, 2 * kb + it, 2 * kb, bh, pol);
+                    bulk_commit();
+                }
                 if (it == 0 && j > 0 && !mbar_wait(&bar->dkv_free, (j - 1) & 1, abort_flag, nullptr)) return false;
                 tc_fence_after();
                 const uint64_t bq = ring_mn + (uint64_t)(2 * pe * (TQ >> 4));
@@ -1020,12 +1054,16 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
                     tc_mma_ts(td, tV, bd, ID_ST, 0u);
 #pragma unroll
                     for (int kk = 1; kk < HD / 16; ++kk) tc_mma_ts(td, tV + 8 * kk, bd + 2 * kk, ID_ST, 1u);
+                    // the staging block of this parity is rewritten once S^T of this block is ready:
+                    // the store of block g - 2 must have read it by then
+                    if (store_ds) bulk_wait_read<0>();
                     tc_commit(&bar->st_full[bb]);
                     if (g > 0 && !(ok = grads(g - 1, pj, pit, plast))) break;
                     pj = j, pit = it, plast = it == nit - 1;
                 }
             }
             if (ok && g > 0) grads(g - 1, pj, pit, plast);
+            if (store_ds) bulk_wait_all();
             tc_commit(&bar->drain);
             mbar_drain(&bar->drain, 0);
         }
@@ -1107,6 +1145,13 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
                 }
                 tmem_st8(cs, wp);  // P^T over the first 8 of this thread's S^T columns
                 tmem_st8(cd, wd);  // dS^T over the first 8 of its dP^T columns
+                if (store_ds) {  // the same 16 values of dS^T into the block's staging tile (row r, 128-byte swizzle)
+                    uint8_t *row = sm + dkv::OFF_DS + bb * dkv::TDS + r * 128;
+                    *reinterpret_cast<uint4 *>(row + (((2 * sub) ^ (r & 7)) << 4)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                    *reinterpret_cast<uint4 *>(row + (((2 * sub + 1) ^ (r & 7)) << 4)) =
+                        make_uint4(wd[4], wd[5], wd[6], wd[7]);
+                    fence_async_smem();  // visible to the TMA store the MMA thread issues after pds_full
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -1151,6 +1196,266 @@ __global__ void __launch_bounds__(dkv::NTH, 1)
     }
 }
 
+// ---------------------------------------------------------------- D and the value-bias sums
+// D[b*H + h, t] = sum_d dO[b, t, h, d] O[b, t, h, d] (fp32) for the dK/dV
+// kernel, and, with dbv, dbv[c] += the column sums of dO over all rows (the
+// value-bias gradient: every row of P sums to one).  One warp per row at a time;
+// in pass i lane l holds columns [8 (l + 32 i), +8), so the 8 lanes of a head
+// finish its dot product with three shuffles.  NIT = ceil(C / 256) passes, C = 64 H <= 2048.
+namespace rdot {
+constexpr int WARPS = 16, MAXIT = 8;
+}
+template <int NIT>
+__global__ void __launch_bounds__(32 * rdot::WARPS)
+    bwd_rowdot_kernel(const bf16 *__restrict__ dout, const bf16 *__restrict__ o, int64_t ors,
+                      float *__restrict__ Dscr, float *__restrict__ dbv, int BT, int T, int H) {
+    __shared__ float cs[NIT * 256];
+    const int C = H * HD, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (dbv)
+        for (int c = threadIdx.x; c < NIT * 256; c += blockDim.x) cs[c] = 0.f;
+    float acc[NIT][8];
+#pragma unroll
+    for (int i = 0; i < NIT; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[i][k] = 0.f;
+    // RPI rows per pass: all of their loads are in flight before the first is used
+    constexpr int RPI = NIT <= 4 ? 2 : 1;
+    for (int row0 = (blockIdx.x * rdot::WARPS + warp) * RPI; row0 < BT; row0 += gridDim.x * rdot::WARPS * RPI) {
+        uint4 a[RPI][NIT], v[RPI][NIT];
+#pragma unroll
+        for (int rr = 0; rr < RPI; ++rr)
+#pragma unroll
+            for (int i = 0; i < NIT; ++i) {
+                const int row = row0 + rr, c = (lane + 32 * i) * 8;
+                a[rr][i] = v[rr][i] = make_uint4(0u, 0u, 0u, 0u);
+                if (row < BT && c < C) {
+                    a[rr][i] = *reinterpret_cast<const uint4 *>(dout + (int64_t)row * ors + c);
+                    v[rr][i] = *reinterpret_cast<const uint4 *>(o + (int64_t)row * ors + c);
+                }
+            }
+#pragma unroll
+        for (int rr = 0; rr < RPI; ++rr) {
+            const int row = row0 + rr;
+            if (row >= BT) break;  // the same for the whole warp
+            const int b = row / T, t = row - b * T;
+#pragma unroll
+            for (int i = 0; i < NIT; ++i) {
+                const int c = (lane + 32 * i) * 8;
+                const uint32_t aw[4] = {a[rr][i].x, a[rr][i].y, a[rr][i].z, a[rr][i].w};
+                const uint32_t vw[4] = {v[rr][i].x, v[rr][i].y, v[rr][i].z, v[rr][i].w};
+                float s = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {  // columns past C hold zeros
+                    s = fmaf(bf16_lo(aw[w]), bf16_lo(vw[w]), s);
+                    s = fmaf(bf16_hi(aw[w]), bf16_hi(vw[w]), s);
+                    acc[i][2 * w] += bf16_lo(aw[w]);
+                    acc[i][2 * w + 1] += bf16_hi(aw[w]);
+                }
+                s += __shfl_xor_sync(~0u, s, 1);
+                s += __shfl_xor_sync(~0u, s, 2);
+                s += __shfl_xor_sync(~0u, s, 4);
+                if ((lane & 7) == 0 && c < C) Dscr[((int64_t)b * H + c / HD) * T + t] = s;
+            }
+        }
+    }
+    if (dbv) {
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NIT; ++i) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int c = (lane + 32 * i) * 8 + k;
+                if (c < C) atomicAdd(cs + c, acc[i][k]);
+            }
+        }
+        __syncthreads();
+        for (int c = threadIdx.x; c < C; c += blockDim.x)
+            if (cs[c] != 0.f) atomicAdd(dbv + c, cs[c]);
+    }
+}
+
+// ---------------------------------------------------------------- dQ from the stored dS
+// dQ = scale dS K per (128-query block, b*h) item, over the key blocks of 64 up
+// to the item's diagonal.  The dK/dV kernel stored dS^T as bf16 in 64 x 64 blocks
+// (row = key, the queries contiguous; see encode_ds_map): the A operand (M =
+// queries, K = keys) is MN-major; K is the MN-major B operand (N = the head's 64
+// columns).  The
+// accumulator (128 x 64 fp32) is double-buffered in TMEM, so the read-out of an
+// item overlaps the products of the next.  With dbq, the column sums of dQ
+// (query-bias gradient) are added to it.
+// Warps: 0 loads (TMA), 1 issues the MMAs, 2-5 read out (one per TMEM lane quadrant).
+namespace dqs {
+constexpr int BQ = 128, BK = 64, NST = 8, EWARPS = 4;
+constexpr int NTH = 64 + 32 * EWARPS;
+constexpr int A_BYTES = BQ * BK * 2;  // 16 KB: two 64-query MN-major blocks
+constexpr int B_BYTES = BK * HD * 2;  // 8 KB
+constexpr int STAGE = A_BYTES + B_BYTES;
+constexpr int MAXC = 2048;
+constexpr int OFF_BSUM = NST * STAGE;
+constexpr int OFF_BAR = OFF_BSUM + MAXC * 4;
+constexpr int SMEM = 1024 + OFF_BAR + 256;
+constexpr uint32_t TCOLS = 128;
+}  // namespace dqs
+
+__global__ void __launch_bounds__(dqs::NTH, 1)
+    bwd_dq_from_ds_kernel(const __grid_constant__ CUtensorMap tds, const __grid_constant__ CUtensorMap tk,
+                          bf16 *__restrict__ dqo, int64_t rs, int T, int H, int nitems, float scale,
+                          float *__restrict__ dbq) {
+    constexpr int BQ = dqs::BQ, BK = dqs::BK, NST = dqs::NST, EWARPS = dqs::EWARPS, A_BYTES = dqs::A_BYTES,
+                  STAGE = dqs::STAGE;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = align_smem_1024(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + dqs::OFF_BAR), *empty = full + NST, *tfull = empty + NST,
+             *tempty = tfull + 2, *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *bsum = reinterpret_cast<float *>(sm + dqs::OFF_BSUM);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nqb = (T + BQ - 1) / BQ, nkb = (T + BK - 1) / BK, BH = nitems / nqb;
+    // item p: query block nqb - 1 - p / BH (heaviest first), b*h = p % BH
+    auto item_qb = [&](int p) { return nqb - 1 - p / BH; };
+    auto item_nk = [&](int qb) { return min(nkb, 2 * (qb + 1)); };
+    if (dbq)
+        for (int c = threadIdx.x; c < H * HD; c += blockDim.x) bsum[c] = 0.f;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], EWARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&tds);
+        tma_prefetch_desc(&tk);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, dqs::TCOLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            const uint64_t pol = l2_evict_first_policy();  // dS is read once
+            for (int j = 0; ok; ++j) {
+                const int p = item_of(j, nitems);
+                if (p < 0) break;
+                const int qb = item_qb(p), bh = p % BH, b = bh / H, h = bh % H, nk = item_nk(qb);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!(ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, nullptr))) break;
+                    uint8_t *a_dst = sm + stage * STAGE, *b_dst = a_dst + A_BYTES;
+                    mbar_expect_tx(&full[stage], STAGE);
+                    tma_load_ds_hint(a_dst, &tds, &full[stage], 2 * qb, kb, bh, pol);  // both 64-query halves
+                    tma_load_3d(b_dst, &tk, &full[stage], h * HD, kb * BK, b);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == NST) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok)  // let the copies already issued land before the CTA exits
+                for (int s = 0; s < NST; ++s)
+                    if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t IDESC = instr_desc(HD, true, true);  // 128 x 64, A and B MN-major
+            int stage = 0, t = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int j = 0; ok; ++j, ++t) {
+                const int p = item_of(j, nitems);
+                if (p < 0) break;
+                const int nk = item_nk(item_qb(p)), acc = t & 1;
+                if (!(ok = mbar_wait(&tempty[acc], ((t >> 1) & 1) ^ 1, abort_flag, nullptr))) break;
+                tc_fence_after();
+                const uint32_t d = tmem + acc * HD;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!(ok = mbar_wait(&full[stage], phase, abort_flag, nullptr))) break;
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sm + stage * STAGE), b_addr = a_addr + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma(d, smem_desc(a_addr + kk * 2048, A_BYTES / 2, 1024),
+                               smem_desc(b_addr + kk * 2048, A_BYTES / 2, 1024), IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&empty[stage]);
+                    if (++stage == NST) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&tfull[acc]);
+            }
+            tc_commit(drain);  // all MMAs issued by this thread have completed once it flips
+            mbar_drain(drain, 0);
+        }
+    } else {
+        const int quad = warp & 3, r = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        int t = 0;
+        for (int j = 0;; ++j, ++t) {
+            const int p = item_of(j, nitems);
+            if (p < 0) break;
+            const int qb = item_qb(p), bh = p % BH, b = bh / H, h = bh % H, acc = t & 1;
+            if (!mbar_wait(&tfull[acc], (t >> 1) & 1, abort_flag, nullptr)) break;
+            tc_fence_after();
+            uint32_t ra[32], rb[32];
+            tmem_ld32(tmem + lane_off + acc * HD, ra);
+            tmem_ld32(tmem + lane_off + acc * HD + 32, rb);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            const int q = qb * BQ + r;
+            if (dbq) {  // query-bias gradient: column sums of dQ (one warp = 32 rows) into the CTA's partials
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float cv[16];
+#pragma unroll
+                    for (int d = 0; d < 16; ++d)
+                        cv[d] = q < T ? __uint_as_float(g < 2 ? ra[16 * g + d] : rb[16 * (g - 2) + d]) * scale : 0.f;
+                    warp_colsum16_add(cv, bsum + h * HD + 16 * g, lane);
+                }
+            }
+            if (q < T) {
+                bf16 *row = dqo + ((int64_t)b * T + q) * rs + h * HD;
+#pragma unroll
+                for (int d = 0; d < 64; d += 8) {
+                    const uint32_t *x = d < 32 ? ra + d : rb + (d - 32);
+                    uint4 u;
+                    u.x = pack_bf16x2(__uint_as_float(x[0]) * scale, __uint_as_float(x[1]) * scale);
+                    u.y = pack_bf16x2(__uint_as_float(x[2]) * scale, __uint_as_float(x[3]) * scale);
+                    u.z = pack_bf16x2(__uint_as_float(x[4]) * scale, __uint_as_float(x[5]) * scale);
+                    u.w = pack_bf16x2(__uint_as_float(x[6]) * scale, __uint_as_float(x[7]) * scale);
+                    *reinterpret_cast<uint4 *>(row + d) = u;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, dqs::TCOLS);
+    }
+    if (dbq)  // one atomic per head column and CTA
+        for (int c = threadIdx.x; c < H * HD; c += blockDim.x)
+            if (bsum[c] != 0.f) atomicAdd(dbq + c, bsum[c]);
+}
+
 // 3-D map over one operand: (column within H*64, row t, batch b), row stride rs
 static int encode_qkv_map(CUtensorMap *tm, const bf16 *base, int64_t rs, int T, int B, int H, int box_rows = 128) {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1168,6 +1473,35 @@ static int encode_qkv_map(CUtensorMap *tm, const bf16 *base, int64_t rs, int T, 
     cuuint32_t box[3] = {HD, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<bf16 *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+// Map over the stored dS^T in blocks: for each b*h, key block kb and query block qb
+// (blocks of 64), the 64 x 64 block [key][query] is contiguous (8 KB), blocks in
+// (bh, kb, qb) order, so that a box of two query blocks (the dQ loads) is 16 KB of
+// consecutive memory and one of two key blocks (the dK/dV stores) two runs of 8 KB.
+// Dimensions, innermost first: query in block, key in block, qb, kb, bh; the box
+// is 64 x 64 x box_qb x box_kb x 1, which lands in shared memory as box_qb * box_kb
+// row-major 64 x 64 blocks (128-byte rows, 128-byte swizzle).
+static int encode_ds_map(CUtensorMap *tm, const void *base, int BH, int Tp, int box_qb, int box_kb) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
+                cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess)
+            return GPT2_ERR_CUDA;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    const cuuint64_t nb = (cuuint64_t)Tp / 64;
+    cuuint64_t dims[5] = {64, 64, nb, nb, (cuuint64_t)BH};
+    cuuint64_t strides[4] = {128, 8192, 8192 * nb, 8192 * nb * nb};
+    cuuint32_t box[5] = {64, 64, (cuuint32_t)box_qb, (cuuint32_t)box_kb, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GPT2_OK : GPT2_ERR_CUDA;
@@ -1207,9 +1541,14 @@ int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs
     return GPT2_OK;
 }
 
+size_t attention_backward_ds_bytes(int B, int T, int H) {
+    const int64_t Tp = ((int64_t)T + 127) / 128 * 128;
+    return (size_t)B * H * Tp * Tp * 2;
+}
+
 int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
                           int64_t ors, const float *lse, bf16 *dq_out, bf16 *dk_out, bf16 *dv_out, float *Dscr, int B,
-                          int T, int H, cudaStream_t st, float *dbias) {
+                          int T, int H, cudaStream_t st, float *dbias, bf16 *ds_ws) {
     using namespace fatc;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
          reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq_out) |
@@ -1232,6 +1571,8 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
             GPT2_CUDA_TRY(cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::SMEM));
             GPT2_CUDA_TRY(
                 cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::SMEM));
+            GPT2_CUDA_TRY(
+                cudaFuncSetAttribute(bwd_dq_from_ds_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dqs::SMEM));
             v = 1;
             return GPT2_OK;
         }))
@@ -1240,6 +1581,44 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
     int dev = 0, sms = 0;
     GPT2_CUDA_TRY(cudaGetDevice(&dev));
     GPT2_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int nitems = ((T + dkv::BKY - 1) / dkv::BKY) * B * H;
+    if (ds_ws && H * HD <= rdot::MAXIT * 256) {
+        // D (and the value-bias sums) first; the dK/dV kernel stores dS^T, from which a
+        // plain tcgen05 product forms dQ (and the query-bias sums)
+        if (reinterpret_cast<uintptr_t>(ds_ws) & 15) return GPT2_ERR_BAD_ARG;
+        const int Tp = (T + 127) / 128 * 128;
+        CUtensorMap tds_ld, tds_st;  // boxes of 128 queries x 64 keys (dQ loads), 64 x 128 (dK/dV stores)
+        if (int rc = encode_ds_map(&tds_ld, ds_ws, B * H, Tp, 2, 1)) return rc;
+        if (int rc = encode_ds_map(&tds_st, ds_ws, B * H, Tp, 1, 2)) return rc;
+        const int BT = B * T;
+        const int rblocks = std::min((BT + 2 * rdot::WARPS - 1) / (2 * rdot::WARPS), sms);  // one per SM at most
+        float *dbv = dbias ? dbias + 2 * H * HD : nullptr;
+        switch ((H * HD + 255) / 256) {
+#define ROWDOT_CASE(n)                                                                                      \
+    case n:                                                                                                 \
+        bwd_rowdot_kernel<n><<<rblocks, 32 * rdot::WARPS, 0, st>>>(dout, o, ors, Dscr, dbv, BT, T, H); \
+        break;
+            ROWDOT_CASE(1)
+            ROWDOT_CASE(2)
+            ROWDOT_CASE(3)
+            ROWDOT_CASE(4)
+            ROWDOT_CASE(5)
+            ROWDOT_CASE(6)
+            ROWDOT_CASE(7)
+            ROWDOT_CASE(8)
+#undef ROWDOT_CASE
+        }
+        GPT2_CUDA_TRY(cudaGetLastError());
+        bwd_dkv_tc_kernel<<<std::min(nitems, sms), dkv::NTH, dkv::SMEM, st>>>(
+            q64, do64, k128, v128, tds_st, lse, Dscr, dk_out, dv_out, rs, T, H, nitems, sl2, scale, 1);
+        GPT2_CUDA_TRY(cudaGetLastError());
+        const int nq_items = ((T + dqs::BQ - 1) / dqs::BQ) * B * H;
+        bwd_dq_from_ds_kernel<<<std::min(nq_items, sms), dqs::NTH, dqs::SMEM, st>>>(tds_ld, k64, dq_out, rs, T, H,
+                                                                                    nq_items, scale, dbias);
+        GPT2_CUDA_TRY(cudaGetLastError());
+        gpt2_note_launches(3);
+        return GPT2_OK;
+    }
     // persistent dQ grid: one CTA per SM over (query block, b*h) items, heaviest first
     const int nq_items = ((T + dq::BQ - 1) / dq::BQ) * B * H;
     bwd_dq_tc_kernel<<<std::min(nq_items, sms), dq::NTH, dq::SMEM, st>>>(q128, do128, o128, k64, v64, lse, dq_out, rs,
@@ -1247,9 +1626,8 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
                                                                          dbias ? dbias + 2 * H * HD : nullptr);
     GPT2_CUDA_TRY(cudaGetLastError());
     // persistent dK/dV grid: one CTA per SM over (key block, b*h) items, heaviest first
-    const int nitems = ((T + dkv::BKY - 1) / dkv::BKY) * B * H;
-    bwd_dkv_tc_kernel<<<std::min(nitems, sms), dkv::NTH, dkv::SMEM, st>>>(q64, do64, k128, v128, lse, Dscr, dk_out,
-                                                                          dv_out, rs, T, H, nitems, sl2, scale);
+    bwd_dkv_tc_kernel<<<std::min(nitems, sms), dkv::NTH, dkv::SMEM, st>>>(
+        q64, do64, k128, v128, q64 /* unused */, lse, Dscr, dk_out, dv_out, rs, T, H, nitems, sl2, scale, 0);
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(2);
     return GPT2_OK;

@@ -77,16 +77,8 @@ __device__ __forceinline__ F2 f2(float lo, float hi) {
     asm("mov.b64 %0, {%1, %2};" : "=l"(r.u) : "f"(lo), "f"(hi));
     return r;
 }
-__device__ __forceinline__ float f2_lo(F2 v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v.u));
-    return lo;
-}
-__device__ __forceinline__ float f2_hi(F2 v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v.u));
-    return hi;
-}
+__device__ __forceinline__ float f2_lo(F2 v) { return __uint_as_float((uint32_t)v.u); }
+__device__ __forceinline__ float f2_hi(F2 v) { return __uint_as_float((uint32_t)(v.u >> 32)); }
 __device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) {
     F2 d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.u) : "l"(a.u), "l"(b.u), "l"(c.u));

@@ -19,10 +19,10 @@ int attention_forward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, b
 
 int attention_backward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
                        int64_t ors, const float *lse, bf16 *dq, bf16 *dk, bf16 *dv, float *Dscr, int B, int T, int H,
-                       int hd, cudaStream_t st, float *dbias) {
+                       int hd, cudaStream_t st, float *dbias, bf16 *ds_ws) {
     if (hd != 64 || rs % 8 || ors % 8 || B <= 0 || T <= 0 || H <= 0) return GPT2_ERR_BAD_SHAPE;
     if (!grid_fits(B, T, H)) return GPT2_ERR_BAD_SHAPE;
-    return attention_backward_tc(q, k, v, rs, o, dout, ors, lse, dq, dk, dv, Dscr, B, T, H, st, dbias);
+    return attention_backward_tc(q, k, v, rs, o, dout, ors, lse, dq, dk, dv, Dscr, B, T, H, st, dbias, ds_ws);
 }
 
 }  // namespace fa

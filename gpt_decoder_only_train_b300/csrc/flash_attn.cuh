@@ -21,7 +21,11 @@ int attention_forward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs
 // tcgen05 implementation of attention_backward (attn_tc.cu).
 int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
                           int64_t ors, const float *lse, bf16 *dq, bf16 *dk, bf16 *dv, float *Dscr, int B, int T,
-                          int H, cudaStream_t st, float *dbias = nullptr);
+                          int H, cudaStream_t st, float *dbias = nullptr, bf16 *ds_ws = nullptr);
+
+// Bytes of the dS workspace of attention_backward: B H Tp^2 bf16 with Tp = T
+// rounded up to a multiple of 128.
+size_t attention_backward_ds_bytes(int B, int T, int H);
 
 // dq/dk/dv (row stride rs) from O, dO (row stride ors) and lse; Dscr holds
 // D = rowsum(dO * O) as fp32 [B, H, T].  With dbias (fp32 [3 H 64], columns
@@ -31,8 +35,13 @@ int attention_backward_tc(const bf16 *q, const bf16 *k, const bf16 *v, int64_t r
 // P sums to one, so the rows of dv sum to the rows of dout); nothing for the
 // key part, which is zero (a key bias moves all scores of a query by the same
 // amount).
+//
+// ds_ws (optional, attention_backward_ds_bytes bytes, 16-byte aligned, contents
+// need not be initialised): with it the dK/dV kernel also stores dS^T there and
+// dQ = scale dS K is formed from it by one product over the causal blocks,
+// instead of a second kernel that recomputes S and dP per query block.
 int attention_backward(const bf16 *q, const bf16 *k, const bf16 *v, int64_t rs, const bf16 *o, const bf16 *dout,
                        int64_t ors, const float *lse, bf16 *dq, bf16 *dk, bf16 *dv, float *Dscr, int B, int T, int H,
-                       int hd, cudaStream_t st, float *dbias = nullptr);
+                       int hd, cudaStream_t st, float *dbias = nullptr, bf16 *ds_ws = nullptr);
 
 }  // namespace fa

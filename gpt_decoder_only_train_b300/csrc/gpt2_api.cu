@@ -112,6 +112,7 @@ struct gpt2_model {
     int *tokens, *targets;
     void *dres, *dbig, *dqkv, *datt, *dsmall, *gelu_buf;
     float *attn_D;
+    void *attn_ds;  // attention backward: dS^T of the causal blocks (bf16 path)
     void *emb_ws;  // embedding backward: sorted keys and partial sums
     double *norm_partials;
     unsigned *barrier;
@@ -293,6 +294,7 @@ void plan(gpt2_model &m, uint8_t *base) {
     m.dsmall = b.take<void>(BT * C * es);
     m.gelu_buf = take_opt<void>(b, c.recompute_gelu != 0, BT * 4 * C * es);
     m.attn_D = b.take<float>((int64_t)c.B * c.H * c.T * 4);
+    m.attn_ds = take_opt<void>(b, c.dtype == GPT2_DTYPE_BF16, fa::attention_backward_ds_bytes(c.B, c.T, c.H));
     m.emb_ws = b.take<void>(k::embed_backward_workspace((int)BT, c.C));
     m.norm_partials = b.take<double>((size_t)m.max_adam_blocks * 8);
     m.barrier = b.take<unsigned>(64);
@@ -518,7 +520,8 @@ int attn_bwd(gpt2_model *m, const T *qkv, const T *o, const T *dout, const float
     return timed(m, GPT2_PROF_ATTENTION, 2.0 * attn_flops(B, Tn, H, hd), [&] {
         if constexpr (sizeof(T) == 2)
             return fa::attention_backward(qkv, qkv + C, qkv + 2 * C, 3 * C, o, dout, C, lse, dqkv, dqkv + C,
-                                          dqkv + 2 * C, m->attn_D, B, Tn, H, hd, m->stream, dbias);
+                                          dqkv + 2 * C, m->attn_D, B, Tn, H, hd, m->stream, dbias,
+                                          (bf16 *)m->attn_ds);
         else
             return k::attention_backward_simt<T>(qkv, qkv + C, qkv + 2 * C, 3 * C, o, dout, C, lse, dqkv, dqkv + C,
                                                  dqkv + 2 * C, m->attn_D, B, Tn, H, hd, m->stream);
@@ -1204,6 +1207,25 @@ extern "C" int gpt2_op_attention_backward(const void *q, const void *kk, const v
     return fa::attention_backward((const bf16 *)q, (const bf16 *)kk, (const bf16 *)v, qkv_row_stride, (const bf16 *)o,
                                   (const bf16 *)dout, o_row_stride, lse, (bf16 *)dq, (bf16 *)dk, (bf16 *)dv, d_scratch,
                                   B, T, H, hd, (cudaStream_t)stream);
+}
+
+extern "C" size_t gpt2_attention_backward_ds_bytes(int B, int T, int H) {
+    if (B <= 0 || T <= 0 || H <= 0) return 0;
+    return fa::attention_backward_ds_bytes(B, T, H);
+}
+
+extern "C" int gpt2_op_attention_backward_ds(const void *q, const void *kk, const void *v, int64_t qkv_row_stride,
+                                             const void *o, const void *dout, int64_t o_row_stride, const float *lse,
+                                             void *dq, void *dk, void *dv, float *d_scratch, void *d_ds,
+                                             size_t ds_bytes, int B, int T, int H, int hd, void *stream) {
+    if (!q || !kk || !v || !o || !dout || !lse || !dq || !dk || !dv || !d_scratch) return GPT2_ERR_BAD_ARG;
+    if (B <= 0 || T <= 0 || H <= 0 || hd != 64 || qkv_row_stride % 8 || o_row_stride % 8) return GPT2_ERR_BAD_SHAPE;
+    if (H * hd > 2048) return GPT2_ERR_UNSUPPORTED;
+    if (!d_ds || (reinterpret_cast<uintptr_t>(d_ds) & 15) || ds_bytes < fa::attention_backward_ds_bytes(B, T, H))
+        return GPT2_ERR_BAD_ARG;
+    return fa::attention_backward((const bf16 *)q, (const bf16 *)kk, (const bf16 *)v, qkv_row_stride, (const bf16 *)o,
+                                  (const bf16 *)dout, o_row_stride, lse, (bf16 *)dq, (bf16 *)dk, (bf16 *)dv, d_scratch,
+                                  B, T, H, hd, (cudaStream_t)stream, nullptr, (bf16 *)d_ds);
 }
 
 extern "C" int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const void *B, int64_t ldb, int b_kmajor,

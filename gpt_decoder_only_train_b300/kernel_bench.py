@@ -98,7 +98,7 @@ def attn_flops(B, T, H, hd=64):
     return 4.0 * hd * (T * (T + 1) / 2) * B * H
 
 
-def bench_attention(B, T, H, bwd, iters, warmup):
+def bench_attention(B, T, H, bwd, iters, warmup, recompute=False):
     hd = 64
     gen = torch.Generator(device="cuda").manual_seed(0)
     mk = lambda: torch.randn(B, T, H, hd, device="cuda", generator=gen).to(torch.bfloat16)
@@ -112,10 +112,15 @@ def bench_attention(B, T, H, bwd, iters, warmup):
     else:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
         sc = torch.empty(B * H * T, device="cuda")
-        ms = _time(lambda i: g.attention_backward(q, k, v, o, do, lse, dq, dk, dv, sc, B, T, H), iters, warmup)
+        if recompute:
+            ms = _time(lambda i: g.attention_backward(q, k, v, o, do, lse, dq, dk, dv, sc, B, T, H), iters, warmup)
+        else:  # the model's backward: dS kept in a workspace, dQ formed from it
+            ds = torch.empty(g.attention_backward_ds_bytes(B, T, H), dtype=torch.uint8, device="cuda")
+            ms = _time(lambda i: g.attention_backward_ds(q, k, v, o, do, lse, dq, dk, dv, sc, ds, B, T, H), iters,
+                       warmup)
         fl = 2.0 * attn_flops(B, T, H)
-    return {"op": "attention_" + ("bwd" if bwd else "fwd"), "B": B, "T": T, "H": H, "ms": ms,
-            "TFLOP/s": fl / ms / 1e9}
+    op = "attention_" + ("fwd" if not bwd else "bwd_recompute" if recompute else "bwd")
+    return {"op": op, "B": B, "T": T, "H": H, "ms": ms, "TFLOP/s": fl / ms / 1e9}
 
 
 def bench_attention_fb(B, T, H, iters, warmup):
@@ -128,10 +133,11 @@ def bench_attention_fb(B, T, H, iters, warmup):
     lse = torch.empty(B, H, T, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     sc = torch.empty(B * H * T, device="cuda")
+    ds = torch.empty(g.attention_backward_ds_bytes(B, T, H), dtype=torch.uint8, device="cuda")
 
     def run(i):
         g.attention_forward(q, k, v, o, lse, B, T, H)
-        g.attention_backward(q, k, v, o, do, lse, dq, dk, dv, sc, B, T, H)
+        g.attention_backward_ds(q, k, v, o, do, lse, dq, dk, dv, sc, ds, B, T, H)
 
     ms = _time(run, iters, warmup)
     return {"op": "attention_fwd_bwd", "B": B, "T": T, "H": H, "ms": ms, "TFLOP/s": 3.0 * attn_flops(B, T, H) / ms / 1e9}
@@ -230,6 +236,8 @@ def main(argv=None):
     ap.add_argument("--prompt", type=int, default=32)
     ap.add_argument("--new", type=int, default=64)
     ap.add_argument("--top-k", type=int, default=50)
+    ap.add_argument("--recompute", action="store_true",
+                    help="attention: time the backward without the dS workspace (S and dP recomputed for dQ)")
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     a = ap.parse_args(argv)
@@ -239,7 +247,7 @@ def main(argv=None):
     if a.op == "matmul":
         out = [bench_matmul(a)]
     elif a.op == "attention":
-        out = [bench_attention(a.B, a.T, a.H, a.bwd, a.iters, a.warmup)]
+        out = [bench_attention(a.B, a.T, a.H, a.bwd, a.iters, a.warmup, a.recompute)]
     elif a.op == "classifier":
         out = [bench_classifier(a)]
     elif a.op == "layernorm":
@@ -253,8 +261,8 @@ def main(argv=None):
     else:
         out = []
         for T, B in ((256, 256), (1024, 64), (2048, 32), (4096, 16)):
-            for bwd in (False, True):
-                out.append(bench_attention(B, T, 12, bwd, a.iters, a.warmup))
+            for bwd, rc in ((False, False), (True, False), (True, True)):
+                out.append(bench_attention(B, T, 12, bwd, a.iters, a.warmup, rc))
     for r in out:
         print(json.dumps(r), flush=True)
 

@@ -308,6 +308,29 @@ int gpt2_op_attention_backward(const void *q, const void *k, const void *v, int6
                                void *stream);
 
 /*
+ * The same attention backward with the dS matrix kept: the kernel that forms
+ * dK and dV also writes dS^T (bf16, in 64 x 64 blocks) of every causal block to
+ * d_ds, and dQ =
+ * dS K / sqrt(hd) is then one tensor-core product over those blocks, instead
+ * of a second pass that recomputes S and dP for each block of queries.  Same
+ * results up to rounding order (dS is rounded to bf16 once, as the dK product
+ * uses it).
+ * d_ds: caller-owned device workspace of at least
+ * gpt2_attention_backward_ds_bytes(B, T, H) bytes, 16-byte aligned; its
+ * contents need not be initialised and are overwritten.  The other arguments
+ * are those of gpt2_op_attention_backward.  H*hd above 2048 returns
+ * GPT2_ERR_UNSUPPORTED; a NULL or short d_ds returns GPT2_ERR_BAD_ARG.
+ */
+int gpt2_op_attention_backward_ds(const void *q, const void *k, const void *v, int64_t qkv_row_stride,
+                                  const void *o, const void *dout, int64_t o_row_stride, const float *lse,
+                                  void *dq, void *dk, void *dv, float *d_scratch, void *d_ds, size_t ds_bytes, int B,
+                                  int T, int H, int hd, void *stream);
+
+/* Bytes of the d_ds workspace: B*H*Tp*Tp*2 with Tp = T rounded up to a
+ * multiple of 128 (0 for non-positive sizes). */
+size_t gpt2_attention_backward_ds_bytes(int B, int T, int H);
+
+/*
  * Attention backward that allocates nothing.  The source pages have no
  * counterpart to this entry point; it exists for callers of this library that
  * cannot allocate device memory when they call it (for example, when a

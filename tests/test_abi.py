@@ -119,3 +119,31 @@ def test_attention_entries_check_shapes_before_any_device_work(libh):
         assert call(2, 128, 1, 64, rs=100) == bad_shape  # row stride not a multiple of 8
         assert call(0, 128, 1, 64) == bad_shape
     assert L.gpt2_op_attention_forward(None, p, p, 192, p, 64, f, 2, 128, 1, 64, None) == -8  # NULL pointer
+
+
+def test_attention_ds_entry_sizes_and_checks_its_workspace(libh):
+    """The workspace of the stored-dS backward is B H Tp^2 bf16 (Tp = T rounded up to
+    128); the entry refuses a missing, misaligned or short workspace, and shapes its
+    kernels cannot take, before any pointer is touched."""
+    import gpt_decoder_only_train_b300 as g
+
+    L = g.lib()
+    assert L.gpt2_attention_backward_ds_bytes(16, 1024, 12) == 16 * 12 * 1024 * 1024 * 2
+    assert L.gpt2_attention_backward_ds_bytes(1, 129, 1) == 256 * 256 * 2
+    assert L.gpt2_attention_backward_ds_bytes(3, 128, 2) == 3 * 2 * 128 * 128 * 2
+    assert L.gpt2_attention_backward_ds_bytes(0, 8, 1) == 0
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its checks first
+    f = ctypes.cast(p, ctypes.POINTER(ctypes.c_float))
+
+    def bwd(B, T, H, hd, ds, nbytes, rs=192):
+        return L.gpt2_op_attention_backward_ds(p, p, p, rs, p, p, 64, f, p, p, p, f, ds, nbytes, B, T, H, hd, None)
+
+    n = L.gpt2_attention_backward_ds_bytes(2, 128, 1)
+    bad_arg, bad_shape, unsupported = -8, -2, -9
+    assert bwd(2, 128, 1, 64, p, n - 1) == bad_arg  # short workspace
+    assert bwd(2, 128, 1, 64, None, n) == bad_arg  # no workspace
+    assert bwd(2, 128, 1, 64, ctypes.c_void_p((1 << 20) + 8), n) == bad_arg  # not 16-byte aligned
+    assert bwd(2, 128, 1, 32, p, n) == bad_shape  # head dim other than 64
+    assert bwd(2, 128, 1, 64, p, n, rs=100) == bad_shape  # row stride not a multiple of 8
+    assert bwd(0, 128, 1, 64, p, n) == bad_shape
+    assert bwd(1, 128, 33, 64, p, 1 << 40, rs=33 * 64 * 3) == unsupported  # H * 64 above 2048

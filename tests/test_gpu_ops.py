@@ -186,6 +186,52 @@ def test_attention_forward_backward_parity(g, B, T, H):
         _close(out, ref, rel_elem=3e-2, rel_fro=2e-2)
 
 
+@pytest.mark.parametrize("B,T,H", [(2, 200, 3), (1, 1, 1), (3, 129, 2), (40, 129, 8), (2, 1000, 2), (1, 384, 3)])
+def test_attention_backward_with_stored_ds_parity(g, B, T, H):
+    """The backward that keeps dS^T in a workspace (dQ = dS K from it): same oracle and
+    tolerances as the recomputing backward.  The workspace starts filled with NaN, so a
+    block that dQ read without the dK/dV kernel having written it would show."""
+    q, k, v, do = _attn_inputs(B, T, H, seed=T + 7)
+    dev = lambda a: a.to(torch.bfloat16).cuda().contiguous()
+    qd, kd, vd, dod = dev(q), dev(k), dev(v), dev(do)
+    o = torch.empty_like(qd)
+    lse = torch.empty(B, H, T, dtype=torch.float32, device="cuda")
+    g.attention_forward(qd, kd, vd, o, lse, B, T, H)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+    scratch = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
+    nbytes = g.attention_backward_ds_bytes(B, T, H)
+    Tp = (T + 127) // 128 * 128
+    assert nbytes == B * H * Tp * Tp * 2
+    ds = torch.full((nbytes // 2,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    g.attention_backward_ds(qd, kd, vd, o, dod, lse, dq, dk, dv, scratch, ds, B, T, H)
+    torch.cuda.synchronize()
+    _, _, rdq, rdk, rdv = _attn_oracle(q, k, v, do)
+    for out, ref in ((dq, rdq), (dk, rdk), (dv, rdv)):
+        assert torch.isfinite(out.float()).all()
+        if ref.abs().max().item() == 0.0:
+            # T = 1: P = 1, so dS = dP - D = 0 exactly; D and dP are summed in different
+            # orders here, which leaves fp32 rounding noise only
+            assert out.double().abs().max().item() <= 1e-6
+        else:
+            _close(out, ref, rel_elem=3e-2, rel_fro=2e-2)
+    # the stored blocks are dS^T (row = key, column = query) in 64 x 64 blocks, ordered
+    # (b*h, key block, query block): finite on the causal side; in the blocks written
+    # (queries from the start of the key's 128-block on) zero above the diagonal; blocks
+    # further above the diagonal are never written nor read
+    nb = Tp // 64
+    dsm = ds.view(B * H, nb, nb, 64, 64).permute(0, 1, 3, 2, 4).reshape(B * H, Tp, Tp)[:, :T, :T].float().cpu()
+    key, qry = torch.arange(T)[:, None], torch.arange(T)[None, :]
+    assert torch.isfinite(dsm[:, key <= qry]).all()
+    assert (dsm[:, (key > qry) & (qry >= key // 128 * 128)] == 0).all()
+    # against the recomputing backward: dK and dV from the same kernel, dQ from another route
+    dq2, dk2, dv2 = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+    g.attention_backward(qd, kd, vd, o, dod, lse, dq2, dk2, dv2, scratch, B, T, H)
+    torch.cuda.synchronize()
+    for a, b in ((dq, dq2), (dk, dk2), (dv, dv2)):
+        if b.abs().max().item() > 1e-6:
+            _close(a, b.double(), rel_elem=2e-2, rel_fro=1e-2)
+
+
 def test_attention_fused_qkv_layout(g):
     """q/k/v read with row stride 3C out of one [B*T, 3C] buffer, as the model does."""
     B, T, H = 2, 96, 2
