@@ -141,8 +141,8 @@ GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
     "workload": "gpt2_124m",
-    "sha256": "3df45b041602d180f09f4f2ce2e7c689e19c30612c585784bbbea39b93a13a13",
-    "bytes_per_launch": 22.96e9 / 147,
+    "sha256": "3a2fee67fe66be9695b685dd042c99d874f51e6b6761395012eee59eb8d2fd3b",
+    "bytes_per_launch": 21.99e9 / 147,
 }
 
 
