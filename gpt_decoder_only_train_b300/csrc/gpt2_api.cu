@@ -127,6 +127,7 @@ struct gpt2_model {
         cudaEvent_t a, b;
         int cat;
         double work;
+        long long kernels;  // kernels the recorded call launched
     };
     std::vector<Rec> prof;
     size_t prof_used = 0;
@@ -351,7 +352,7 @@ int prof_flush(gpt2_model *m) {
         GPT2_CUDA_TRY(cudaEventElapsedTime(&ms, m->prof[i].a, m->prof[i].b));
         m->prof_ms[m->prof[i].cat] += ms;
         m->prof_work[m->prof[i].cat] += m->prof[i].work;
-        m->prof_n[m->prof[i].cat] += 1;
+        m->prof_n[m->prof[i].cat] += m->prof[i].kernels;
     }
     m->prof_used = 0;
     return GPT2_OK;
@@ -374,7 +375,9 @@ template <typename F> int timed(gpt2_model *m, int cat, double work, F &&launch)
     r.cat = cat;
     r.work = work;
     GPT2_CUDA_TRY(cudaEventRecord(r.a, m->stream));
+    const long long n0 = g_launches.load(std::memory_order_relaxed);
     const int rc = launch();
+    r.kernels = g_launches.load(std::memory_order_relaxed) - n0;
     GPT2_CUDA_TRY(cudaEventRecord(r.b, m->stream));
     m->prof_used++;
     return rc;

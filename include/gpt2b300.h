@@ -264,7 +264,9 @@ long long gpt2_launch_count(void);
  * together with its algorithmic work (FLOP for matmul and attention, bytes for
  * the memory-bound kernels).  gpt2_profile(m, 1) clears the totals and starts
  * recording, gpt2_profile(m, 0) stops; gpt2_profile_read synchronises the
- * stream and returns the totals of one category.                            */
+ * stream and returns the totals of one category: event time, work, and the
+ * number of kernels the recorded calls launched (an attention backward call
+ * launches two or three).                                                   */
 #define GPT2_PROF_MATMUL     0  /* tcgen05 / SIMT matmuls: work = 2 M N K FLOP */
 #define GPT2_PROF_ATTENTION  1  /* causal attention: work = 4 hd T(T+1)/2 per head (fwd), 2x that (bwd) FLOP */
 #define GPT2_PROF_CLASSIFIER 2  /* fused classifier: work = bytes read + written */
