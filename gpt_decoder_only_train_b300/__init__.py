@@ -81,6 +81,7 @@ _SIGS = {
                                            _I, _I, _I, _I, _P]),
     "gpt2_attention_backward_ds_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "gpt2_op_matmul": (_I, [_P, _I64, _I, _P, _I64, _I, _P, _P, _P, _I64, _P, _I, _I, _I, _I, _P]),
+    "gpt2_op_matmul_accum2": (_I, [_P, _I64, _P, _I64, _P, _I, _I, _P, _I64, _P, _I64, _P, _I, _I, _I, _P]),
     "gpt2_op_classifier": (_I, [_P, _P, _P, _I, _I, _I, _F, _P]),
     "gpt2_op_sample": (_I, [_P, _I64, _I, _I, _P, _F, _I, _P, _P]),
     "gpt2_generate": (_I, [_P, _P, _I, _I, _I, _P, _F, _I]),
@@ -330,6 +331,14 @@ def matmul(A, lda, a_kmajor, B, ldb, b_kmajor, D, ldd, M, N, K, epilogue=EPI_STO
     check("gpt2_op_matmul", lib().gpt2_op_matmul(
         _ptr(A), lda, int(a_kmajor), _ptr(B), ldb, int(b_kmajor), _ptr(D), _ptr(D2), _ptr(R), ldd, _ptr(bias),
         M, N, K, epilogue, _stream(stream)))
+
+
+def matmul_accum2(A0, lda0, B0, ldb0, D0, M0, N0, A1, lda1, B1, ldb1, D1, M1, N1, K, stream=None):
+    """D_i += A_i^T B_i for two weight-gradient products in one launch (A_i [K, M_i], B_i [K, N_i]
+    bf16, D_i fp32 [M_i, N_i])."""
+    check("gpt2_op_matmul_accum2", lib().gpt2_op_matmul_accum2(
+        _ptr(A0), lda0, _ptr(B0), ldb0, _ptr(D0), M0, N0, _ptr(A1), lda1, _ptr(B1), ldb1, _ptr(D1), M1, N1, K,
+        _stream(stream)))
 
 
 def layernorm_forward(x, g, b, y, mean, rstd, N, C, stream=None):

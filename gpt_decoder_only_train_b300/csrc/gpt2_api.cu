@@ -434,6 +434,46 @@ int mm(gpt2_model *m, const void *A, int64_t lda, bool a_km, const void *B, int6
     }
 }
 
+// Two weight-gradient products D_i += A_i^T B_i (A_i: [K, M_i], B_i: [K, N_i], both
+// MN-major, K = B*T rows; D_i fp32 [M_i, N_i]) of one block: one grouped launch in
+// bf16 mode, two products otherwise.
+struct DwProduct {
+    const void *A;
+    int64_t lda;
+    const void *B;
+    int64_t ldb;
+    float *D;
+    int M, N;
+};
+template <typename T> int mm_dw2(gpt2_model *m, const DwProduct &x, const DwProduct &y, int K) {
+    if constexpr (sizeof(T) == 2) {
+        tcg::GemmDesc g[2];
+        const DwProduct *d[2] = {&x, &y};
+        for (int i = 0; i < 2; ++i) {
+            g[i].A = (const bf16 *)d[i]->A;
+            g[i].lda = d[i]->lda;
+            g[i].a_kmajor = false;
+            g[i].B = (const bf16 *)d[i]->B;
+            g[i].ldb = d[i]->ldb;
+            g[i].b_kmajor = false;
+            g[i].D = d[i]->D;
+            g[i].ldd = d[i]->N;
+            g[i].M = d[i]->M;
+            g[i].N = d[i]->N;
+            g[i].K = K;
+            g[i].epi = GPT2_EPI_ACCUM_F32;
+            g[i].err = m->err_dev;
+        }
+        return timed(m, GPT2_PROF_MATMUL, 2.0 * K * ((double)x.M * x.N + (double)y.M * y.N),
+                     [&] { return tcg::launch_gemm_tc_grouped(g[0], g[1], m->num_sms, m->stream); });
+    } else {
+        TRY(mm<T>(m, x.A, x.lda, false, x.B, x.ldb, false, x.D, nullptr, nullptr, x.N, nullptr, x.M, x.N, K,
+                  GPT2_EPI_ACCUM_F32));
+        return mm<T>(m, y.A, y.lda, false, y.B, y.ldb, false, y.D, nullptr, nullptr, y.N, nullptr, y.M, y.N, K,
+                     GPT2_EPI_ACCUM_F32);
+    }
+}
+
 // E4M3 product for the forward projections: D = a8_inv[m] w8_inv[slot] (A8 B8^T) + bias, with
 // the bf16 epilogue `epi` (both operands K-major byte rows).
 int mm8(gpt2_model *m, const uint8_t *A8, int64_t lda, const float *a_inv, int w_id, int slot, void *D, void *D2,
@@ -661,34 +701,31 @@ int backward_impl(gpt2_model *m, float grad_scale) {
             g_in = (T *)m->gelu_buf;
             TIMED(GPT2_PROF_OTHER, 8 * act, k::gelu_forward<T>((T *)y.fch, g_in, (int64_t)BT * 4 * C, st));
         }
-        // FC projection: x' = x1 + g Wfcproj^T + b
-        TRY(mm<T>(m, dres, C, false, g_in, 4 * C, false, Gf(m, p.fcprojw), nullptr, nullptr, 4 * C, nullptr, C, 4 * C,
-                  BT, GPT2_EPI_ACCUM_F32));
         // bf16: bias gradients from the kernels that read the gradients they sum: the GELU-backward
         // product sums its output's columns into the FC bias gradient; the attention backward adds
         // the QKV bias gradient (query part: column sums of dq; value part: column sums of dO, since
         // every row of P sums to one; key part: zero, a key bias moves all scores of a query alike)
         constexpr bool fold_bias = sizeof(T) == 2;
+        // FC projection x' = x1 + g Wfcproj^T + b: dX (GELU backward) first, then both MLP weight
+        // gradients (FC projection from dres and g, FC from dH and y2) as one launch
         TRY(mm<T>(m, dres, C, true, W<T>(m, p.fcprojw), 4 * C, false, dbig, nullptr, y.fch, 4 * C, nullptr, BT, 4 * C,
                   C, GPT2_EPI_GELU_BWD, 1.0f, fold_bias ? Gf(m, p.fcb) : nullptr));
-        // FC: h = y2 Wfc^T + b
-        TRY(mm<T>(m, dbig, 4 * C, false, y.ln2, C, false, Gf(m, p.fcw), nullptr, nullptr, C, nullptr, 4 * C, C, BT,
-                  GPT2_EPI_ACCUM_F32));
+        TRY(mm_dw2<T>(m, DwProduct{dres, C, g_in, 4 * C, Gf(m, p.fcprojw), C, 4 * C},
+                      DwProduct{dbig, 4 * C, y.ln2, C, Gf(m, p.fcw), 4 * C, C}, BT));
         if (!fold_bias) TIMED(GPT2_PROF_OTHER, 4 * act, k::column_sum<T>(dbig, BT, 4 * C, Gf(m, p.fcb), st));
         TRY(mm<T>(m, dbig, 4 * C, true, W<T>(m, p.fcw), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, 4 * C,
                   GPT2_EPI_STORE));
         TIMED(GPT2_PROF_LAYERNORM, 4 * act + stats,
               k::layernorm_backward<T>(dsmall, (T *)y.resid_mid, y.ln2_mean, y.ln2_rstd, Pf(m, p.ln2g), dres, dres,
                                        Gf(m, p.ln2g), Gf(m, p.ln2b), BT, C, st, Gf(m, p.projb)));
-        // attention projection: x1 = x + O Wproj^T + b
-        TRY(mm<T>(m, dres, C, false, y.att, C, false, Gf(m, p.projw), nullptr, nullptr, C, nullptr, C, C, BT,
-                  GPT2_EPI_ACCUM_F32));
+        // attention projection x1 = x + O Wproj^T + b: dO, the attention backward, then the
+        // projection's and the QKV product's weight gradients (from dres and O, dqkv and y) as one
+        // launch (dres keeps its value until the LN1 backward)
         TRY(mm<T>(m, dres, C, true, W<T>(m, p.projw), C, false, datt, nullptr, nullptr, C, nullptr, BT, C, C,
                   GPT2_EPI_STORE));
         TRY(attn_bwd<T>(m, (T *)y.qkv, (T *)y.att, datt, y.lse, dqkv, B, Tn, fold_bias ? Gf(m, p.qkvb) : nullptr));
-        // QKV: qkv = y Wqkv^T + b
-        TRY(mm<T>(m, dqkv, 3 * C, false, y.ln1, C, false, Gf(m, p.qkvw), nullptr, nullptr, C, nullptr, 3 * C, C, BT,
-                  GPT2_EPI_ACCUM_F32));
+        TRY(mm_dw2<T>(m, DwProduct{dres, C, y.att, C, Gf(m, p.projw), C, C},
+                      DwProduct{dqkv, 3 * C, y.ln1, C, Gf(m, p.qkvw), 3 * C, C}, BT));
         if (!fold_bias) TIMED(GPT2_PROF_OTHER, 3 * act, k::column_sum<T>(dqkv, BT, 3 * C, Gf(m, p.qkvb), st));
         TRY(mm<T>(m, dqkv, 3 * C, true, W<T>(m, p.qkvw), C, false, dsmall, nullptr, nullptr, C, nullptr, BT, C, 3 * C,
                   GPT2_EPI_STORE));
@@ -1253,6 +1290,32 @@ extern "C" int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const vo
     g.alpha = 1.0f;
     g.err = nullptr;
     return tcg::launch_gemm_tc(g, op_sms(), (cudaStream_t)stream);
+}
+
+extern "C" int gpt2_op_matmul_accum2(const void *A0, int64_t lda0, const void *B0, int64_t ldb0, float *D0, int M0,
+                                     int N0, const void *A1, int64_t lda1, const void *B1, int64_t ldb1, float *D1,
+                                     int M1, int N1, int K, void *stream) {
+    tcg::GemmDesc g[2];
+    const void *A[2] = {A0, A1}, *Bp[2] = {B0, B1};
+    const int64_t lda[2] = {lda0, lda1}, ldb[2] = {ldb0, ldb1};
+    float *D[2] = {D0, D1};
+    const int M[2] = {M0, M1}, N[2] = {N0, N1};
+    for (int i = 0; i < 2; ++i) {
+        g[i].A = (const bf16 *)A[i];
+        g[i].lda = lda[i];
+        g[i].a_kmajor = false;
+        g[i].B = (const bf16 *)Bp[i];
+        g[i].ldb = ldb[i];
+        g[i].b_kmajor = false;
+        g[i].D = D[i];
+        g[i].ldd = N[i];
+        g[i].M = M[i];
+        g[i].N = N[i];
+        g[i].K = K;
+        g[i].epi = GPT2_EPI_ACCUM_F32;
+        g[i].err = nullptr;
+    }
+    return tcg::launch_gemm_tc_grouped(g[0], g[1], op_sms(), (cudaStream_t)stream);
 }
 
 extern "C" int gpt2_op_layernorm_forward(const void *x, const float *g, const float *b, void *y, float *mean,

@@ -36,11 +36,18 @@ int encode_tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer
     return encode_tmap_t(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, inner, outer, ld_elems, box_inner, box_outer);
 }
 
-// units: work units (tiles x splits); the grid is one CTA per SM (or one pair
-// of CTAs per two SMs) up to that count.
+// Everything a launch passes to the kernel.  P.num_work work units (tiles x
+// splits, of one or two products); the grid is one CTA per SM (or one pair of
+// CTAs per two SMs) up to that count.
+struct LaunchArgs {
+    CUtensorMap ta, tb, td, td2;
+    GroupMaps gm;
+    Params P;
+};
+
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR, bool F8 = false>
-static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td, const CUtensorMap &td2,
-                      const Params &P, int units, int num_sms, cudaStream_t st) {
+static int launch_one(const LaunchArgs &L, int num_sms, cudaStream_t st) {
+    const int units = L.P.num_work;
     using Lay = SmemLayout<BN, STAGES, PAIR>;
     auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, PAIR, F8>;
     static PerDevice attr_pd, pairs_pd;
@@ -73,9 +80,9 @@ static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
             }))
             return rc;
         cfg.gridDim = dim3(2 * std::min(units, max_pairs));
-        GPT2_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, td, td2, P));
+        GPT2_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, L.ta, L.tb, L.td, L.td2, L.gm, L.P));
     } else {
-        kern<<<std::min(units, num_sms), NUM_THREADS, Lay::TOTAL, st>>>(ta, tb, td, td2, P);
+        kern<<<std::min(units, num_sms), NUM_THREADS, Lay::TOTAL, st>>>(L.ta, L.tb, L.td, L.td2, L.gm, L.P);
     }
     GPT2_CUDA_TRY(cudaGetLastError());
     gpt2_note_launches(1);
@@ -83,17 +90,19 @@ static int launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const CUtens
 }
 
 template <int BN, int STAGES, bool PAIR>
-static int dispatch_major(bool a_mn, bool b_mn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &td,
-                          const CUtensorMap &td2, const Params &P, int units, int num_sms, cudaStream_t st) {
-    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false, PAIR>(ta, tb, td, td2, P, units, num_sms, st);
-    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true, PAIR>(ta, tb, td, td2, P, units, num_sms, st);
-    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true, PAIR>(ta, tb, td, td2, P, units, num_sms, st);
-    return launch_one<BN, STAGES, true, false, PAIR>(ta, tb, td, td2, P, units, num_sms, st);
+static int dispatch_major(bool a_mn, bool b_mn, const LaunchArgs &L, int num_sms, cudaStream_t st) {
+    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false, PAIR>(L, num_sms, st);
+    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true, PAIR>(L, num_sms, st);
+    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true, PAIR>(L, num_sms, st);
+    return launch_one<BN, STAGES, true, false, PAIR>(L, num_sms, st);
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
+// Checks one product and fills L (maps, tile and split choice).  other_tiles: the
+// tiles of a second product launched with this one (the split-K choice then
+// fills the waves of both together).
+static int prepare(const GemmDesc &g, int num_sms, LaunchArgs &L, int &BN_out, bool &pair_out, int other_tiles) {
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPT2_ERR_BAD_SHAPE;
     const bool lse = g.epi == EPI_LSE, dz = g.epi == EPI_DZ;
     if (!g.A || !g.B || (!g.D && !lse)) return GPT2_ERR_BAD_ARG;
@@ -133,7 +142,8 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     // (-3%).
     const bool pair = BN == 256 && (g.epi != GPT2_EPI_RESIDUAL || g.K >= 1024);
     const int conc = pair ? num_sms / 2 : num_sms;  // work units that run at once
-    Params P;
+    Params &P = L.P;
+    P = Params{};
     P.M = g.M;
     P.N = g.N;
     P.K = g.K;
@@ -146,7 +156,7 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
         // fill whole waves of the persistent grid: the smallest split count
         // whose last wave is at least 95% busy, else the best one found.  Each
         // split keeps at least 4 K blocks.
-        const int tiles = P.num_m_blocks * P.num_n_blocks;
+        const int tiles = P.num_m_blocks * P.num_n_blocks + other_tiles;
         if (tiles < 2 * conc) {
             const int max_splits = std::max(1, P.num_k_blocks / 4);
             int best = 1;
@@ -190,7 +200,7 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     P.ldd = g.ldd;
     P.err = g.err;
 
-    CUtensorMap ta, tb;
+    CUtensorMap &ta = L.ta, &tb = L.tb;
     int rc;
     if (g.fp8) {  // bytes: 128 E4M3 values per 128-byte k-block row
         rc = encode_tmap_t(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.A, g.K, g.M, g.lda, 128, BM);
@@ -206,7 +216,9 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     }
 
     // bf16 outputs leave through TMA stores from the epilogue's staging blocks (box 64 x 32)
-    CUtensorMap td = ta, td2 = ta;  // unused copies when the output has no tensor map
+    CUtensorMap &td = L.td, &td2 = L.td2;
+    td = ta;  // unused copies when the output has no tensor map
+    td2 = ta;
     if (g.epi != GPT2_EPI_ACCUM_F32 && !lse && (rc = encode_tmap(&td, g.D, g.N, g.M, g.ldd, 64, 32))) return rc;
     // fp32 outputs are added through TMA reduce-adds of 32 x 32 blocks (BN of 128 and up)
     if (g.epi == GPT2_EPI_ACCUM_F32 && BN >= 128 &&
@@ -214,7 +226,18 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
         return rc;
     if (g.epi == GPT2_EPI_GELU && (rc = encode_tmap(&td2, g.D2, g.N, g.M, g.ldd, 64, 32))) return rc;
 
-    const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;
+    P.num_work = P.num_m_blocks * P.num_n_blocks * P.splits;
+    P.ngroups = 1;
+    P.work1 = P.num_work;
+    L.gm.a = ta;  // unused copies: no second product
+    L.gm.b = tb;
+    L.gm.d = td;
+    BN_out = BN;
+    pair_out = pair;
+    return GPT2_OK;
+}
+
+static int dispatch(const GemmDesc &g, const LaunchArgs &L, int BN, bool pair, int num_sms, cudaStream_t stream) {
     const bool a_mn = !g.a_kmajor, b_mn = !g.b_kmajor;
     const bool reads_r = g.epi == GPT2_EPI_RESIDUAL || g.epi == GPT2_EPI_GELU_BWD;
     // epilogues with a second staging block per warp (the prefetched operand, or the GELU
@@ -222,27 +245,72 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
     const bool two_bufs = (reads_r || g.epi == GPT2_EPI_GELU) && !a_mn;
     if (g.fp8) {  // E4M3 operands: K-major, BN 256 (pairs or single CTAs) or 128
         if (BN == 256 && pair)
-            return two_bufs ? launch_one<256, 5, false, false, true, true>(ta, tb, td, td2, P, num_work, num_sms, stream)
-                            : launch_one<256, 6, false, false, true, true>(ta, tb, td, td2, P, num_work, num_sms, stream);
+            return two_bufs ? launch_one<256, 5, false, false, true, true>(L, num_sms, stream)
+                            : launch_one<256, 6, false, false, true, true>(L, num_sms, stream);
         if (BN == 256)
-            return two_bufs ? launch_one<256, 3, false, false, false, true>(ta, tb, td, td2, P, num_work, num_sms, stream)
-                            : launch_one<256, 4, false, false, false, true>(ta, tb, td, td2, P, num_work, num_sms, stream);
-        return launch_one<128, 6, false, false, false, true>(ta, tb, td, td2, P, num_work, num_sms, stream);
+            return two_bufs ? launch_one<256, 3, false, false, false, true>(L, num_sms, stream)
+                            : launch_one<256, 4, false, false, false, true>(L, num_sms, stream);
+        return launch_one<128, 6, false, false, false, true>(L, num_sms, stream);
     }
     if (BN == 256 && pair) {
         if (two_bufs)
-            return b_mn ? launch_one<256, 5, false, true, true>(ta, tb, td, td2, P, num_work, num_sms, stream)
-                        : launch_one<256, 5, false, false, true>(ta, tb, td, td2, P, num_work, num_sms, stream);
-        return dispatch_major<256, 6, true>(a_mn, b_mn, ta, tb, td, td2, P, num_work, num_sms, stream);
+            return b_mn ? launch_one<256, 5, false, true, true>(L, num_sms, stream)
+                        : launch_one<256, 5, false, false, true>(L, num_sms, stream);
+        return dispatch_major<256, 6, true>(a_mn, b_mn, L, num_sms, stream);
     }
     if (BN == 256) {
         if (two_bufs)
-            return b_mn ? launch_one<256, 3, false, true, false>(ta, tb, td, td2, P, num_work, num_sms, stream)
-                        : launch_one<256, 3, false, false, false>(ta, tb, td, td2, P, num_work, num_sms, stream);
-        return dispatch_major<256, 4, false>(a_mn, b_mn, ta, tb, td, td2, P, num_work, num_sms, stream);
+            return b_mn ? launch_one<256, 3, false, true, false>(L, num_sms, stream)
+                        : launch_one<256, 3, false, false, false>(L, num_sms, stream);
+        return dispatch_major<256, 4, false>(a_mn, b_mn, L, num_sms, stream);
     }
-    if (BN == 128) return dispatch_major<128, 6, false>(a_mn, b_mn, ta, tb, td, td2, P, num_work, num_sms, stream);
-    return dispatch_major<64, 8, false>(a_mn, b_mn, ta, tb, td, td2, P, num_work, num_sms, stream);
+    if (BN == 128) return dispatch_major<128, 6, false>(a_mn, b_mn, L, num_sms, stream);
+    return dispatch_major<64, 8, false>(a_mn, b_mn, L, num_sms, stream);
+}
+
+int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
+    LaunchArgs L;
+    int BN = 0;
+    bool pair = false;
+    if (int rc = prepare(g, num_sms, L, BN, pair, 0)) return rc;
+    return dispatch(g, L, BN, pair, num_sms, stream);
+}
+
+int launch_gemm_tc_grouped(const GemmDesc &g0, const GemmDesc &g1, int num_sms, cudaStream_t stream) {
+    // fp32-accumulate products on CTA pairs with both operands MN-major and the same K
+    // (the weight gradients of one block); anything else runs as two launches
+    const auto groupable = [](const GemmDesc &g) {
+        return g.epi == GPT2_EPI_ACCUM_F32 && !g.fp8 && !g.a_kmajor && !g.b_kmajor && !g.a_scale && !g.b_scale &&
+               !g.bias && !g.dbias && g.N >= 256;
+    };
+    if (!groupable(g0) || !groupable(g1) || g0.K != g1.K || g0.alpha != g1.alpha) {
+        if (int rc = launch_gemm_tc(g0, num_sms, stream)) return rc;
+        return launch_gemm_tc(g1, num_sms, stream);
+    }
+    const int tiles0 = ceil_div(g0.M, 2 * BM) * ceil_div(g0.N, 256), tiles1 = ceil_div(g1.M, 2 * BM) * ceil_div(g1.N, 256);
+    LaunchArgs L, L1;
+    int BN0 = 0, BN1 = 0;
+    bool pair0 = false, pair1 = false;
+    if (int rc = prepare(g0, num_sms, L, BN0, pair0, tiles1)) return rc;
+    if (int rc = prepare(g1, num_sms, L1, BN1, pair1, tiles0)) return rc;
+    Params &P = L.P;
+    const Params &Q = L1.P;
+    if (BN0 != 256 || BN1 != 256 || !pair0 || !pair1 || P.splits != Q.splits ||
+        P.k_blocks_per_split != Q.k_blocks_per_split || P.num_m_blocks * P.num_n_blocks != tiles0 ||
+        Q.num_m_blocks * Q.num_n_blocks != tiles1)
+        return GPT2_ERR_UNSUPPORTED;  // the two choices agree by construction
+    P.ngroups = 2;
+    P.work1 = tiles0 * P.splits;
+    P.num_work = (tiles0 + tiles1) * P.splits;
+    P.g2_M = Q.M;
+    P.g2_N = Q.N;
+    P.g2_num_m_blocks = Q.num_m_blocks;
+    P.g2_num_n_blocks = Q.num_n_blocks;
+    P.g2_n_fastest = Q.n_fastest;
+    L.gm.a = L1.ta;
+    L.gm.b = L1.tb;
+    L.gm.d = L1.td;
+    return launch_one<256, 6, true, true, true>(L, num_sms, stream);
 }
 
 }  // namespace tcg

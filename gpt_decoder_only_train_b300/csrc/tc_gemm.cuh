@@ -73,6 +73,16 @@ struct Params {
     bf16 *D2;
     int64_t ldd;
     int *err;
+    // Work units of the launch.  With ngroups = 2 a second product runs in the same
+    // launch (fp32 accumulate, same K and splits): units at or past work1 are its
+    // tiles, with the geometry below and the tensor maps of GroupMaps.
+    int num_work, ngroups, work1;
+    int g2_M, g2_N, g2_num_m_blocks, g2_num_n_blocks, g2_n_fastest;
+};
+
+// Tensor maps of the second product of a grouped launch (A, B, fp32 D).
+struct alignas(64) GroupMaps {
+    CUtensorMap a, b, d;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -356,6 +366,28 @@ __device__ __forceinline__ int tile_m(const Params &P, int tile) {
 }
 __device__ __forceinline__ int tile_n(const Params &P, int tile) {
     return P.n_fastest ? tile % P.num_n_blocks : tile / P.num_m_blocks;
+}
+
+// Work unit w: its tile (m, n blocks), K-block range and product (0, or 1 for the
+// second product of a grouped launch).
+struct UnitView {
+    int tm, tn, kb0, kb1, second;
+};
+__device__ __forceinline__ UnitView unit_view(const Params &P, int w) {
+    UnitView u;
+    u.second = P.ngroups > 1 && w >= P.work1;
+    const int wl = u.second ? w - P.work1 : w;
+    const int split = wl % P.splits, tile = wl / P.splits;
+    if (u.second) {
+        u.tm = P.g2_n_fastest ? tile / P.g2_num_n_blocks : tile % P.g2_num_m_blocks;
+        u.tn = P.g2_n_fastest ? tile % P.g2_num_n_blocks : tile / P.g2_num_m_blocks;
+    } else {
+        u.tm = tile_m(P, tile);
+        u.tn = tile_n(P, tile);
+    }
+    u.kb0 = split * P.k_blocks_per_split;
+    u.kb1 = min(P.num_k_blocks, u.kb0 + P.k_blocks_per_split);
+    return u;
 }
 
 // ---- epilogue -----------------------------------------------------------------
@@ -703,7 +735,8 @@ __device__ __forceinline__ void epilogue_group64(const Params &P, const CUtensor
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool PAIR = false, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2, const Params P) {
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmD2,
+                   const __grid_constant__ GroupMaps gm, const Params P) {
     using Lay = SmemLayout<BN, STAGES, PAIR>;
     static_assert(!F8 || (!A_MN && !B_MN), "E4M3 operands are K-major");
     constexpr uint32_t IDESC = PAIR ? instr_desc_pair(BN, A_MN, B_MN, F8) : instr_desc(BN, A_MN, B_MN, F8);
@@ -742,6 +775,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tmB);
         if (P.epi != EPI_LSE) tma_prefetch_desc(&tmD);
         if (P.epi == GPT2_EPI_GELU) tma_prefetch_desc(&tmD2);
+        if (P.ngroups > 1) {
+            tma_prefetch_desc(&gm.a);
+            tma_prefetch_desc(&gm.b);
+            tma_prefetch_desc(&gm.d);
+        }
     }
     if (warp == 1) {
         if constexpr (PAIR) {  // one warp of each CTA of the pair allocates collectively
@@ -760,7 +798,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_work = P.num_m_blocks * P.num_n_blocks * P.splits;
+    const int num_work = P.num_work;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -770,10 +808,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
             for (int w = unit0; w < num_work && ok; w += ustep) {
-                const int split = w % P.splits, tile = w / P.splits;
-                const int m0 = tile_m(P, tile) * TM + row_off, n0 = tile_n(P, tile) * BN + (PAIR ? (int)rank * BN_CTA : 0);
-                const int kb0 = split * P.k_blocks_per_split;
-                const int kb1 = min(P.num_k_blocks, kb0 + P.k_blocks_per_split);
+                const UnitView u = unit_view(P, w);
+                const int m0 = u.tm * TM + row_off, n0 = u.tn * BN + (PAIR ? (int)rank * BN_CTA : 0);
+                const int kb0 = u.kb0, kb1 = u.kb1;
+                const CUtensorMap *ta = u.second ? &gm.a : &tmA, *tb = u.second ? &gm.b : &tmB;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.err)) {
                         ok = false;
@@ -787,32 +825,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (rank == 0) mbar_expect_tx(&full[stage], 2 * Lay::STAGE_BYTES);
                         const uint32_t fb = smem_in_rank(&full[stage], 0);
                         if (!A_MN) {
-                            tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
+                            tma_load_2d_pair(a_dst, ta, fb, k0, m0);
                         } else {
-                            tma_load_2d_pair(a_dst, &tmA, fb, m0, k0);
-                            tma_load_2d_pair(a_dst + MN_BLOCK_BYTES, &tmA, fb, m0 + 64, k0);
+                            tma_load_2d_pair(a_dst, ta, fb, m0, k0);
+                            tma_load_2d_pair(a_dst + MN_BLOCK_BYTES, ta, fb, m0 + 64, k0);
                         }
                         if (!B_MN) {
-                            tma_load_2d_pair(b_dst, &tmB, fb, k0, n0);
+                            tma_load_2d_pair(b_dst, tb, fb, k0, n0);
                         } else {
 #pragma unroll
                             for (int i = 0; i < BN_CTA / 64; ++i)
-                                tma_load_2d_pair(b_dst + i * MN_BLOCK_BYTES, &tmB, fb, n0 + 64 * i, k0);
+                                tma_load_2d_pair(b_dst + i * MN_BLOCK_BYTES, tb, fb, n0 + 64 * i, k0);
                         }
                     } else {
                         mbar_expect_tx(&full[stage], Lay::STAGE_BYTES);
                         if (!A_MN) {
-                            tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
+                            tma_load_2d(a_dst, ta, &full[stage], k0, m0);
                         } else {
-                            tma_load_2d(a_dst, &tmA, &full[stage], m0, k0);
-                            tma_load_2d(a_dst + MN_BLOCK_BYTES, &tmA, &full[stage], m0 + 64, k0);
+                            tma_load_2d(a_dst, ta, &full[stage], m0, k0);
+                            tma_load_2d(a_dst + MN_BLOCK_BYTES, ta, &full[stage], m0 + 64, k0);
                         }
                         if (!B_MN) {
-                            tma_load_2d(b_dst, &tmB, &full[stage], k0, n0);
+                            tma_load_2d(b_dst, tb, &full[stage], k0, n0);
                         } else {
 #pragma unroll
                             for (int i = 0; i < BN / 64; ++i)
-                                tma_load_2d(b_dst + i * MN_BLOCK_BYTES, &tmB, &full[stage], n0 + 64 * i, k0);
+                                tma_load_2d(b_dst + i * MN_BLOCK_BYTES, tb, &full[stage], n0 + 64 * i, k0);
                         }
                     }
                     issued_mask |= 1u << stage;
@@ -836,9 +874,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int t = 0;
             bool ok = true;
             for (int w = unit0; w < num_work && ok; w += ustep, ++t) {
-                const int split = w % P.splits;
-                const int kb0 = split * P.k_blocks_per_split;
-                const int kb1 = min(P.num_k_blocks, kb0 + P.k_blocks_per_split);
+                const UnitView u = unit_view(P, w);
+                const int kb0 = u.kb0, kb1 = u.kb1;
                 const int acc = t & 1;
                 const uint32_t aph = (t >> 1) & 1;
                 if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, P.err)) {
@@ -909,8 +946,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         int t = 0;
         for (int w = unit0; w < num_work; w += ustep, ++t) {
-            const int tile = w / P.splits;
-            const int m0 = tile_m(P, tile) * TM + row_off, n0 = tile_n(P, tile) * BN;
+            const UnitView u = unit_view(P, w);
+            const int m0 = u.tm * TM + row_off, n0 = u.tn * BN;
+            const int Nu = u.second ? P.g2_N : P.N;  // the product's N (grouped launches: fp32 accumulate only)
             const int acc = t & 1;
             const uint32_t aph = (t >> 1) & 1;
             if (!mbar_wait(&tfull[acc], aph, abort_flag, P.err)) break;
@@ -964,8 +1002,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                     if (P.epi == GPT2_EPI_ACCUM_F32) {
-                        if (col < P.N) reduce_block32(P, &tmD, stage, row0, col, lane, r0);
-                        if (col + 32 < P.N) reduce_block32(P, &tmD, stage, row0, col + 32, lane, r1);
+                        const CUtensorMap *td = u.second ? &gm.d : &tmD;
+                        if (col < Nu) reduce_block32(P, td, stage, row0, col, lane, r0);
+                        if (col + 32 < Nu) reduce_block32(P, td, stage, row0, col + 32, lane, r1);
                     } else if (col < P.N) {
                         epilogue_group64(P, &tmD, &tmD2, stage, gstage, rstage, row0, col, lane, r0, r1);
                     }
@@ -1054,5 +1093,10 @@ struct GemmDesc {
 };
 
 int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream);
+
+// Two fp32-accumulate products (both operands MN-major, the same K: the weight
+// gradients of one block) in one persistent launch, their tiles sharing the
+// waves and one prologue and drain; other pairs of products run as two launches.
+int launch_gemm_tc_grouped(const GemmDesc &g0, const GemmDesc &g1, int num_sms, cudaStream_t stream);
 
 }  // namespace tcg

@@ -94,6 +94,23 @@ def bench_matmul(a):
             "b_major": "mn" if a.b_mn else "k", "epi": a.epi, "ms": ms, "TFLOP/s": flops / ms / 1e9}
 
 
+def bench_matmul_accum2(a):
+    """Two weight-gradient products (M0 x N0 and M1 x N1, both K) in one grouped launch."""
+    K = a.K
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    A0 = torch.randn(K, a.M, device="cuda", generator=gen).to(torch.bfloat16)
+    B0 = torch.randn(K, a.N, device="cuda", generator=gen).to(torch.bfloat16)
+    A1 = torch.randn(K, a.M2, device="cuda", generator=gen).to(torch.bfloat16)
+    B1 = torch.randn(K, a.N2, device="cuda", generator=gen).to(torch.bfloat16)
+    D0 = torch.zeros(a.M, a.N, device="cuda")
+    D1 = torch.zeros(a.M2, a.N2, device="cuda")
+    ms = _time(lambda i: g.matmul_accum2(A0, a.M, B0, a.N, D0, a.M, a.N, A1, a.M2, B1, a.N2, D1, a.M2, a.N2, K),
+               a.iters, a.warmup)
+    flops = 2.0 * K * (a.M * a.N + a.M2 * a.N2)
+    return {"op": "matmul_accum2", "M0": a.M, "N0": a.N, "M1": a.M2, "N1": a.N2, "K": K, "ms": ms,
+            "TFLOP/s": flops / ms / 1e9}
+
+
 def attn_flops(B, T, H, hd=64):
     return 4.0 * hd * (T * (T + 1) / 2) * B * H
 
@@ -217,12 +234,14 @@ def bench_layernorm(a):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["matmul", "attention", "classifier", "layernorm", "attention-sweep", "generate",
+    ap.add_argument("op", choices=["matmul", "matmul-accum2", "attention", "classifier", "layernorm", "attention-sweep", "generate",
                                    "attention-fb", "adamw"])
     ap.add_argument("--C", type=int, default=768)
     ap.add_argument("--M", type=int, default=16384)
     ap.add_argument("--N", type=int, default=2304)
     ap.add_argument("--K", type=int, default=768)
+    ap.add_argument("--M2", type=int, default=3072, help="matmul-accum2: the second product's M")
+    ap.add_argument("--N2", type=int, default=768, help="matmul-accum2: the second product's N")
     ap.add_argument("--a-mn", action="store_true")
     ap.add_argument("--b-mn", action="store_true")
     ap.add_argument("--epi", default="store", choices=sorted(EPIS))
@@ -246,6 +265,8 @@ def main(argv=None):
     build.build()
     if a.op == "matmul":
         out = [bench_matmul(a)]
+    elif a.op == "matmul-accum2":
+        out = [bench_matmul_accum2(a)]
     elif a.op == "attention":
         out = [bench_attention(a.B, a.T, a.H, a.bwd, a.iters, a.warmup, a.recompute)]
     elif a.op == "classifier":

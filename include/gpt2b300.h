@@ -399,6 +399,24 @@ int gpt2_op_matmul(const void *A, int64_t lda, int a_kmajor, const void *B, int6
                    void *D2, const void *R, int64_t ldd, const float *bias, int M, int N, int K, int epilogue,
                    void *stream);
 
+/*
+ * Two weight-gradient products in one launch ("Let's reproduce GPT-2 (124M)",
+ * §Video özeti: the backward pass of each linear layer):
+ *   D0[m, n] += sum_k A0[k, m] B0[k, n]   (m < M0, n < N0)
+ *   D1[m, n] += sum_k A1[k, m] B1[k, n]   (m < M1, n < N1)
+ * A_i, B_i bf16 row-major [K, M_i] and [K, N_i] with leading dimensions lda_i,
+ * ldb_i (the activation and the output gradient of a layer, as stored); D_i fp32
+ * row-major [M_i, N_i] with leading dimension N_i.  Both products share K, run as
+ * one persistent tcgen05 kernel whose work units are the tiles of both, and add
+ * their fp32 results through TMA reduce-adds; results are those of two
+ * gpt2_op_matmul calls with GPT2_EPI_ACCUM_F32 up to the order of fp32 additions.
+ * Products with N_i < 256 run as two launches.  Requirements as for
+ * gpt2_op_matmul (leading dimensions multiples of 8, 16-byte aligned pointers).
+ */
+int gpt2_op_matmul_accum2(const void *A0, int64_t lda0, const void *B0, int64_t ldb0, float *D0, int M0, int N0,
+                          const void *A1, int64_t lda1, const void *B1, int64_t ldb1, float *D1, int M1, int N1, int K,
+                          void *stream);
+
 /* ---- E4M3 (FP8) matmul -------------------------------------------------------
  * The pages name FP8 as the next precision step of this training code ("llm.c
  * kullanarak GPT-2 modelini düşük maliyetle yeniden uygulamak", §SSS; the

@@ -138,6 +138,27 @@ def test_matmul_accumulate_fp32_touches_only_its_block(g, M, N, ldd, K):
     assert (out[:, :N] - ref).abs().max().item() < 1e-4 * ref.abs().max().item() + 1e-5
 
 
+@pytest.mark.parametrize("p0,p1,K", [((768, 3072), (3072, 768), 2048), ((300, 520), (130, 264), 1000),
+                                      ((768, 768), (2304, 768), 4096), ((200, 136), (256, 512), 512)])
+def test_matmul_accum2_is_two_products(g, p0, p1, K):
+    """Two weight-gradient products in one launch (the last case has N < 256 on one side
+    and runs as two launches): each output gets its own product added, fp32 bounds."""
+    outs = []
+    for (M, N), seed in ((p0, 20), (p1, 30)):
+        A, As, lda = _operand(M, K, 0, seed)
+        B, Bs, ldb = _operand(N, K, 0, seed + 1)
+        base = torch.randn(M, N, dtype=torch.float32)
+        outs.append((A, As, lda, B, Bs, ldb, base, base.clone().cuda(), M, N))
+    (A0, As0, lda0, B0, Bs0, ldb0, base0, D0, M0, N0), (A1, As1, lda1, B1, Bs1, ldb1, base1, D1, M1, N1) = outs
+    g.matmul_accum2(As0.cuda(), lda0, Bs0.cuda(), ldb0, D0, M0, N0, As1.cuda(), lda1, Bs1.cuda(), ldb1, D1, M1, N1, K)
+    torch.cuda.synchronize()
+    for A, B, base, D in ((A0, B0, base0, D0), (A1, B1, base1, D1)):
+        ref = base.double() + A.double() @ B.double().T
+        out = D.double().cpu()
+        assert ((out - ref).norm() / ref.norm()).item() < 1e-5
+        assert (out - ref).abs().max().item() < 1e-4 * ref.abs().max().item() + 1e-5
+
+
 def test_matmul_rejects_bad_shapes(g):
     a = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
     d = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
