@@ -141,8 +141,8 @@ GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
     "workload": "gpt2_124m",
-    "sha256": "3a2fee67fe66be9695b685dd042c99d874f51e6b6761395012eee59eb8d2fd3b",
-    "bytes_per_launch": 21.99e9 / 147,
+    "sha256": "4da3d4151f0386d6fb7ec0d7d432a68ce16097574cb39686f2030b3db3ed7539",
+    "bytes_per_launch": 21.856e9 / 123,
 }
 
 
