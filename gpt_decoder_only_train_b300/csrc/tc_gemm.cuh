@@ -80,8 +80,9 @@ struct Params {
     int g2_M, g2_N, g2_num_m_blocks, g2_num_n_blocks, g2_n_fastest;
 };
 
-// Tensor maps of the second product of a grouped launch (A, B, fp32 D).
-struct alignas(64) GroupMaps {
+// Tensor maps of the second product of a grouped launch (A, B, fp32 D); each
+// CUtensorMap carries its own 128-byte alignment.
+struct GroupMaps {
     CUtensorMap a, b, d;
 };
 

@@ -297,7 +297,12 @@ def test_attention_sweep(g, T, B):
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
     scratch = torch.empty(B * H * T, dtype=torch.float32, device="cuda")
     g.attention_backward(qd, kd, vd, o, dod, lse, dq, dk, dv, scratch, B, T, H)
+    # and the backward the model and the sweep's "bwd" run: dS kept in a workspace
+    dq2, dk2, dv2 = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+    ds = torch.empty(g.attention_backward_ds_bytes(B, T, H), dtype=torch.uint8, device="cuda")
+    g.attention_backward_ds(qd, kd, vd, o, dod, lse, dq2, dk2, dv2, scratch, ds, B, T, H)
     torch.cuda.synchronize()
+    del ds
     if T == 256:
         heads = [(b, h) for b in range(B) for h in range(H)]
     else:
@@ -305,6 +310,7 @@ def test_attention_sweep(g, T, B):
         heads = [(int(rng.integers(B)), int(rng.integers(H))) for _ in range(3)] + [(B - 1, H - 1)]
     o_c, lse_c = o.cpu().double(), lse.cpu().double()
     outs = [t.cpu().double() for t in (dq, dk, dv)]
+    outs2 = [t.cpu().double() for t in (dq2, dk2, dv2)]
     bs = sorted({b for b, _ in heads})
     for b in bs:
         hs = [h for bb, h in heads if bb == b]
@@ -319,5 +325,5 @@ def test_attention_sweep(g, T, B):
                 assert err <= tol_e * ref.abs().max().item() and fro <= tol_f, (T, b, h, err, fro)
             chk(o_c[b, :, h], ro[hi], 2e-2, 1e-2)
             assert (lse_c[b, h] - rl[hi]).abs().max().item() < 2e-3
-            for out, ref in zip(outs, (rq, rk, rv)):
+            for out, ref in zip(outs + outs2, (rq, rk, rv) * 2):
                 chk(out[b, :, h], ref[hi], 4e-2, 2e-2)
