@@ -141,8 +141,8 @@ GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
     "workload": "gpt2_124m",
-    "sha256": "4da3d4151f0386d6fb7ec0d7d432a68ce16097574cb39686f2030b3db3ed7539",
-    "bytes_per_launch": 21.856e9 / 123,
+    "sha256": "e930089904042c0ff8ee06f8f019156aa2535d54e9ea35f102f64b08fb973bac",
+    "bytes_per_launch": 21.824e9 / 123,
 }
 
 
