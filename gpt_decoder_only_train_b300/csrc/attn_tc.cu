@@ -874,6 +874,12 @@ __global__ void __launch_bounds__(dq::NTH, 1)
 // dK [320,384), K[s] [384+64s, +32), V[s] [416+64s, +32) (bf16 pairs).
 // Warps: 0 loads (TMA, cp.async), 1 issues the MMAs, 2-17 are the softmax
 // warps: four per TMEM lane quadrant, each owning 16 of a block's 64 queries.
+// With store_ds (the backward with the dS workspace), the softmax warps also
+// write their dS^T values into the block's 128 x 64 staging tile (two tiles,
+// by block parity) and fence them for the async proxy; once pds_full has
+// completed, the MMA thread stores the tile with one TMA store (L2 evict-first)
+// into the 64 x 64-blocked dS^T layout, and waits for the store of block g - 2
+// to have read its tile before it lets block g's S^T be consumed.
 namespace dkv {
 constexpr int BKY = 128, BQ = 64, SLOTS = 12, SWARPS = 16, NLD = SLOTS / 2;
 constexpr int NTH = 64 + 32 * SWARPS;
