@@ -99,10 +99,8 @@ static int dispatch_major(bool a_mn, bool b_mn, const LaunchArgs &L, int num_sms
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Checks one product and fills L (maps, tile and split choice).  other_tiles: the
-// tiles of a second product launched with this one (the split-K choice then
-// fills the waves of both together).
-static int prepare(const GemmDesc &g, int num_sms, LaunchArgs &L, int &BN_out, bool &pair_out, int other_tiles) {
+// Argument checks of one product (no device or driver call).
+static int check_desc(const GemmDesc &g) {
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPT2_ERR_BAD_SHAPE;
     const bool lse = g.epi == EPI_LSE, dz = g.epi == EPI_DZ;
     if (!g.A || !g.B || (!g.D && !lse)) return GPT2_ERR_BAD_ARG;
@@ -129,9 +127,17 @@ static int prepare(const GemmDesc &g, int num_sms, LaunchArgs &L, int &BN_out, b
     if (g.epi == GPT2_EPI_GELU && (!g.D2 || !aligned16(g.D2))) return GPT2_ERR_BAD_ARG;
     if (g.bias && (reinterpret_cast<uintptr_t>(g.bias) & 15)) return GPT2_ERR_BAD_ARG;
     if (g.dbias && (reinterpret_cast<uintptr_t>(g.dbias) & 7)) return GPT2_ERR_BAD_ARG;
+    if (g.dbias && g.epi != GPT2_EPI_ACCUM_F32 && g.N <= 64) return GPT2_ERR_UNSUPPORTED;  // staged epilogue only
+    return GPT2_OK;
+}
 
+// Checks one product and fills L (maps, tile and split choice).  other_tiles: the
+// tiles of a second product launched with this one (the split-K choice then
+// fills the waves of both together).
+static int prepare(const GemmDesc &g, int num_sms, LaunchArgs &L, int &BN_out, bool &pair_out, int other_tiles) {
+    if (int rc = check_desc(g)) return rc;
+    const bool lse = g.epi == EPI_LSE;
     const int BN = g.N >= 256 ? 256 : (g.N > 64 ? 128 : 64);
-    if (g.dbias && g.epi != GPT2_EPI_ACCUM_F32 && BN < 128) return GPT2_ERR_UNSUPPORTED;  // staged epilogue only
     // CTA pairs on 256 x 256 tiles (cta_group::2): each SM reads half of the B
     // tile per stage, which keeps shared-memory traffic per MMA within what the
     // SM delivers, at the cost of pair synchronisation per tile.  Measured on
@@ -278,21 +284,26 @@ int launch_gemm_tc(const GemmDesc &g, int num_sms, cudaStream_t stream) {
 
 int launch_gemm_tc_grouped(const GemmDesc &g0, const GemmDesc &g1, int num_sms, cudaStream_t stream) {
     // fp32-accumulate products on CTA pairs with both operands MN-major and the same K
-    // (the weight gradients of one block); anything else runs as two launches
+    // (the weight gradients of one block); anything else runs as two launches.  Both
+    // products are checked before either is launched.
     const auto groupable = [](const GemmDesc &g) {
         return g.epi == GPT2_EPI_ACCUM_F32 && !g.fp8 && !g.a_kmajor && !g.b_kmajor && !g.a_scale && !g.b_scale &&
                !g.bias && !g.dbias && g.N >= 256;
     };
-    if (!groupable(g0) || !groupable(g1) || g0.K != g1.K || g0.alpha != g1.alpha) {
-        if (int rc = launch_gemm_tc(g0, num_sms, stream)) return rc;
-        return launch_gemm_tc(g1, num_sms, stream);
-    }
-    const int tiles0 = ceil_div(g0.M, 2 * BM) * ceil_div(g0.N, 256), tiles1 = ceil_div(g1.M, 2 * BM) * ceil_div(g1.N, 256);
+    const bool grouped = groupable(g0) && groupable(g1) && g0.K == g1.K && g0.alpha == g1.alpha;
+    const int tiles0 = grouped ? ceil_div(g0.M, 2 * BM) * ceil_div(g0.N, 256) : 0,
+              tiles1 = grouped ? ceil_div(g1.M, 2 * BM) * ceil_div(g1.N, 256) : 0;
+    if (int rc = check_desc(g0)) return rc;
+    if (int rc = check_desc(g1)) return rc;
     LaunchArgs L, L1;
     int BN0 = 0, BN1 = 0;
     bool pair0 = false, pair1 = false;
     if (int rc = prepare(g0, num_sms, L, BN0, pair0, tiles1)) return rc;
     if (int rc = prepare(g1, num_sms, L1, BN1, pair1, tiles0)) return rc;
+    if (!grouped) {
+        if (int rc = dispatch(g0, L, BN0, pair0, num_sms, stream)) return rc;
+        return dispatch(g1, L1, BN1, pair1, num_sms, stream);
+    }
     Params &P = L.P;
     const Params &Q = L1.P;
     if (BN0 != 256 || BN1 != 256 || !pair0 || !pair1 || P.splits != Q.splits ||

@@ -147,3 +147,26 @@ def test_attention_ds_entry_sizes_and_checks_its_workspace(libh):
     assert bwd(2, 128, 1, 64, p, n, rs=100) == bad_shape  # row stride not a multiple of 8
     assert bwd(0, 128, 1, 64, p, n) == bad_shape
     assert bwd(1, 128, 33, 64, p, 1 << 40, rs=33 * 64 * 3) == unsupported  # H * 64 above 2048
+
+
+def test_grouped_matmul_checks_both_products_before_any_device_work(libh):
+    """gpt2_op_matmul_accum2 rejects a bad first or second product with the same codes as
+    gpt2_op_matmul, before any tensor map is built or kernel launched (so a bad second
+    product never leaves the first one applied)."""
+    import gpt_decoder_only_train_b300 as g
+
+    L = g.lib()
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its checks first
+    f = ctypes.cast(p, ctypes.POINTER(ctypes.c_float))
+
+    def call(M0=768, N0=3072, M1=3072, N1=768, K=1024, lda0=768, ldb0=3072, lda1=3072, ldb1=768, a1=p):
+        return L.gpt2_op_matmul_accum2(p, lda0, p, ldb0, f, M0, N0, a1, lda1, p, ldb1, f, M1, N1, K, None)
+
+    bad_shape, bad_arg = -2, -8
+    assert call(K=0) == bad_shape
+    assert call(M0=0) == bad_shape
+    assert call(lda0=770) == bad_shape  # leading dimension not a multiple of 8
+    assert call(N1=100) == bad_shape  # the second product: N not a multiple of 8
+    assert call(ldb1=772) == bad_shape
+    assert call(a1=None) == bad_arg  # the second product's A missing
+    assert call(a1=ctypes.c_void_p((1 << 20) + 8)) == bad_arg  # not 16-byte aligned
