@@ -141,8 +141,8 @@ GEMM_TRAFFIC = {
     "sources": ["gpt_decoder_only_train_b300/csrc/tc_gemm.cu", "gpt_decoder_only_train_b300/csrc/tc_gemm.cuh",
                 "gpt_decoder_only_train_b300/csrc/common.cuh"],
     "workload": "gpt2_124m",
-    "sha256": "e930089904042c0ff8ee06f8f019156aa2535d54e9ea35f102f64b08fb973bac",
-    "bytes_per_launch": 21.824e9 / 123,
+    "sha256": "ffb2b0d940636f3b58d2a5886e13260ecca3761adc6cee2861fd3ac139c9a4c7",
+    "bytes_per_launch": 21.786e9 / 123,
 }
 
 
