@@ -67,3 +67,27 @@ def test_bench_learning_rate_is_the_oracle_schedule():
     """bench.py restates the warmup + cosine schedule; it must give the oracle's values."""
     for it in (0, 1, 19, 20, 698, 699, 700, 701, 5000, 9886, 19072, 19073, 19074, 25000):
         assert bench.lr_at(it) == og.lr_schedule(it), it
+
+
+def test_stored_gemm_traffic_is_gated_on_the_gemm_sources(monkeypatch):
+    """The stored per-launch GEMM DRAM traffic is reported only while the GEMM sources hash to
+    the version it was captured from, and then it is plausible against the algorithmic bytes
+    (every operand read once, every output written once, fp32 weight gradients read and
+    written): below them (L2 keeps some re-reads off DRAM) but not by more than half."""
+    w = synthetic.WORKLOADS["gpt2_124m"]
+    BT, C, V = w["B"] * w["T"], w["C"], w["Vp"]
+    algo = 0.0
+    for k, n in [(C, 3 * C), (C, C), (C, 4 * C), (4 * C, C)]:  # per block: in, out
+        act_in, act_out, weight = BT * k * 2, BT * n * 2, k * n
+        algo += w["L"] * (act_in + act_out + weight * 2)  # forward: x, W read, y written
+        algo += w["L"] * (act_out + weight * 2 + act_in)  # dX: dy, W read, dx written
+        algo += w["L"] * (act_out + act_in + weight * 8)  # dW: dy, x read, fp32 dW read + written
+    algo += BT * C * 2 + V * C * 2 + BT * V * 2  # LM head forward
+    algo += BT * V * 2 + V * C * 2 + BT * C * 2  # dX
+    algo += BT * V * 2 + BT * C * 2 + V * C * 8  # dW
+    traffic = bench.gemm_traffic()
+    if traffic is not None:
+        per_step = traffic * 123
+        assert 0.5 * algo <= per_step <= 1.05 * algo, (per_step / 1e9, algo / 1e9)
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, "sha256", "0" * 64)
+    assert bench.gemm_traffic() is None
