@@ -73,7 +73,8 @@ def test_stored_gemm_traffic_is_gated_on_the_gemm_sources(monkeypatch):
     """The stored per-launch GEMM DRAM traffic is reported only while the GEMM sources hash to
     the version it was captured from, and then it is plausible against the algorithmic bytes
     (every operand read once, every output written once, fp32 weight gradients read and
-    written): below them (L2 keeps some re-reads off DRAM) but not by more than half."""
+    written: 24.0 GB a step): below them (L2 keeps some re-reads off DRAM) but not by more than
+    half."""
     w = synthetic.WORKLOADS["gpt2_124m"]
     BT, C, V = w["B"] * w["T"], w["C"], w["Vp"]
     algo = 0.0
@@ -82,12 +83,16 @@ def test_stored_gemm_traffic_is_gated_on_the_gemm_sources(monkeypatch):
         algo += w["L"] * (act_in + act_out + weight * 2)  # forward: x, W read, y written
         algo += w["L"] * (act_out + weight * 2 + act_in)  # dX: dy, W read, dx written
         algo += w["L"] * (act_out + act_in + weight * 8)  # dW: dy, x read, fp32 dW read + written
+    # epilogue operands: the FC product's second output (GELU), the GELU backward reading h,
+    # the residual read by the two output projections
+    algo += w["L"] * (BT * 4 * C * 2 + BT * 4 * C * 2 + 2 * BT * C * 2)
     algo += BT * C * 2 + V * C * 2 + BT * V * 2  # LM head forward
     algo += BT * V * 2 + V * C * 2 + BT * C * 2  # dX
     algo += BT * V * 2 + BT * C * 2 + V * C * 8  # dW
     traffic = bench.gemm_traffic()
     if traffic is not None:
         per_step = traffic * 123
+        assert abs(algo / 1e9 - 24.0) < 0.05
         assert 0.5 * algo <= per_step <= 1.05 * algo, (per_step / 1e9, algo / 1e9)
     monkeypatch.setitem(bench.GEMM_TRAFFIC, "sha256", "0" * 64)
     assert bench.gemm_traffic() is None
