@@ -112,7 +112,7 @@ struct gpt2_model {
     int *tokens, *targets;
     void *dres, *dbig, *dqkv, *datt, *dsmall, *gelu_buf;
     float *attn_D;
-    void *attn_ds;  // attention backward: dS^T of the causal blocks (bf16 path)
+    void *attn_ds;  // attention backward: dS^T of the causal blocks (bf16 path, up to kMaxAttnDsBytes)
     void *emb_ws;  // embedding backward: sorted keys and partial sums
     double *norm_partials;
     unsigned *barrier;
@@ -234,6 +234,10 @@ void make_tensors(const gpt2_config &c, std::vector<TensorInfo> &ts, std::vector
 template <typename P> P *take_opt(Bump &b, bool on, size_t bytes) { return on ? b.take<P>(bytes) : nullptr; }
 
 constexpr int64_t kLmChunkRows = 8192;  // positions per chunk of the fused LM head's backward
+// Largest stored-dS workspace of the attention backward the model keeps (B H T^2 bf16:
+// 0.4 GB at B=16, T=1024, H=12; 6.4 GB at T=4096); past it the backward recomputes S
+// and dP for dQ instead of growing the arena with T^2.
+constexpr size_t kMaxAttnDsBytes = size_t(16) << 30;
 
 void plan(gpt2_model &m, uint8_t *base) {
     const gpt2_config &c = m.cfg;
@@ -295,7 +299,8 @@ void plan(gpt2_model &m, uint8_t *base) {
     m.dsmall = b.take<void>(BT * C * es);
     m.gelu_buf = take_opt<void>(b, c.recompute_gelu != 0, BT * 4 * C * es);
     m.attn_D = b.take<float>((int64_t)c.B * c.H * c.T * 4);
-    m.attn_ds = take_opt<void>(b, c.dtype == GPT2_DTYPE_BF16, fa::attention_backward_ds_bytes(c.B, c.T, c.H));
+    const size_t ds_bytes = fa::attention_backward_ds_bytes(c.B, c.T, c.H);
+    m.attn_ds = take_opt<void>(b, c.dtype == GPT2_DTYPE_BF16 && ds_bytes <= kMaxAttnDsBytes, ds_bytes);
     m.emb_ws = b.take<void>(k::embed_backward_workspace((int)BT, c.C));
     m.norm_partials = b.take<double>((size_t)m.max_adam_blocks * 8);
     m.barrier = b.take<unsigned>(64);

@@ -170,3 +170,21 @@ def test_grouped_matmul_checks_both_products_before_any_device_work(libh):
     assert call(ldb1=772) == bad_shape
     assert call(a1=None) == bad_arg  # the second product's A missing
     assert call(a1=ctypes.c_void_p((1 << 20) + 8)) == bad_arg  # not 16-byte aligned
+
+
+def test_arena_keeps_the_stored_ds_only_below_its_cap(libh):
+    """The model keeps the attention backward's dS workspace (B H Tp^2 bf16) up to 16 GiB:
+    one position block past that size the arena shrinks by the workspace it no longer holds
+    (the backward then recomputes S and dP for dQ)."""
+    import gpt_decoder_only_train_b300 as g
+
+    L = g.lib()
+
+    def arena(T):
+        c = g.make_config(dict(L=1, C=768, H=12, V=256, Vp=256, T=T, B=1, dtype="bf16"))
+        return L.gpt2_arena_bytes(ctypes.byref(c))
+
+    ds = lambda T: L.gpt2_attention_backward_ds_bytes(1, T, 12)
+    assert ds(26752) <= 16 << 30 < ds(26880)
+    assert arena(26880) < arena(26752) - ds(26752) + (1 << 30)
+    assert arena(1024) > ds(1024)  # small T: kept
