@@ -2,7 +2,8 @@
 
     python -m gpt_decoder_only_train_b300.kernel_bench matmul --M 16384 --N 50304 --K 768
     python -m gpt_decoder_only_train_b300.kernel_bench matmul --M 768 --N 768 --K 16384 --a-mn --b-mn --epi accum
-    python -m gpt_decoder_only_train_b300.kernel_bench attention --B 16 --T 1024 --H 12 [--bwd]
+    python -m gpt_decoder_only_train_b300.kernel_bench matmul-accum2 --M 768 --N 3072 --M2 3072 --N2 768 --K 16384
+    python -m gpt_decoder_only_train_b300.kernel_bench attention --B 16 --T 1024 --H 12 [--bwd [--recompute]]
     python -m gpt_decoder_only_train_b300.kernel_bench classifier --N 16384 --V 50257 --Vp 50304
     python -m gpt_decoder_only_train_b300.kernel_bench layernorm --N 16384 --C 768
     python -m gpt_decoder_only_train_b300.kernel_bench attention-sweep
@@ -13,6 +14,9 @@
 
 Inputs are seeded random bf16 on the device; each line reports the mean time
 per launch (CUDA events, after warm-up) and the algorithmic FLOP/s or bytes/s.
+`matmul-accum2` times two weight-gradient products in one grouped launch;
+`attention --bwd` times the backward with the dS workspace (the model's),
+`--recompute` the one without it.
 Repeated launches reuse the same inputs, so operands smaller than L2 (126 MB)
 may be served from L2.
 """
